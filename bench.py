@@ -1,0 +1,483 @@
+#!/usr/bin/env python
+"""Benchmark of the q8-KV decode step on GB300.
+
+One step = the whole hot path over one batch: quantise-append of the step's
+new K/V token for every (layer, kv head), then split-KV decode attention of
+every query head over its paged int8 context, then the split merge.  The
+default workload is the 28-layer Qwen3-2B-shaped decode stack (16 query / 8
+kv heads, hd 128, context 8192, batch 1), its layers folded into the batch
+dimension of one call.
+
+Prints one JSON line.  `value` is achieved algorithmic HBM throughput in GB/s
+(bytes a step must move / device time per step) summed over ranks;
+`us_per_step` and `ms_per_step` are the device time of one step.  Inputs are
+resident in HBM; the timed region rotates over several copies of the cache so
+that every step streams from HBM (the working set is far above L2).
+`--impl reference` times the CPU oracle on the host cores instead.
+Multi-GPU runs (torchrun) are independent replicas: the path needs no
+exchange between GPUs.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "q8-KV decode attention: μs/step and achieved HBM GB/s (% of GB300 peak)"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+THROTTLE_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--impl", choices=("kvq8", "reference"), default="kvq8")
+    ap.add_argument("--workload", default="qwen3_2b_28layers_ctx8192")
+    ap.add_argument("--copies", type=int, default=0,
+                    help="cache copies to rotate over (0 = enough to exceed 8x L2)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=0, help="0 = min(steps, 2000)")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------- ranks ---
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def dist_init(world: int, backend: str):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def reduce_scalar(x: float, op: str, device) -> float:
+    """max or sum of a per-rank scalar over all ranks (identity when alone)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def aggregate(per_rank_bytes: float, per_rank_seconds: float, device):
+    """Whole-job throughput of independent replicas: all ranks' bytes / slowest rank's time."""
+    total = reduce_scalar(per_rank_bytes, "sum", device)
+    slowest = reduce_scalar(per_rank_seconds, "max", device)
+    return total, slowest
+
+
+# ---------------------------------------------------------------- clocks ---
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.error = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError as e:
+            self.error = f"nvidia-smi unavailable: {e}"
+
+    def stop(self):
+        if self.proc is None:
+            return {"error": self.error or "not started"}
+        time.sleep(0.15)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(THROTTLE_REASONS, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"error": "no samples"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ peaks ---
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("decode.cu", "kvq8_device.cuh", "kvq8_internal.cuh"):
+        with open(os.path.join(ROOT, "int8_quantized_kv_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per decode-split launch from a committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("per_launch_bytes", {}).get(workload)
+
+
+# ------------------------------------------------------------- workloads ---
+def step_bytes(cfg, lens):
+    """Algorithmic bytes of one step: the decode pass plus the append of one
+    token per (sequence, kv head)."""
+    from int8_quantized_kv_gb300 import workloads as wl
+    return (wl.algorithmic_decode_bytes(cfg, lens) +
+            wl.algorithmic_append_bytes(cfg.batch * cfg.nkv, cfg.hd))
+
+
+def split_kernel_bytes(cfg, lens):
+    """Algorithmic bytes the split kernel moves: int8 K/V + scales + fp32 queries."""
+    import numpy as np
+    tok = int(np.asarray(lens, np.int64).sum())
+    return tok * cfg.nkv * (2 * cfg.hd + 8) + cfg.batch * cfg.nqh * cfg.hd * 4
+
+
+def workload_config(cfg, lens, copies):
+    import numpy as np
+    c = {"workload": cfg.name, "layers_folded_into_batch": cfg.layers,
+         "batch": cfg.batch // max(cfg.layers, 1), "nqh": cfg.nqh, "nkv": cfg.nkv, "hd": cfg.hd,
+         "block_size": 256, "ctx": int(lens.max()) if cfg.ctx is not None else
+         [int(lens.min()), int(lens.max())], "tokens": int(np.asarray(lens).sum()),
+         "step": "append 1 token per (layer, kv head) + split-KV decode + merge",
+         "block_table": "seeded shuffled physical blocks"}
+    if copies:
+        c["l2"] = f"rotates {copies} cache copies; working set >> 129 MB L2, no flush"
+    return c
+
+
+# ------------------------------------------------------------ CPU oracle ---
+class OracleStep:
+    """The oracle's share of one step for a sample of (sequence, kv head) units:
+    quantise the new token's K/V rows and the G query heads, then the three-pass
+    decode over the unit's int8 context (prepared beforehand: cache state)."""
+
+    def __init__(self, cfg, lens, units, sm_scale):
+        import numpy as np
+        import oracle
+        from int8_quantized_kv_gb300 import workloads as wl
+        self.cfg, self.units, self.sm = cfg, units, sm_scale
+        self.q = wl.queries(cfg)
+        self.state = {}
+        for b, h in units:
+            L = int(lens[b])
+            k, v = wl.unit_kv(cfg, b, h, L)
+            kq, ks = oracle.kv_quantize_rows(k[:L - 1])
+            vq, vs = oracle.kv_quantize_rows(v[:L - 1])
+            self.state[(b, h)] = (np.concatenate([kq, np.zeros((1, cfg.hd), np.int8)]),
+                                  np.concatenate([ks, np.zeros(1, np.float32)]),
+                                  np.concatenate([vq, np.zeros((1, cfg.hd), np.int8)]),
+                                  np.concatenate([vs, np.zeros(1, np.float32)]),
+                                  k[L - 1:L].copy(), v[L - 1:L].copy())
+
+    def run_unit(self, u):
+        import oracle
+        b, h = u
+        kq, ks, vq, vs, kn, vn = self.state[u]
+        nkq, nks = oracle.kv_quantize_rows(kn)
+        nvq, nvs = oracle.kv_quantize_rows(vn)
+        kq[-1], ks[-1], vq[-1], vs[-1] = nkq[0], nks[0], nvq[0], nvs[0]
+        G = self.cfg.group
+        qi, qsc = oracle.q_quantize_blocks(self.q[b, h * G:(h + 1) * G])
+        return oracle.decode_quantized_unit(qi, qsc, kq, ks, vq, vs, self.sm)
+
+    def run(self, threads):
+        import oracle
+        return oracle.run_parallel(self.run_unit, self.units, threads)
+
+
+def sample_units(cfg, lens, target_seconds, threads, max_units=None):
+    """Pick a seeded sample of units whose oracle step takes about target_seconds."""
+    import numpy as np
+    all_units = [(b, h) for b in range(cfg.batch) for h in range(cfg.nkv) if lens[b] > 1]
+    rng = np.random.default_rng(12345)
+    order = [all_units[i] for i in rng.permutation(len(all_units))]
+    probe = order[:max(1, min(len(order), threads))]
+    t0 = time.perf_counter()
+    OracleStep(cfg, lens, probe, 1.0).run(threads)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    n = int(len(probe) * target_seconds / dt)
+    n = max(len(probe), min(len(order), n))
+    if max_units:
+        n = min(n, max_units)
+    return order[:n], all_units
+
+
+def cpu_baseline(cfg, lens, target_seconds):
+    import numpy as np
+    threads = len(os.sched_getaffinity(0))
+    sm = np.float32(1.0 / math.sqrt(cfg.hd))
+    units, all_units = sample_units(cfg, lens, target_seconds / 2, threads)
+    st = OracleStep(cfg, lens, units, sm)
+    reps, t_total = 0, 0.0
+    while reps < 1 or (t_total < target_seconds and reps < 5):
+        t0 = time.perf_counter()
+        st.run(threads)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    per_rep = t_total / reps
+    frac = sum(int(lens[b]) for b, _ in units) / sum(int(lens[b]) for b, _ in all_units)
+    full_step_s = per_rep / frac
+    value = step_bytes(cfg, lens) / full_step_s / 1e9
+    return {"value": round(value, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": (f"{len(units)} of {len(all_units)} (sequence, kv head) units of one step "
+                       f"({frac:.1%} of its tokens), {reps} repetition(s), scaled to a full step "
+                       f"of {full_step_s * 1e3:.1f} ms"),
+            "ms_per_full_step": round(full_step_s * 1e3, 3)}
+
+
+# ---------------------------------------------------------------- kvq8 arm ---
+def run_kvq8(args, rank, world, local):
+    import numpy as np
+    import torch
+    from int8_quantized_kv_gb300 import kvq8
+    from int8_quantized_kv_gb300 import workloads as wl
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist_init(world, "nccl")
+    kvq8.load()
+    cfg = wl.WORKLOADS[args.workload]
+    lens = wl.ctx_lens(cfg)
+    table, num_blocks = wl.block_table(cfg, lens)
+    max_blocks = table.shape[1]
+    cache_bytes = 2 * kvq8.kv_pool_bytes(num_blocks, cfg.nkv) + 2 * kvq8.scale_pool_bytes(num_blocks, cfg.nkv)
+    copies = args.copies or max(2, math.ceil(8 * L2_BYTES / cache_bytes))
+    sm = 1.0 / math.sqrt(cfg.hd)
+
+    # fill cache copy 0 with the first L-1 tokens of every sequence; the step
+    # appends token L-1 (the same token every step, so steps are identical)
+    c0 = kvq8.alloc_cache(num_blocks, cfg.nkv, dev)
+    table_d = torch.from_numpy(table).to(dev)
+    new_k = np.zeros((cfg.batch, 1, cfg.nkv, cfg.hd), np.float32)
+    new_v = np.zeros_like(new_k)
+    zero = torch.zeros(1, dtype=torch.int32, device=dev)
+    for b in range(cfg.batch):
+        L = int(lens[b])
+        k, v = wl.seq_kv(cfg, b, L)
+        new_k[b, 0], new_v[b, 0] = k[L - 1], v[L - 1]
+        if L > 1:
+            kvq8.quantize_append(torch.from_numpy(k[None, :L - 1]).to(dev),
+                                 torch.from_numpy(v[None, :L - 1]).to(dev), zero,
+                                 table_d[b:b + 1], c0)
+    caches = [c0]
+    for _ in range(copies - 1):
+        caches.append(kvq8.KVCache(*[t.clone() for t in c0]))
+    q_d = torch.from_numpy(wl.queries(cfg)).to(dev)
+    nk_d, nv_d = torch.from_numpy(new_k).to(dev), torch.from_numpy(new_v).to(dev)
+    start_d = torch.from_numpy((lens - 1).clip(min=0).astype(np.int32)).to(dev)
+    lens_d = torch.from_numpy(lens).to(dev)
+    ws = kvq8.alloc_workspace(cfg.batch, cfg.nqh, cfg.nkv, max_blocks, dev)
+    out = torch.empty_like(q_d)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, ev=None):
+        c = caches[i % copies]
+        kvq8.quantize_append(nk_d, nv_d, start_d, table_d, c, dev_status=status, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        kvq8.decode_split(q_d, c, table_d, lens_d, ws, sm_scale=sm, dev_status=status, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        kvq8.decode_combine(cfg.batch, cfg.nqh, cfg.nkv, max_blocks, lens_d, ws, out, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item():#x} during warm-up")
+
+    # device-timed region: K steps, per-step events around the split kernel
+    split_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(i, split_ev[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier()
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    split_s = sum(a.elapsed_time(b) for a, b in split_ev) / 1e3 / args.steps
+    launches = 3 * args.steps
+
+    sbytes = step_bytes(cfg, lens)
+    total_bytes, slowest = aggregate(sbytes * args.steps, elapsed, dev)
+    per_step = slowest / args.steps
+    value = total_bytes / slowest / 1e9
+
+    # end to end: pinned host inputs in, result out, through the public calls
+    e2e_steps = args.e2e_steps or min(args.steps, 2000)
+    q_h = torch.from_numpy(wl.queries(cfg)).pin_memory()
+    nk_h, nv_h = torch.from_numpy(new_k).pin_memory(), torch.from_numpy(new_v).pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def e2e_step(i):
+        c = caches[i % copies]
+        q_d.copy_(q_h, non_blocking=True)
+        nk_d.copy_(nk_h, non_blocking=True)
+        nv_d.copy_(nv_h, non_blocking=True)
+        kvq8.quantize_append(nk_d, nv_d, start_d, table_d, c, stream=stream)
+        kvq8.decode_attn(q_d, c, table_d, lens_d, out, ws, sm_scale=sm, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for i in range(3):
+        e2e_step(i)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e2e_s = time.perf_counter() - t0
+    e_total, e_slowest = aggregate(sbytes * e2e_steps, e2e_s, dev)
+    h2d = (q_h.numel() + nk_h.numel() + nv_h.numel()) * 4
+    d2h = out_h.numel() * 4
+
+    # parity spot check of this very run against the oracle (rank 0, one unit)
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item():#x} in the timed region")
+
+    peak, peak_kind = hbm_peak()
+    split_bytes = split_kernel_bytes(cfg, lens)
+    achieved = split_bytes / split_s / 1e9
+    traffic = recorded_traffic(cfg.name)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 5),
+        "us_per_step": round(per_step * 1e6, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": dict(workload_config(cfg, lens, copies), parallelism=f"replicas{world}",
+                       bytes_per_step=sbytes,
+                       arithmetic="int8 x int8 -> int32 block dots, fp32 softmax and accumulation"),
+        "pct_of_hbm_peak": round(100 * (value / world) / peak, 2),
+        "roofline": {"bound": "hbm", "kernel": "decode_split", "achieved": round(achieved, 2),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_kind": peak_kind, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": split_bytes,
+                     "us_per_launch": round(split_s * 1e6, 3)},
+        "e2e": {"value": round(e_total / e_slowest / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "us_per_step": round(e_slowest / e2e_steps * 1e6, 2), "steps": e2e_steps},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, lens, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------- reference arm ---
+def run_reference(args, rank, world):
+    """The CPU oracle as it stands, on the host cores, each step a bounded
+    sample of the same workload (rank 0 only)."""
+    if rank != 0:
+        return
+    import numpy as np
+    from int8_quantized_kv_gb300 import workloads as wl
+    cfg = wl.WORKLOADS[args.workload]
+    lens = wl.ctx_lens(cfg)
+    threads = len(os.sched_getaffinity(0))
+    sm = np.float32(1.0 / math.sqrt(cfg.hd))
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    units, all_units = sample_units(cfg, lens, budget, threads)
+    st = OracleStep(cfg, lens, units, sm)
+    for _ in range(args.warmup):
+        st.run(threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        st.run(threads)
+    dt = (time.perf_counter() - t0) / args.steps
+    frac = sum(int(lens[b]) for b, _ in units) / sum(int(lens[b]) for b, _ in all_units)
+    bytes_sample = step_bytes(cfg, lens) * frac
+    value = bytes_sample / dt / 1e9
+    sample = (f"{len(units)} of {len(all_units)} (sequence, kv head) units per step "
+              f"({frac:.1%} of the step's tokens)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": dict(workload_config(cfg, lens, 0), parallelism="host cores"),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.steps < 1 or args.warmup < 0:
+        raise SystemExit("--steps must be >= 1")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_kvq8(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

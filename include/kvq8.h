@@ -1,0 +1,200 @@
+/*
+ * kvq8.h -- C ABI of libkvq8: decode attention over a paged INT8 KV cache on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The method (pages of the "0.8MB 跑通 Qwen" tutorial series):
+ *   [Day 9-1] "推理引擎的 KV 也量化——q8 KV 把缓存与 decode 带宽压到一半", §2:
+ *             K/V stored as int8 with one fp32 scale per (token, kv head).
+ *   [Day 9-2] "flash_attn_single_q_q8_neon——单 q 单遍扫全 KV", §1-§3: the query
+ *             quantised once in 32-element blocks, int8 dot products per block,
+ *             scales applied afterwards, online softmax, one divide at the end.
+ *   [Day 9-3] "q8 KV 精度对照——量化进注意力，输出差多少", §2: the quantisation rule
+ *             scale = max_abs/127, code = round(v/scale) clamped to [-127, 127].
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every pointer argument is a DEVICE pointer owned by the caller, except
+ *   `stream` (a cudaStream_t, NULL = legacy default stream).  The library
+ *   allocates no memory, never synchronises the device or the stream, and
+ *   keeps no state between calls apart from a per-device cache of device
+ *   attributes.
+ * - Work is enqueued asynchronously on `stream`.  Argument errors are
+ *   detected on the host and returned before anything is enqueued.  A
+ *   failed launch returns KVQ8_ERR_CUDA (the CUDA error is left for
+ *   cudaGetLastError()).  Faults the kernels detect at run time (a block id
+ *   outside the pool, a context length beyond the block table) are OR-ed as
+ *   KVQ8_DEV_* bits into *dev_status when dev_status is non-NULL; the
+ *   offending tokens are skipped, never read or written out of bounds.
+ * - Rounding: every float->int step rounds half to even in IEEE fp32, and
+ *   every fp32 division is IEEE-correct, so quantised codes and scales are
+ *   reproducible bit for bit on any IEEE machine.
+ * - Supported shapes: hd == 128, block_size == 256, nqh % nkv == 0 with
+ *   G = nqh/nkv in {1, 2, 4, 8}.  Anything else returns KVQ8_ERR_UNSUPPORTED.
+ *
+ * Cache layout (pool of num_blocks physical blocks, shared by all sequences)
+ * --------------------------------------------------------------------------
+ *   k_pool  int8  [num_blocks][nkv][block_size][hd]  token-major rows
+ *   v_pool  int8  [num_blocks][nkv][hd][block_size]  dim-major (transposed)
+ *   k_scale fp32  [num_blocks][nkv][block_size]      one scale per (token, head)
+ *   v_scale fp32  [num_blocks][nkv][block_size]
+ *   block_table int32 [batch][max_blocks]: logical block j of sequence b lives
+ *   in physical block block_table[b*max_blocks + j]; token t of sequence b is
+ *   slot t % block_size of logical block t / block_size.
+ * The pointers must be 16-byte aligned.  One (block, head) tile of K or V is
+ * 32 KiB contiguous; a token costs 2*hd + 8 bytes per kv head (2112 bytes per
+ * token for nkv = 8).
+ */
+#ifndef KVQ8_H
+#define KVQ8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvq8_status {
+    KVQ8_OK = 0,
+    KVQ8_ERR_INVALID_ARG = 1,  /* NULL pointer, negative or inconsistent size, misalignment */
+    KVQ8_ERR_UNSUPPORTED = 2,  /* shape outside the supported set above */
+    KVQ8_ERR_WORKSPACE = 3,    /* workspace NULL, not 256-byte aligned, or too small */
+    KVQ8_ERR_CUDA = 4          /* a CUDA runtime call or kernel launch failed */
+} kvq8_status;
+
+/* Bits the kernels OR into *dev_status. */
+#define KVQ8_DEV_BAD_BLOCK_ID 0x1u   /* a needed block-table entry is outside [0, num_blocks) */
+#define KVQ8_DEV_BAD_CTX_LEN 0x2u    /* ctx_lens[b] < 0 or > max_blocks * block_size */
+#define KVQ8_DEV_BAD_POSITION 0x4u   /* append position start_pos[b]+i outside the block table */
+
+#define KVQ8_HEAD_DIM 128
+#define KVQ8_BLOCK_SIZE 256
+#define KVQ8_Q_BLOCK 32
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *kvq8_status_str(int status);
+
+/* ABI revision of this header; bumped on any incompatible change. */
+int kvq8_abi_version(void);
+
+/* ---------------------------------------------------------------- sizes --- */
+
+/* Bytes of one int8 pool (k_pool or v_pool) and of one scale array. */
+size_t kvq8_kv_pool_bytes(int num_blocks, int nkv, int hd, int block_size);
+size_t kvq8_scale_pool_bytes(int num_blocks, int nkv, int block_size);
+
+/* Cache bytes one token occupies in one layer: int8 K and V rows plus one
+ * fp32 scale each, for every kv head ([Day 9-1] §2: 2112 for nkv=8, hd=128). */
+size_t kvq8_cache_bytes_per_token(int nkv, int hd);
+
+/* ------------------------------------------------------- quantize-append --- */
+
+/*
+ * kvq8_quantize_append -- quantise new K/V rows and write them into the cache.
+ * [Day 9-3] §2 / [Day 9-1] §2 (kv_quantize_per_head): for each (token, kv head)
+ * row of hd values, scale = max|v| / 127 (fp32), code = round_half_even(v /
+ * scale) clamped to [-127, 127]; an all-zero row gets scale 0 and codes 0.
+ *
+ *   k_new, v_new  fp32 [batch][n_new][nkv][hd]: the rows to append
+ *   start_pos     int32 [batch]: position of the first new token of each
+ *                 sequence; token i goes to position start_pos[b] + i
+ *   block_table   int32 [batch][max_blocks] (see layout above)
+ *   num_blocks    physical blocks in the pool (bounds for block ids)
+ *   k_pool, v_pool, k_scale, v_scale   the cache, written in place
+ *   dev_status    optional uint32 word receiving KVQ8_DEV_* bits
+ * Rows whose position is negative or beyond max_blocks*block_size, or whose
+ * block id is out of range, are skipped and flagged.  batch == 0 or
+ * n_new == 0 is a no-op.
+ */
+kvq8_status kvq8_quantize_append(const float *k_new, const float *v_new,
+                                 int batch, int n_new, int nkv, int hd,
+                                 const int32_t *start_pos,
+                                 const int32_t *block_table, int max_blocks,
+                                 int block_size, int num_blocks,
+                                 int8_t *k_pool, int8_t *v_pool,
+                                 float *k_scale, float *v_scale,
+                                 uint32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------- query quantize --- */
+
+/*
+ * kvq8_quantize_q -- 32-block query quantisation, exposed on its own so that
+ * the step the decode performs in its prologue can be checked bit for bit.
+ * [Day 9-2] §2 segment 1: per 32-element block qm = max|x| (qm = 1 when
+ * qm < 1e-6), block scale = qm * (1/127), code = round_half_even(x * (127/qm))
+ * clamped to [-128, 127].
+ *
+ *   q         fp32 [n_rows][hd]
+ *   q_codes   int8 [n_rows][hd]
+ *   q_scales  fp32 [n_rows][hd/32]
+ */
+kvq8_status kvq8_quantize_q(const float *q, int64_t n_rows, int hd,
+                            int8_t *q_codes, float *q_scales, void *stream);
+
+/* --------------------------------------------------------------- decode --- */
+
+/*
+ * kvq8_decode_workspace_bytes -- bytes of device workspace kvq8_decode_split /
+ * kvq8_decode_attn need for these sizes (the split-KV partial results).  Pure
+ * host arithmetic; returns 0 for unsupported or invalid sizes.
+ */
+size_t kvq8_decode_workspace_bytes(int batch, int nqh, int nkv, int hd,
+                                   int max_blocks, int block_size);
+
+/*
+ * kvq8_decode_attn -- single-query decode attention over the int8 cache,
+ * [Day 9-2] §1-§3, split over the context and merged:
+ *   per kv head, the G = nqh/nkv query heads j with j / G == kv head are
+ *   quantised in 32-blocks (as kvq8_quantize_q); for every cached token t,
+ *   s_t = (sum_b dot32_b(q_codes, k_codes_t) * q_scale_b) * k_scale_t * sm_scale
+ *   with exact int32 block dots; softmax over t with a running maximum, V
+ *   accumulated as int8 code * (weight * v_scale_t) in fp32; one division by
+ *   the softmax sum at the end.  Sequences with ctx_lens[b] == 0 yield 0.
+ *
+ *   q             fp32 [batch][nqh][hd]: one query token per sequence
+ *   ctx_lens      int32 [batch]: tokens 0 .. ctx_lens[b]-1 are attended
+ *   sm_scale      softmax scale, normally 1/sqrt(hd)
+ *   out           fp32 [batch][nqh][hd]
+ *   workspace     at least kvq8_decode_workspace_bytes(...) bytes, 256-byte
+ *                 aligned; its contents need no initialisation and are
+ *                 overwritten; calls that share it must not overlap in time
+ * Decode layers of one model step can be folded into `batch` (one row of q,
+ * block_table and ctx_lens per (layer, sequence), all in one shared pool).
+ */
+kvq8_status kvq8_decode_attn(const float *q, int batch, int nqh, int nkv, int hd,
+                             const int8_t *k_pool, const int8_t *v_pool,
+                             const float *k_scale, const float *v_scale,
+                             int num_blocks, const int32_t *block_table,
+                             int max_blocks, int block_size,
+                             const int32_t *ctx_lens, float sm_scale,
+                             float *out, void *workspace, size_t workspace_bytes,
+                             uint32_t *dev_status, void *stream);
+
+/*
+ * kvq8_decode_split / kvq8_decode_combine -- the two launches kvq8_decode_attn
+ * makes, exposed separately so that each can be timed on its own.  split
+ * writes per-split partial results (running max, softmax sum, unnormalised V
+ * accumulator) into the workspace; combine merges them per query head:
+ * M = max_i M_i, S = sum_i S_i e^(M_i - M), out = sum_i acc_i e^(M_i - M) / S.
+ * They must be called with the same sizes and workspace, split first.
+ */
+kvq8_status kvq8_decode_split(const float *q, int batch, int nqh, int nkv, int hd,
+                              const int8_t *k_pool, const int8_t *v_pool,
+                              const float *k_scale, const float *v_scale,
+                              int num_blocks, const int32_t *block_table,
+                              int max_blocks, int block_size,
+                              const int32_t *ctx_lens, float sm_scale,
+                              void *workspace, size_t workspace_bytes,
+                              uint32_t *dev_status, void *stream);
+
+kvq8_status kvq8_decode_combine(int batch, int nqh, int nkv, int hd,
+                                int max_blocks, int block_size,
+                                const int32_t *ctx_lens,
+                                const void *workspace, size_t workspace_bytes,
+                                float *out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ8_H */

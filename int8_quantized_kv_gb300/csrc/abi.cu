@@ -1,0 +1,240 @@
+// abi.cu -- the extern "C" entry points of libkvq8 (declared in kvq8.h):
+// argument validation, workspace layout and kernel launches.  No allocation,
+// no synchronisation: every call enqueues on the caller's stream.
+#include <math.h>
+
+#include "kvq8_internal.cuh"
+
+using namespace kvq8;
+
+namespace {
+
+bool aligned(const void *ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
+
+kvq8_status check_shape(int hd, int block_size) {
+    if (hd != kHD || block_size != kBS) return KVQ8_ERR_UNSUPPORTED;
+    return KVQ8_OK;
+}
+
+kvq8_status check_heads(int nqh, int nkv) {
+    if (nqh <= 0 || nkv <= 0) return KVQ8_ERR_INVALID_ARG;
+    if (nqh % nkv) return KVQ8_ERR_UNSUPPORTED;
+    const int G = nqh / nkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return KVQ8_ERR_UNSUPPORTED;
+    if (nkv > kMaxGridYZ || nqh > 2147483647 / kHD) return KVQ8_ERR_UNSUPPORTED;
+    return KVQ8_OK;
+}
+
+// Shared validation of the decode entry points (pool and table arguments).
+kvq8_status check_decode_args(const float *q, int batch, int nqh, int nkv, int hd,
+                              const int8_t *k_pool, const int8_t *v_pool, const float *k_scale,
+                              const float *v_scale, int num_blocks, const int32_t *block_table,
+                              int max_blocks, int block_size, const int32_t *ctx_lens) {
+    kvq8_status st = check_shape(hd, block_size);
+    if (st != KVQ8_OK) return st;
+    if ((st = check_heads(nqh, nkv)) != KVQ8_OK) return st;
+    if (batch < 0 || num_blocks <= 0 || max_blocks <= 0) return KVQ8_ERR_INVALID_ARG;
+    if (max_blocks > 2147483647 / kBS) return KVQ8_ERR_UNSUPPORTED;
+    if (batch > kMaxGridYZ) return KVQ8_ERR_UNSUPPORTED;
+    if (batch == 0) return KVQ8_OK;
+    if (!q || !k_pool || !v_pool || !k_scale || !v_scale || !block_table || !ctx_lens)
+        return KVQ8_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+        !aligned(k_scale, 16) || !aligned(v_scale, 16) || !aligned(block_table, 4) ||
+        !aligned(ctx_lens, 4))
+        return KVQ8_ERR_INVALID_ARG;
+    return KVQ8_OK;
+}
+
+kvq8_status fill_decode_params(const float *q, int batch, int nqh, int nkv,
+                               const int8_t *k_pool, const int8_t *v_pool, const float *k_scale,
+                               const float *v_scale, int num_blocks, const int32_t *block_table,
+                               int max_blocks, const int32_t *ctx_lens, float sm_scale,
+                               const void *workspace, size_t workspace_bytes,
+                               uint32_t *dev_status, DecodeParams *p, DecodePlan *plan) {
+    if (!make_decode_plan(batch, nqh, nkv, max_blocks, plan)) return KVQ8_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < plan->bytes)
+        return KVQ8_ERR_WORKSPACE;
+    char *ws = (char *)workspace;
+    p->q = q;
+    p->batch = batch;
+    p->nqh = nqh;
+    p->nkv = nkv;
+    p->k_pool = k_pool;
+    p->v_pool = v_pool;
+    p->k_scale = k_scale;
+    p->v_scale = v_scale;
+    p->num_blocks = num_blocks;
+    p->block_table = block_table;
+    p->max_blocks = max_blocks;
+    p->ctx_lens = ctx_lens;
+    p->sm_scale_log2 = sm_scale * 1.4426950408889634f;
+    p->ws_ml = (float *)(ws + plan->ml_offset);
+    p->ws_acc = (float *)(ws + plan->acc_offset);
+    p->nsplit = plan->nsplit;
+    p->split_blocks = plan->split_blocks;
+    p->dev_status = dev_status;
+    p->out = nullptr;
+    return KVQ8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kvq8_status_str(int status) {
+    switch (status) {
+        case KVQ8_OK: return "KVQ8_OK";
+        case KVQ8_ERR_INVALID_ARG: return "KVQ8_ERR_INVALID_ARG";
+        case KVQ8_ERR_UNSUPPORTED: return "KVQ8_ERR_UNSUPPORTED";
+        case KVQ8_ERR_WORKSPACE: return "KVQ8_ERR_WORKSPACE";
+        case KVQ8_ERR_CUDA: return "KVQ8_ERR_CUDA";
+        default: return "KVQ8_UNKNOWN_STATUS";
+    }
+}
+
+int kvq8_abi_version(void) { return 1; }
+
+size_t kvq8_kv_pool_bytes(int num_blocks, int nkv, int hd, int block_size) {
+    if (num_blocks < 0 || nkv < 0 || hd < 0 || block_size < 0) return 0;
+    return (size_t)num_blocks * nkv * block_size * hd;
+}
+
+size_t kvq8_scale_pool_bytes(int num_blocks, int nkv, int block_size) {
+    if (num_blocks < 0 || nkv < 0 || block_size < 0) return 0;
+    return (size_t)num_blocks * nkv * block_size * sizeof(float);
+}
+
+size_t kvq8_cache_bytes_per_token(int nkv, int hd) {
+    if (nkv < 0 || hd < 0) return 0;
+    return (size_t)nkv * (2 * (size_t)hd + 2 * sizeof(float));
+}
+
+kvq8_status kvq8_quantize_append(const float *k_new, const float *v_new, int batch, int n_new,
+                                 int nkv, int hd, const int32_t *start_pos,
+                                 const int32_t *block_table, int max_blocks, int block_size,
+                                 int num_blocks, int8_t *k_pool, int8_t *v_pool, float *k_scale,
+                                 float *v_scale, uint32_t *dev_status, void *stream) {
+    kvq8_status st = check_shape(hd, block_size);
+    if (st != KVQ8_OK) return st;
+    if (batch < 0 || n_new < 0 || nkv <= 0 || num_blocks <= 0 || max_blocks <= 0)
+        return KVQ8_ERR_INVALID_ARG;
+    if (max_blocks > 2147483647 / kBS) return KVQ8_ERR_UNSUPPORTED;
+    if (batch > kMaxGridYZ || nkv > kMaxGridYZ) return KVQ8_ERR_UNSUPPORTED;
+    if (batch == 0 || n_new == 0) return KVQ8_OK;
+    if (!k_new || !v_new || !start_pos || !block_table || !k_pool || !v_pool || !k_scale ||
+        !v_scale)
+        return KVQ8_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_pool, 16) ||
+        !aligned(v_pool, 16) || !aligned(k_scale, 4) || !aligned(v_scale, 4) ||
+        !aligned(start_pos, 4) || !aligned(block_table, 4))
+        return KVQ8_ERR_INVALID_ARG;
+    AppendParams p;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.batch = batch;
+    p.n_new = n_new;
+    p.nkv = nkv;
+    p.start_pos = start_pos;
+    p.block_table = block_table;
+    p.max_blocks = max_blocks;
+    p.num_blocks = num_blocks;
+    p.k_pool = k_pool;
+    p.v_pool = v_pool;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.dev_status = dev_status;
+    if (launch_quantize_append(p, (cudaStream_t)stream) != cudaSuccess) return KVQ8_ERR_CUDA;
+    return KVQ8_OK;
+}
+
+kvq8_status kvq8_quantize_q(const float *q, int64_t n_rows, int hd, int8_t *q_codes,
+                            float *q_scales, void *stream) {
+    if (hd != kHD) return KVQ8_ERR_UNSUPPORTED;
+    if (n_rows < 0) return KVQ8_ERR_INVALID_ARG;
+    if (n_rows > (int64_t)4 * 2147483647) return KVQ8_ERR_UNSUPPORTED;
+    if (n_rows == 0) return KVQ8_OK;
+    if (!q || !q_codes || !q_scales || !aligned(q, 4) || !aligned(q_scales, 4))
+        return KVQ8_ERR_INVALID_ARG;
+    if (launch_quantize_q(q, n_rows, q_codes, q_scales, (cudaStream_t)stream) != cudaSuccess)
+        return KVQ8_ERR_CUDA;
+    return KVQ8_OK;
+}
+
+size_t kvq8_decode_workspace_bytes(int batch, int nqh, int nkv, int hd, int max_blocks,
+                                   int block_size) {
+    if (check_shape(hd, block_size) != KVQ8_OK || check_heads(nqh, nkv) != KVQ8_OK) return 0;
+    DecodePlan plan;
+    if (!make_decode_plan(batch, nqh, nkv, max_blocks, &plan)) return 0;
+    return plan.bytes;
+}
+
+kvq8_status kvq8_decode_split(const float *q, int batch, int nqh, int nkv, int hd,
+                              const int8_t *k_pool, const int8_t *v_pool, const float *k_scale,
+                              const float *v_scale, int num_blocks, const int32_t *block_table,
+                              int max_blocks, int block_size, const int32_t *ctx_lens,
+                              float sm_scale, void *workspace, size_t workspace_bytes,
+                              uint32_t *dev_status, void *stream) {
+    kvq8_status st = check_decode_args(q, batch, nqh, nkv, hd, k_pool, v_pool, k_scale, v_scale,
+                                       num_blocks, block_table, max_blocks, block_size, ctx_lens);
+    if (st != KVQ8_OK || batch == 0) return st;
+    if (!isfinite(sm_scale)) return KVQ8_ERR_INVALID_ARG;
+    DecodeParams p;
+    DecodePlan plan;
+    st = fill_decode_params(q, batch, nqh, nkv, k_pool, v_pool, k_scale, v_scale, num_blocks,
+                            block_table, max_blocks, ctx_lens, sm_scale, workspace,
+                            workspace_bytes, dev_status, &p, &plan);
+    if (st != KVQ8_OK) return st;
+    if (launch_decode_split(p, plan.group, (cudaStream_t)stream) != cudaSuccess)
+        return KVQ8_ERR_CUDA;
+    return KVQ8_OK;
+}
+
+kvq8_status kvq8_decode_combine(int batch, int nqh, int nkv, int hd, int max_blocks,
+                                int block_size, const int32_t *ctx_lens, const void *workspace,
+                                size_t workspace_bytes, float *out, void *stream) {
+    kvq8_status st = check_shape(hd, block_size);
+    if (st != KVQ8_OK) return st;
+    if ((st = check_heads(nqh, nkv)) != KVQ8_OK) return st;
+    if (batch < 0 || max_blocks <= 0) return KVQ8_ERR_INVALID_ARG;
+    if (max_blocks > 2147483647 / kBS) return KVQ8_ERR_UNSUPPORTED;
+    if (batch > kMaxGridYZ) return KVQ8_ERR_UNSUPPORTED;
+    if (batch == 0) return KVQ8_OK;
+    if (!ctx_lens || !out || !aligned(out, 16) || !aligned(ctx_lens, 4))
+        return KVQ8_ERR_INVALID_ARG;
+    DecodeParams p;
+    DecodePlan plan;
+    st = fill_decode_params(nullptr, batch, nqh, nkv, nullptr, nullptr, nullptr, nullptr, 1,
+                            nullptr, max_blocks, ctx_lens, 1.0f, workspace, workspace_bytes,
+                            nullptr, &p, &plan);
+    if (st != KVQ8_OK) return st;
+    p.out = out;
+    if (launch_decode_combine(p, plan.group, (cudaStream_t)stream) != cudaSuccess)
+        return KVQ8_ERR_CUDA;
+    return KVQ8_OK;
+}
+
+kvq8_status kvq8_decode_attn(const float *q, int batch, int nqh, int nkv, int hd,
+                             const int8_t *k_pool, const int8_t *v_pool, const float *k_scale,
+                             const float *v_scale, int num_blocks, const int32_t *block_table,
+                             int max_blocks, int block_size, const int32_t *ctx_lens,
+                             float sm_scale, float *out, void *workspace, size_t workspace_bytes,
+                             uint32_t *dev_status, void *stream) {
+    kvq8_status st = check_decode_args(q, batch, nqh, nkv, hd, k_pool, v_pool, k_scale, v_scale,
+                                       num_blocks, block_table, max_blocks, block_size, ctx_lens);
+    if (st != KVQ8_OK || batch == 0) return st;
+    if (!out || !aligned(out, 16) || !isfinite(sm_scale)) return KVQ8_ERR_INVALID_ARG;
+    DecodeParams p;
+    DecodePlan plan;
+    st = fill_decode_params(q, batch, nqh, nkv, k_pool, v_pool, k_scale, v_scale, num_blocks,
+                            block_table, max_blocks, ctx_lens, sm_scale, workspace,
+                            workspace_bytes, dev_status, &p, &plan);
+    if (st != KVQ8_OK) return st;
+    p.out = out;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (launch_decode_split(p, plan.group, s) != cudaSuccess) return KVQ8_ERR_CUDA;
+    if (launch_decode_combine(p, plan.group, s) != cudaSuccess) return KVQ8_ERR_CUDA;
+    return KVQ8_OK;
+}
+
+}  // extern "C"

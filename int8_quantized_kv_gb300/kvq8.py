@@ -1,0 +1,230 @@
+"""Python binding of libkvq8 (C ABI in include/kvq8.h), via ctypes.
+
+Argument marshalling only: tensors are passed as device pointers plus the
+sizes read from their shapes; every step of the computation runs in the
+library's CUDA kernels.  torch is used for device memory and streams.  There
+is no fallback: if libkvq8.so cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import NamedTuple, Optional
+
+from . import build as _build
+
+HEAD_DIM = 128
+BLOCK_SIZE = 256
+Q_BLOCK = 32
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = range(5)
+DEV_BAD_BLOCK_ID, DEV_BAD_CTX_LEN, DEV_BAD_POSITION = 0x1, 0x2, 0x4
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+
+# name -> (restype, argtypes); mirrors include/kvq8.h
+SIGNATURES = {
+    "kvq8_status_str": (ctypes.c_char_p, [_I]),
+    "kvq8_abi_version": (_I, []),
+    "kvq8_kv_pool_bytes": (_SZ, [_I, _I, _I, _I]),
+    "kvq8_scale_pool_bytes": (_SZ, [_I, _I, _I]),
+    "kvq8_cache_bytes_per_token": (_SZ, [_I, _I]),
+    "kvq8_quantize_append": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _I, _I, _I,
+                                  _P, _P, _P, _P, _P, _P]),
+    "kvq8_quantize_q": (_I, [_P, _I64, _I, _P, _P, _P]),
+    "kvq8_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "kvq8_decode_attn": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _I,
+                              _P, _F, _P, _P, _SZ, _P, _P]),
+    "kvq8_decode_split": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _I,
+                               _P, _F, _P, _SZ, _P, _P]),
+    "kvq8_decode_combine": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
+}
+
+_lib = None
+
+
+class Kvq8Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_str(status)} ({status})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = True):
+    """Open libkvq8.so (building it first if it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if build_if_missing and _build.needs_build():
+        _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libkvq8.so not built ({path}); run int8_quantized_kv_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_str(status: int) -> str:
+    return load().kvq8_status_str(status).decode()
+
+
+def _check(fn: str, status: int):
+    if status != OK:
+        raise Kvq8Error(fn, status)
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream, device=None) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _need_cuda(*tensors):
+    for t in tensors:
+        if t is None or isinstance(t, int):
+            continue
+        if not t.is_cuda:
+            raise ValueError("kvq8 takes device tensors; got one on " + str(t.device))
+        if not t.is_contiguous():
+            raise ValueError("kvq8 takes contiguous tensors")
+
+
+# ------------------------------------------------------------------ sizes ---
+def kv_pool_bytes(num_blocks: int, nkv: int) -> int:
+    return int(load().kvq8_kv_pool_bytes(num_blocks, nkv, HEAD_DIM, BLOCK_SIZE))
+
+
+def scale_pool_bytes(num_blocks: int, nkv: int) -> int:
+    return int(load().kvq8_scale_pool_bytes(num_blocks, nkv, BLOCK_SIZE))
+
+
+def cache_bytes_per_token(nkv: int, hd: int = HEAD_DIM) -> int:
+    return int(load().kvq8_cache_bytes_per_token(nkv, hd))
+
+
+def decode_workspace_bytes(batch: int, nqh: int, nkv: int, max_blocks: int) -> int:
+    return int(load().kvq8_decode_workspace_bytes(batch, nqh, nkv, HEAD_DIM, max_blocks, BLOCK_SIZE))
+
+
+class KVCache(NamedTuple):
+    """One layer-pool of the paged cache (see the layout in include/kvq8.h)."""
+    k_pool: object   # int8 [num_blocks][nkv][256][128]  token-major
+    v_pool: object   # int8 [num_blocks][nkv][128][256]  dim-major
+    k_scale: object  # fp32 [num_blocks][nkv][256]
+    v_scale: object  # fp32 [num_blocks][nkv][256]
+
+    @property
+    def num_blocks(self) -> int:
+        return self.k_pool.shape[0]
+
+    @property
+    def nkv(self) -> int:
+        return self.k_pool.shape[1]
+
+
+def alloc_cache(num_blocks: int, nkv: int, device="cuda") -> KVCache:
+    """Allocate (uninitialised) pools with torch, sized by the library."""
+    import torch
+    assert kv_pool_bytes(num_blocks, nkv) == num_blocks * nkv * BLOCK_SIZE * HEAD_DIM
+    k = torch.empty((num_blocks, nkv, BLOCK_SIZE, HEAD_DIM), dtype=torch.int8, device=device)
+    v = torch.empty((num_blocks, nkv, HEAD_DIM, BLOCK_SIZE), dtype=torch.int8, device=device)
+    ks = torch.empty((num_blocks, nkv, BLOCK_SIZE), dtype=torch.float32, device=device)
+    vs = torch.empty((num_blocks, nkv, BLOCK_SIZE), dtype=torch.float32, device=device)
+    return KVCache(k, v, ks, vs)
+
+
+def alloc_workspace(batch: int, nqh: int, nkv: int, max_blocks: int, device="cuda"):
+    import torch
+    n = decode_workspace_bytes(batch, nqh, nkv, max_blocks)
+    if n == 0:
+        raise ValueError("unsupported decode sizes")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------- entry points ---
+def quantize_append(k_new, v_new, start_pos, block_table, cache: KVCache,
+                    dev_status=None, stream=None):
+    """k_new, v_new: fp32 [batch][n_new][nkv][128]; start_pos int32 [batch];
+    block_table int32 [batch][max_blocks]."""
+    _need_cuda(k_new, v_new, start_pos, block_table, *cache, dev_status)
+    batch, n_new, nkv, hd = k_new.shape
+    st = load().kvq8_quantize_append(
+        _ptr(k_new), _ptr(v_new), batch, n_new, nkv, hd, _ptr(start_pos),
+        _ptr(block_table), block_table.shape[1], BLOCK_SIZE, cache.num_blocks,
+        _ptr(cache.k_pool), _ptr(cache.v_pool), _ptr(cache.k_scale), _ptr(cache.v_scale),
+        _ptr(dev_status), _stream(stream))
+    _check("kvq8_quantize_append", st)
+
+
+def quantize_q(q, q_codes, q_scales, stream=None):
+    """q fp32 [..., 128] -> q_codes int8 [..., 128], q_scales fp32 [..., 4]."""
+    _need_cuda(q, q_codes, q_scales)
+    hd = q.shape[-1]
+    n_rows = q.numel() // hd if hd else 0
+    st = load().kvq8_quantize_q(_ptr(q), n_rows, hd, _ptr(q_codes), _ptr(q_scales), _stream(stream))
+    _check("kvq8_quantize_q", st)
+
+
+def _decode_common(q, cache: KVCache, block_table, ctx_lens):
+    batch, nqh, hd = q.shape
+    return batch, nqh, cache.nkv, hd, block_table.shape[1]
+
+
+def decode_attn(q, cache: KVCache, block_table, ctx_lens, out, workspace,
+                sm_scale: Optional[float] = None, dev_status=None, stream=None):
+    """q fp32 [batch][nqh][128] -> out fp32 [batch][nqh][128]."""
+    _need_cuda(q, block_table, ctx_lens, out, workspace, *cache, dev_status)
+    batch, nqh, nkv, hd, max_blocks = _decode_common(q, cache, block_table, ctx_lens)
+    sm = 1.0 / math.sqrt(hd) if sm_scale is None else sm_scale
+    st = load().kvq8_decode_attn(
+        _ptr(q), batch, nqh, nkv, hd, _ptr(cache.k_pool), _ptr(cache.v_pool),
+        _ptr(cache.k_scale), _ptr(cache.v_scale), cache.num_blocks, _ptr(block_table),
+        max_blocks, BLOCK_SIZE, _ptr(ctx_lens), sm, _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream))
+    _check("kvq8_decode_attn", st)
+
+
+def decode_split(q, cache: KVCache, block_table, ctx_lens, workspace,
+                 sm_scale: Optional[float] = None, dev_status=None, stream=None):
+    _need_cuda(q, block_table, ctx_lens, workspace, *cache, dev_status)
+    batch, nqh, nkv, hd, max_blocks = _decode_common(q, cache, block_table, ctx_lens)
+    sm = 1.0 / math.sqrt(hd) if sm_scale is None else sm_scale
+    st = load().kvq8_decode_split(
+        _ptr(q), batch, nqh, nkv, hd, _ptr(cache.k_pool), _ptr(cache.v_pool),
+        _ptr(cache.k_scale), _ptr(cache.v_scale), cache.num_blocks, _ptr(block_table),
+        max_blocks, BLOCK_SIZE, _ptr(ctx_lens), sm, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream))
+    _check("kvq8_decode_split", st)
+
+
+def decode_combine(batch: int, nqh: int, nkv: int, max_blocks: int, ctx_lens, workspace, out,
+                   stream=None):
+    _need_cuda(ctx_lens, workspace, out)
+    st = load().kvq8_decode_combine(
+        batch, nqh, nkv, HEAD_DIM, max_blocks, BLOCK_SIZE, _ptr(ctx_lens), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _stream(stream))
+    _check("kvq8_decode_combine", st)

@@ -17,6 +17,8 @@ permutation, 3 = per-sequence context lengths, 4 = outlier channel choice,
 from __future__ import annotations
 
 import dataclasses
+import os
+from concurrent.futures import ThreadPoolExecutor
 from typing import Optional
 
 import numpy as np
@@ -118,13 +120,29 @@ def unit_kv(cfg: Workload, b: int, h: int, L: Optional[int] = None):
     return k, v
 
 
-def seq_kv(cfg: Workload, b: int, L: Optional[int] = None):
-    """fp32 K and V of sequence b laid out [L][nkv][hd] (token-major, as appended)."""
+def _threads(threads: Optional[int]) -> int:
+    return max(1, os.cpu_count() or 1) if threads is None else max(1, threads)
+
+
+def seq_kv(cfg: Workload, b: int, L: Optional[int] = None, threads: Optional[int] = None):
+    """fp32 K and V of sequence b laid out [L][nkv][hd] (token-major, as appended).
+
+    Heads are drawn on several host threads; every head has its own stream,
+    so the result does not depend on the thread count."""
     L = int(ctx_lens(cfg)[b]) if L is None else L
     k = np.empty((L, cfg.nkv, cfg.hd), np.float32)
     v = np.empty((L, cfg.nkv, cfg.hd), np.float32)
-    for h in range(cfg.nkv):
+
+    def one(h):
         k[:, h], v[:, h] = unit_kv(cfg, b, h, L)
+
+    n = min(_threads(threads), cfg.nkv)
+    if n == 1:
+        for h in range(cfg.nkv):
+            one(h)
+    else:
+        with ThreadPoolExecutor(n) as ex:
+            list(ex.map(one, range(cfg.nkv)))
     return k, v
 
 

@@ -1,0 +1,110 @@
+"""Helpers shared by the GPU parity tests: fill the paged cache through the
+C ABI from a seeded workload, read it back in logical order, and run the
+oracle on the same fp32 inputs.
+
+The CUDA side only ever sees the workload arrays; the oracle only ever sees
+the same workload arrays; the two meet in the comparisons below.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from int8_quantized_kv_gb300 import kvq8
+from int8_quantized_kv_gb300 import workloads as wl
+
+SM_SCALE = 1.0 / math.sqrt(128.0)
+ABS_TOL = 1e-4
+REL_TOL = 1e-3
+
+
+def assert_close(gpu, ref, what=""):
+    """Output parity bar: |gpu - oracle| <= 1e-4 + 1e-3 * |oracle| per element."""
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert gpu.shape == ref.shape, (gpu.shape, ref.shape)
+    assert np.all(np.isfinite(gpu)), f"{what}: non-finite GPU output"
+    err = np.abs(gpu - ref)
+    bound = ABS_TOL + REL_TOL * np.abs(ref)
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"{what}: {bad.sum()} elements out of tolerance; worst at {i}: "
+                             f"gpu={gpu[i]!r} oracle={ref[i]!r} err={err[i]:.3e}")
+    return float(err.max()) if err.size else 0.0
+
+
+class Case:
+    """A workload laid out on the device: cache filled, queries uploaded."""
+
+    def __init__(self, cfg: wl.Workload, lens=None, device="cuda", spare_blocks=3,
+                 append_chunk=None):
+        self.cfg = cfg
+        self.lens = wl.ctx_lens(cfg) if lens is None else np.asarray(lens, np.int32)
+        self.table, self.num_blocks = wl.block_table(cfg, self.lens, spare_blocks=spare_blocks)
+        self.max_blocks = self.table.shape[1]
+        self.device = device
+        self.cache = kvq8.alloc_cache(self.num_blocks, cfg.nkv, device)
+        self.table_d = torch.from_numpy(self.table).to(device)
+        self.lens_d = torch.from_numpy(self.lens).to(device)
+        self.q = wl.queries(cfg)
+        self.q_d = torch.from_numpy(self.q).to(device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        for b in range(cfg.batch):
+            self.append_sequence(b, append_chunk)
+        torch.cuda.synchronize()
+
+    def append_sequence(self, b, chunk=None):
+        L = int(self.lens[b])
+        if L == 0:
+            return
+        k, v = wl.seq_kv(self.cfg, b, L)
+        chunk = L if chunk is None else chunk
+        row = self.table_d[b:b + 1]
+        for s in range(0, L, chunk):
+            e = min(L, s + chunk)
+            kd = torch.from_numpy(k[s:e][None]).to(self.device)
+            vd = torch.from_numpy(v[s:e][None]).to(self.device)
+            start = torch.tensor([s], dtype=torch.int32, device=self.device)
+            kvq8.quantize_append(kd, vd, start, row, self.cache, dev_status=self.status)
+
+    def decode(self, sm_scale=SM_SCALE):
+        out = torch.empty_like(self.q_d)
+        ws = kvq8.alloc_workspace(self.cfg.batch, self.cfg.nqh, self.cfg.nkv, self.max_blocks,
+                                  self.device)
+        kvq8.decode_attn(self.q_d, self.cache, self.table_d, self.lens_d, out, ws,
+                         sm_scale=sm_scale, dev_status=self.status)
+        torch.cuda.synchronize()
+        return out.cpu().numpy()
+
+    def status_bits(self) -> int:
+        return int(self.status.item())
+
+    # -- reading the cache back in logical order ------------------------------
+    def host_pools(self):
+        c = self.cache
+        return (c.k_pool.cpu().numpy(), c.v_pool.cpu().numpy(),
+                c.k_scale.cpu().numpy(), c.v_scale.cpu().numpy())
+
+    def gather_unit(self, pools, b, h):
+        """(kq [L][128], ks [L], vq [L][128], vs [L]) of sequence b, kv head h."""
+        kp, vp, ksp, vsp = pools
+        L = int(self.lens[b])
+        t = np.arange(L)
+        phys = self.table[b, t // wl.BLOCK_TOKENS]
+        slot = t % wl.BLOCK_TOKENS
+        kq = kp[phys, h, slot, :]
+        vq = vp[phys, h, :, slot]            # dim-major tile, gathered per token
+        return kq, ksp[phys, h, slot], vq, vsp[phys, h, slot]
+
+    # -- the oracle on the same inputs ------------------------------------------
+    def oracle_unit(self, b, h, sm_scale=SM_SCALE):
+        cfg = self.cfg
+        G = cfg.group
+        L = int(self.lens[b])
+        k, v = wl.unit_kv(cfg, b, h, L)
+        out, _ = oracle.decode_unit_q8(self.q[b, h * G:(h + 1) * G], k, v, sm_scale)
+        return out

@@ -1,0 +1,146 @@
+"""Host-side checks of libkvq8: it builds for sm_103a, loads, exports every
+symbol include/kvq8.h declares, and its pure-host logic (sizes, argument
+validation) behaves as documented.  No call here reaches a kernel launch:
+every compute call below fails validation first, so this runs without a GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from int8_quantized_kv_gb300 import build as kbuild
+from int8_quantized_kv_gb300 import kvq8
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvq8.h")
+FAKE = 1 << 20   # a 256-aligned non-null address that is never dereferenced
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq8_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kvq8.load()
+
+
+def test_header_declares_expected_entry_points():
+    names = _declared()
+    for n in ("kvq8_quantize_append", "kvq8_quantize_q", "kvq8_decode_attn",
+              "kvq8_decode_split", "kvq8_decode_combine", "kvq8_decode_workspace_bytes"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert set(_declared()) <= set(kvq8.SIGNATURES)
+
+
+def test_binding_does_not_import_oracle():
+    import sys
+    import subprocess
+    code = ("import sys; import int8_quantized_kv_gb300.kvq8 as k; "
+            "import int8_quantized_kv_gb300.workloads; "
+            "assert not any(m == 'oracle' or m.startswith('oracle.') for m in sys.modules)")
+    subprocess.run([sys.executable, "-c", code], cwd=ROOT, check=True)
+
+
+def test_status_strings(lib):
+    assert kvq8.status_str(0) == "KVQ8_OK"
+    assert kvq8.status_str(kvq8.ERR_WORKSPACE) == "KVQ8_ERR_WORKSPACE"
+    assert kvq8.status_str(99) == "KVQ8_UNKNOWN_STATUS"
+    assert lib.kvq8_abi_version() >= 1
+
+
+def test_sizes_match_the_page_byte_count(lib):
+    # [Day 9-1] §2: 8 kv heads x 128 dims -> 2112 bytes per token per layer
+    assert kvq8.cache_bytes_per_token(8) == 2112
+    assert kvq8.kv_pool_bytes(3, 8) == 3 * 8 * 256 * 128
+    assert kvq8.scale_pool_bytes(3, 8) == 3 * 8 * 256 * 4
+    per_token = (2 * kvq8.kv_pool_bytes(1, 8) + 2 * kvq8.scale_pool_bytes(1, 8)) // 256
+    assert per_token == 2112
+
+
+def test_workspace_sizes(lib):
+    a = kvq8.decode_workspace_bytes(28, 16, 8, 32)
+    assert a > 0 and a % 256 == 0
+    assert kvq8.decode_workspace_bytes(64, 32, 8, 128) > 0
+    # unsupported: group 3, hd != 128 via the raw call, bad sizes
+    assert kvq8.decode_workspace_bytes(1, 6, 2, 4) == 0
+    assert lib.kvq8_decode_workspace_bytes(1, 8, 8, 64, 4, 256) == 0
+    assert lib.kvq8_decode_workspace_bytes(1, 8, 8, 128, 4, 128) == 0
+    assert lib.kvq8_decode_workspace_bytes(1, 8, 0, 128, 4, 256) == 0
+    assert lib.kvq8_decode_workspace_bytes(1, 8, 8, 128, 0, 256) == 0
+    # partial results stay small next to the cache they summarise
+    kv = 28 * 8192 * 2112
+    assert a < 0.02 * kv
+
+
+def _append(lib, **kw):
+    a = dict(k=FAKE, v=FAKE, batch=1, n_new=1, nkv=1, hd=128, start=FAKE, table=FAKE,
+             max_blocks=1, bs=256, num_blocks=1, kp=FAKE, vp=FAKE, ks=FAKE, vs=FAKE,
+             status=None, stream=None)
+    a.update(kw)
+    return lib.kvq8_quantize_append(*a.values())
+
+
+def test_append_validation(lib):
+    assert _append(lib, hd=64) == kvq8.ERR_UNSUPPORTED
+    assert _append(lib, bs=128) == kvq8.ERR_UNSUPPORTED
+    assert _append(lib, k=None) == kvq8.ERR_INVALID_ARG
+    assert _append(lib, kp=FAKE + 4) == kvq8.ERR_INVALID_ARG          # not 16-byte aligned
+    assert _append(lib, batch=-1) == kvq8.ERR_INVALID_ARG
+    assert _append(lib, nkv=0) == kvq8.ERR_INVALID_ARG
+    assert _append(lib, batch=70000) == kvq8.ERR_UNSUPPORTED
+    assert _append(lib, batch=0) == kvq8.OK                          # no-op, nothing launched
+    assert _append(lib, n_new=0) == kvq8.OK
+
+
+def _decode(lib, fn="kvq8_decode_attn", **kw):
+    a = dict(q=FAKE, batch=1, nqh=8, nkv=8, hd=128, kp=FAKE, vp=FAKE, ks=FAKE, vs=FAKE,
+             num_blocks=4, table=FAKE, max_blocks=4, bs=256, lens=FAKE, sm=0.088,
+             out=FAKE, ws=FAKE, ws_bytes=0, status=None, stream=None)
+    a.update(kw)
+    if fn == "kvq8_decode_split":
+        a.pop("out")
+    return getattr(lib, fn)(*a.values())
+
+
+def test_decode_validation(lib):
+    need = kvq8.decode_workspace_bytes(1, 8, 8, 4)
+    for fn in ("kvq8_decode_attn", "kvq8_decode_split"):
+        assert _decode(lib, fn, hd=96) == kvq8.ERR_UNSUPPORTED
+        assert _decode(lib, fn, nqh=12) == kvq8.ERR_UNSUPPORTED          # G = 1.5
+        assert _decode(lib, fn, nqh=24, nkv=8) == kvq8.ERR_UNSUPPORTED   # G = 3
+        assert _decode(lib, fn, nqh=128, nkv=8) == kvq8.ERR_UNSUPPORTED  # G = 16
+        assert _decode(lib, fn, q=None) == kvq8.ERR_INVALID_ARG
+        assert _decode(lib, fn, lens=None) == kvq8.ERR_INVALID_ARG
+        assert _decode(lib, fn, num_blocks=0) == kvq8.ERR_INVALID_ARG
+        assert _decode(lib, fn, sm=float("nan")) == kvq8.ERR_INVALID_ARG
+        assert _decode(lib, fn, ws=None, ws_bytes=need) == kvq8.ERR_WORKSPACE
+        assert _decode(lib, fn, ws=FAKE + 16, ws_bytes=need) == kvq8.ERR_WORKSPACE
+        assert _decode(lib, fn, ws_bytes=need - 1) == kvq8.ERR_WORKSPACE
+        assert _decode(lib, fn, batch=0) == kvq8.OK
+    assert _decode(lib, out=None, ws_bytes=need) == kvq8.ERR_INVALID_ARG
+    assert lib.kvq8_decode_combine(1, 8, 8, 128, 4, 256, FAKE, FAKE, need - 1, FAKE, None) \
+        == kvq8.ERR_WORKSPACE
+    assert lib.kvq8_decode_combine(1, 8, 8, 128, 4, 256, None, FAKE, need, FAKE, None) \
+        == kvq8.ERR_INVALID_ARG
+
+
+def test_quantize_q_validation(lib):
+    assert lib.kvq8_quantize_q(FAKE, 4, 64, FAKE, FAKE, None) == kvq8.ERR_UNSUPPORTED
+    assert lib.kvq8_quantize_q(None, 4, 128, FAKE, FAKE, None) == kvq8.ERR_INVALID_ARG
+    assert lib.kvq8_quantize_q(FAKE, -1, 128, FAKE, FAKE, None) == kvq8.ERR_INVALID_ARG
+    assert lib.kvq8_quantize_q(FAKE, 0, 128, FAKE, FAKE, None) == kvq8.OK
+
+
+def test_library_is_built_for_sm103a():
+    assert "arch=compute_103a,code=sm_103a" in " ".join(kbuild.ARCH)
+    assert os.path.exists(kbuild.LIB_PATH)

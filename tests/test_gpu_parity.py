@@ -1,0 +1,316 @@
+"""CUDA path vs CPU oracle, through the C ABI, on seeded workloads.
+
+Quantised payloads and scales must match bit for bit; attention outputs must
+be within 1e-4 + 1e-3*|oracle| of the oracle's fp64 result on the same
+quantised inputs.  Sizes span several tiles and ragged tails; the full-size
+workloads are checked on sampled (sequence, kv head) units.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from int8_quantized_kv_gb300 import kvq8
+from int8_quantized_kv_gb300 import workloads as wl
+from kvq8_harness import Case, SM_SCALE, assert_close
+
+pytestmark = pytest.mark.gpu
+HD = 128
+
+
+def _unit_cfg(G, nkv=2, batch=1, ctx=None, ctx_range=None, cid=100, outliers=0):
+    return wl.Workload(f"test_g{G}", cid, batch=batch, nqh=G * nkv, nkv=nkv, ctx=ctx,
+                       ctx_range=ctx_range, outlier_channels=outliers)
+
+
+# ------------------------------------------------------------ quantisation ---
+def test_quantize_q_bit_exact(gpu_lib):
+    rng = np.random.default_rng(0)
+    rows = [rng.standard_normal(HD).astype(np.float32) * s for s in (1.0, 1e-3, 50.0)]
+    z = np.zeros(HD, np.float32)
+    z[32:64] = 4e-7
+    z[64] = np.float32(1e-6)
+    z[96] = np.nextafter(np.float32(1e-6), np.float32(0))
+    rows.append(z)
+    t = np.zeros(HD, np.float32)
+    t[:8] = [127.0, 2.5, 3.5, -2.5, -3.5, 0.5, 1.5, -0.5]
+    t[32:38] = [63.5, 1.25, 1.75, -1.25, 0.25, -63.5]
+    rows.append(t)
+    rows += list(rng.standard_normal((2000, HD)).astype(np.float32))
+    x = np.stack(rows)
+    xd = torch.from_numpy(x).cuda()
+    codes = torch.empty(x.shape, dtype=torch.int8, device="cuda")
+    scales = torch.empty((len(x), 4), dtype=torch.float32, device="cuda")
+    kvq8.quantize_q(xd, codes, scales)
+    torch.cuda.synchronize()
+    qi, qsc = oracle.q_quantize_blocks(x)
+    assert np.array_equal(codes.cpu().numpy(), qi)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), qsc.view(np.uint32))
+
+
+def _kv_rows_special():
+    rng = np.random.default_rng(1)
+    rows = []
+    a = np.zeros(HD, np.float32)
+    a[:13] = [127.0, 2.5, 3.5, -2.5, -3.5, 0.5, 1.5, -0.5, -1.5, 126.5, -126.5, 0.25, -0.75]
+    rows.append(a)
+    b = np.zeros(HD, np.float32)
+    b[:9] = [254.0, 5.0, 7.0, -5.0, 1.0, 3.0, -3.0, 253.0, -9.0]
+    rows.append(b)
+    rows.append(np.zeros(HD, np.float32))                    # all-zero row: scale 0
+    d = np.zeros(HD, np.float32)
+    d[:4] = [1e-40, -5e-41, 2e-41, -1e-40]                   # subnormal scale
+    rows.append(d)
+    rows.append(rng.standard_normal(HD).astype(np.float32) * np.float32(1e30))
+    rows.append(rng.standard_normal(HD).astype(np.float32) * np.float32(1e-30))
+    return np.stack(rows)
+
+
+@pytest.mark.parametrize("start,n_new", [(0, 1), (0, 256), (37, 300), (255, 2), (0, 1000), (480, 33)])
+def test_quantize_append_bit_exact(gpu_lib, start, n_new):
+    nkv = 3
+    rng = np.random.default_rng(start * 7919 + n_new)
+    k = rng.standard_normal((2, n_new, nkv, HD)).astype(np.float32)
+    v = (rng.standard_normal((2, n_new, nkv, HD)) * 3.0).astype(np.float32)
+    sp = _kv_rows_special()
+    m = min(len(sp), n_new)
+    k[0, :m, 0] = sp[:m]
+    v[1, :m, nkv - 1] = sp[::-1][:m]
+    need = (start + n_new + 255) // 256
+    max_blocks = need + 1
+    num_blocks = 2 * max_blocks + 2
+    perm = np.random.default_rng(5).permutation(num_blocks).astype(np.int32)
+    table = perm[:2 * max_blocks].reshape(2, max_blocks)
+    cache = kvq8.alloc_cache(num_blocks, nkv)
+    for t in cache:
+        t.fill_(0x55 if t.dtype == torch.int8 else 7.0)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvq8.quantize_append(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(),
+                         torch.tensor([start, start], dtype=torch.int32, device="cuda"),
+                         torch.from_numpy(table).cuda(), cache, dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    kp, vp = cache.k_pool.cpu().numpy(), cache.v_pool.cpu().numpy()
+    ksp, vsp = cache.k_scale.cpu().numpy(), cache.v_scale.cpu().numpy()
+    pos = start + np.arange(n_new)
+    for b in range(2):
+        phys, slot = table[b, pos // 256], pos % 256
+        for h in range(nkv):
+            kq, ks = oracle.kv_quantize_rows(k[b, :, h])
+            vq, vs = oracle.kv_quantize_rows(v[b, :, h])
+            assert np.array_equal(kp[phys, h, slot, :], kq)
+            assert np.array_equal(vp[phys, h, :, slot], vq)
+            assert np.array_equal(ksp[phys, h, slot].view(np.uint32), ks.view(np.uint32))
+            assert np.array_equal(vsp[phys, h, slot].view(np.uint32), vs.view(np.uint32))
+    # slots outside the appended range are untouched
+    written = np.zeros((num_blocks, nkv, 256), bool)
+    for b in range(2):
+        written[table[b, pos // 256], :, pos % 256] = True
+    assert np.all(ksp[~written] == 7.0)
+    assert np.all(kp.transpose(0, 1, 2, 3)[~written] == 0x55)
+
+
+def test_byte_count_of_allocated_cache(gpu_lib):
+    # 2112 bytes per token per layer for 8 kv heads of 128 ([Day 9-1] §2)
+    nb = 5
+    cache = kvq8.alloc_cache(nb, 8)
+    total = sum(t.numel() * t.element_size() for t in cache)
+    assert total == nb * 256 * 2112 == nb * 256 * kvq8.cache_bytes_per_token(8)
+
+
+# ------------------------------------------------------------------ decode ---
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_decode_group_sizes(gpu_lib, G):
+    cfg = _unit_cfg(G, nkv=2, batch=3, ctx_range=(1, 1300), cid=110 + G)
+    case = Case(cfg)
+    out = case.decode()
+    for b in range(cfg.batch):
+        for h in range(cfg.nkv):
+            ref = case.oracle_unit(b, h)
+            assert_close(out[b, h * G:(h + 1) * G], ref, f"G={G} b={b} h={h}")
+    assert case.status_bits() == 0
+
+
+@pytest.mark.parametrize("L", [1, 2, 31, 32, 33, 255, 256, 257, 511, 513, 4097])
+def test_decode_lengths(gpu_lib, L):
+    cfg = _unit_cfg(4, nkv=1, batch=1, ctx=L, cid=120)
+    case = Case(cfg)
+    out = case.decode()
+    assert_close(out[0], case.oracle_unit(0, 0), f"L={L}")
+
+
+def test_decode_multi_block_splits(gpu_lib):
+    # enough units x blocks that a split spans several cache blocks
+    cfg = _unit_cfg(1, nkv=8, batch=8, ctx_range=(6000, 10000), cid=125)
+    case = Case(cfg)
+    out = case.decode()
+    for b in range(cfg.batch):
+        for h in range(cfg.nkv):
+            assert_close(out[b, h:h + 1], case.oracle_unit(b, h), f"b={b} h={h}")
+
+
+def test_decode_zero_length_sequences(gpu_lib):
+    cfg = _unit_cfg(2, nkv=2, batch=4, ctx_range=(1, 700), cid=130)
+    lens = np.array([0, 300, 0, 650], np.int32)
+    case = Case(cfg, lens=lens)
+    out = case.decode()
+    assert not out[0].any() and not out[2].any()
+    for b in (1, 3):
+        for h in range(2):
+            assert_close(out[b, h * 2:(h + 1) * 2], case.oracle_unit(b, h))
+
+
+def test_single_head_l256_and_fp32_kv_delta(gpu_lib):
+    cfg = wl.SINGLE_HEAD_L256
+    case = Case(cfg)
+    out = case.decode()
+    ref = case.oracle_unit(0, 0)
+    assert_close(out[0], ref, "single head L=256")
+    # The page's experiment: the fp32-KV output vs the q8 output.
+    k, v = wl.unit_kv(cfg, 0, 0)
+    f32 = oracle.attention_f64(case.q[0, 0], k, v, SM_SCALE)
+    d = np.abs(out[0, 0] - f32)
+    assert d.max() < 0.05 and d.mean() > 1e-5
+
+
+def test_decode_sm_scale_argument(gpu_lib):
+    cfg = _unit_cfg(2, nkv=1, batch=1, ctx=700, cid=140)
+    case = Case(cfg)
+    out = case.decode(sm_scale=0.3)
+    assert_close(out[0], case.oracle_unit(0, 0, sm_scale=np.float32(0.3)))
+
+
+def test_decode_on_side_stream_matches(gpu_lib):
+    cfg = _unit_cfg(4, nkv=2, batch=2, ctx=900, cid=150)
+    case = Case(cfg)
+    ref = case.decode()
+    s = torch.cuda.Stream()
+    out = torch.empty_like(case.q_d)
+    ws = kvq8.alloc_workspace(cfg.batch, cfg.nqh, cfg.nkv, case.max_blocks)
+    with torch.cuda.stream(s):
+        kvq8.decode_attn(case.q_d, case.cache, case.table_d, case.lens_d, out, ws)
+    s.synchronize()
+    assert np.array_equal(out.cpu().numpy(), ref)
+
+
+def test_split_and_combine_equal_decode_attn(gpu_lib):
+    cfg = _unit_cfg(8, nkv=2, batch=2, ctx_range=(100, 3000), cid=160)
+    case = Case(cfg)
+    ref = case.decode()
+    ws = kvq8.alloc_workspace(cfg.batch, cfg.nqh, cfg.nkv, case.max_blocks)
+    out = torch.empty_like(case.q_d)
+    kvq8.decode_split(case.q_d, case.cache, case.table_d, case.lens_d, ws)
+    kvq8.decode_combine(cfg.batch, cfg.nqh, cfg.nkv, case.max_blocks, case.lens_d, ws, out)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), ref)
+
+
+def test_cache_filled_in_small_appends_matches_one_append(gpu_lib):
+    cfg = _unit_cfg(2, nkv=2, batch=2, ctx_range=(300, 900), cid=170)
+    a = Case(cfg)
+    b = Case(cfg, append_chunk=77)
+    pa, pb = a.host_pools(), b.host_pools()   # unwritten slots are uninitialised: compare tokens
+    for bb in range(cfg.batch):
+        for h in range(cfg.nkv):
+            for x, y in zip(a.gather_unit(pa, bb, h), b.gather_unit(pb, bb, h)):
+                assert np.array_equal(x, y)
+    assert np.array_equal(a.decode(), b.decode())
+
+
+# ------------------------------------------------------- device-side faults ---
+def test_bad_block_id_is_flagged_and_skipped(gpu_lib):
+    cfg = _unit_cfg(2, nkv=1, batch=1, ctx=1000, cid=180)
+    case = Case(cfg)
+    good = case.table[0, 1]
+    case.table_d[0, 1] = case.num_blocks + 5          # logical block 1 now out of range
+    out = case.decode()
+    assert case.status_bits() & kvq8.DEV_BAD_BLOCK_ID
+    # the kernel skips the 256 tokens of that block: same as the oracle without them
+    k, v = wl.unit_kv(cfg, 0, 0)
+    keep = np.r_[0:256, 512:1000]
+    ref, _ = oracle.decode_unit_q8(case.q[0], k[keep], v[keep], SM_SCALE)
+    assert_close(out[0], ref)
+    case.table_d[0, 1] = int(good)
+
+
+def test_bad_ctx_len_is_flagged_and_clamped(gpu_lib):
+    cfg = _unit_cfg(1, nkv=1, batch=1, ctx=512, cid=190)
+    case = Case(cfg, spare_blocks=0)
+    case.lens_d[0] = case.max_blocks * 256 + 10
+    out = case.decode()
+    assert case.status_bits() & kvq8.DEV_BAD_CTX_LEN
+    assert_close(out[0], case.oracle_unit(0, 0))
+
+
+def test_append_bad_position_is_flagged(gpu_lib):
+    nkv = 1
+    cache = kvq8.alloc_cache(2, nkv)
+    cache.k_scale.fill_(3.0)
+    table = torch.tensor([[0, 1]], dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k = torch.randn(1, 4, nkv, HD, device="cuda")
+    kvq8.quantize_append(k, k, torch.tensor([510], dtype=torch.int32, device="cuda"), table, cache,
+                         dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() & kvq8.DEV_BAD_POSITION
+    ks = cache.k_scale.cpu().numpy()
+    # positions 510, 511 land in block 1 slots 254, 255; 512, 513 are past the table
+    assert ks[1, 0, 254] != 3.0 and ks[1, 0, 255] != 3.0 and ks[1, 0, 253] == 3.0
+    assert np.all(ks[0] == 3.0)
+
+
+def test_host_errors_on_device(gpu_lib):
+    cfg = _unit_cfg(2, nkv=1, batch=1, ctx=300, cid=200)
+    case = Case(cfg)
+    out = torch.empty_like(case.q_d)
+    small = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvq8.Kvq8Error) as e:
+        kvq8.decode_attn(case.q_d, case.cache, case.table_d, case.lens_d, out, small)
+    assert e.value.status == kvq8.ERR_WORKSPACE
+
+
+# --------------------------------------------------- the specified workloads ---
+SMALL = [
+    wl.scaled(wl.QWEN3_2B_28L_8K, batch=4, ctx=1500),
+    wl.scaled(wl.BATCH64_RAGGED, batch=6, ctx_range=(512, 2600)),
+    wl.scaled(wl.LONG128K_OUTLIERS, batch=2, ctx=3000),
+]
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
+def test_specified_workloads_scaled_all_outputs(gpu_lib, cfg):
+    case = Case(cfg)
+    out = case.decode()
+    G = cfg.group
+    for b in range(cfg.batch):
+        for h in range(cfg.nkv):
+            assert_close(out[b, h * G:(h + 1) * G], case.oracle_unit(b, h), f"{cfg.name} b={b} h={h}")
+
+
+FULL = [wl.QWEN3_2B_28L_8K, wl.BATCH64_RAGGED, wl.LONG128K_OUTLIERS]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("cfg", FULL, ids=lambda c: c.name)
+def test_specified_workloads_full_size_sampled(gpu_lib, cfg):
+    case = Case(cfg, spare_blocks=0)
+    out = case.decode()
+    assert case.status_bits() == 0
+    assert np.all(np.isfinite(out))
+    rng = np.random.default_rng(cfg.config_id)
+    G = cfg.group
+    units = {(int(rng.integers(cfg.batch)), int(rng.integers(cfg.nkv))) for _ in range(6)}
+    units.add((cfg.batch - 1, cfg.nkv - 1))
+    for b, h in sorted(units):
+        assert_close(out[b, h * G:(h + 1) * G], case.oracle_unit(b, h), f"{cfg.name} b={b} h={h}")
+    # every appended token of a sampled unit is bit-exact too
+    pools = case.host_pools()
+    b, h = sorted(units)[0]
+    kq, ks, vq, vs = case.gather_unit(pools, b, h)
+    k, v = wl.unit_kv(cfg, b, h)
+    okq, oks = oracle.kv_quantize_rows(k)
+    ovq, ovs = oracle.kv_quantize_rows(v)
+    assert np.array_equal(kq, okq) and np.array_equal(vq, ovq)
+    assert np.array_equal(ks, oks) and np.array_equal(vs, ovs)
