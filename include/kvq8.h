@@ -193,6 +193,41 @@ kvq8_status kvq8_decode_combine(int batch, int nqh, int nkv, int hd,
                                 const void *workspace, size_t workspace_bytes,
                                 float *out, void *stream);
 
+/* ------------------------------------------- decode without allocation --- */
+
+/* Size of the static device scratch kvq8_decode_attn_noalloc uses (16 MiB). */
+#define KVQ8_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * kvq8_decode_attn_noalloc -- kvq8_decode_attn for callers that cannot
+ * allocate device memory.  The pages have no counterpart: this entry point
+ * exists for library users who are given only their inputs, outputs and a
+ * stream (plugin hosts that own the allocator, paths where cudaMalloc would
+ * synchronise the device or is forbidden), and so cannot pass a workspace.
+ *
+ * Same arguments and results as kvq8_decode_attn, without the workspace: the
+ * split partial results go to a static device array of
+ * KVQ8_NOALLOC_SCRATCH_BYTES that every GPU which loads the library holds
+ * until the process exits.  The call allocates nothing.
+ *   - Sizes whose kvq8_decode_workspace_bytes(...) exceeds
+ *     KVQ8_NOALLOC_SCRATCH_BYTES are rejected with KVQ8_ERR_WORKSPACE before
+ *     anything is enqueued.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and remembers it; make
+ *     that first call before any stream capture on the device.
+ *   - All calls share the one array and leave their partial results in it; no
+ *     part of it needs to start at zero, since a call writes every record it
+ *     reads.  Calls that overlap on the GPU (other streams, other threads)
+ *     race on it: serialise them.
+ */
+kvq8_status kvq8_decode_attn_noalloc(const float *q, int batch, int nqh, int nkv, int hd,
+                                     const int8_t *k_pool, const int8_t *v_pool,
+                                     const float *k_scale, const float *v_scale,
+                                     int num_blocks, const int32_t *block_table,
+                                     int max_blocks, int block_size,
+                                     const int32_t *ctx_lens, float sm_scale,
+                                     float *out, uint32_t *dev_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -17,6 +17,7 @@ from . import build as _build
 HEAD_DIM = 128
 BLOCK_SIZE = 256
 Q_BLOCK = 32
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024   # KVQ8_NOALLOC_SCRATCH_BYTES in kvq8.h
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = range(5)
 DEV_BAD_BLOCK_ID, DEV_BAD_CTX_LEN, DEV_BAD_POSITION = 0x1, 0x2, 0x4
@@ -43,6 +44,8 @@ SIGNATURES = {
     "kvq8_decode_split": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _I,
                                _P, _F, _P, _SZ, _P, _P]),
     "kvq8_decode_combine": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
+    "kvq8_decode_attn_noalloc": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _I,
+                                      _P, _F, _P, _P, _P]),
 }
 
 _lib = None
@@ -228,3 +231,19 @@ def decode_combine(batch: int, nqh: int, nkv: int, max_blocks: int, ctx_lens, wo
         batch, nqh, nkv, HEAD_DIM, max_blocks, BLOCK_SIZE, _ptr(ctx_lens), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(out), _stream(stream))
     _check("kvq8_decode_combine", st)
+
+
+def decode_attn_noalloc(q, cache: KVCache, block_table, ctx_lens, out,
+                        sm_scale: Optional[float] = None, dev_status=None, stream=None):
+    """decode_attn without a workspace, for callers that cannot allocate device
+    memory: the partial results live in the library's static 16 MiB device
+    scratch (see kvq8_decode_attn_noalloc in kvq8.h; concurrent calls race)."""
+    _need_cuda(q, block_table, ctx_lens, out, *cache, dev_status)
+    batch, nqh, nkv, hd, max_blocks = _decode_common(q, cache, block_table, ctx_lens)
+    sm = 1.0 / math.sqrt(hd) if sm_scale is None else sm_scale
+    st = load().kvq8_decode_attn_noalloc(
+        _ptr(q), batch, nqh, nkv, hd, _ptr(cache.k_pool), _ptr(cache.v_pool),
+        _ptr(cache.k_scale), _ptr(cache.v_scale), cache.num_blocks, _ptr(block_table),
+        max_blocks, BLOCK_SIZE, _ptr(ctx_lens), sm, _ptr(out), _ptr(dev_status),
+        _stream(stream))
+    _check("kvq8_decode_attn_noalloc", st)
