@@ -33,16 +33,24 @@
  *
  * Cache layout (pool of num_blocks physical blocks, shared by all sequences)
  * --------------------------------------------------------------------------
- *   k_pool  int8  [num_blocks][nkv][block_size][hd]  token-major rows
- *   v_pool  int8  [num_blocks][nkv][hd][block_size]  dim-major (transposed)
- *   k_scale fp32  [num_blocks][nkv][block_size]      one scale per (token, head)
- *   v_scale fp32  [num_blocks][nkv][block_size]
+ * A (block, kv head) tile holds block_size = 256 tokens:
+ *   k_pool  int8  [num_blocks][nkv][256][128]      token-major rows; the 16-byte
+ *                 chunk j (dims 16j..16j+15) of the row of slot t is stored at
+ *                 chunk position j ^ (t & 7)
+ *   v_pool  int8  [num_blocks][nkv][4][128][64]    per 64-token quarter, dim-major:
+ *                 the code of slot t, dim d is at [t / 64][d][t % 64]
+ *   k_scale fp32  [num_blocks][nkv][256]           one scale per (token, head)
+ *   v_scale fp32  [num_blocks][nkv][256]
+ * This is the order in which the decode kernel consumes the cache: every
+ * 64-token window is four contiguous runs (8 KiB of K, 8 KiB of V, 256 B of
+ * each scale) that one bulk copy each brings into shared memory, where the
+ * chunk permutation keeps the reads free of bank conflicts.
  *   block_table int32 [batch][max_blocks]: logical block j of sequence b lives
  *   in physical block block_table[b*max_blocks + j]; token t of sequence b is
  *   slot t % block_size of logical block t / block_size.
- * The pointers must be 16-byte aligned.  One (block, head) tile of K or V is
- * 32 KiB contiguous; a token costs 2*hd + 8 bytes per kv head (2112 bytes per
- * token for nkv = 8).
+ * The pointers must be 16-byte aligned.  One tile of K or V is 32 KiB
+ * contiguous; a token costs 2*hd + 8 bytes per kv head (2112 bytes per token
+ * for nkv = 8).
  */
 #ifndef KVQ8_H
 #define KVQ8_H
@@ -66,6 +74,8 @@ typedef enum kvq8_status {
 #define KVQ8_DEV_BAD_BLOCK_ID 0x1u   /* a needed block-table entry is outside [0, num_blocks) */
 #define KVQ8_DEV_BAD_CTX_LEN 0x2u    /* ctx_lens[b] < 0 or > max_blocks * block_size */
 #define KVQ8_DEV_BAD_POSITION 0x4u   /* append position start_pos[b]+i outside the block table */
+#define KVQ8_DEV_TIMEOUT 0x8u        /* an internal pipeline wait gave up (never expected); the
+                                        affected results are unspecified */
 
 #define KVQ8_HEAD_DIM 128
 #define KVQ8_BLOCK_SIZE 256

@@ -69,10 +69,9 @@ kvq8_status fill_decode_params(const float *q, int batch, int nqh, int nkv,
     p->max_blocks = max_blocks;
     p->ctx_lens = ctx_lens;
     p->sm_scale_log2 = sm_scale * 1.4426950408889634f;
+    p->ws_meta = (int2 *)(ws + plan->meta_offset);
     p->ws_ml = (float *)(ws + plan->ml_offset);
     p->ws_acc = (float *)(ws + plan->acc_offset);
-    p->nsplit = plan->nsplit;
-    p->split_blocks = plan->split_blocks;
     p->dev_status = dev_status;
     p->out = nullptr;
     return KVQ8_OK;

@@ -8,8 +8,9 @@
 // One CTA takes 32 consecutive new tokens of one (sequence, kv head); each of
 // its 8 warps quantises 4 tokens, one row per warp-iteration with a float4 per
 // lane (a row is one coalesced 512-byte read).  K codes go straight to the
-// token-major K tile (one 128-byte row); V codes are transposed through shared
-// memory so that the dim-major V tile is written as runs of consecutive slots.
+// token-major K tile (one 128-byte row, its 16-byte chunks permuted by slot);
+// V codes are transposed through shared memory so that the dim-major V
+// quarters are written as runs of consecutive slots.
 #include "kvq8_device.cuh"
 #include "kvq8_internal.cuh"
 
@@ -64,7 +65,9 @@ quantize_append_kernel(AppendParams p) {
             const float s = kv_row_scale(m);
             const uint32_t w = pack4(kv_code(x.x, s), kv_code(x.y, s), kv_code(x.z, s),
                                      kv_code(x.w, s));
-            reinterpret_cast<uint32_t *>(p.k_pool + (tile * kBS + slot) * kHD)[lane] = w;
+            // 16-byte chunk lane/4 of the row goes to chunk position (lane/4) ^ (slot & 7)
+            unsigned char *row = reinterpret_cast<unsigned char *>(p.k_pool) + (tile * kBS + slot) * kHD;
+            reinterpret_cast<uint32_t *>(row + (((lane >> 2) ^ (slot & 7)) << 4))[lane & 3] = w;
             if (lane == 0) p.k_scale[tile * kBS + slot] = s;
         }
         // V row -> staged for the dim-major write
@@ -82,14 +85,16 @@ quantize_append_kernel(AppendParams p) {
     }
     __syncthreads();
 
-    // Dim-major V write: a warp stores one dim row for the CTA's 32 tokens
-    // (consecutive slots of the same block, or two blocks at a boundary).
+    // Dim-major V write (per 64-token quarter): a warp stores one dim row for
+    // the CTA's 32 tokens, which are consecutive slots except at a boundary.
     const int r = lane;
     const int phys = tok_phys[r];
     if (phys >= 0) {
-        const size_t base = ((size_t)phys * p.nkv + h) * kHD * kBS + tok_slot[r];
+        const int slot = tok_slot[r];
+        const size_t base = ((size_t)phys * p.nkv + h) * kHD * kBS +
+                            (size_t)(slot / kStageTok) * kTileVQuarter + (slot % kStageTok);
         for (int d = warp; d < kHD; d += kAppendWarps)
-            p.v_pool[base + (size_t)d * kBS] = v_stage[d][r];
+            p.v_pool[base + (size_t)d * kStageTok] = v_stage[d][r];
     }
 }
 

@@ -1,281 +1,574 @@
-// decode.cu -- split-KV single-query decode attention over the paged INT8
-// cache, and the merge of the split results.
+// decode.cu -- single-query decode attention over the paged INT8 cache:
+// a persistent split-KV kernel and the merge of its partial results.
 //
 // Method: [Day 9-2] "flash_attn_single_q_q8_neon" §1-§3.  The query heads that
 // share a kv head are quantised once in 32-blocks (segment 1); every cached
 // token's score is rebuilt from exact int32 block dots times the query block
 // scales, times the token's K scale and the softmax scale (segment 2, "three
 // key points"); the softmax runs online with a running maximum, rescaling the
-// running sum and the V accumulator when the maximum grows; V enters as int8
-// code * (weight * V scale) in fp32; one division by the sum at the end
-// (segment 3).
+// running sum and the V accumulator when the maximum grows; V enters as
+// int8 code * (weight * V scale) with fp32 accumulation; one division by the
+// sum at the end (segment 3).  The softmax runs in base 2 (scores are
+// pre-multiplied by log2(e)), which leaves the normalised weights unchanged.
 //
-// GB300 layout of the work: one CTA = (split of a unit, kv head, sequence); its
-// 4 warps walk the split in 32-token chunks, each warp with its own online
-// softmax state.  Inside a chunk, lane t scores token t for all G query heads
-// (dp4a over the K row staged in shared memory) and then the warp accumulates
-// P.V with lane l owning dims l, l+32, l+64, l+96.  The 4 warp states are
-// merged in shared memory into one partial record per query head; a second
-// kernel merges the records of all splits and divides by the sum.
-// The softmax runs in base 2: scores are pre-multiplied by log2(e), which
-// leaves the normalised weights unchanged.
+// GB300 structure of the split kernel (one CTA per SM, 8 warps):
+//  * Work: the cache is a sequence of 64-token stages, unit by unit (unit =
+//    (sequence, kv head)); CTA c takes stages [c*T/C, (c+1)*T/C), i.e. an
+//    equal share regardless of how ragged the contexts are.  Where a unit
+//    starts or ends inside the range, the CTA emits one partial record for
+//    that (CTA, unit) segment.
+//  * Warp 7 is the producer: for every stage it issues four 1-D bulk copies
+//    (K 8 KiB, V 8 KiB, two 256 B scale runs) into a ring of shared-memory
+//    slots, tracked by full/empty mbarriers.  The KV stream uses an L2
+//    evict-first policy: it is read exactly once.
+//  * Warps 0..6 take the stages of a segment from a shared counter, in order,
+//    each with its own online-softmax state (two warps per SM sub-partition
+//    leave room for 255 registers a thread).  Q.K: lane = token (two tokens per lane), dp4a on int8 codes,
+//    exact int32 per 32-block.  P.V: tensor-core MMA m16n8k16 with
+//    A = V (int8 codes -> fp16, exact) and B = P, the weights times the V
+//    scale, split into fp16 high + low parts (two MMAs) and scaled per stage
+//    by a power of two so that fp16 range and precision lose nothing that
+//    fp32 accumulation keeps; D accumulates in fp32.
+//  * At the end of a segment the 7 warp states are merged in shared memory
+//    and written as one record per query head.
+// All waits are bounded: a wait that times out sets KVQ8_DEV_TIMEOUT and the
+// CTA unwinds without leaving copies in flight.
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "kvq8_device.cuh"
 #include "kvq8_internal.cuh"
+#include "kvq8_ptx.cuh"
 
 namespace kvq8 {
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kChunk = 32;            // tokens per warp iteration
-constexpr int kKRow = kHD + 16;       // padded K row in shared memory (bytes)
-constexpr int kVRow = kChunk + 4;     // padded V dim row in shared memory (bytes)
+constexpr int kConsumerWarps = 7;
+constexpr int kSplitThreads = (kConsumerWarps + 1) * 32;
+constexpr int kSmemLimit = 232448;          // 227 KiB opt-in per CTA on sm_103a
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+constexpr int kPRowHalves = 72;             // P row: 64 tokens + 8 halves of padding
 
 template <int G>
-struct SplitSmem {
-    int8_t q_codes[G][kHD];
-    float q_scale[G][kNQB];
-    union {
-        struct {
-            int8_t k_tile[kWarps][kChunk][kKRow];
-            int8_t v_tile[kWarps][kHD][kVRow];
-            float p[kWarps][kChunk][G];
-        } loop;
-        float red_acc[kWarps][G][kHD];
-    } u;
-    float red_ml[kWarps][G][2];
+struct SplitLayout {
+    // per consumer warp: P (hi, lo) [G][72] halves during a stage, or the
+    // warp's final state (acc [G][128], M [G], S [G]) when a segment ends
+    static constexpr int kScratch = ((G * 520) + 15) / 16 * 16;
+    static constexpr int kQCodes = G * kHD;
+    static constexpr int kQScale = G * kNQB * 4;
+    static constexpr int kMisc = 128;
+    static constexpr int kFixed = kConsumerWarps * kScratch + kQCodes + kQScale + kMisc;
+    static constexpr int kStages = (kSmemLimit - kFixed - 512) / (kStageBytes + 16 + 16);
+    static constexpr int oRing = 0;
+    static constexpr int oScratch = kStages * kStageBytes;
+    static constexpr int oQCodes = oScratch + kConsumerWarps * kScratch;
+    static constexpr int oQScale = oQCodes + kQCodes;
+    static constexpr int oMisc = oQScale + kQScale;
+    static constexpr int oFull = oMisc + kMisc;
+    static constexpr int oEmpty = oFull + kStages * 8;
+    static constexpr int oSkip = oEmpty + kStages * 8;
+    static constexpr int kBytes = oSkip + kStages * 4;
+    static_assert(oMisc % 16 == 0 && oFull % 16 == 0 && oScratch % 16 == 0, "alignment");
+    static_assert(kBytes <= kSmemLimit, "shared memory budget");
+    static_assert(kStages >= 8, "ring too shallow");
+    static_assert(G * 2 * kPRowHalves * 2 <= kScratch, "P fits the warp scratch");
 };
 
-template <int G>
-__global__ void __launch_bounds__(kWarps * 32)
-decode_split_kernel(DecodeParams p) {
-    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+struct Misc {
+    long long warp_tot[kSplitThreads / 32];
+    long long base;   // stage prefix at the first unit of sequence b0
+    int b0;
+    int next;         // next segment-local stage to hand out to a consumer warp
+};
 
-    const int cap = p.max_blocks * kBS;
-    int L = p.ctx_lens[b];
-    if (L < 0 || L > cap) {
-        if (threadIdx.x == 0 && split == 0 && h == 0) flag_status(p.dev_status, KVQ8_DEV_BAD_CTX_LEN);
-        L = max(0, min(L, cap));
-    }
-    const int tok_begin = split * p.split_blocks * kBS;
-    if (tok_begin >= L) return;  // this split is empty; combine does not read its record
-    const int tok_end = min(L, tok_begin + p.split_blocks * kBS);
+__device__ __forceinline__ int clamp_len(int L, int cap) { return max(0, min(L, cap)); }
 
-    __shared__ __align__(16) SplitSmem<G> sm;
+__device__ __forceinline__ uint32_t half2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 
-    // segment 1: quantise the G query heads of this kv head once
-    for (int g = warp; g < G; g += kWarps)
-        quantize_q_row_warp(p.q + ((size_t)b * p.nqh + (size_t)h * G + g) * kHD, lane,
-                            sm.q_codes[g], sm.q_scale[g]);
-    __syncthreads();
-
-    float M[G], S[G], acc[G][4];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        M[g] = -INFINITY;
-        S[g] = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[g][j] = 0.0f;
-    }
-
-    const int nchunks = (tok_end - tok_begin + kChunk - 1) / kChunk;
-    for (int c = warp; c < nchunks; c += kWarps) {
-        const int t0 = tok_begin + c * kChunk;
-        const int slot0 = t0 % kBS;
-        const int phys = p.block_table[(size_t)b * p.max_blocks + t0 / kBS];
-        if (phys < 0 || phys >= p.num_blocks) {  // warp-uniform
-            if (lane == 0) flag_status(p.dev_status, KVQ8_DEV_BAD_BLOCK_ID);
-            continue;
-        }
-        const size_t tile = (size_t)phys * p.nkv + h;
-
-        // stage the chunk's 32 K rows and the V dim rows (coalesced 16-byte loads)
-        const int8_t *kg = p.k_pool + (tile * kBS + slot0) * kHD;
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-            const int row = it * 4 + (lane >> 3), ch = lane & 7;
-            const int4 v = *reinterpret_cast<const int4 *>(kg + row * kHD + ch * 16);
-            *reinterpret_cast<int4 *>(&sm.u.loop.k_tile[warp][row][ch * 16]) = v;
-        }
-        const int8_t *vg = p.v_pool + tile * kHD * kBS + slot0;
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-            const int e = it * 32 + lane, d = e >> 1, half = e & 1;
-            const int4 v = *reinterpret_cast<const int4 *>(vg + (size_t)d * kBS + half * 16);
-            int *dst = reinterpret_cast<int *>(&sm.u.loop.v_tile[warp][d][half * 16]);
-            dst[0] = v.x;
-            dst[1] = v.y;
-            dst[2] = v.z;
-            dst[3] = v.w;
-        }
-        const bool valid = (t0 + lane) < tok_end;
-        const float ks = p.k_scale[tile * kBS + slot0 + lane];
-        const float vs = p.v_scale[tile * kBS + slot0 + lane];
-        __syncwarp();
-
-        // segment 2a: integer block dots, lane = token
-        int dot[G][kNQB];
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int k = 0; k < kNQB; ++k) dot[g][k] = 0;
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-            const int4 kw = *reinterpret_cast<const int4 *>(&sm.u.loop.k_tile[warp][lane][cc * 16]);
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const int4 qw = *reinterpret_cast<const int4 *>(&sm.q_codes[g][cc * 16]);
-                int d = dot[g][cc >> 1];
-                d = __dp4a(kw.x, qw.x, d);
-                d = __dp4a(kw.y, qw.y, d);
-                d = __dp4a(kw.z, qw.z, d);
-                d = __dp4a(kw.w, qw.w, d);
-                dot[g][cc >> 1] = d;
-            }
-        }
-
-        // segment 2b: scales, online softmax (one rescale per chunk)
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float s = -INFINITY;
-            if (valid) {
-                float a = (float)dot[g][0] * sm.q_scale[g][0];
-#pragma unroll
-                for (int k = 1; k < kNQB; ++k) a += (float)dot[g][k] * sm.q_scale[g][k];
-                s = a * ks * p.sm_scale_log2;
-            }
-            const float m_new = fmaxf(M[g], warp_max(s));  // finite: lane 0 is valid
-            const float alpha = exp2f(M[g] - m_new);       // 0 while M is -inf
-            const float w = valid ? exp2f(s - m_new) : 0.0f;
-            S[g] = S[g] * alpha + warp_sum(w);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[g][j] *= alpha;
-            M[g] = m_new;
-            sm.u.loop.p[warp][lane][g] = valid ? w * vs : 0.0f;
-        }
-        __syncwarp();
-
-        // segment 2c: acc += int8 V * (weight * V scale), lane = dims
-#pragma unroll
-        for (int wi = 0; wi < kChunk / 4; ++wi) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int word = *reinterpret_cast<const int *>(&sm.u.loop.v_tile[warp][lane + 32 * j][wi * 4]);
-#pragma unroll
-                for (int tt = 0; tt < 4; ++tt) {
-                    const float v = (float)(int8_t)(word >> (8 * tt));
-#pragma unroll
-                    for (int g = 0; g < G; ++g) acc[g][j] += sm.u.loop.p[warp][wi * 4 + tt][g] * v;
-                }
-            }
-        }
-        __syncwarp();
-    }
-
-    // merge the 4 warp states into one record per query head
-    __syncthreads();
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) sm.u.red_acc[warp][g][lane + 32 * j] = acc[g][j];
-        if (lane == 0) {
-            sm.red_ml[warp][g][0] = M[g];
-            sm.red_ml[warp][g][1] = S[g];
-        }
-    }
-    __syncthreads();
-    const int i = threadIdx.x;  // one dim per thread
-    const size_t rec = ((size_t)b * p.nkv + h) * p.nsplit + split;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        float m = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) m = fmaxf(m, sm.red_ml[w][g][0]);
-        float s_sum = 0.0f, a = 0.0f;
-        if (m != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float f = exp2f(sm.red_ml[w][g][0] - m);
-                s_sum += sm.red_ml[w][g][1] * f;
-                a += sm.u.red_acc[w][g][i] * f;
-            }
-        }
-        p.ws_acc[(rec * G + g) * kHD + i] = a;
-        if (i == 0) {
-            p.ws_ml[(rec * G + g) * 2 + 0] = m;
-            p.ws_ml[(rec * G + g) * 2 + 1] = s_sum;
-        }
-    }
+// int8 codes of 4 consecutive tokens -> two fp16 pairs (tokens 0,1 and 2,3),
+// exact: (1024 + (v + 128)) - 1152 = v.
+__device__ __forceinline__ void codes_to_half2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t x = w ^ 0x80808080u;
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+    uint32_t l = __byte_perm(x, 0x64646464u, 0x4140);
+    uint32_t h = __byte_perm(x, 0x64646464u, 0x4342);
+    lo = half2_bits(__hsub2(*reinterpret_cast<__half2 *>(&l), bias));
+    hi = half2_bits(__hsub2(*reinterpret_cast<__half2 *>(&h), bias));
 }
 
-// Merge of the split records of one (sequence, query head); thread = dim.
+__device__ __forceinline__ int4 lds128(const void *p) { return *reinterpret_cast<const int4 *>(p); }
+
+template <int G>
+__global__ void __launch_bounds__(kSplitThreads, 1)
+decode_split_kernel(DecodeParams p) {
+    using Lay = SplitLayout<G>;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x;
+    const int cap = p.max_blocks * kBS;
+    Misc *misc = reinterpret_cast<Misc *>(smem + Lay::oMisc);
+    int8_t *q_codes = reinterpret_cast<int8_t *>(smem + Lay::oQCodes);
+    float *q_scale = reinterpret_cast<float *>(smem + Lay::oQScale);
+    volatile int *skip = reinterpret_cast<volatile int *>(smem + Lay::oSkip);
+    const uint32_t full0 = smem_addr(smem + Lay::oFull), empty0 = smem_addr(smem + Lay::oEmpty);
+
+    if (tid == 0) {
+        for (int i = 0; i < Lay::kStages; ++i) {
+            mbar_init(full0 + 8 * i, 1);
+            mbar_init(empty0 + 8 * i, 1);
+        }
+        fence_mbar_init();
+    }
+
+    // ---- prologue: total stage count T and where this CTA's range starts ----
+    const int per = (p.batch + kSplitThreads - 1) / kSplitThreads;
+    const int b_lo = min(p.batch, tid * per), b_hi = min(p.batch, b_lo + per);
+    long long mine = 0;
+    for (int b = b_lo; b < b_hi; ++b) {
+        const int L = p.ctx_lens[b];
+        if (c == 0 && (L < 0 || L > cap)) flag_status(p.dev_status, KVQ8_DEV_BAD_CTX_LEN);
+        mine += (long long)p.nkv * ((clamp_len(L, cap) + kStageTok - 1) / kStageTok);
+    }
+    long long incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) misc->warp_tot[warp] = incl;
+    __syncthreads();
+    if (tid == 0) {
+        long long run = 0;
+        for (int w = 0; w < kSplitThreads / 32; ++w) {
+            const long long t = misc->warp_tot[w];
+            misc->warp_tot[w] = run;
+            run += t;
+        }
+        misc->base = run;  // temporarily: T
+    }
+    __syncthreads();
+    const long long T = misc->base;
+    const long long excl = misc->warp_tot[warp] + incl - mine;
+    // the stages are shared by min(gridDim.x, T) CTAs so that every active CTA
+    // owns at least one stage and the CTAs covering a unit are consecutive
+    const int C = (int)min((long long)gridDim.x, T);
+    const long long lo = c < C ? (long long)c * T / C : 0, hi = c < C ? (long long)(c + 1) * T / C : 0;
+    __syncthreads();
+    if (mine > 0 && excl <= lo && lo < excl + mine) {
+        long long acc = excl;
+        for (int b = b_lo; b < b_hi; ++b) {
+            const long long n =
+                (long long)p.nkv * ((clamp_len(p.ctx_lens[b], cap) + kStageTok - 1) / kStageTok);
+            if (lo < acc + n) {
+                misc->b0 = b;
+                misc->base = acc;
+                break;
+            }
+            acc += n;
+        }
+    }
+    __syncthreads();
+
+    int b = 0, h = 0, off = 0;
+    if (hi > lo) {
+        b = misc->b0;
+        const int nb = (clamp_len(p.ctx_lens[b], cap) + kStageTok - 1) / kStageTok;
+        const long long rel = lo - misc->base;
+        h = (int)(rel / nb);
+        off = (int)(rel % nb);
+    }
+
+    if (warp == kConsumerWarps) {
+        // =========================== producer warp ===========================
+        const uint64_t pol = l2_evict_first_policy();
+        bool aborted = false;
+        long long remaining = hi - lo;
+        int kbase = 0;
+        while (remaining > 0 && b < p.batch) {
+            const int L = clamp_len(p.ctx_lens[b], cap);
+            const int nb = (L + kStageTok - 1) / kStageTok;
+            if (nb == 0) { ++b; h = 0; off = 0; continue; }
+            const int seg_n = (int)min((long long)(nb - off), remaining);
+            const int32_t *row = p.block_table + (size_t)b * p.max_blocks;
+            int tbl_base = -1, tbl_reg = -1;
+            for (int j = 0; j < seg_n; ++j) {
+                const int k = kbase + j, slot = k % Lay::kStages;
+                const uint32_t par = ((k / Lay::kStages) & 1) ^ 1;
+                const int t0 = (off + j) * kStageTok;
+                const int lb = t0 / kBS, quarter = (t0 / kStageTok) & 3;
+                if (tbl_base < 0 || lb >= tbl_base + 32) {
+                    tbl_base = lb;
+                    tbl_reg = (lb + lane < p.max_blocks) ? row[lb + lane] : -1;
+                }
+                const int phys = __shfl_sync(0xffffffffu, tbl_reg, lb - tbl_base);
+                if (lane == 0) {
+                    const uint32_t fb = full0 + 8 * slot;
+                    if (!aborted && !mbar_wait_bounded(empty0 + 8 * slot, par, kWaitTimeoutNs)) {
+                        aborted = true;
+                        flag_status(p.dev_status, KVQ8_DEV_TIMEOUT);
+                    }
+                    if (aborted) {
+                        // leave the slot unfilled; its consumer times out and unwinds
+                    } else if (phys >= 0 && phys < p.num_blocks) {
+                        skip[slot] = 0;
+                        const size_t tile = (size_t)phys * p.nkv + h;
+                        unsigned char *st = smem + Lay::oRing + (size_t)slot * kStageBytes;
+                        mbar_arrive_expect_tx(fb, kStageBytes);
+                        bulk_copy_g2s(smem_addr(st), p.k_pool + (tile * kBS + quarter * kStageTok) * kHD,
+                                      kStageKBytes, fb, pol);
+                        bulk_copy_g2s(smem_addr(st + kStageKBytes),
+                                      p.v_pool + tile * kHD * kBS + quarter * kTileVQuarter,
+                                      kStageVBytes, fb, pol);
+                        bulk_copy_g2s(smem_addr(st + kStageKBytes + kStageVBytes),
+                                      p.k_scale + tile * kBS + quarter * kStageTok, kStageSBytes, fb, pol);
+                        bulk_copy_g2s(smem_addr(st + kStageKBytes + kStageVBytes + kStageSBytes),
+                                      p.v_scale + tile * kBS + quarter * kStageTok, kStageSBytes, fb, pol);
+                    } else {
+                        skip[slot] = 1;
+                        flag_status(p.dev_status, KVQ8_DEV_BAD_BLOCK_ID);
+                        mbar_arrive(fb);
+                    }
+                }
+                __syncwarp();
+            }
+            remaining -= seg_n;
+            kbase += seg_n;
+            off = 0;
+            if (++h == p.nkv) { h = 0; ++b; }
+        }
+        // no copy may still be in flight when the CTA exits
+        if (lane == 0) {
+            for (int k = max(0, kbase - Lay::kStages); k < kbase; ++k)
+                mbar_wait_bounded(full0 + 8 * (k % Lay::kStages), (k / Lay::kStages) & 1, kWaitTimeoutNs);
+        }
+    } else {
+        // =========================== consumer warps ==========================
+        unsigned char *scratch = smem + Lay::oScratch + warp * Lay::kScratch;
+        __half *p_hi = reinterpret_cast<__half *>(scratch);
+        __half *p_lo = p_hi + G * kPRowHalves;
+        float *red_acc = reinterpret_cast<float *>(scratch);
+        float *red_m = red_acc + G * kHD;
+        float *red_s = red_m + G;
+        const int n = lane >> 2, t4 = lane & 3;  // MMA fragment coordinates
+        bool aborted = false;
+        long long remaining = hi - lo;
+        int kbase = 0;
+        while (remaining > 0 && b < p.batch) {
+            const int L = clamp_len(p.ctx_lens[b], cap);
+            const int nb = (L + kStageTok - 1) / kStageTok;
+            if (nb == 0) { ++b; h = 0; off = 0; continue; }
+            const int seg_n = (int)min((long long)(nb - off), remaining);
+            const int u = b * p.nkv + h;
+
+            // segment 1: quantise this unit's G query heads once
+            named_barrier_sync(1, kConsumerWarps * 32);
+            if (tid == 0) misc->next = 0;
+            for (int g = warp; g < G; g += kConsumerWarps)
+                quantize_q_row_warp(p.q + ((size_t)b * p.nqh + (size_t)h * G + g) * kHD, lane,
+                                    q_codes + g * kHD, q_scale + g * kNQB);
+            named_barrier_sync(1, kConsumerWarps * 32);
+
+            float M[G], Sl[G], acc[8][4];
+#pragma unroll
+            for (int g = 0; g < G; ++g) { M[g] = -INFINITY; Sl[g] = 0.0f; }
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[mt][i] = 0.0f;
+            int e_cur = 0;  // acc holds values in units of 2^e_cur
+
+            for (;;) {
+                int j = 0;
+                if (lane == 0) j = atomicAdd(&misc->next, 1);
+                j = __shfl_sync(0xffffffffu, j, 0);
+                if (j >= seg_n) break;
+                const int k = kbase + j, slot = k % Lay::kStages;
+                const uint32_t par = (k / Lay::kStages) & 1;
+                if (!aborted && !mbar_wait_bounded(full0 + 8 * slot, par, kWaitTimeoutNs)) {
+                    aborted = true;
+                    if (lane == 0) flag_status(p.dev_status, KVQ8_DEV_TIMEOUT);
+                }
+                if (!aborted && !skip[slot]) {
+                    const unsigned char *st = smem + Lay::oRing + (size_t)slot * kStageBytes;
+                    const int8_t *kst = reinterpret_cast<const int8_t *>(st);
+                    const int8_t *vst = kst + kStageKBytes;
+                    const float *ks_st = reinterpret_cast<const float *>(st + kStageKBytes + kStageVBytes);
+                    const float *vs_st = ks_st + kStageTok;
+                    const int nvalid = min(kStageTok, L - (off + j) * kStageTok);
+                    const int ta = lane, tb = lane + 32;
+                    const bool va = ta < nvalid, vb = tb < nvalid;
+
+                    // ---- segment 2a: int32 block dots, lane = token ----
+                    int da[G][kNQB], db[G][kNQB];
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+#pragma unroll
+                        for (int q = 0; q < kNQB; ++q) { da[g][q] = 0; db[g][q] = 0; }
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        const int4 ka = lds128(kst + ta * kHD + ((cc ^ (ta & 7)) << 4));
+                        const int4 kb = lds128(kst + tb * kHD + ((cc ^ (tb & 7)) << 4));
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            const int4 qw = lds128(q_codes + g * kHD + cc * 16);
+                            int x = da[g][cc >> 1], y = db[g][cc >> 1];
+                            x = __dp4a(ka.x, qw.x, x); y = __dp4a(kb.x, qw.x, y);
+                            x = __dp4a(ka.y, qw.y, x); y = __dp4a(kb.y, qw.y, y);
+                            x = __dp4a(ka.z, qw.z, x); y = __dp4a(kb.z, qw.z, y);
+                            x = __dp4a(ka.w, qw.w, x); y = __dp4a(kb.w, qw.w, y);
+                            da[g][cc >> 1] = x;
+                            db[g][cc >> 1] = y;
+                        }
+                    }
+                    const float ksa = ks_st[ta], ksb = ks_st[tb];
+                    const float vsa = va ? vs_st[ta] : 0.0f, vsb = vb ? vs_st[tb] : 0.0f;
+
+                    // power-of-two scale of this stage's V scales: p' = w*vs*2^-e <= 1
+                    const float vmax = warp_max(fmaxf(vsa, vsb));
+                    // 2^e > vmax: the exponent field of vmax (subnormals count as 2^-126)
+                    int e = e_cur;
+                    if (vmax > 0.0f) e = max(-120, min(120, ((__float_as_int(vmax) >> 23) & 0xff) - 126));
+                    const float inv = __int_as_float((127 - e) << 23);
+
+                    // ---- segment 2b: scores, online softmax (one rescale per stage) ----
+                    float alpha[G];
+                    bool rescale = (e != e_cur);
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const float4 qs = *reinterpret_cast<const float4 *>(q_scale + g * kNQB);
+                        float sa = -INFINITY, sb = -INFINITY;
+                        if (va) {
+                            float a = (float)da[g][0] * qs.x;
+                            a = fmaf((float)da[g][1], qs.y, a);
+                            a = fmaf((float)da[g][2], qs.z, a);
+                            a = fmaf((float)da[g][3], qs.w, a);
+                            sa = a * ksa * p.sm_scale_log2;
+                        }
+                        if (vb) {
+                            float a = (float)db[g][0] * qs.x;
+                            a = fmaf((float)db[g][1], qs.y, a);
+                            a = fmaf((float)db[g][2], qs.z, a);
+                            a = fmaf((float)db[g][3], qs.w, a);
+                            sb = a * ksb * p.sm_scale_log2;
+                        }
+                        const float m_new = fmaxf(M[g], warp_max(fmaxf(sa, sb)));  // finite: token 0 valid
+                        alpha[g] = exp2f(M[g] - m_new);
+                        rescale |= (m_new != M[g]);
+                        M[g] = m_new;
+                        const float wa = va ? exp2f(sa - m_new) : 0.0f;
+                        const float wb = vb ? exp2f(sb - m_new) : 0.0f;
+                        Sl[g] = fmaf(Sl[g], alpha[g], wa + wb);
+                        const float pa = wa * vsa * inv, pb = wb * vsb * inv;
+                        const __half ha = __float2half_rn(pa), hb = __float2half_rn(pb);
+                        p_hi[g * kPRowHalves + ta] = ha;
+                        p_hi[g * kPRowHalves + tb] = hb;
+                        p_lo[g * kPRowHalves + ta] = __float2half_rn(pa - __half2float(ha));
+                        p_lo[g * kPRowHalves + tb] = __float2half_rn(pb - __half2float(hb));
+                    }
+                    if (rescale) {  // warp-uniform
+                        const float two = __int_as_float((127 + max(-126, min(127, e_cur - e))) << 23);
+                        float f0 = 0.0f, f1 = 0.0f;
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            if (g == 2 * t4) f0 = alpha[g] * two;
+                            if (g == 2 * t4 + 1) f1 = alpha[g] * two;
+                        }
+#pragma unroll
+                        for (int mt = 0; mt < 8; ++mt) {
+                            acc[mt][0] *= f0; acc[mt][1] *= f1;
+                            acc[mt][2] *= f0; acc[mt][3] *= f1;
+                        }
+                        e_cur = e;
+                    }
+                    __syncwarp();
+
+                    // ---- segment 2c: acc += V . P on the tensor cores ----
+                    uint32_t bh[8], bl[8];
+                    if (n < G) {
+                        const int4 h0 = lds128(p_hi + n * kPRowHalves + t4 * 16);
+                        const int4 h1 = lds128(p_hi + n * kPRowHalves + t4 * 16 + 8);
+                        const int4 l0 = lds128(p_lo + n * kPRowHalves + t4 * 16);
+                        const int4 l1 = lds128(p_lo + n * kPRowHalves + t4 * 16 + 8);
+                        bh[0] = h0.x; bh[1] = h0.y; bh[2] = h0.z; bh[3] = h0.w;
+                        bh[4] = h1.x; bh[5] = h1.y; bh[6] = h1.z; bh[7] = h1.w;
+                        bl[0] = l0.x; bl[1] = l0.y; bl[2] = l0.z; bl[3] = l0.w;
+                        bl[4] = l1.x; bl[5] = l1.y; bl[6] = l1.z; bl[7] = l1.w;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) { bh[i] = 0u; bl[i] = 0u; }
+                    }
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) {
+                        const int d = mt * 16 + n;
+                        const int4 v0 = lds128(vst + d * kStageTok + t4 * 16);
+                        const int4 v1 = lds128(vst + (d + 8) * kStageTok + t4 * 16);
+                        const uint32_t w0[4] = {(uint32_t)v0.x, (uint32_t)v0.y, (uint32_t)v0.z, (uint32_t)v0.w};
+                        const uint32_t w1[4] = {(uint32_t)v1.x, (uint32_t)v1.y, (uint32_t)v1.z, (uint32_t)v1.w};
+#pragma unroll
+                        for (int s = 0; s < 4; ++s) {
+                            uint32_t a0, a2, a1, a3;
+                            codes_to_half2(w0[s], a0, a2);
+                            codes_to_half2(w1[s], a1, a3);
+                            mma_f16_16816(acc[mt], a0, a1, a2, a3, bh[2 * s], bh[2 * s + 1]);
+                            mma_f16_16816(acc[mt], a0, a1, a2, a3, bl[2 * s], bl[2 * s + 1]);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+            }
+
+            // ---- merge the 7 warp states of this segment into one record ----
+            const float unit_scale = __int_as_float((127 + max(-126, min(127, e_cur))) << 23);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float s_w = warp_sum(Sl[g]);
+                if (lane == 0) { red_m[g] = M[g]; red_s[g] = s_w; }
+            }
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                const int d0 = mt * 16 + n, h0 = 2 * t4, h1 = 2 * t4 + 1;
+                if (h0 < G) {
+                    red_acc[h0 * kHD + d0] = acc[mt][0] * unit_scale;
+                    red_acc[h0 * kHD + d0 + 8] = acc[mt][2] * unit_scale;
+                }
+                if (h1 < G) {
+                    red_acc[h1 * kHD + d0] = acc[mt][1] * unit_scale;
+                    red_acc[h1 * kHD + d0 + 8] = acc[mt][3] * unit_scale;
+                }
+            }
+            named_barrier_sync(1, kConsumerWarps * 32);
+            const size_t rec = (size_t)c + u;
+            for (int idx = tid; idx < G * kHD; idx += kConsumerWarps * 32) {
+                const int g = idx / kHD, d = idx % kHD;
+                float m = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w)
+                    m = fmaxf(m, reinterpret_cast<const float *>(smem + Lay::oScratch + w * Lay::kScratch)[G * kHD + g]);
+                float s_sum = 0.0f, a = 0.0f;
+                if (m != -INFINITY) {
+#pragma unroll
+                    for (int w = 0; w < kConsumerWarps; ++w) {
+                        const float *r = reinterpret_cast<const float *>(smem + Lay::oScratch + w * Lay::kScratch);
+                        const float f = exp2f(r[G * kHD + g] - m);
+                        s_sum = fmaf(r[G * kHD + G + g], f, s_sum);
+                        a = fmaf(r[g * kHD + d], f, a);
+                    }
+                }
+                p.ws_acc[(rec * G + g) * kHD + d] = a;
+                if (d == 0) {
+                    p.ws_ml[(rec * G + g) * 2 + 0] = m;
+                    p.ws_ml[(rec * G + g) * 2 + 1] = s_sum;
+                }
+            }
+            if (tid == 0 && off == 0) {
+                // this CTA holds the unit's first stage: publish where its records are
+                const long long start_u = lo + kbase;
+                const long long end_u = start_u + nb;
+                const int c_last = (int)((end_u * C + T - 1) / T) - 1;
+                p.ws_meta[u] = make_int2(c, c_last - c + 1);
+            }
+            remaining -= seg_n;
+            kbase += seg_n;
+            off = 0;
+            if (++h == p.nkv) { h = 0; ++b; }
+        }
+    }
+    pdl_launch_dependents();
+    __syncthreads();
+}
+
+// Merge of the partial records of one (sequence, query head); thread = dim.
 // [Day 9-2] §2 segment 3 generalised to several partial states:
 // M = max_i M_i, S = sum_i S_i 2^(M_i - M), out = sum_i acc_i 2^(M_i - M) / S.
 __global__ void __launch_bounds__(kHD)
 decode_combine_kernel(DecodeParams p, int G) {
-    const int qh = blockIdx.x, b = blockIdx.y, i = threadIdx.x;
+    pdl_wait();  // the split kernel's records are visible after this
+    const int qh = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
     const int h = qh / G, g = qh % G;
-    const int cap = p.max_blocks * kBS;
-    const int L = max(0, min(p.ctx_lens[b], cap));
-    const int split_tokens = p.split_blocks * kBS;
-    const int nvalid = (L + split_tokens - 1) / split_tokens;
-    const size_t rec0 = ((size_t)b * p.nkv + h) * p.nsplit;
-
+    const int L = max(0, min(p.ctx_lens[b], p.max_blocks * kBS));
+    float *o = p.out + ((size_t)b * p.nqh + qh) * kHD + d;
+    if (L == 0) { *o = 0.0f; return; }
+    const size_t u = (size_t)b * p.nkv + h;
+    const int2 meta = p.ws_meta[u];
+    const size_t rec0 = (size_t)meta.x + u;
     float m = -INFINITY;
-    for (int j = 0; j < nvalid; ++j) m = fmaxf(m, p.ws_ml[((rec0 + j) * G + g) * 2]);
+    for (int j = 0; j < meta.y; ++j) m = fmaxf(m, p.ws_ml[((rec0 + j) * G + g) * 2]);
     float s_sum = 0.0f, a = 0.0f;
     if (m != -INFINITY) {
-        for (int j = 0; j < nvalid; ++j) {
+        for (int j = 0; j < meta.y; ++j) {
             const size_t r = (rec0 + j) * G + g;
             const float f = exp2f(p.ws_ml[r * 2] - m);
-            s_sum += p.ws_ml[r * 2 + 1] * f;
-            a += p.ws_acc[r * kHD + i] * f;
+            s_sum = fmaf(p.ws_ml[r * 2 + 1], f, s_sum);
+            a = fmaf(p.ws_acc[r * kHD + d], f, a);
         }
     }
-    p.out[((size_t)b * p.nqh + qh) * kHD + i] = s_sum > 0.0f ? a / s_sum : 0.0f;
+    *o = s_sum > 0.0f ? a / s_sum : 0.0f;
+}
+
+int device_sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+template <int G>
+cudaError_t launch_split_g(const DecodeParams &p, cudaStream_t s) {
+    using Lay = SplitLayout<G>;
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
+    if (e != cudaSuccess) return e;
+    const int sms = device_sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int grid = min(sms, kMaxCtas);
+    decode_split_kernel<G><<<grid, kSplitThreads, Lay::kBytes, s>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
-// The split size aims at enough CTAs for several waves on a 152-SM GB300
-// while keeping each split long (partials stay well under 1% of KV bytes).
 bool make_decode_plan(int batch, int nqh, int nkv, int max_blocks, DecodePlan *plan) {
     if (batch < 0 || nqh <= 0 || nkv <= 0 || max_blocks <= 0 || nqh % nkv) return false;
     const int G = nqh / nkv;
-    const int64_t units = (int64_t)batch * nkv;
-    const int64_t target_ctas = 152 * 8;
-    int64_t sb = (units * max_blocks + target_ctas - 1) / target_ctas;
-    sb = sb < 1 ? 1 : (sb > 16 ? 16 : sb);
-    plan->group = G;
-    plan->split_blocks = (int)sb;
-    plan->nsplit = (int)((max_blocks + sb - 1) / sb);
-    plan->records = units * plan->nsplit;
     auto align = [](size_t x) { return (x + 255) & ~(size_t)255; };
-    plan->ml_offset = 0;
-    plan->acc_offset = align((size_t)plan->records * G * 2 * sizeof(float));
+    plan->group = G;
+    plan->units = (int64_t)batch * nkv;
+    plan->records = kMaxCtas + plan->units;
+    plan->meta_offset = 0;
+    plan->ml_offset = align((size_t)plan->units * sizeof(int2));
+    plan->acc_offset = plan->ml_offset + align((size_t)plan->records * G * 2 * sizeof(float));
     plan->bytes = plan->acc_offset + align((size_t)plan->records * G * kHD * sizeof(float));
-    if (plan->bytes == 0) plan->bytes = 256;
     return true;
 }
 
 cudaError_t launch_decode_split(const DecodeParams &p, int group, cudaStream_t s) {
-    dim3 grid(p.nsplit, p.nkv, p.batch);
     switch (group) {
-        case 1: decode_split_kernel<1><<<grid, kWarps * 32, 0, s>>>(p); break;
-        case 2: decode_split_kernel<2><<<grid, kWarps * 32, 0, s>>>(p); break;
-        case 4: decode_split_kernel<4><<<grid, kWarps * 32, 0, s>>>(p); break;
-        case 8: decode_split_kernel<8><<<grid, kWarps * 32, 0, s>>>(p); break;
+        case 1: return launch_split_g<1>(p, s);
+        case 2: return launch_split_g<2>(p, s);
+        case 4: return launch_split_g<4>(p, s);
+        case 8: return launch_split_g<8>(p, s);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_decode_combine(const DecodeParams &p, int group, cudaStream_t s) {
-    dim3 grid(p.nqh, p.batch);
-    decode_combine_kernel<<<grid, kHD, 0, s>>>(p, group);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.nqh, p.batch);
+    cfg.blockDim = dim3(kHD);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_combine_kernel, p, group);
 }
 
 }  // namespace kvq8

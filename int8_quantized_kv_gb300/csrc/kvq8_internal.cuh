@@ -31,14 +31,30 @@ cudaError_t launch_quantize_q(const float *q, int64_t n_rows, int8_t *codes,
                               float *scales, cudaStream_t s);
 
 // ----------------------------------------------------------------- decode --
-// Split-KV plan: every (sequence, kv head) unit is cut into splits of
-// split_blocks cache blocks; a split writes one partial record per query head.
+// Cache tile geometry.  One (block, kv head) tile holds 256 tokens:
+//   K: [256 tokens][128 B]; the 16-byte chunk j of token row t is stored at
+//      chunk position j ^ (t & 7), so lanes reading one row each hit distinct
+//      shared-memory banks after a plain copy.
+//   V: [4 quarters][128 dims][64 B]: dim-major per 64-token quarter.
+// A 64-token window of a tile (a decode "stage") is therefore four contiguous
+// runs: 8 KiB of K, 8 KiB of V and 256 B of each scale array.
+constexpr int kStageTok = 64;
+constexpr int kStageKBytes = kStageTok * kHD;     // 8192
+constexpr int kStageVBytes = kHD * kStageTok;     // 8192
+constexpr int kStageSBytes = kStageTok * 4;       // 256
+constexpr int kStageBytes = kStageKBytes + kStageVBytes + 2 * kStageSBytes;
+constexpr int kTileVQuarter = kHD * kStageTok;    // bytes of one V quarter
+constexpr int kMaxCtas = 1024;                    // upper bound of the split grid
+
+// Split-KV plan: the split kernel runs one persistent CTA per SM; the global
+// sequence of 64-token stages (units in order (sequence, kv head)) is cut into
+// equal contiguous ranges, one per CTA.  A (CTA c, unit u) segment writes
+// partial record c + u; meta[u] names the first CTA of unit u and its count.
 struct DecodePlan {
     int group;          // G = nqh / nkv
-    int split_blocks;   // cache blocks per split
-    int nsplit;         // splits per unit (covering max_blocks blocks)
-    int64_t records;    // batch * nkv * nsplit
-    size_t ml_offset, acc_offset, bytes;  // workspace layout
+    int64_t units;      // batch * nkv
+    int64_t records;    // kMaxCtas + units
+    size_t meta_offset, ml_offset, acc_offset, bytes;  // workspace layout
 };
 bool make_decode_plan(int batch, int nqh, int nkv, int max_blocks, DecodePlan *plan);
 
@@ -52,9 +68,9 @@ struct DecodeParams {
     int max_blocks;
     const int32_t *ctx_lens;
     float sm_scale_log2;          // sm_scale * log2(e): softmax runs in base 2
+    int2 *ws_meta;                // [units]: (first CTA, CTA count)
     float *ws_ml;                 // [records][G][2]  (running max M, sum S)
     float *ws_acc;                // [records][G][hd] (unnormalised V accumulator)
-    int nsplit, split_blocks;
     uint32_t *dev_status;
     float *out;                   // [batch][nqh][hd] (combine only)
 };

@@ -20,7 +20,7 @@ Q_BLOCK = 32
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024   # KVQ8_NOALLOC_SCRATCH_BYTES in kvq8.h
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = range(5)
-DEV_BAD_BLOCK_ID, DEV_BAD_CTX_LEN, DEV_BAD_POSITION = 0x1, 0x2, 0x4
+DEV_BAD_BLOCK_ID, DEV_BAD_CTX_LEN, DEV_BAD_POSITION, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -135,8 +135,8 @@ def decode_workspace_bytes(batch: int, nqh: int, nkv: int, max_blocks: int) -> i
 
 class KVCache(NamedTuple):
     """One layer-pool of the paged cache (see the layout in include/kvq8.h)."""
-    k_pool: object   # int8 [num_blocks][nkv][256][128]  token-major
-    v_pool: object   # int8 [num_blocks][nkv][128][256]  dim-major
+    k_pool: object   # int8 [num_blocks][nkv][256][128]  token-major, 16-B chunks permuted
+    v_pool: object   # int8 [num_blocks][nkv][4][128][64] dim-major per 64-token quarter
     k_scale: object  # fp32 [num_blocks][nkv][256]
     v_scale: object  # fp32 [num_blocks][nkv][256]
 
@@ -154,7 +154,7 @@ def alloc_cache(num_blocks: int, nkv: int, device="cuda") -> KVCache:
     import torch
     assert kv_pool_bytes(num_blocks, nkv) == num_blocks * nkv * BLOCK_SIZE * HEAD_DIM
     k = torch.empty((num_blocks, nkv, BLOCK_SIZE, HEAD_DIM), dtype=torch.int8, device=device)
-    v = torch.empty((num_blocks, nkv, HEAD_DIM, BLOCK_SIZE), dtype=torch.int8, device=device)
+    v = torch.empty((num_blocks, nkv, BLOCK_SIZE // 64, HEAD_DIM, 64), dtype=torch.int8, device=device)
     ks = torch.empty((num_blocks, nkv, BLOCK_SIZE), dtype=torch.float32, device=device)
     vs = torch.empty((num_blocks, nkv, BLOCK_SIZE), dtype=torch.float32, device=device)
     return KVCache(k, v, ks, vs)

@@ -21,6 +21,21 @@ ABS_TOL = 1e-4
 REL_TOL = 1e-3
 
 
+def k_rows_logical(kp, phys, h, slots):
+    """K codes of the given (physical block, slot)s in dim order: the cache stores
+    the 16-byte chunk j of a slot's row at chunk position j ^ (slot & 7)."""
+    slots = np.asarray(slots)
+    rows = kp[phys, h, slots, :].reshape(len(slots), 8, 16)
+    pos = np.arange(8)[None, :] ^ (slots & 7)[:, None]
+    return np.take_along_axis(rows, pos[:, :, None], axis=1).reshape(len(slots), 128)
+
+
+def v_rows_logical(vp, phys, h, slots):
+    """V codes of the given (physical block, slot)s: quarters of 64 slots, dim-major."""
+    slots = np.asarray(slots)
+    return vp[phys, h, slots // 64, :, slots % 64]
+
+
 def assert_close(gpu, ref, what=""):
     """Output parity bar: |gpu - oracle| <= 1e-4 + 1e-3 * |oracle| per element."""
     gpu = np.asarray(gpu, np.float64)
@@ -96,8 +111,8 @@ class Case:
         t = np.arange(L)
         phys = self.table[b, t // wl.BLOCK_TOKENS]
         slot = t % wl.BLOCK_TOKENS
-        kq = kp[phys, h, slot, :]
-        vq = vp[phys, h, :, slot]            # dim-major tile, gathered per token
+        kq = k_rows_logical(kp, phys, h, slot)
+        vq = v_rows_logical(vp, phys, h, slot)
         return kq, ksp[phys, h, slot], vq, vsp[phys, h, slot]
 
     # -- the oracle on the same inputs ------------------------------------------

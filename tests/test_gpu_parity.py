@@ -14,7 +14,7 @@ import torch
 import oracle
 from int8_quantized_kv_gb300 import kvq8
 from int8_quantized_kv_gb300 import workloads as wl
-from kvq8_harness import Case, SM_SCALE, assert_close
+from kvq8_harness import Case, SM_SCALE, assert_close, k_rows_logical, v_rows_logical
 
 pytestmark = pytest.mark.gpu
 HD = 128
@@ -100,8 +100,8 @@ def test_quantize_append_bit_exact(gpu_lib, start, n_new):
         for h in range(nkv):
             kq, ks = oracle.kv_quantize_rows(k[b, :, h])
             vq, vs = oracle.kv_quantize_rows(v[b, :, h])
-            assert np.array_equal(kp[phys, h, slot, :], kq)
-            assert np.array_equal(vp[phys, h, :, slot], vq)
+            assert np.array_equal(k_rows_logical(kp, phys, h, slot), kq)
+            assert np.array_equal(v_rows_logical(vp, phys, h, slot), vq)
             assert np.array_equal(ksp[phys, h, slot].view(np.uint32), ks.view(np.uint32))
             assert np.array_equal(vsp[phys, h, slot].view(np.uint32), vs.view(np.uint32))
     # slots outside the appended range are untouched
