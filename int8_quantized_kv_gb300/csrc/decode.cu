@@ -58,7 +58,7 @@ struct SplitLayout {
     static constexpr int kQScale = G * kNQB * 4;
     static constexpr int kMisc = 128;
     static constexpr int kFixed = kConsumerWarps * kScratch + kQCodes + kQScale + kMisc;
-    static constexpr int kStages = (kSmemLimit - kFixed - 512) / (kStageBytes + 16 + 16);
+    static constexpr int kStages = (kSmemLimit - kFixed - 512) / (kStageBytes + 16 + 16 + 4);
     static constexpr int oRing = 0;
     static constexpr int oScratch = kStages * kStageBytes;
     static constexpr int oQCodes = oScratch + kConsumerWarps * kScratch;
@@ -67,7 +67,8 @@ struct SplitLayout {
     static constexpr int oFull = oMisc + kMisc;
     static constexpr int oEmpty = oFull + kStages * 8;
     static constexpr int oSkip = oEmpty + kStages * 8;
-    static constexpr int kBytes = oSkip + kStages * 4;
+    static constexpr int oDone = oSkip + kStages * 4;
+    static constexpr int kBytes = oDone + kStages * 4;
     static_assert(oMisc % 16 == 0 && oFull % 16 == 0 && oScratch % 16 == 0, "alignment");
     static_assert(kBytes <= kSmemLimit, "shared memory budget");
     static_assert(kStages >= 8, "ring too shallow");
@@ -98,6 +99,17 @@ __device__ __forceinline__ void codes_to_half2(uint32_t w, uint32_t &lo, uint32_
 
 __device__ __forceinline__ int4 lds128(const void *p) { return *reinterpret_cast<const int4 *>(p); }
 
+// Waits until *done reaches `round` (the slot's earlier stages are consumed);
+// false after timeout_ns.
+__device__ __forceinline__ bool slot_turn_bounded(volatile int *done, int round, uint64_t timeout_ns) {
+    if (*done >= round) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (*done < round) {
+        if (global_timer_ns() - t0 > timeout_ns) return false;
+    }
+    return true;
+}
+
 template <int G>
 __global__ void __launch_bounds__(kSplitThreads, 1)
 decode_split_kernel(DecodeParams p) {
@@ -110,12 +122,18 @@ decode_split_kernel(DecodeParams p) {
     int8_t *q_codes = reinterpret_cast<int8_t *>(smem + Lay::oQCodes);
     float *q_scale = reinterpret_cast<float *>(smem + Lay::oQScale);
     volatile int *skip = reinterpret_cast<volatile int *>(smem + Lay::oSkip);
+    // done[s] = how many stages of slot s have been consumed.  A consumer waits
+    // on a slot's full barrier only once the slot's previous stage is consumed,
+    // so every wait targets the barrier's current phase (a parity wait cannot
+    // tell a phase two rounds ahead from the previous one).
+    volatile int *done = reinterpret_cast<volatile int *>(smem + Lay::oDone);
     const uint32_t full0 = smem_addr(smem + Lay::oFull), empty0 = smem_addr(smem + Lay::oEmpty);
 
     if (tid == 0) {
         for (int i = 0; i < Lay::kStages; ++i) {
             mbar_init(full0 + 8 * i, 1);
             mbar_init(empty0 + 8 * i, 1);
+            done[i] = 0;
         }
         fence_mbar_init();
     }
@@ -282,12 +300,11 @@ decode_split_kernel(DecodeParams p) {
                 if (lane == 0) j = atomicAdd(&misc->next, 1);
                 j = __shfl_sync(0xffffffffu, j, 0);
                 if (j >= seg_n) break;
-                const int k = kbase + j, slot = k % Lay::kStages;
-                const uint32_t par = (k / Lay::kStages) & 1;
-                if (!aborted && !mbar_wait_bounded(full0 + 8 * slot, par, kWaitTimeoutNs)) {
-                    aborted = true;
-                    if (lane == 0) flag_status(p.dev_status, KVQ8_DEV_TIMEOUT);
-                }
+                const int k = kbase + j, slot = k % Lay::kStages, round = k / Lay::kStages;
+                const uint32_t par = round & 1;
+                if (!aborted && !slot_turn_bounded(done + slot, round, kWaitTimeoutNs)) aborted = true;
+                if (!aborted && !mbar_wait_bounded(full0 + 8 * slot, par, kWaitTimeoutNs)) aborted = true;
+                if (aborted && lane == 0) flag_status(p.dev_status, KVQ8_DEV_TIMEOUT);
                 if (!aborted && !skip[slot]) {
                     const unsigned char *st = smem + Lay::oRing + (size_t)slot * kStageBytes;
                     const int8_t *kst = reinterpret_cast<const int8_t *>(st);
@@ -415,7 +432,10 @@ decode_split_kernel(DecodeParams p) {
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+                if (lane == 0) {
+                    done[slot] = round + 1;
+                    mbar_arrive(empty0 + 8 * slot);
+                }
             }
 
             // ---- merge the 7 warp states of this segment into one record ----
