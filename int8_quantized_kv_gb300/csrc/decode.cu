@@ -48,6 +48,7 @@ constexpr int kSplitThreads = (kConsumerWarps + 1) * 32;
 constexpr int kSmemLimit = 232448;          // 227 KiB opt-in per CTA on sm_103a
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 constexpr int kPRowHalves = 72;             // P row: 64 tokens + 8 halves of padding
+constexpr float kLazyLog2 = 8.0f;           // running-max slack (log2 units), see segment 2b
 
 template <int G>
 struct SplitLayout {
@@ -98,6 +99,19 @@ __device__ __forceinline__ void codes_to_half2(uint32_t w, uint32_t &lo, uint32_
 }
 
 __device__ __forceinline__ int4 lds128(const void *p) { return *reinterpret_cast<const int4 *>(p); }
+
+// Warp-wide maxima in one redux instruction.  Floats are mapped to integers
+// whose signed order is the float order (negative values get their magnitude
+// bits flipped), reduced, and mapped back.
+__device__ __forceinline__ int redux_max_i32(int v) { return __reduce_max_sync(0xffffffffu, v); }
+
+__device__ __forceinline__ float redux_max_f32(float x) {
+    int k = __float_as_int(x);
+    k ^= (k >> 31) & 0x7fffffff;
+    k = __reduce_max_sync(0xffffffffu, k);
+    k ^= (k >> 31) & 0x7fffffff;
+    return __int_as_float(k);
+}
 
 // Waits until *done reaches `round` (the slot's earlier stages are consumed);
 // false after timeout_ns.
@@ -293,7 +307,7 @@ decode_split_kernel(DecodeParams p) {
             for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) acc[mt][i] = 0.0f;
-            int e_cur = 0;  // acc holds values in units of 2^e_cur
+            int e_cur = 1000;  // acc holds values in units of 2^e_cur (first stage sets it)
 
             for (;;) {
                 int j = 0;
@@ -340,40 +354,55 @@ decode_split_kernel(DecodeParams p) {
                     const float ksa = ks_st[ta], ksb = ks_st[tb];
                     const float vsa = va ? vs_st[ta] : 0.0f, vsb = vb ? vs_st[tb] : 0.0f;
 
-                    // power-of-two scale of this stage's V scales: p' = w*vs*2^-e <= 1
-                    const float vmax = warp_max(fmaxf(vsa, vsb));
-                    // 2^e > vmax: the exponent field of vmax (subnormals count as 2^-126)
+                    // power-of-two unit of this stage's P: 2^e > max vs, so that
+                    // p' = w * vs * 2^-e stays below 2^8 (w < 2^8, see below).  e only
+                    // moves when it must grow or has become 2^12 too large.
+                    const int e_need = redux_max_i32(
+                        ((__float_as_int(fmaxf(vsa, vsb)) >> 23) & 0xff) - 126);  // 0 -> -126
                     int e = e_cur;
-                    if (vmax > 0.0f) e = max(-120, min(120, ((__float_as_int(vmax) >> 23) & 0xff) - 126));
+                    if (e_need > e_cur || e_need < e_cur - 12) e = max(-120, min(120, e_need));
                     const float inv = __int_as_float((127 - e) << 23);
 
-                    // ---- segment 2b: scores, online softmax (one rescale per stage) ----
-                    float alpha[G];
-                    bool rescale = (e != e_cur);
+                    // ---- segment 2b: scores, online softmax ----
+                    float sa[G], sb[G];
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         const float4 qs = *reinterpret_cast<const float4 *>(q_scale + g * kNQB);
-                        float sa = -INFINITY, sb = -INFINITY;
-                        if (va) {
-                            float a = (float)da[g][0] * qs.x;
-                            a = fmaf((float)da[g][1], qs.y, a);
-                            a = fmaf((float)da[g][2], qs.z, a);
-                            a = fmaf((float)da[g][3], qs.w, a);
-                            sa = a * ksa * p.sm_scale_log2;
+                        float a = (float)da[g][0] * qs.x;
+                        a = fmaf((float)da[g][1], qs.y, a);
+                        a = fmaf((float)da[g][2], qs.z, a);
+                        a = fmaf((float)da[g][3], qs.w, a);
+                        float bb = (float)db[g][0] * qs.x;
+                        bb = fmaf((float)db[g][1], qs.y, bb);
+                        bb = fmaf((float)db[g][2], qs.z, bb);
+                        bb = fmaf((float)db[g][3], qs.w, bb);
+                        sa[g] = va ? a * ksa * p.sm_scale_log2 : -INFINITY;
+                        sb[g] = vb ? bb * ksb * p.sm_scale_log2 : -INFINITY;
+                    }
+                    // The running maximum M is raised only when a score exceeds it by
+                    // more than 2^kLazyLog2; below that the weights 2^(s-M) stay < 2^8
+                    // and every quantity remains exact to fp32 rounding.
+                    bool grow = false;
+#pragma unroll
+                    for (int g = 0; g < G; ++g) grow |= fmaxf(sa[g], sb[g]) > M[g] + kLazyLog2;
+                    float alpha[G];
+                    bool rescale = (e != e_cur);
+                    if (__any_sync(0xffffffffu, grow)) {
+                        rescale = true;
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            const float m_new = fmaxf(M[g], redux_max_f32(fmaxf(sa[g], sb[g])));
+                            alpha[g] = exp2f(M[g] - m_new);   // 0 while M is -inf
+                            M[g] = m_new;
                         }
-                        if (vb) {
-                            float a = (float)db[g][0] * qs.x;
-                            a = fmaf((float)db[g][1], qs.y, a);
-                            a = fmaf((float)db[g][2], qs.z, a);
-                            a = fmaf((float)db[g][3], qs.w, a);
-                            sb = a * ksb * p.sm_scale_log2;
-                        }
-                        const float m_new = fmaxf(M[g], warp_max(fmaxf(sa, sb)));  // finite: token 0 valid
-                        alpha[g] = exp2f(M[g] - m_new);
-                        rescale |= (m_new != M[g]);
-                        M[g] = m_new;
-                        const float wa = va ? exp2f(sa - m_new) : 0.0f;
-                        const float wb = vb ? exp2f(sb - m_new) : 0.0f;
+                    } else {
+#pragma unroll
+                        for (int g = 0; g < G; ++g) alpha[g] = 1.0f;
+                    }
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const float wa = va ? exp2f(sa[g] - M[g]) : 0.0f;
+                        const float wb = vb ? exp2f(sb[g] - M[g]) : 0.0f;
                         Sl[g] = fmaf(Sl[g], alpha[g], wa + wb);
                         const float pa = wa * vsa * inv, pb = wb * vsb * inv;
                         const __half ha = __float2half_rn(pa), hb = __float2half_rn(pb);
