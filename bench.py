@@ -2,11 +2,13 @@
 """Benchmark of the q8-KV decode step on GB300.
 
 One step = the whole hot path over one batch: quantise-append of the step's
-new K/V token for every (layer, kv head), then split-KV decode attention of
-every query head over its paged int8 context, then the split merge.  The
-default workload is the 28-layer Qwen3-2B-shaped decode stack (16 query / 8
-kv heads, hd 128, context 8192, batch 1), its layers folded into the batch
-dimension of one call.
+new K/V token for every (layer, kv head), split-KV decode attention of every
+query head over its paged int8 context, and the split merge: one
+kvq8_decode_step call (three launches, each overlapping the previous one's
+tail through programmatic dependent launch; the same three kernels called one
+by one through their own entry points are timed beside it as `unfused`).  The default workload is the 28-layer
+Qwen3-2B-shaped decode stack (16 query / 8 kv heads, hd 128, context 8192,
+batch 1), its layers folded into the batch dimension of one call.
 
 Prints one JSON line.  `value` is achieved algorithmic HBM throughput in GB/s
 (bytes a step must move / device time per step) summed over ranks;
@@ -182,7 +184,8 @@ def step_bytes(cfg, lens):
 
 
 def split_kernel_bytes(cfg, lens):
-    """Algorithmic bytes the split kernel moves: int8 K/V + scales + fp32 queries."""
+    """Algorithmic bytes the split kernel moves: int8 K/V + two fp32 scales per
+    (token, kv head), and the fp32 queries."""
     import numpy as np
     tok = int(np.asarray(lens, np.int64).sum())
     return tok * cfg.nkv * (2 * cfg.hd + 8) + cfg.batch * cfg.nqh * cfg.hd * 4
@@ -327,14 +330,28 @@ def run_kvq8(args, rank, world, local):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    nk1, nv1 = nk_d[:, 0], nv_d[:, 0]   # the step's token, [batch][nkv][hd]
+
     def step(i, ev=None):
         c = caches[i % copies]
-        kvq8.quantize_append(nk_d, nv_d, start_d, table_d, c, dev_status=status, stream=stream)
-        if ev is not None:
+        if ev is None:
+            kvq8.decode_step(q_d, nk1, nv1, c, table_d, lens_d, out, ws, sm_scale=sm,
+                             dev_status=status, stream=stream)
+        else:
+            # the same three kernels through their own entry points, with events
+            # around the split kernel (the roofline's dominant kernel)
+            kvq8.quantize_append(nk_d, nv_d, start_d, table_d, c, dev_status=status, stream=stream)
             ev[0].record(stream)
-        kvq8.decode_split(q_d, c, table_d, lens_d, ws, sm_scale=sm, dev_status=status, stream=stream)
-        if ev is not None:
+            kvq8.decode_split(q_d, c, table_d, lens_d, ws, sm_scale=sm, dev_status=status,
+                              stream=stream)
             ev[1].record(stream)
+            kvq8.decode_combine(cfg.batch, cfg.nqh, cfg.nkv, max_blocks, lens_d, ws, out,
+                                stream=stream)
+
+    def unfused_step(i):
+        c = caches[i % copies]
+        kvq8.quantize_append(nk_d, nv_d, start_d, table_d, c, dev_status=status, stream=stream)
+        kvq8.decode_split(q_d, c, table_d, lens_d, ws, sm_scale=sm, dev_status=status, stream=stream)
         kvq8.decode_combine(cfg.batch, cfg.nqh, cfg.nkv, max_blocks, lens_d, ws, out, stream=stream)
 
     for i in range(args.warmup):
@@ -343,9 +360,12 @@ def run_kvq8(args, rank, world, local):
     if status.item() != 0:
         raise RuntimeError(f"device status {status.item():#x} during warm-up")
 
-    # device-timed region: K steps, per-step events around the split kernel
+    # device-timed region: K steps; every k_sample-th step runs as three calls
+    # with events around the split kernel for its roofline (a recorded event
+    # costs the stream about a microsecond, so not every step carries them)
+    k_sample = 10
     split_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(args.steps)]
+                for _ in range(0, args.steps, k_sample)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     barrier()
@@ -353,14 +373,27 @@ def run_kvq8(args, rank, world, local):
     sampler.start()
     t_start.record(stream)
     for i in range(args.steps):
-        step(i, split_ev[i])
+        step(i, split_ev[i // k_sample] if i % k_sample == 0 else None)
     t_end.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
     barrier()
     elapsed = t_start.elapsed_time(t_end) / 1e3
-    split_s = sum(a.elapsed_time(b) for a, b in split_ev) / 1e3 / args.steps
+    split_s = sum(a.elapsed_time(b) for a, b in split_ev) / 1e3 / len(split_ev)
     launches = 3 * args.steps
+
+    # the same step as three launches (append, split, combine), for comparison
+    n_unf = min(args.steps, 1000)
+    for i in range(3):
+        unfused_step(i)
+    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    u0.record(stream)
+    for i in range(n_unf):
+        unfused_step(i)
+    u1.record(stream)
+    torch.cuda.synchronize()
+    unfused_us = u0.elapsed_time(u1) * 1e3 / n_unf
 
     sbytes = step_bytes(cfg, lens)
     total_bytes, slowest = aggregate(sbytes * args.steps, elapsed, dev)
@@ -378,8 +411,7 @@ def run_kvq8(args, rank, world, local):
         q_d.copy_(q_h, non_blocking=True)
         nk_d.copy_(nk_h, non_blocking=True)
         nv_d.copy_(nv_h, non_blocking=True)
-        kvq8.quantize_append(nk_d, nv_d, start_d, table_d, c, stream=stream)
-        kvq8.decode_attn(q_d, c, table_d, lens_d, out, ws, sm_scale=sm, stream=stream)
+        kvq8.decode_step(q_d, nk1, nv1, c, table_d, lens_d, out, ws, sm_scale=sm, stream=stream)
         out_h.copy_(out, non_blocking=True)
         stream.synchronize()
 
@@ -411,7 +443,8 @@ def run_kvq8(args, rank, world, local):
                        bytes_per_step=sbytes,
                        arithmetic="int8 x int8 -> int32 block dots, fp32 softmax and accumulation"),
         "pct_of_hbm_peak": round(100 * (value / world) / peak, 2),
-        "roofline": {"bound": "hbm", "kernel": "decode_split", "achieved": round(achieved, 2),
+        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel",
+                     "achieved": round(achieved, 2),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": peak_kind, "traffic": traffic,
                      "algorithmic_bytes_per_launch": split_bytes,
@@ -420,6 +453,8 @@ def run_kvq8(args, rank, world, local):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "us_per_step": round(e_slowest / e2e_steps * 1e6, 2), "steps": e2e_steps},
         "gpu_launches": launches,
+        "unfused": {"us_per_step": round(unfused_us, 2), "launches_per_step": 3, "calls_per_step": 3,
+                    "path": "kvq8_quantize_append + kvq8_decode_split + kvq8_decode_combine"},
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

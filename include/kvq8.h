@@ -203,6 +203,30 @@ kvq8_status kvq8_decode_combine(int batch, int nqh, int nkv, int hd,
                                 const void *workspace, size_t workspace_bytes,
                                 float *out, void *stream);
 
+/*
+ * kvq8_decode_step -- one decode step in one call: append the step's new
+ * token of every sequence at position ctx_lens[b] - 1 and attend over the
+ * context including it.  Same results as kvq8_quantize_append (n_new = 1,
+ * start_pos[b] = ctx_lens[b] - 1) followed by kvq8_decode_attn; the three
+ * kernels are launched back to back, each as a programmatic dependent of the
+ * previous one so that their launches overlap.
+ *
+ *   k_new, v_new  fp32 [batch][nkv][hd]: the step's token ([Day 9-3] §2 rule)
+ *                 (sequences with ctx_lens[b] == 0 append nothing and yield 0;
+ *                 a ctx_lens[b] beyond the table is flagged, clamped, and
+ *                 appends nothing)
+ *   pools         written at the new token's slot only
+ * Other arguments, workspace included, as kvq8_decode_attn.
+ */
+kvq8_status kvq8_decode_step(const float *q, const float *k_new, const float *v_new,
+                             int batch, int nqh, int nkv, int hd,
+                             int8_t *k_pool, int8_t *v_pool, float *k_scale, float *v_scale,
+                             int num_blocks, const int32_t *block_table,
+                             int max_blocks, int block_size,
+                             const int32_t *ctx_lens, float sm_scale, float *out,
+                             void *workspace, size_t workspace_bytes,
+                             uint32_t *dev_status, void *stream);
+
 /* ------------------------------------------- decode without allocation --- */
 
 /* Size of the static device scratch kvq8_decode_attn_noalloc uses (16 MiB). */

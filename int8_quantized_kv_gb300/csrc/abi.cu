@@ -143,6 +143,7 @@ kvq8_status kvq8_quantize_append(const float *k_new, const float *v_new, int bat
     p.k_scale = k_scale;
     p.v_scale = v_scale;
     p.dev_status = dev_status;
+    p.ctx_lens = nullptr;
     if (launch_quantize_append(p, (cudaStream_t)stream) != cudaSuccess) return KVQ8_ERR_CUDA;
     return KVQ8_OK;
 }
@@ -231,6 +232,47 @@ kvq8_status kvq8_decode_attn(const float *q, int batch, int nqh, int nkv, int hd
     if (st != KVQ8_OK) return st;
     p.out = out;
     cudaStream_t s = (cudaStream_t)stream;
+    if (launch_decode_split(p, plan.group, s) != cudaSuccess) return KVQ8_ERR_CUDA;
+    if (launch_decode_combine(p, plan.group, s) != cudaSuccess) return KVQ8_ERR_CUDA;
+    return KVQ8_OK;
+}
+
+kvq8_status kvq8_decode_step(const float *q, const float *k_new, const float *v_new, int batch,
+                             int nqh, int nkv, int hd, int8_t *k_pool, int8_t *v_pool,
+                             float *k_scale, float *v_scale, int num_blocks,
+                             const int32_t *block_table, int max_blocks, int block_size,
+                             const int32_t *ctx_lens, float sm_scale, float *out, void *workspace,
+                             size_t workspace_bytes, uint32_t *dev_status, void *stream) {
+    kvq8_status st = check_decode_args(q, batch, nqh, nkv, hd, k_pool, v_pool, k_scale, v_scale,
+                                       num_blocks, block_table, max_blocks, block_size, ctx_lens);
+    if (st != KVQ8_OK || batch == 0) return st;
+    if (!out || !aligned(out, 16) || !isfinite(sm_scale)) return KVQ8_ERR_INVALID_ARG;
+    if (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)) return KVQ8_ERR_INVALID_ARG;
+    DecodeParams p;
+    DecodePlan plan;
+    st = fill_decode_params(q, batch, nqh, nkv, k_pool, v_pool, k_scale, v_scale, num_blocks,
+                            block_table, max_blocks, ctx_lens, sm_scale, workspace,
+                            workspace_bytes, dev_status, &p, &plan);
+    if (st != KVQ8_OK) return st;
+    p.out = out;
+    AppendParams a;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.batch = batch;
+    a.n_new = 1;
+    a.nkv = nkv;
+    a.start_pos = nullptr;   // the new token goes to ctx_lens[b] - 1
+    a.ctx_lens = ctx_lens;
+    a.block_table = block_table;
+    a.max_blocks = max_blocks;
+    a.num_blocks = num_blocks;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.dev_status = dev_status;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (launch_quantize_append(a, s) != cudaSuccess) return KVQ8_ERR_CUDA;
     if (launch_decode_split(p, plan.group, s) != cudaSuccess) return KVQ8_ERR_CUDA;
     if (launch_decode_combine(p, plan.group, s) != cudaSuccess) return KVQ8_ERR_CUDA;
     return KVQ8_OK;

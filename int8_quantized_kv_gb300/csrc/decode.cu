@@ -21,10 +21,11 @@
 //    (K 8 KiB, V 8 KiB, two 256 B scale runs) into a ring of shared-memory
 //    slots, tracked by full/empty mbarriers.  The KV stream uses an L2
 //    evict-first policy: it is read exactly once.
-//  * Warps 0..6 take the stages of a segment from a shared counter, in order,
-//    each with its own online-softmax state (two warps per SM sub-partition
-//    leave room for 255 registers a thread).  Q.K: lane = token (two tokens per lane), dp4a on int8 codes,
-//    exact int32 per 32-block.  P.V: tensor-core MMA m16n8k16 with
+//  * Warps 0..6 take the stages of a segment round-robin (a fixed assignment,
+//    so results are reproducible bit for bit), each with its own
+//    online-softmax state (two warps per SM sub-partition leave room for 255
+//    registers a thread).  Q.K: lane = token (two tokens per lane), dp4a on
+//    int8 codes, exact int32 per 32-block.  P.V: tensor-core MMA m16n8k16 with
 //    A = V (int8 codes -> fp16, exact) and B = P, the weights times the V
 //    scale, split into fp16 high + low parts (two MMAs) and scaled per stage
 //    by a power of two so that fp16 range and precision lose nothing that
@@ -32,7 +33,9 @@
 //  * At the end of a segment the 7 warp states are merged in shared memory
 //    and written as one record per query head.
 // All waits are bounded: a wait that times out sets KVQ8_DEV_TIMEOUT and the
-// CTA unwinds without leaving copies in flight.
+// CTA unwinds without leaving copies in flight.  The kernel is launched as a
+// programmatic dependent of the previous kernel in its stream, so its launch
+// overlaps that kernel; it waits for that kernel's results before reading.
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -80,7 +83,6 @@ struct Misc {
     long long warp_tot[kSplitThreads / 32];
     long long base;   // stage prefix at the first unit of sequence b0
     int b0;
-    int next;         // next segment-local stage to hand out to a consumer warp
 };
 
 __device__ __forceinline__ int clamp_len(int L, int cap) { return max(0, min(L, cap)); }
@@ -132,6 +134,9 @@ decode_split_kernel(DecodeParams p) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
     const int cap = p.max_blocks * kBS;
+    // launched as a programmatic dependent of the previous kernel in the stream
+    // (the step's append): its results are visible after this wait
+    pdl_wait();
     Misc *misc = reinterpret_cast<Misc *>(smem + Lay::oMisc);
     int8_t *q_codes = reinterpret_cast<int8_t *>(smem + Lay::oQCodes);
     float *q_scale = reinterpret_cast<float *>(smem + Lay::oQScale);
@@ -294,7 +299,6 @@ decode_split_kernel(DecodeParams p) {
 
             // segment 1: quantise this unit's G query heads once
             named_barrier_sync(1, kConsumerWarps * 32);
-            if (tid == 0) misc->next = 0;
             for (int g = warp; g < G; g += kConsumerWarps)
                 quantize_q_row_warp(p.q + ((size_t)b * p.nqh + (size_t)h * G + g) * kHD, lane,
                                     q_codes + g * kHD, q_scale + g * kNQB);
@@ -309,11 +313,7 @@ decode_split_kernel(DecodeParams p) {
                 for (int i = 0; i < 4; ++i) acc[mt][i] = 0.0f;
             int e_cur = 1000;  // acc holds values in units of 2^e_cur (first stage sets it)
 
-            for (;;) {
-                int j = 0;
-                if (lane == 0) j = atomicAdd(&misc->next, 1);
-                j = __shfl_sync(0xffffffffu, j, 0);
-                if (j >= seg_n) break;
+            for (int j = warp; j < seg_n; j += kConsumerWarps) {
                 const int k = kbase + j, slot = k % Lay::kStages, round = k / Lay::kStages;
                 const uint32_t par = round & 1;
                 if (!aborted && !slot_turn_bounded(done + slot, round, kWaitTimeoutNs)) aborted = true;
@@ -575,9 +575,17 @@ cudaError_t launch_split_g(const DecodeParams &p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    const int grid = min(sms, kMaxCtas);
-    decode_split_kernel<G><<<grid, kSplitThreads, Lay::kBytes, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(min(sms, kMaxCtas));
+    cfg.blockDim = dim3(kSplitThreads);
+    cfg.dynamicSmemBytes = Lay::kBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_split_kernel<G>, p);
 }
 
 }  // namespace

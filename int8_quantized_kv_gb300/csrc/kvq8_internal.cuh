@@ -19,7 +19,8 @@ constexpr int kMaxGridYZ = 65535;  // launch limit on gridDim.y / gridDim.z
 struct AppendParams {
     const float *k_new, *v_new;   // [batch][n_new][nkv][hd]
     int batch, n_new, nkv;
-    const int32_t *start_pos;     // [batch]
+    const int32_t *start_pos;     // [batch]; null: position ctx_lens[b] - 1 (decode step)
+    const int32_t *ctx_lens;      // decode step only: [batch]
     const int32_t *block_table;   // [batch][max_blocks]
     int max_blocks, num_blocks;
     int8_t *k_pool, *v_pool;

@@ -44,6 +44,8 @@ SIGNATURES = {
     "kvq8_decode_split": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _I,
                                _P, _F, _P, _SZ, _P, _P]),
     "kvq8_decode_combine": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
+    "kvq8_decode_step": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _I,
+                              _P, _F, _P, _P, _SZ, _P, _P]),
     "kvq8_decode_attn_noalloc": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _I,
                                       _P, _F, _P, _P, _P]),
 }
@@ -209,6 +211,22 @@ def decode_attn(q, cache: KVCache, block_table, ctx_lens, out, workspace,
         max_blocks, BLOCK_SIZE, _ptr(ctx_lens), sm, _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream))
     _check("kvq8_decode_attn", st)
+
+
+def decode_step(q, k_new, v_new, cache: KVCache, block_table, ctx_lens, out, workspace,
+                sm_scale: Optional[float] = None, dev_status=None, stream=None):
+    """One decode step: append k_new/v_new (fp32 [batch][nkv][128]) at position
+    ctx_lens-1 and attend over ctx_lens tokens (two launches)."""
+    _need_cuda(q, k_new, v_new, block_table, ctx_lens, out, workspace, *cache, dev_status)
+    batch, nqh, nkv, hd, max_blocks = _decode_common(q, cache, block_table, ctx_lens)
+    sm = 1.0 / math.sqrt(hd) if sm_scale is None else sm_scale
+    st = load().kvq8_decode_step(
+        _ptr(q), _ptr(k_new), _ptr(v_new), batch, nqh, nkv, hd, _ptr(cache.k_pool),
+        _ptr(cache.v_pool), _ptr(cache.k_scale), _ptr(cache.v_scale), cache.num_blocks,
+        _ptr(block_table), max_blocks, BLOCK_SIZE, _ptr(ctx_lens), sm, _ptr(out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status),
+        _stream(stream))
+    _check("kvq8_decode_step", st)
 
 
 def decode_split(q, cache: KVCache, block_table, ctx_lens, workspace,

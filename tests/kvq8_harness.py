@@ -123,3 +123,41 @@ class Case:
         k, v = wl.unit_kv(cfg, b, h, L)
         out, _ = oracle.decode_unit_q8(self.q[b, h * G:(h + 1) * G], k, v, sm_scale)
         return out
+
+
+class StepCase(Case):
+    """The cache holds the first L-1 tokens of every sequence; a decode step
+    appends token L-1 (k_new, v_new) and attends over all L."""
+
+    def __init__(self, cfg: wl.Workload, lens=None, device="cuda", spare_blocks=3):
+        self._full = {}
+        super().__init__(cfg, lens=lens, device=device, spare_blocks=spare_blocks)
+        kn = np.zeros((cfg.batch, cfg.nkv, cfg.hd), np.float32)
+        vn = np.zeros_like(kn)
+        for b in range(cfg.batch):
+            if b in self._full:
+                kn[b], vn[b] = self._full[b][0][-1], self._full[b][1][-1]
+        self.k_new, self.v_new = kn, vn
+        self.k_new_d = torch.from_numpy(kn).to(device)
+        self.v_new_d = torch.from_numpy(vn).to(device)
+
+    def append_sequence(self, b, chunk=None):
+        L = int(self.lens[b])
+        if L == 0:
+            return
+        k, v = wl.seq_kv(self.cfg, b, L)
+        self._full[b] = (k, v)
+        if L > 1:
+            kvq8.quantize_append(torch.from_numpy(k[None, :L - 1]).to(self.device),
+                                 torch.from_numpy(v[None, :L - 1]).to(self.device),
+                                 torch.zeros(1, dtype=torch.int32, device=self.device),
+                                 self.table_d[b:b + 1], self.cache, dev_status=self.status)
+
+    def step(self, workspace=None, sm_scale=SM_SCALE):
+        out = torch.full_like(self.q_d, float("nan"))
+        ws = workspace if workspace is not None else kvq8.alloc_workspace(
+            self.cfg.batch, self.cfg.nqh, self.cfg.nkv, self.max_blocks, self.device)
+        kvq8.decode_step(self.q_d, self.k_new_d, self.v_new_d, self.cache, self.table_d,
+                         self.lens_d, out, ws, sm_scale=sm_scale, dev_status=self.status)
+        torch.cuda.synchronize()
+        return out.cpu().numpy()

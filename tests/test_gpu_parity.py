@@ -314,3 +314,95 @@ def test_specified_workloads_full_size_sampled(gpu_lib, cfg):
     ovq, ovs = oracle.kv_quantize_rows(v)
     assert np.array_equal(kq, okq) and np.array_equal(vq, ovq)
     assert np.array_equal(ks, oks) and np.array_equal(vs, ovs)
+
+
+# ------------------------------------------------------ fused decode step ---
+from kvq8_harness import StepCase  # noqa: E402
+
+
+def _check_step(case, out):
+    cfg = case.cfg
+    G = cfg.group
+    pools = case.host_pools()
+    for b in range(cfg.batch):
+        L = int(case.lens[b])
+        if L == 0:
+            assert not out[b].any()
+            continue
+        for h in range(cfg.nkv):
+            assert_close(out[b, h * G:(h + 1) * G], case.oracle_unit(b, h), f"step b={b} h={h} L={L}")
+            kq, ks, vq, vs = case.gather_unit(pools, b, h)       # the appended token is bit-exact
+            okq, oks = oracle.kv_quantize_rows(case.k_new[b, h][None])
+            ovq, ovs = oracle.kv_quantize_rows(case.v_new[b, h][None])
+            assert np.array_equal(kq[L - 1], okq[0]) and np.array_equal(vq[L - 1], ovq[0])
+            assert ks[L - 1] == oks[0] and vs[L - 1] == ovs[0]
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_decode_step_group_sizes(gpu_lib, G):
+    cfg = _unit_cfg(G, nkv=2, batch=4, ctx_range=(1, 1500), cid=400 + G)
+    lens = wl.ctx_lens(cfg).copy()
+    lens[0] = 1                                    # the new token is the whole context
+    case = StepCase(cfg, lens=lens)
+    out = case.step()
+    _check_step(case, out)
+    assert case.status_bits() == 0
+
+
+@pytest.mark.parametrize("L", [1, 2, 63, 64, 65, 255, 256, 257, 4097])
+def test_decode_step_token_positions(gpu_lib, L):
+    cfg = _unit_cfg(2, nkv=1, batch=1, ctx=L, cid=410)
+    case = StepCase(cfg)
+    _check_step(case, case.step())
+
+
+def test_decode_step_empty_sequences_and_ragged_batch(gpu_lib):
+    cfg = _unit_cfg(4, nkv=2, batch=5, ctx_range=(1, 900), cid=420)
+    lens = np.array([0, 700, 0, 1, 333], np.int32)
+    case = StepCase(cfg, lens=lens)
+    _check_step(case, case.step())
+
+
+def test_decode_step_unit_over_many_ctas(gpu_lib):
+    # one long unit spread over most CTAs: the last CTA to finish merges them all
+    cfg = _unit_cfg(8, nkv=1, batch=1, ctx=30001, cid=430)
+    case = StepCase(cfg)
+    _check_step(case, case.step())
+
+
+def test_decode_step_twice_on_one_workspace(gpu_lib):
+    cfg = wl.scaled(wl.QWEN3_2B_28L_8K, batch=6, ctx=2500)
+    case = StepCase(cfg)
+    ws = kvq8.alloc_workspace(cfg.batch, cfg.nqh, cfg.nkv, case.max_blocks)
+    first = case.step(ws)
+    second = case.step(ws)          # appending the same token again: identical results
+    assert np.array_equal(first, second)
+    _check_step(case, second)
+
+
+def test_decode_step_equals_append_then_decode(gpu_lib):
+    cfg = wl.scaled(wl.BATCH64_RAGGED, batch=5, ctx_range=(512, 3000))
+    a = StepCase(cfg)
+    fused = a.step()
+    b = StepCase(cfg)
+    start = torch.from_numpy((b.lens - 1).astype(np.int32)).cuda()
+    kvq8.quantize_append(b.k_new_d[:, None], b.v_new_d[:, None], start, b.table_d, b.cache)
+    two_call = b.decode()
+    assert_close(fused, two_call, "fused step vs append + decode_attn")
+    pa, pb = a.host_pools(), b.host_pools()
+    for bb in range(cfg.batch):
+        for h in range(cfg.nkv):
+            for x, y in zip(a.gather_unit(pa, bb, h), b.gather_unit(pb, bb, h)):
+                assert np.array_equal(x, y)
+
+
+@pytest.mark.slow
+def test_decode_step_full_size_qwen3_2b(gpu_lib):
+    cfg = wl.QWEN3_2B_28L_8K
+    case = StepCase(cfg, spare_blocks=0)
+    out = case.step()
+    rng = np.random.default_rng(5)
+    G = cfg.group
+    for b, h in {(int(rng.integers(cfg.batch)), int(rng.integers(cfg.nkv))) for _ in range(5)}:
+        assert_close(out[b, h * G:(h + 1) * G], case.oracle_unit(b, h), f"full step b={b} h={h}")
+    assert case.status_bits() == 0
