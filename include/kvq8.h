@@ -227,6 +227,53 @@ kvq8_status kvq8_decode_step(const float *q, const float *k_new, const float *v_
                              void *workspace, size_t workspace_bytes,
                              uint32_t *dev_status, void *stream);
 
+/* -------------------------------------------- 4-bit cache (NEXT row) --- */
+
+/*
+ * The asymmetric INT4 group-64 cache of [UltraQuant] §3.2 ("方差均衡化分组量化的
+ * 具体实现", its code): per group of 64 consecutive values of a (token, kv head)
+ * row, scale = (max - min)/15 (1 when max == min), zero = round_half_even
+ * (-min/scale) kept in fp32 (not clamped), code = clamp(round_half_even(x/scale
+ * + zero), 0, 15), two codes per byte with the even element in the high
+ * nibble; value = (code - zero) * scale.  The page's variance-dependent scale
+ * tweak is marked there as an example, not the formula, and is not applied.
+ *
+ * Layout per (block, kv head) tile of 256 tokens:
+ *   k_codes, v_codes uint8 [num_blocks][nkv][256][hd/2]   token-major
+ *   k_param, v_param fp32  [num_blocks][nkv][256][4]      (scale0, zero0, scale1, zero1)
+ * 160 bytes per (token, kv head): 1280 bytes per token per layer for nkv = 8.
+ */
+size_t kvq4_code_pool_bytes(int num_blocks, int nkv, int hd, int block_size);
+size_t kvq4_param_pool_bytes(int num_blocks, int nkv, int block_size);
+size_t kvq4_cache_bytes_per_token(int nkv, int hd);
+
+/* kvq4_quantize_append -- as kvq8_quantize_append, into the 4-bit cache. */
+kvq8_status kvq4_quantize_append(const float *k_new, const float *v_new,
+                                 int batch, int n_new, int nkv, int hd,
+                                 const int32_t *start_pos,
+                                 const int32_t *block_table, int max_blocks,
+                                 int block_size, int num_blocks,
+                                 uint8_t *k_codes, uint8_t *v_codes,
+                                 float *k_param, float *v_param,
+                                 uint32_t *dev_status, void *stream);
+
+/*
+ * kvq4_decode_attn -- decode attention of the fp32 query over the dequantised
+ * 4-bit cache ([UltraQuant] §4.1 / §5.3: dequantise, then standard attention):
+ * s_t = sm_scale * q . dequant(k_t), softmax with a running maximum, fp32
+ * accumulation of dequant(v_t), split over the context and merged as in
+ * kvq8_decode_attn.  Workspace: kvq8_decode_workspace_bytes(...) for the same
+ * sizes.  Other arguments as kvq8_decode_attn.
+ */
+kvq8_status kvq4_decode_attn(const float *q, int batch, int nqh, int nkv, int hd,
+                             const uint8_t *k_codes, const uint8_t *v_codes,
+                             const float *k_param, const float *v_param,
+                             int num_blocks, const int32_t *block_table,
+                             int max_blocks, int block_size,
+                             const int32_t *ctx_lens, float sm_scale,
+                             float *out, void *workspace, size_t workspace_bytes,
+                             uint32_t *dev_status, void *stream);
+
 /* ------------------------------------------- decode without allocation --- */
 
 /* Size of the static device scratch kvq8_decode_attn_noalloc uses (16 MiB). */

@@ -78,4 +78,35 @@ struct DecodeParams {
 cudaError_t launch_decode_split(const DecodeParams &p, int group, cudaStream_t s);
 cudaError_t launch_decode_combine(const DecodeParams &p, int group, cudaStream_t s);
 
+// ------------------------------------------------------------ INT4 cache --
+struct Int4AppendParams {
+    const float *k_new, *v_new;   // [batch][n_new][nkv][hd]
+    int batch, n_new, nkv;
+    const int32_t *start_pos;     // [batch]
+    const int32_t *block_table;
+    int max_blocks, num_blocks;
+    uint8_t *k_codes, *v_codes;   // [num_blocks][nkv][256][64]
+    float *k_param, *v_param;     // [num_blocks][nkv][256][4]
+    uint32_t *dev_status;
+};
+
+struct Int4DecodeParams {
+    const float *q;               // [batch][nqh][hd]
+    int batch, nqh, nkv;
+    const uint8_t *k_codes, *v_codes;
+    const float *k_param, *v_param;
+    int num_blocks;
+    const int32_t *block_table;
+    int max_blocks;
+    const int32_t *ctx_lens;
+    float sm_scale_log2;
+    int nsplit, split_tokens;     // unit u's split j writes record u*nsplit + j
+    int2 *ws_meta;
+    float *ws_ml, *ws_acc;        // same record format as DecodeParams
+    uint32_t *dev_status;
+};
+bool make_int4_plan(int batch, int nkv, int max_blocks, int *nsplit, int *split_tokens);
+cudaError_t launch_int4_append(const Int4AppendParams &p, cudaStream_t s);
+cudaError_t launch_int4_decode_split(const Int4DecodeParams &p, int group, cudaStream_t s);
+
 }  // namespace kvq8

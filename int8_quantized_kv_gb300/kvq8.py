@@ -46,6 +46,13 @@ SIGNATURES = {
     "kvq8_decode_combine": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
     "kvq8_decode_step": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _I,
                               _P, _F, _P, _P, _SZ, _P, _P]),
+    "kvq4_code_pool_bytes": (_SZ, [_I, _I, _I, _I]),
+    "kvq4_param_pool_bytes": (_SZ, [_I, _I, _I]),
+    "kvq4_cache_bytes_per_token": (_SZ, [_I, _I]),
+    "kvq4_quantize_append": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _I, _I, _I,
+                                  _P, _P, _P, _P, _P, _P]),
+    "kvq4_decode_attn": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _I,
+                              _P, _F, _P, _P, _SZ, _P, _P]),
     "kvq8_decode_attn_noalloc": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _I,
                                       _P, _F, _P, _P, _P]),
 }
@@ -265,3 +272,62 @@ def decode_attn_noalloc(q, cache: KVCache, block_table, ctx_lens, out,
         max_blocks, BLOCK_SIZE, _ptr(ctx_lens), sm, _ptr(out), _ptr(dev_status),
         _stream(stream))
     _check("kvq8_decode_attn_noalloc", st)
+
+
+# ------------------------------------------------------------ 4-bit cache ---
+class KV4Cache(NamedTuple):
+    """The asymmetric INT4 group-64 cache (layout in include/kvq8.h)."""
+    k_codes: object  # uint8 [num_blocks][nkv][256][64]
+    v_codes: object  # uint8 [num_blocks][nkv][256][64]
+    k_param: object  # fp32 [num_blocks][nkv][256][4]  (scale0, zero0, scale1, zero1)
+    v_param: object  # fp32 [num_blocks][nkv][256][4]
+
+    @property
+    def num_blocks(self) -> int:
+        return self.k_codes.shape[0]
+
+    @property
+    def nkv(self) -> int:
+        return self.k_codes.shape[1]
+
+
+def cache4_bytes_per_token(nkv: int, hd: int = HEAD_DIM) -> int:
+    return int(load().kvq4_cache_bytes_per_token(nkv, hd))
+
+
+def alloc_cache4(num_blocks: int, nkv: int, device="cuda") -> KV4Cache:
+    import torch
+    lib = load()
+    assert lib.kvq4_code_pool_bytes(num_blocks, nkv, HEAD_DIM, BLOCK_SIZE) == num_blocks * nkv * BLOCK_SIZE * 64
+    kc = torch.empty((num_blocks, nkv, BLOCK_SIZE, HEAD_DIM // 2), dtype=torch.uint8, device=device)
+    vc = torch.empty_like(kc)
+    kp = torch.empty((num_blocks, nkv, BLOCK_SIZE, 4), dtype=torch.float32, device=device)
+    vp = torch.empty_like(kp)
+    return KV4Cache(kc, vc, kp, vp)
+
+
+def quantize_append4(k_new, v_new, start_pos, block_table, cache: KV4Cache, dev_status=None,
+                     stream=None):
+    """k_new, v_new: fp32 [batch][n_new][nkv][128] into the 4-bit cache."""
+    _need_cuda(k_new, v_new, start_pos, block_table, *cache, dev_status)
+    batch, n_new, nkv, hd = k_new.shape
+    st = load().kvq4_quantize_append(
+        _ptr(k_new), _ptr(v_new), batch, n_new, nkv, hd, _ptr(start_pos), _ptr(block_table),
+        block_table.shape[1], BLOCK_SIZE, cache.num_blocks, _ptr(cache.k_codes),
+        _ptr(cache.v_codes), _ptr(cache.k_param), _ptr(cache.v_param), _ptr(dev_status),
+        _stream(stream))
+    _check("kvq4_quantize_append", st)
+
+
+def decode_attn4(q, cache: KV4Cache, block_table, ctx_lens, out, workspace,
+                 sm_scale: Optional[float] = None, dev_status=None, stream=None):
+    """fp32 q [batch][nqh][128] over the 4-bit cache -> out fp32 [batch][nqh][128]."""
+    _need_cuda(q, block_table, ctx_lens, out, workspace, *cache, dev_status)
+    batch, nqh, hd = q.shape
+    sm = 1.0 / math.sqrt(hd) if sm_scale is None else sm_scale
+    st = load().kvq4_decode_attn(
+        _ptr(q), batch, nqh, cache.nkv, hd, _ptr(cache.k_codes), _ptr(cache.v_codes),
+        _ptr(cache.k_param), _ptr(cache.v_param), cache.num_blocks, _ptr(block_table),
+        block_table.shape[1], BLOCK_SIZE, _ptr(ctx_lens), sm, _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream))
+    _check("kvq4_decode_attn", st)

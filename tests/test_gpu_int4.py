@@ -1,0 +1,168 @@
+"""The 4-bit (asymmetric INT4 group-64) cache path against the oracle.
+
+Codes, scales and zeros must match the oracle's quantiser bit for bit; decode
+outputs (fp32 query over dequantised K/V) must be within 1e-4 + 1e-3*|ref|
+of fp64 attention over the oracle's dequantised K/V.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from int8_quantized_kv_gb300 import kvq8
+from int8_quantized_kv_gb300 import workloads as wl
+from kvq8_harness import SM_SCALE, assert_close
+
+pytestmark = pytest.mark.gpu
+HD = 128
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+class Int4Case:
+    def __init__(self, cfg, lens=None, spare_blocks=2):
+        self.cfg = cfg
+        self.lens = wl.ctx_lens(cfg) if lens is None else np.asarray(lens, np.int32)
+        self.table, self.num_blocks = wl.block_table(cfg, self.lens, spare_blocks=spare_blocks)
+        self.max_blocks = self.table.shape[1]
+        self.cache = kvq8.alloc_cache4(self.num_blocks, cfg.nkv)
+        self.table_d = torch.from_numpy(self.table).cuda()
+        self.lens_d = torch.from_numpy(self.lens).cuda()
+        self.q = wl.queries(cfg)
+        self.q_d = torch.from_numpy(self.q).cuda()
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        zero = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for b in range(cfg.batch):
+            L = int(self.lens[b])
+            if L:
+                k, v = wl.seq_kv(cfg, b, L)
+                kvq8.quantize_append4(torch.from_numpy(k[None]).cuda(), torch.from_numpy(v[None]).cuda(),
+                                      zero, self.table_d[b:b + 1], self.cache, dev_status=self.status)
+        torch.cuda.synchronize()
+
+    def decode(self):
+        out = torch.full_like(self.q_d, float("nan"))
+        ws = kvq8.alloc_workspace(self.cfg.batch, self.cfg.nqh, self.cfg.nkv, self.max_blocks)
+        kvq8.decode_attn4(self.q_d, self.cache, self.table_d, self.lens_d, out, ws, sm_scale=SM_SCALE,
+                          dev_status=self.status)
+        torch.cuda.synchronize()
+        return out.cpu().numpy()
+
+    def oracle_unit(self, b, h):
+        G = self.cfg.group
+        L = int(self.lens[b])
+        k, v = wl.unit_kv(self.cfg, b, h, L)
+        kd = oracle.int4_dequantize_groups(*oracle.int4_quantize_groups(k, 64), 64)
+        vd = oracle.int4_dequantize_groups(*oracle.int4_quantize_groups(v, 64), 64)
+        return np.stack([oracle.attention_f64(self.q[b, h * G + g], kd, vd, SM_SCALE) for g in range(G)])
+
+
+def _rows_with_fixtures(n, seed):
+    rng = np.random.default_rng(seed)
+    m = max(n, 4)
+    x = (rng.standard_normal((m, HD)) * rng.uniform(0.01, 30, (m, 1))).astype(np.float32)
+    g = json.load(open(os.path.join(GOLDEN, "int4_group64_hand_example.json")))
+    row = np.full(HD, g["row_fill_group0"], np.float32)
+    row[:len(g["row_head"])] = g["row_head"]
+    row[64:] = g["row_group1_constant"]
+    x[0] = row                                   # hand-worked example (one constant group)
+    x[1] = 0.0                                   # all-zero row: both groups constant
+    x[2, :64] = np.abs(x[2, :64]) + 1.0          # all-positive group: zero below 0
+    x[3, 64:] = -np.abs(x[3, 64:]) - 1.0         # all-negative group: zero above 15
+    return x[:n] if n >= 4 else np.roll(x, -(4 - n), axis=0)[:n]
+
+
+@pytest.mark.parametrize("start,n_new", [(0, 1), (5, 37), (250, 300)])
+def test_int4_append_bit_exact(gpu_lib, start, n_new):
+    nkv = 2
+    k = np.stack([_rows_with_fixtures(n_new * nkv, 11 + n_new).reshape(n_new, nkv, HD)])
+    v = np.stack([_rows_with_fixtures(n_new * nkv, 13 + n_new).reshape(n_new, nkv, HD)])
+    need = (start + n_new + 255) // 256
+    table = np.random.default_rng(3).permutation(need + 2)[:need].astype(np.int32)[None]
+    cache = kvq8.alloc_cache4(need + 2, nkv)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvq8.quantize_append4(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(),
+                          torch.tensor([start], dtype=torch.int32, device="cuda"),
+                          torch.from_numpy(table).cuda(), cache, dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    kc, vc = cache.k_codes.cpu().numpy(), cache.v_codes.cpu().numpy()
+    kp, vp = cache.k_param.cpu().numpy(), cache.v_param.cpu().numpy()
+    pos = start + np.arange(n_new)
+    phys, slot = table[0, pos // 256], pos % 256
+    for h in range(nkv):
+        for x, codes, par in ((k[0, :, h], kc, kp), (v[0, :, h], vc, vp)):
+            packed, sc, zr = oracle.int4_quantize_groups(x, 64)
+            assert np.array_equal(codes[phys, h, slot], packed)
+            got = par[phys, h, slot]
+            assert np.array_equal(got[:, [0, 2]].view(np.uint32), sc.view(np.uint32))
+            assert np.array_equal(got[:, [1, 3]].view(np.uint32), zr.view(np.uint32))
+
+
+def test_int4_byte_count(gpu_lib):
+    # 64 code bytes + 4 fp32 per (token, head) for K and V: 1280 B per token per layer at nkv = 8
+    assert kvq8.cache4_bytes_per_token(8) == 1280
+    c = kvq8.alloc_cache4(3, 8)
+    assert sum(t.numel() * t.element_size() for t in c) == 3 * 256 * 1280
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_int4_decode_group_sizes(gpu_lib, G):
+    cfg = wl.Workload(f"int4_g{G}", 500 + G, batch=3, nqh=2 * G, nkv=2, ctx_range=(1, 1400))
+    case = Int4Case(cfg)
+    out = case.decode()
+    for b in range(cfg.batch):
+        for h in range(cfg.nkv):
+            assert_close(out[b, h * G:(h + 1) * G], case.oracle_unit(b, h), f"int4 G={G} b={b} h={h}")
+    assert case.status.item() == 0
+
+
+@pytest.mark.parametrize("L", [1, 31, 32, 33, 257, 3000])
+def test_int4_decode_lengths(gpu_lib, L):
+    cfg = wl.Workload("int4_len", 510, batch=1, nqh=4, nkv=1, ctx=L)
+    case = Int4Case(cfg)
+    assert_close(case.decode()[0], case.oracle_unit(0, 0), f"int4 L={L}")
+
+
+def test_int4_decode_empty_and_bad_block(gpu_lib):
+    cfg = wl.Workload("int4_edge", 520, batch=3, nqh=4, nkv=2, ctx_range=(300, 900))
+    case = Int4Case(cfg, lens=np.array([0, 700, 600], np.int32))
+    out = case.decode()
+    assert not out[0].any()
+    case.table_d[2, 1] = case.num_blocks + 3          # block 1 of sequence 2 out of range
+    out = case.decode()
+    assert case.status.item() & kvq8.DEV_BAD_BLOCK_ID
+    G = cfg.group
+    for h in range(cfg.nkv):
+        assert_close(out[1, h * G:(h + 1) * G], case.oracle_unit(1, h))
+        k, v = wl.unit_kv(cfg, 2, h, 600)
+        keep = np.r_[0:256, 512:600]
+        kd = oracle.int4_dequantize_groups(*oracle.int4_quantize_groups(k[keep], 64), 64)
+        vd = oracle.int4_dequantize_groups(*oracle.int4_quantize_groups(v[keep], 64), 64)
+        ref = np.stack([oracle.attention_f64(case.q[2, h * G + g], kd, vd, SM_SCALE) for g in range(G)])
+        assert_close(out[2, h * G:(h + 1) * G], ref)
+
+
+def test_int4_workload_scaled(gpu_lib):
+    cfg = wl.scaled(wl.INT4_G64_32K, batch=2, ctx=2500)
+    case = Int4Case(cfg)
+    out = case.decode()
+    G = cfg.group
+    for b in range(cfg.batch):
+        for h in range(cfg.nkv):
+            assert_close(out[b, h * G:(h + 1) * G], case.oracle_unit(b, h), f"b={b} h={h}")
+
+
+@pytest.mark.slow
+def test_int4_workload_full_size_sampled(gpu_lib):
+    cfg = wl.INT4_G64_32K
+    case = Int4Case(cfg, spare_blocks=0)
+    out = case.decode()
+    assert case.status.item() == 0 and np.all(np.isfinite(out))
+    rng = np.random.default_rng(6)
+    G = cfg.group
+    for b, h in {(int(rng.integers(cfg.batch)), int(rng.integers(cfg.nkv))) for _ in range(4)}:
+        assert_close(out[b, h * G:(h + 1) * G], case.oracle_unit(b, h), f"full int4 b={b} h={h}")
