@@ -463,6 +463,233 @@ def run_kvq8(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------ 4-bit cache ---
+def int4_step_bytes(cfg, lens):
+    """Algorithmic bytes of one 4-bit step: 64 code bytes + 4 fp32 per (token,
+    kv head) for K and V, the fp32 query and output, and the one-token append
+    (fp32 rows in, codes and parameters out)."""
+    import numpy as np
+    tok = int(np.asarray(lens, np.int64).sum())
+    rows = cfg.batch * cfg.nkv
+    return (tok * cfg.nkv * 2 * (cfg.hd // 2 + 16) + 2 * cfg.batch * cfg.nqh * cfg.hd * 4 +
+            rows * 2 * (cfg.hd * 4 + cfg.hd // 2 + 16))
+
+
+def run_kvq4(args, rank, world, local):
+    """The 4-bit (asymmetric INT4 group-64) cache: a step appends one token per
+    (sequence, kv head) and decodes with the fp32 query over the dequantised cache."""
+    import numpy as np
+    import torch
+    from int8_quantized_kv_gb300 import kvq8
+    from int8_quantized_kv_gb300 import workloads as wl
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist_init(world, "nccl")
+    kvq8.load()
+    cfg = wl.WORKLOADS[args.workload]
+    lens = wl.ctx_lens(cfg)
+    table, num_blocks = wl.block_table(cfg, lens)
+    max_blocks = table.shape[1]
+    cache_bytes = num_blocks * 256 * kvq8.cache4_bytes_per_token(cfg.nkv)
+    copies = args.copies or max(2, math.ceil(8 * L2_BYTES / cache_bytes))
+    sm = 1.0 / math.sqrt(cfg.hd)
+    c0 = kvq8.alloc_cache4(num_blocks, cfg.nkv, dev)
+    table_d = torch.from_numpy(table).to(dev)
+    new_k = np.zeros((cfg.batch, 1, cfg.nkv, cfg.hd), np.float32)
+    new_v = np.zeros_like(new_k)
+    zero = torch.zeros(1, dtype=torch.int32, device=dev)
+    for b in range(cfg.batch):
+        L = int(lens[b])
+        k, v = wl.seq_kv(cfg, b, L)
+        new_k[b, 0], new_v[b, 0] = k[L - 1], v[L - 1]
+        if L > 1:
+            kvq8.quantize_append4(torch.from_numpy(k[None, :L - 1]).to(dev),
+                                  torch.from_numpy(v[None, :L - 1]).to(dev), zero,
+                                  table_d[b:b + 1], c0)
+    caches = [c0] + [kvq8.KV4Cache(*[t.clone() for t in c0]) for _ in range(copies - 1)]
+    q_d = torch.from_numpy(wl.queries(cfg)).to(dev)
+    nk_d, nv_d = torch.from_numpy(new_k).to(dev), torch.from_numpy(new_v).to(dev)
+    start_d = torch.from_numpy((lens - 1).clip(min=0).astype(np.int32)).to(dev)
+    lens_d = torch.from_numpy(lens).to(dev)
+    ws = kvq8.alloc_workspace(cfg.batch, cfg.nqh, cfg.nkv, max_blocks, dev)
+    out = torch.empty_like(q_d)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, ev=None):
+        c = caches[i % copies]
+        kvq8.quantize_append4(nk_d, nv_d, start_d, table_d, c, dev_status=status, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        kvq8.decode_attn4(q_d, c, table_d, lens_d, out, ws, sm_scale=sm, dev_status=status,
+                          stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item():#x} during warm-up")
+    k_sample = 10
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(0, args.steps, k_sample)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(i, evs[i // k_sample] if i % k_sample == 0 else None)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier()
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item():#x} in the timed region")
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    dec_s = sum(a.elapsed_time(b) for a, b in evs) / 1e3 / len(evs)
+    sbytes = int4_step_bytes(cfg, lens)
+    total_bytes, slowest = aggregate(sbytes * args.steps, elapsed, dev)
+    per_step = slowest / args.steps
+    value = total_bytes / slowest / 1e9
+
+    e2e_steps = args.e2e_steps or min(args.steps, 2000)
+    q_h = torch.from_numpy(wl.queries(cfg)).pin_memory()
+    nk_h, nv_h = torch.from_numpy(new_k).pin_memory(), torch.from_numpy(new_v).pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def e2e_step(i):
+        q_d.copy_(q_h, non_blocking=True)
+        nk_d.copy_(nk_h, non_blocking=True)
+        nv_d.copy_(nv_h, non_blocking=True)
+        step(i)
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for i in range(3):
+        e2e_step(i)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e2e_s = time.perf_counter() - t0
+    e_total, e_slowest = aggregate(sbytes * e2e_steps, e2e_s, dev)
+    peak, peak_kind = hbm_peak()
+    dec_bytes = sbytes - cfg.batch * cfg.nkv * 2 * (cfg.hd * 4 + cfg.hd // 2 + 16)
+    achieved = dec_bytes / dec_s / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 5),
+        "us_per_step": round(per_step * 1e6, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4", "data": "synthetic",
+        "config": dict(workload_config(cfg, lens, copies), parallelism=f"replicas{world}",
+                       bytes_per_step=sbytes, format="asymmetric INT4 group-64 cache",
+                       arithmetic="fp32 query x dequantised codes, fp32 softmax and accumulation"),
+        "pct_of_hbm_peak": round(100 * (value / world) / peak, 2),
+        "roofline": {"bound": "hbm", "kernel": "kvq4_decode_attn (int4 split + combine)",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind, "traffic": None,
+                     "algorithmic_bytes_per_launch": dec_bytes, "us_per_launch": round(dec_s * 1e6, 3)},
+        "e2e": {"value": round(e_total / e_slowest / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": (q_h.numel() + nk_h.numel() + nv_h.numel()) * 4,
+                "d2h_bytes_per_step": out_h.numel() * 4,
+                "us_per_step": round(e_slowest / e2e_steps * 1e6, 2), "steps": e2e_steps},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------- bulk append ---
+def run_append(args, rank, world, local):
+    """Quantise-append of n_new tokens per sequence (all kv heads) into the q8
+    cache: 1288 algorithmic bytes per (token, kv head)."""
+    import numpy as np
+    import torch
+    from int8_quantized_kv_gb300 import kvq8
+    from int8_quantized_kv_gb300 import workloads as wl
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist_init(world, "nccl")
+    kvq8.load()
+    cfg = wl.WORKLOADS[args.workload]
+    n_new = int(wl.ctx_lens(cfg).max())
+    lens = np.full(cfg.batch, n_new, np.int32)
+    table, num_blocks = wl.block_table(cfg, lens)
+    cache = kvq8.alloc_cache(num_blocks, cfg.nkv, dev)
+    k = np.stack([wl.seq_kv(cfg, b, n_new)[0] for b in range(cfg.batch)])
+    v = np.stack([wl.seq_kv(cfg, b, n_new)[1] for b in range(cfg.batch)])
+    k_d, v_d = torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev)
+    start_d = torch.zeros(cfg.batch, dtype=torch.int32, device=dev)
+    table_d = torch.from_numpy(table).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kvq8.quantize_append(k_d, v_d, start_d, table_d, cache, dev_status=status, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier()
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item():#x}")
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    rows = cfg.batch * n_new * cfg.nkv
+    sbytes = wl.algorithmic_append_bytes(rows, cfg.hd)
+    total_bytes, slowest = aggregate(sbytes * args.steps, elapsed, dev)
+    per_step = slowest / args.steps
+    value = total_bytes / slowest / 1e9
+    peak, peak_kind = hbm_peak()
+    k_h, v_h = torch.from_numpy(k).pin_memory(), torch.from_numpy(v).pin_memory()
+    e2e_steps = args.e2e_steps or min(args.steps, 50)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        k_d.copy_(k_h, non_blocking=True)
+        v_d.copy_(v_h, non_blocking=True)
+        step()
+        stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    e_total, e_slowest = aggregate(sbytes * e2e_steps, e2e_s, dev)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 5),
+        "us_per_step": round(per_step * 1e6, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32->int8", "data": "synthetic",
+        "config": {"workload": cfg.name, "batch": cfg.batch, "n_new": n_new, "nkv": cfg.nkv,
+                   "hd": cfg.hd, "parallelism": f"replicas{world}", "bytes_per_step": sbytes,
+                   "l2": f"inputs {2 * k.nbytes / 2**20:.0f} MiB fp32 >> 129 MB L2, no flush"},
+        "pct_of_hbm_peak": round(100 * (value / world) / peak, 2),
+        "roofline": {"bound": "hbm", "kernel": "quantize_append_kernel", "achieved": round(value / world, 2),
+                     "peak": peak, "unit": "GB/s", "frac": round(value / world / peak, 4),
+                     "peak_kind": peak_kind, "traffic": None, "algorithmic_bytes_per_launch": sbytes,
+                     "us_per_launch": round(per_step * 1e6, 3)},
+        "e2e": {"value": round(e_total / e_slowest / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": 2 * k.nbytes, "d2h_bytes_per_step": 0,
+                "us_per_step": round(e_slowest / e2e_steps * 1e6, 2), "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------- reference arm ---
 def run_reference(args, rank, world):
     """The CPU oracle as it stands, on the host cores, each step a bounded
@@ -471,6 +698,8 @@ def run_reference(args, rank, world):
         return
     import numpy as np
     from int8_quantized_kv_gb300 import workloads as wl
+    if args.workload.startswith(("int4", "append")):
+        raise SystemExit("the reference arm times the q8 decode step; pick a decode workload")
     cfg = wl.WORKLOADS[args.workload]
     lens = wl.ctx_lens(cfg)
     threads = len(os.sched_getaffinity(0))
@@ -510,6 +739,10 @@ def main(argv=None):
         raise SystemExit("--steps must be >= 1")
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.workload.startswith("int4"):
+        run_kvq4(args, rank, world, local)
+    elif args.workload.startswith("append"):
+        run_append(args, rank, world, local)
     else:
         run_kvq8(args, rank, world, local)
 

@@ -125,7 +125,7 @@ kvq8_status kvq8_quantize_append(const float *k_new, const float *v_new, int bat
         !v_scale)
         return KVQ8_ERR_INVALID_ARG;
     if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_pool, 16) ||
-        !aligned(v_pool, 16) || !aligned(k_scale, 4) || !aligned(v_scale, 4) ||
+        !aligned(v_pool, 16) || !aligned(k_scale, 16) || !aligned(v_scale, 16) ||
         !aligned(start_pos, 4) || !aligned(block_table, 4))
         return KVQ8_ERR_INVALID_ARG;
     AppendParams p;

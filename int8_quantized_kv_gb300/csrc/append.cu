@@ -20,10 +20,12 @@
 namespace kvq8 {
 namespace {
 
-constexpr int kAppendTokens = 32;  // tokens per CTA
-constexpr int kAppendWarps = 8;
-constexpr int kVStride = kAppendTokens + 4;  // bytes per staged V dim row
-constexpr int kNoAppend = INT_MIN;            // this sequence appends nothing
+constexpr int kAppendWarps = 8;                  // one-token kernel: warps per CTA
+constexpr int kQWarps = 16;                      // quarter kernel: warps per CTA
+constexpr int kQTok = kStageTok;                 // tokens per CTA: one 64-token quarter
+constexpr int kRowsPerWarp = kQTok / kQWarps;
+constexpr int kVStride = kQTok + 4;              // staged V dim row: 17 words, conflict-free
+constexpr int kNoAppend = INT_MIN;               // this sequence appends nothing
 
 // Position of the first new token of sequence b: start_pos[b], or in a decode
 // step ctx_lens[b] - 1 (nothing for an empty or out-of-table context, which
@@ -34,82 +36,107 @@ __device__ __forceinline__ int start_position(const AppendParams &p, int b, int 
     return (L >= 1 && L <= cap) ? L - 1 : kNoAppend;
 }
 
-__global__ void __launch_bounds__(kAppendWarps * 32)
+// One CTA per 64-token quarter of the cache touched by the new tokens of one
+// (sequence, kv head): CTA x takes quarter floor(start/64) + x.  Every warp
+// first issues the loads of its 4 rows (K and V), then quantises them; K rows
+// go to the token-major tile, V codes through shared memory to the dim-major
+// quarter, which a full quarter writes as one contiguous 8 KiB run.
+__global__ void __launch_bounds__(kQWarps * 32)
 quantize_append_kernel(AppendParams p) {
     const int h = blockIdx.y, b = blockIdx.z;
-    const int i0 = blockIdx.x * kAppendTokens;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     __shared__ __align__(16) int8_t v_stage[kHD][kVStride];
-    __shared__ int tok_phys[kAppendTokens];
-    __shared__ int tok_slot[kAppendTokens];
+    __shared__ __align__(16) float v_sc[kQTok];
 
     pdl_launch_dependents();  // let the next kernel of the step be scheduled now
     const int cap = p.max_blocks * kBS;
     const int start = start_position(p, b, cap);
-    for (int r = warp; r < kAppendTokens; r += kAppendWarps) {
-        const int i = i0 + r;
-        int phys = -1, slot = 0;
-        if (i < p.n_new && start != kNoAppend) {
-            const int pos = start + i;
-            if (pos < 0 || pos >= cap) {
-                if (lane == 0) flag_status(p.dev_status, KVQ8_DEV_BAD_POSITION);
-            } else {
-                phys = p.block_table[(size_t)b * p.max_blocks + pos / kBS];
-                slot = pos % kBS;
-                if (phys < 0 || phys >= p.num_blocks) {
-                    if (lane == 0) flag_status(p.dev_status, KVQ8_DEV_BAD_BLOCK_ID);
-                    phys = -1;
-                }
-            }
-        }
-        if (lane == 0) {
-            tok_phys[r] = phys;
-            tok_slot[r] = slot;
-        }
-        if (phys < 0) continue;  // warp-uniform
+    if (start == kNoAppend) return;
+    const long long q0 = ((long long)start >= 0 ? start / kQTok : -(((long long)-start + kQTok - 1) / kQTok));
+    const long long qpos = (q0 + blockIdx.x) * kQTok;          // first position of this quarter
+    const long long lo = max((long long)start, qpos);
+    const long long hi = min((long long)start + p.n_new, qpos + kQTok);
+    if (lo >= hi) return;                                        // block-uniform
+    if (lo < 0 || hi > cap) {
+        if (threadIdx.x == 0) flag_status(p.dev_status, KVQ8_DEV_BAD_POSITION);
+        if (hi <= 0 || lo >= cap) return;
+    }
+    const long long vlo = max(lo, 0LL), vhi = min(hi, (long long)cap);  // positions inside the table
+    const int phys = p.block_table[(size_t)b * p.max_blocks + (int)(qpos / kBS)];
+    if (phys < 0 || phys >= p.num_blocks) {
+        if (threadIdx.x == 0) flag_status(p.dev_status, KVQ8_DEV_BAD_BLOCK_ID);
+        return;
+    }
+    const size_t tile = (size_t)phys * p.nkv + h;
+    const int slot0 = (int)(qpos % kBS);                         // first slot of the quarter
 
-        const size_t src = (((size_t)b * p.n_new + i) * p.nkv + h) * kHD;
-        const size_t tile = (size_t)phys * p.nkv + h;
-
-        // K row -> token-major K tile
+    // this warp's rows: quarter offsets r = warp + 16j.  K: lane l holds dims
+    // 4l..4l+3 (one packed word of codes); V: lane l holds dims l + 32k, so that
+    // the transposing writes below hit 32 different banks
+    float4 xk[kRowsPerWarp], xv[kRowsPerWarp];
+#pragma unroll
+    for (int j = 0; j < kRowsPerWarp; ++j) {
+        const long long pos = qpos + warp + kQWarps * j;
+        if (pos >= vlo && pos < vhi) {
+            const size_t src = (((size_t)b * p.n_new + (size_t)(pos - start)) * p.nkv + h) * kHD;
+            xk[j] = reinterpret_cast<const float4 *>(p.k_new + src)[lane];
+            const float *vr = p.v_new + src;
+            xv[j] = make_float4(vr[lane], vr[lane + 32], vr[lane + 64], vr[lane + 96]);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < kRowsPerWarp; ++j) {
+        const int r = warp + kQWarps * j;
+        const long long pos = qpos + r;
+        if (pos < vlo || pos >= vhi) continue;                   // warp-uniform
+        const int slot = slot0 + r;
         {
-            const float4 x = reinterpret_cast<const float4 *>(p.k_new + src)[lane];
+            const float4 x = xk[j];
             float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
             m = warp_max(m);
-            const float s = kv_row_scale(m);
-            const uint32_t w = pack4(kv_code(x.x, s), kv_code(x.y, s), kv_code(x.z, s),
-                                     kv_code(x.w, s));
+            const float sc = kv_row_scale(m);
+            const uint32_t w = pack4(kv_code(x.x, sc), kv_code(x.y, sc), kv_code(x.z, sc),
+                                     kv_code(x.w, sc));
             // 16-byte chunk lane/4 of the row goes to chunk position (lane/4) ^ (slot & 7)
             unsigned char *row = reinterpret_cast<unsigned char *>(p.k_pool) + (tile * kBS + slot) * kHD;
             reinterpret_cast<uint32_t *>(row + (((lane >> 2) ^ (slot & 7)) << 4))[lane & 3] = w;
-            if (lane == 0) p.k_scale[tile * kBS + slot] = s;
+            if (lane == 0) p.k_scale[tile * kBS + slot] = sc;
         }
-        // V row -> staged for the dim-major write
         {
-            const float4 x = reinterpret_cast<const float4 *>(p.v_new + src)[lane];
+            const float4 x = xv[j];
             float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
             m = warp_max(m);
-            const float s = kv_row_scale(m);
-            v_stage[4 * lane + 0][r] = (int8_t)kv_code(x.x, s);
-            v_stage[4 * lane + 1][r] = (int8_t)kv_code(x.y, s);
-            v_stage[4 * lane + 2][r] = (int8_t)kv_code(x.z, s);
-            v_stage[4 * lane + 3][r] = (int8_t)kv_code(x.w, s);
-            if (lane == 0) p.v_scale[tile * kBS + slot] = s;
+            const float sc = kv_row_scale(m);
+            v_stage[lane + 0][r] = (int8_t)kv_code(x.x, sc);
+            v_stage[lane + 32][r] = (int8_t)kv_code(x.y, sc);
+            v_stage[lane + 64][r] = (int8_t)kv_code(x.z, sc);
+            v_stage[lane + 96][r] = (int8_t)kv_code(x.w, sc);
+            if (lane == 0) v_sc[r] = sc;
         }
     }
     __syncthreads();
 
-    // Dim-major V write (per 64-token quarter): a warp stores one dim row for
-    // the CTA's 32 tokens, which are consecutive slots except at a boundary.
-    const int r = lane;
-    const int phys = tok_phys[r];
-    if (phys >= 0) {
-        const int slot = tok_slot[r];
-        const size_t base = ((size_t)phys * p.nkv + h) * kHD * kBS +
-                            (size_t)(slot / kStageTok) * kTileVQuarter + (slot % kStageTok);
-        for (int d = warp; d < kHD; d += kAppendWarps)
-            p.v_pool[base + (size_t)d * kStageTok] = v_stage[d][r];
+    int8_t *vq = p.v_pool + tile * kHD * kBS + (size_t)(slot0 / kQTok) * kTileVQuarter;
+    if (vlo == qpos && vhi == qpos + kQTok) {
+        // the whole quarter: 128 dim rows of 64 bytes, one 8 KiB run, 16-byte stores
+        for (int e = threadIdx.x; e < kHD * (kQTok / 16); e += kQWarps * 32) {
+            const int d = e / (kQTok / 16), c16 = e % (kQTok / 16);
+            const uint32_t *w = reinterpret_cast<const uint32_t *>(&v_stage[d][16 * c16]);
+            reinterpret_cast<int4 *>(vq + (size_t)d * kQTok)[c16] =
+                make_int4((int)w[0], (int)w[1], (int)w[2], (int)w[3]);
+        }
+        if (threadIdx.x < kQTok / 4)
+            reinterpret_cast<float4 *>(p.v_scale + tile * kBS + slot0)[threadIdx.x] =
+                reinterpret_cast<const float4 *>(v_sc)[threadIdx.x];
+    } else {
+        // part of a quarter: one byte per (dim, new token)
+        const int r0 = (int)(vlo - qpos), r1 = (int)(vhi - qpos);
+        for (int e = threadIdx.x; e < kHD * kQTok; e += kQWarps * 32) {
+            const int d = e / kQTok, r = e % kQTok;
+            if (r >= r0 && r < r1) vq[(size_t)d * kQTok + r] = v_stage[d][r];
+        }
+        if (threadIdx.x >= r0 && threadIdx.x < r1) p.v_scale[tile * kBS + slot0 + threadIdx.x] = v_sc[threadIdx.x];
     }
 }
 
@@ -175,8 +202,9 @@ cudaError_t launch_quantize_append(const AppendParams &p, cudaStream_t s) {
         quantize_append_token_kernel<<<(unsigned)((warps + kAppendWarps - 1) / kAppendWarps),
                                        kAppendWarps * 32, 0, s>>>(p);
     } else {
-        dim3 grid((p.n_new + kAppendTokens - 1) / kAppendTokens, p.nkv, p.batch);
-        quantize_append_kernel<<<grid, kAppendWarps * 32, 0, s>>>(p);
+        // quarters touched by n_new consecutive positions: at most n_new/64 + 1
+        dim3 grid(p.n_new / kQTok + (p.n_new % kQTok ? 2 : 1), p.nkv, p.batch);
+        quantize_append_kernel<<<grid, kQWarps * 32, 0, s>>>(p);
     }
     return cudaGetLastError();
 }
