@@ -54,6 +54,8 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = min(steps, 2000)")
+    ap.add_argument("--no-f32", action="store_true",
+                    help="skip the fp32-KV decode comparator leg")
     return ap.parse_args(argv)
 
 
@@ -191,6 +193,14 @@ def split_kernel_bytes(cfg, lens):
     return tok * cfg.nkv * (2 * cfg.hd + 8) + cfg.batch * cfg.nqh * cfg.hd * 4
 
 
+def f32_decode_bytes(cfg, lens):
+    """Algorithmic bytes of the fp32-KV decode: fp32 K/V per (token, kv head),
+    the fp32 queries and outputs."""
+    import numpy as np
+    tok = int(np.asarray(lens, np.int64).sum())
+    return tok * cfg.nkv * 2 * cfg.hd * 4 + 2 * cfg.batch * cfg.nqh * cfg.hd * 4
+
+
 def workload_config(cfg, lens, copies):
     import numpy as np
     c = {"workload": cfg.name, "layers_folded_into_batch": cfg.layers,
@@ -310,6 +320,9 @@ def run_kvq8(args, rank, world, local):
     new_k = np.zeros((cfg.batch, 1, cfg.nkv, cfg.hd), np.float32)
     new_v = np.zeros_like(new_k)
     zero = torch.zeros(1, dtype=torch.int32, device=dev)
+    # the fp32 comparator cache holds the same L tokens (the q8 cache has token
+    # L-1 after the first step)
+    cf = None if args.no_f32 else kvq8.alloc_cachef32(num_blocks, cfg.nkv, dev)
     for b in range(cfg.batch):
         L = int(lens[b])
         k, v = wl.seq_kv(cfg, b, L)
@@ -318,6 +331,9 @@ def run_kvq8(args, rank, world, local):
             kvq8.quantize_append(torch.from_numpy(k[None, :L - 1]).to(dev),
                                  torch.from_numpy(v[None, :L - 1]).to(dev), zero,
                                  table_d[b:b + 1], c0)
+        if cf is not None and L > 0:
+            kvq8.appendf32(torch.from_numpy(k[None]).to(dev), torch.from_numpy(v[None]).to(dev), zero,
+                           table_d[b:b + 1], cf)
     caches = [c0]
     for _ in range(copies - 1):
         caches.append(kvq8.KVCache(*[t.clone() for t in c0]))
@@ -426,9 +442,10 @@ def run_kvq8(args, rank, world, local):
     h2d = (q_h.numel() + nk_h.numel() + nv_h.numel()) * 4
     d2h = out_h.numel() * 4
 
-    # parity spot check of this very run against the oracle (rank 0, one unit)
     if status.item() != 0:
         raise RuntimeError(f"device status {status.item():#x} in the timed region")
+    comparator = None if cf is None else f32_comparator(args, cfg, lens, cf, q_d, table_d, lens_d, ws,
+                                                        out, status, stream, split_s)
 
     peak, peak_kind = hbm_peak()
     split_bytes = split_kernel_bytes(cfg, lens)
@@ -457,10 +474,48 @@ def run_kvq8(args, rank, world, local):
                     "path": "kvq8_quantize_append + kvq8_decode_split + kvq8_decode_combine"},
         "clocks": clocks,
     }
+    if comparator is not None:
+        line["fp32_kv_comparator"] = comparator
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, lens, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def f32_comparator(args, cfg, lens, cf, q_d, table_d, lens_d, ws, out_q8, status, stream, split_s):
+    """The fp32-KV decode over the same context (the unquantised arm of the
+    fp32-KV vs q8-KV comparison): its time and bandwidth beside the q8 split
+    kernel's, and the per-dimension output delta between the two."""
+    import torch
+    from int8_quantized_kv_gb300 import kvq8
+    sm = 1.0 / math.sqrt(cfg.hd)
+    out = torch.empty_like(q_d)
+    n = min(args.steps, 500)
+
+    def run():
+        kvq8.decode_attnf32(q_d, cf, table_d, lens_d, out, ws, sm_scale=sm, dev_status=status,
+                            stream=stream)
+
+    for _ in range(3):
+        run()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item():#x} in the fp32 decode")
+    t = e0.elapsed_time(e1) / 1e3 / n
+    nbytes = f32_decode_bytes(cfg, lens)
+    d = (out_q8.double() - out.double()).abs()
+    return {"path": "kvf32_decode_attn (split + combine)", "us_per_decode": round(t * 1e6, 2),
+            "GB_per_s": round(nbytes / t / 1e9, 2), "bytes_per_decode": nbytes,
+            "kv_bytes_ratio_q8_over_f32": round(split_kernel_bytes(cfg, lens) / nbytes, 4),
+            "time_ratio_q8_split_over_f32": round(split_s / t, 4),
+            "cache_l2": "one fp32 cache copy; working set >> 129 MB L2 for this workload",
+            "delta_q8_vs_f32": {"max_abs": float(d.max()), "mean_abs": float(d.mean())}}
 
 
 # ------------------------------------------------------------ 4-bit cache ---

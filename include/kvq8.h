@@ -274,6 +274,50 @@ kvq8_status kvq4_decode_attn(const float *q, int batch, int nqh, int nkv, int hd
                              float *out, void *workspace, size_t workspace_bytes,
                              uint32_t *dev_status, void *stream);
 
+/* --------------------------------------- fp32 cache (comparator row) --- */
+
+/*
+ * The fp32 K/V cache that [Day 9-1] §2-§3 keeps beside the int8 cache for
+ * debugging and comparison, and that [Day 9-3] §1 takes as the unquantised arm
+ * of its fp32-KV vs q8-KV experiment ("change one variable": the same
+ * attention over raw fp32 K/V).  Here it is paged with the same block table
+ * conventions as the int8 cache:
+ *   k_cache, v_cache fp32 [num_blocks][nkv][256][hd]   token-major rows
+ * 1024 bytes per (token, kv head): 8192 bytes per token per layer for nkv = 8,
+ * against 2112 for the int8 cache.
+ */
+size_t kvf32_pool_bytes(int num_blocks, int nkv, int hd, int block_size);
+size_t kvf32_cache_bytes_per_token(int nkv, int hd);
+
+/*
+ * kvf32_append -- copy the new tokens' fp32 K/V rows into the fp32 cache at
+ * positions start_pos[b] + i.  Arguments as kvq8_quantize_append; k_cache and
+ * v_cache 16-byte aligned.  Positions beyond the table and block ids outside
+ * [0, num_blocks) are flagged in *dev_status and skipped.
+ */
+kvq8_status kvf32_append(const float *k_new, const float *v_new,
+                         int batch, int n_new, int nkv, int hd,
+                         const int32_t *start_pos,
+                         const int32_t *block_table, int max_blocks,
+                         int block_size, int num_blocks,
+                         float *k_cache, float *v_cache,
+                         uint32_t *dev_status, void *stream);
+
+/*
+ * kvf32_decode_attn -- decode attention of the fp32 query over the fp32 cache:
+ * s_t = sm_scale * q . k_t, softmax with a running maximum, fp32 accumulation
+ * of v_t, split over the context and merged as in kvq8_decode_attn (one divide
+ * by the summed weights at the end).  Workspace: kvq8_decode_workspace_bytes
+ * (...) for the same sizes.  Other arguments as kvq8_decode_attn.
+ */
+kvq8_status kvf32_decode_attn(const float *q, int batch, int nqh, int nkv, int hd,
+                              const float *k_cache, const float *v_cache,
+                              int num_blocks, const int32_t *block_table,
+                              int max_blocks, int block_size,
+                              const int32_t *ctx_lens, float sm_scale,
+                              float *out, void *workspace, size_t workspace_bytes,
+                              uint32_t *dev_status, void *stream);
+
 /* ------------------------------------------- decode without allocation --- */
 
 /* Size of the static device scratch kvq8_decode_attn_noalloc uses (16 MiB). */

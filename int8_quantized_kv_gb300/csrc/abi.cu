@@ -376,4 +376,90 @@ kvq8_status kvq4_decode_attn(const float *q, int batch, int nqh, int nkv, int hd
     return KVQ8_OK;
 }
 
+size_t kvf32_pool_bytes(int num_blocks, int nkv, int hd, int block_size) {
+    if (num_blocks < 0 || nkv < 0 || hd < 0 || block_size < 0) return 0;
+    return (size_t)num_blocks * nkv * block_size * hd * sizeof(float);
+}
+
+size_t kvf32_cache_bytes_per_token(int nkv, int hd) {
+    if (nkv < 0 || hd < 0) return 0;
+    return (size_t)nkv * 2 * (size_t)hd * sizeof(float);
+}
+
+kvq8_status kvf32_append(const float *k_new, const float *v_new, int batch, int n_new, int nkv,
+                         int hd, const int32_t *start_pos, const int32_t *block_table,
+                         int max_blocks, int block_size, int num_blocks, float *k_cache,
+                         float *v_cache, uint32_t *dev_status, void *stream) {
+    kvq8_status st = check_shape(hd, block_size);
+    if (st != KVQ8_OK) return st;
+    if (batch < 0 || n_new < 0 || nkv <= 0 || num_blocks <= 0 || max_blocks <= 0)
+        return KVQ8_ERR_INVALID_ARG;
+    if (max_blocks > 2147483647 / kBS) return KVQ8_ERR_UNSUPPORTED;
+    if (batch > kMaxGridYZ || nkv > kMaxGridYZ) return KVQ8_ERR_UNSUPPORTED;
+    if (batch == 0 || n_new == 0) return KVQ8_OK;
+    if (!k_new || !v_new || !start_pos || !block_table || !k_cache || !v_cache)
+        return KVQ8_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16) || !aligned(start_pos, 4) || !aligned(block_table, 4))
+        return KVQ8_ERR_INVALID_ARG;
+    F32AppendParams p;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.batch = batch;
+    p.n_new = n_new;
+    p.nkv = nkv;
+    p.start_pos = start_pos;
+    p.block_table = block_table;
+    p.max_blocks = max_blocks;
+    p.num_blocks = num_blocks;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.dev_status = dev_status;
+    if (launch_f32_append(p, (cudaStream_t)stream) != cudaSuccess) return KVQ8_ERR_CUDA;
+    return KVQ8_OK;
+}
+
+kvq8_status kvf32_decode_attn(const float *q, int batch, int nqh, int nkv, int hd,
+                              const float *k_cache, const float *v_cache, int num_blocks,
+                              const int32_t *block_table, int max_blocks, int block_size,
+                              const int32_t *ctx_lens, float sm_scale, float *out,
+                              void *workspace, size_t workspace_bytes, uint32_t *dev_status,
+                              void *stream) {
+    // the scale arguments of the shared check are the caches themselves (non-null, aligned)
+    kvq8_status st = check_decode_args(q, batch, nqh, nkv, hd, (const int8_t *)k_cache,
+                                       (const int8_t *)v_cache, k_cache, v_cache, num_blocks,
+                                       block_table, max_blocks, block_size, ctx_lens);
+    if (st != KVQ8_OK || batch == 0) return st;
+    if (!out || !aligned(out, 16) || !isfinite(sm_scale)) return KVQ8_ERR_INVALID_ARG;
+    DecodeParams c;
+    DecodePlan plan;
+    st = fill_decode_params(q, batch, nqh, nkv, nullptr, nullptr, nullptr, nullptr, num_blocks,
+                            block_table, max_blocks, ctx_lens, sm_scale, workspace,
+                            workspace_bytes, dev_status, &c, &plan);
+    if (st != KVQ8_OK) return st;
+    c.out = out;
+    F32DecodeParams p;
+    p.q = q;
+    p.batch = batch;
+    p.nqh = nqh;
+    p.nkv = nkv;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.num_blocks = num_blocks;
+    p.block_table = block_table;
+    p.max_blocks = max_blocks;
+    p.ctx_lens = ctx_lens;
+    p.sm_scale_log2 = c.sm_scale_log2;
+    if (!make_f32_plan(batch, nkv, max_blocks, &p.nsplit, &p.split_tokens))
+        return KVQ8_ERR_INVALID_ARG;
+    p.ws_meta = c.ws_meta;
+    p.ws_ml = c.ws_ml;
+    p.ws_acc = c.ws_acc;
+    p.dev_status = dev_status;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (launch_f32_decode_split(p, plan.group, s) != cudaSuccess) return KVQ8_ERR_CUDA;
+    if (launch_decode_combine(c, plan.group, s) != cudaSuccess) return KVQ8_ERR_CUDA;
+    return KVQ8_OK;
+}
+
 }  // extern "C"

@@ -109,4 +109,33 @@ bool make_int4_plan(int batch, int nkv, int max_blocks, int *nsplit, int *split_
 cudaError_t launch_int4_append(const Int4AppendParams &p, cudaStream_t s);
 cudaError_t launch_int4_decode_split(const Int4DecodeParams &p, int group, cudaStream_t s);
 
+// ------------------------------------------------------------ fp32 cache --
+struct F32AppendParams {
+    const float *k_new, *v_new;   // [batch][n_new][nkv][hd]
+    int batch, n_new, nkv;
+    const int32_t *start_pos;     // [batch]
+    const int32_t *block_table;
+    int max_blocks, num_blocks;
+    float *k_cache, *v_cache;     // [num_blocks][nkv][256][hd]
+    uint32_t *dev_status;
+};
+
+struct F32DecodeParams {
+    const float *q;               // [batch][nqh][hd]
+    int batch, nqh, nkv;
+    const float *k_cache, *v_cache;
+    int num_blocks;
+    const int32_t *block_table;
+    int max_blocks;
+    const int32_t *ctx_lens;
+    float sm_scale_log2;
+    int nsplit, split_tokens;     // unit u's split j writes record u*nsplit + j
+    int2 *ws_meta;
+    float *ws_ml, *ws_acc;        // same record format as DecodeParams
+    uint32_t *dev_status;
+};
+bool make_f32_plan(int batch, int nkv, int max_blocks, int *nsplit, int *split_tokens);
+cudaError_t launch_f32_append(const F32AppendParams &p, cudaStream_t s);
+cudaError_t launch_f32_decode_split(const F32DecodeParams &p, int group, cudaStream_t s);
+
 }  // namespace kvq8

@@ -53,6 +53,11 @@ SIGNATURES = {
                                   _P, _P, _P, _P, _P, _P]),
     "kvq4_decode_attn": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _I,
                               _P, _F, _P, _P, _SZ, _P, _P]),
+    "kvf32_pool_bytes": (_SZ, [_I, _I, _I, _I]),
+    "kvf32_cache_bytes_per_token": (_SZ, [_I, _I]),
+    "kvf32_append": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _I, _I, _I, _P, _P, _P, _P]),
+    "kvf32_decode_attn": (_I, [_P, _I, _I, _I, _I, _P, _P, _I, _P, _I, _I,
+                               _P, _F, _P, _P, _SZ, _P, _P]),
     "kvq8_decode_attn_noalloc": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _I,
                                       _P, _F, _P, _P, _P]),
 }
@@ -331,3 +336,55 @@ def decode_attn4(q, cache: KV4Cache, block_table, ctx_lens, out, workspace,
         block_table.shape[1], BLOCK_SIZE, _ptr(ctx_lens), sm, _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream))
     _check("kvq4_decode_attn", st)
+
+
+# ------------------------------------------------------------- fp32 cache ---
+class KVF32Cache(NamedTuple):
+    """The fp32 K/V cache, the comparator of the int8 one (layout in include/kvq8.h)."""
+    k_cache: object  # fp32 [num_blocks][nkv][256][128]
+    v_cache: object  # fp32 [num_blocks][nkv][256][128]
+
+    @property
+    def num_blocks(self) -> int:
+        return self.k_cache.shape[0]
+
+    @property
+    def nkv(self) -> int:
+        return self.k_cache.shape[1]
+
+
+def cachef32_bytes_per_token(nkv: int, hd: int = HEAD_DIM) -> int:
+    return int(load().kvf32_cache_bytes_per_token(nkv, hd))
+
+
+def alloc_cachef32(num_blocks: int, nkv: int, device="cuda") -> KVF32Cache:
+    import torch
+    lib = load()
+    assert lib.kvf32_pool_bytes(num_blocks, nkv, HEAD_DIM, BLOCK_SIZE) == num_blocks * nkv * BLOCK_SIZE * HEAD_DIM * 4
+    kc = torch.empty((num_blocks, nkv, BLOCK_SIZE, HEAD_DIM), dtype=torch.float32, device=device)
+    return KVF32Cache(kc, torch.empty_like(kc))
+
+
+def appendf32(k_new, v_new, start_pos, block_table, cache: KVF32Cache, dev_status=None, stream=None):
+    """k_new, v_new: fp32 [batch][n_new][nkv][128] copied into the fp32 cache."""
+    _need_cuda(k_new, v_new, start_pos, block_table, *cache, dev_status)
+    batch, n_new, nkv, hd = k_new.shape
+    st = load().kvf32_append(
+        _ptr(k_new), _ptr(v_new), batch, n_new, nkv, hd, _ptr(start_pos), _ptr(block_table),
+        block_table.shape[1], BLOCK_SIZE, cache.num_blocks, _ptr(cache.k_cache),
+        _ptr(cache.v_cache), _ptr(dev_status), _stream(stream))
+    _check("kvf32_append", st)
+
+
+def decode_attnf32(q, cache: KVF32Cache, block_table, ctx_lens, out, workspace,
+                   sm_scale: Optional[float] = None, dev_status=None, stream=None):
+    """fp32 q [batch][nqh][128] over the fp32 cache -> out fp32 [batch][nqh][128]."""
+    _need_cuda(q, block_table, ctx_lens, out, workspace, *cache, dev_status)
+    batch, nqh, hd = q.shape
+    sm = 1.0 / math.sqrt(hd) if sm_scale is None else sm_scale
+    st = load().kvf32_decode_attn(
+        _ptr(q), batch, nqh, cache.nkv, hd, _ptr(cache.k_cache), _ptr(cache.v_cache),
+        cache.num_blocks, _ptr(block_table), block_table.shape[1], BLOCK_SIZE, _ptr(ctx_lens),
+        sm, _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(dev_status), _stream(stream))
+    _check("kvf32_decode_attn", st)

@@ -20,7 +20,7 @@ FAKE = 1 << 20   # a 256-aligned non-null address that is never dereferenced
 def _declared():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(kvq8_[a-z0-9_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(kv(?:q8|q4|f32)_[a-z0-9_]+)\s*\(", src)))
 
 
 @pytest.fixture(scope="module")
@@ -32,7 +32,9 @@ def lib():
 def test_header_declares_expected_entry_points():
     names = _declared()
     for n in ("kvq8_quantize_append", "kvq8_quantize_q", "kvq8_decode_attn",
-              "kvq8_decode_split", "kvq8_decode_combine", "kvq8_decode_workspace_bytes"):
+              "kvq8_decode_split", "kvq8_decode_combine", "kvq8_decode_workspace_bytes",
+              "kvq8_decode_step", "kvq8_decode_attn_noalloc", "kvq4_quantize_append",
+              "kvq4_decode_attn", "kvf32_append", "kvf32_decode_attn"):
         assert n in names
 
 
@@ -139,6 +141,45 @@ def test_quantize_q_validation(lib):
     assert lib.kvq8_quantize_q(None, 4, 128, FAKE, FAKE, None) == kvq8.ERR_INVALID_ARG
     assert lib.kvq8_quantize_q(FAKE, -1, 128, FAKE, FAKE, None) == kvq8.ERR_INVALID_ARG
     assert lib.kvq8_quantize_q(FAKE, 0, 128, FAKE, FAKE, None) == kvq8.OK
+
+
+def test_fp32_cache_sizes_and_validation(lib):
+    # 8 kv heads x 128 fp32 for K and V: 8192 bytes per token per layer
+    assert kvq8.cachef32_bytes_per_token(8) == 8192
+    assert lib.kvf32_pool_bytes(3, 8, 128, 256) == 3 * 8 * 256 * 128 * 4
+    a = dict(k=FAKE, v=FAKE, batch=1, n_new=1, nkv=1, hd=128, start=FAKE, table=FAKE,
+             max_blocks=1, bs=256, num_blocks=1, kc=FAKE, vc=FAKE, status=None, stream=None)
+    assert lib.kvf32_append(*dict(a, hd=64).values()) == kvq8.ERR_UNSUPPORTED
+    assert lib.kvf32_append(*dict(a, kc=FAKE + 4).values()) == kvq8.ERR_INVALID_ARG
+    assert lib.kvf32_append(*dict(a, v=None).values()) == kvq8.ERR_INVALID_ARG
+    assert lib.kvf32_append(*dict(a, n_new=0).values()) == kvq8.OK
+    need = kvq8.decode_workspace_bytes(1, 8, 8, 4)
+    d = dict(q=FAKE, batch=1, nqh=8, nkv=8, hd=128, kc=FAKE, vc=FAKE, num_blocks=4, table=FAKE,
+             max_blocks=4, bs=256, lens=FAKE, sm=0.088, out=FAKE, ws=FAKE, ws_bytes=need,
+             status=None, stream=None)
+    call = lambda **kw: lib.kvf32_decode_attn(*dict(d, **kw).values())
+    assert call(nqh=24) == kvq8.ERR_UNSUPPORTED
+    assert call(vc=None) == kvq8.ERR_INVALID_ARG
+    assert call(kc=FAKE + 8) == kvq8.ERR_INVALID_ARG
+    assert call(out=None) == kvq8.ERR_INVALID_ARG
+    assert call(ws_bytes=need - 1) == kvq8.ERR_WORKSPACE
+    assert call(batch=0) == kvq8.OK
+
+
+def test_int4_cache_sizes_and_validation(lib):
+    # 64 code bytes and 4 fp32 parameters per (token, head) for K and V
+    assert kvq8.cache4_bytes_per_token(8) == 1280
+    a = dict(k=FAKE, v=FAKE, batch=1, n_new=1, nkv=1, hd=128, start=FAKE, table=FAKE,
+             max_blocks=1, bs=256, num_blocks=1, kc=FAKE, vc=FAKE, kp=FAKE, vp=FAKE,
+             status=None, stream=None)
+    assert lib.kvq4_quantize_append(*dict(a, bs=64).values()) == kvq8.ERR_UNSUPPORTED
+    assert lib.kvq4_quantize_append(*dict(a, kp=FAKE + 4).values()) == kvq8.ERR_INVALID_ARG
+    assert lib.kvq4_quantize_append(*dict(a, batch=0).values()) == kvq8.OK
+    need = kvq8.decode_workspace_bytes(1, 8, 8, 4)
+    assert lib.kvq4_decode_attn(FAKE, 1, 8, 8, 128, FAKE, FAKE, FAKE, FAKE, 4, FAKE, 4, 256,
+                                FAKE, 0.088, FAKE, FAKE, need - 1, None, None) == kvq8.ERR_WORKSPACE
+    assert lib.kvq4_decode_attn(FAKE, 1, 8, 8, 128, FAKE, FAKE, FAKE, FAKE, 4, FAKE, 4, 256,
+                                FAKE, 0.088, None, FAKE, need, None, None) == kvq8.ERR_INVALID_ARG
 
 
 def test_library_is_built_for_sm103a():
