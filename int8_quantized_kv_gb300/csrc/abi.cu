@@ -364,7 +364,8 @@ kvq8_status kvq4_decode_attn(const float *q, int batch, int nqh, int nkv, int hd
     p.max_blocks = max_blocks;
     p.ctx_lens = ctx_lens;
     p.sm_scale_log2 = c.sm_scale_log2;
-    if (!make_int4_plan(batch, nkv, max_blocks, &p.nsplit, &p.split_tokens))
+    if (!make_int4_plan(batch, nkv, max_blocks, int4_resident_ctas(plan.group), &p.nsplit,
+                        &p.split_tokens))
         return KVQ8_ERR_INVALID_ARG;
     p.ws_meta = c.ws_meta;
     p.ws_ml = c.ws_ml;

@@ -20,6 +20,7 @@
 // sum_{d in g} q_d), i.e. exactly q . dequant(k); lane = 4 dims for P.V.  The
 // warps' states are merged into one partial record per query head, in the
 // record format of the q8 decode, so the same combine kernel finishes it.
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "kvq8_device.cuh"
@@ -33,7 +34,6 @@ constexpr int kRowBytes = kHD / 2;          // 64 bytes of codes per (token, hea
 constexpr int kAppendWarps4 = 8;
 constexpr int kWarps4 = 4;
 constexpr int kChunk4 = 32;
-constexpr int kKRow4 = kRowBytes + 16;      // padded K row in shared memory
 
 // 16 lanes (a half warp) reduce one 64-value group.
 __device__ __forceinline__ float half_max(float v) {
@@ -96,24 +96,129 @@ int4_append_kernel(Int4AppendParams p) {
                    p.v_param + row * 4, lane);
 }
 
+// ---- tensor-core decode ----
+// Both contractions run as mma.sync m16n8k16 (fp16 in, fp32 accumulate); codes
+// 0..15 are exact in fp16.
+//
+// Q.K as S^T = Q K^T: A = the fp32 query split into fp16 high + low parts
+// (rows = heads, padded to 16), B = K codes (k = dims, n = 8 tokens).  The
+// S^T fragment (row = head, columns = tokens) is the B operand P.V needs, so
+// P never goes through shared memory.  K codes enter as fp16 by one
+// mask-and-or per two codes: a low nibble as 1024 + c, a high nibble in place
+// as 1024 + 16c (exact: fp16 steps are 1 on [1024, 2048)); the query values
+// facing high nibbles are divided by 16, so each code meets its own q.  The
+// 1024 is removed with the zero point:
+//   s = sm * 2^-k * sum_g scale_g * (D'_g - 1024 Y_g - zero_g Q_g),
+//   D'_g = sum_{d in g} b_d y_d,  Y_g = sum_{d in g} y_d,  Q_g = sum_{d in g} q_d,
+// y = the fed query value (q or q/16, as high + low fp16 parts), q = the query
+// times a power of two 2^k that puts its largest element at 2^13..2^14 (fp16
+// keeps full precision for q/16).  Within a 64-dim group the bias costs at
+// most fp32 rounding of a 64-term sum.
+//
+// P.V as out^T = V^T P: A = V codes (rows = dims, k = tokens, exact after one
+// fp16 subtract), B = P'_g = w * vscale_g(t) * 2^-e per dim group, split into
+// fp16 high + low; V codes enter as exact fp16 (c, or 16c for the high nibble
+// of a byte, which the epilogue divides by 16); the zero point enters as a
+// correction per (head, group),
+//   out[d][h] = sum_t P'_g c_{t,d} - Z[h][g],  Z[h][g] = sum_t P'_g zero_g(t),
+// rescaled with the accumulator.  Row r of m-tile mt is dim 2*B + (r >= 8)
+// with byte B = 32*(mt/4) + 4*(r%8) + mt%4, so a lane reads one 32-bit word
+// per token and dim group.
+//
+// k-order of Q.K (k-step ks: group ks/4, sub = ks%4; lane t4 supplies the
+// nibbles of the word at byte 32*(ks/4) + 8*t4 + 4*(sub/2)): k = 2*t4 + e ->
+// the high nibble of byte (sub%2) + 2e, k = 2*t4 + 8 + e -> its low nibble.
+constexpr uint32_t kFp16x2_1024 = 0x64006400u;
+
+// {1024 + n0, 1024 + n2} of the low nibbles of bytes 0 and 2 of w (mask
+// 0x000F000F), or {1024 + 16 n0', 1024 + 16 n2'} of their high nibbles (mask
+// 0x00F000F0)
+__device__ __forceinline__ uint32_t nib_pair(uint32_t w, uint32_t mask) { return (w & mask) | kFp16x2_1024; }
+
+// the same without the 1024: {n0, n2} or {16 n0', 16 n2'}, exact
+__device__ __forceinline__ uint32_t nib_pair_exact(uint32_t w, uint32_t mask) {
+    uint32_t x = nib_pair(w, mask);
+    const __half2 r = __hsub2(*reinterpret_cast<__half2 *>(&x),
+                              __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+constexpr uint32_t kLoNib = 0x000F000Fu, kHiNib = 0x00F000F0u;
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// dim of k index kk (0..15) of Q.K k-step ks
+__device__ __forceinline__ int qk_dim(int ks, int kk) {
+    const int gr = ks >> 2, sub = ks & 3, t4 = (kk & 7) >> 1, e = kk & 1, lo = kk >> 3;
+    const int byte = 32 * gr + 8 * t4 + 4 * (sub >> 1) + (sub & 1) + 2 * e;
+    return 2 * byte + lo;
+}
+
+// Per-warp staging of one 32-token chunk: K and V code rows and the K and V
+// parameter rows; two buffers per warp, filled by 16-byte cp.async.  The
+// fragment reads are conflict-free: K rows keep 64 B with the two 32-byte
+// halves of rows 2, 3 (mod 4) swapped; V rows are padded to 80 B.
+constexpr int kKPitch4 = 64, kVPitch4 = 80;
+__device__ __forceinline__ int kswz(int r, int seg) { return seg ^ ((r >> 1) & 1); }
+constexpr int kStageKOff = 0;
+constexpr int kStageVOff = kChunk4 * kKPitch4;                    // 3072
+constexpr int kStageKpOff = kStageVOff + kChunk4 * kVPitch4;      // 5632
+constexpr int kStageVpOff = kStageKpOff + kChunk4 * 16;           // 6144
+constexpr int kStageBytes4 = kStageVpOff + kChunk4 * 16;          // 6656
+constexpr int kBufs4 = 2;
+
 template <int G>
 struct Int4Smem {
-    float q[G][kHD];
-    float qsum[G][2];
+    uint4 qa[8][32];                 // per k-step and lane: a0 high, a2 high, a0 low, a2 low
+    float qy[8][2];                  // Y_g per head (rows >= G: 0)
+    float qq[8][2];                  // Q_g per head
+    float qmax[kWarps4];
     union {
+        unsigned char stage[kWarps4][kBufs4][kStageBytes4];
         struct {
-            uint8_t k[kWarps4][kChunk4][kKRow4];
-            uint8_t v[kWarps4][kChunk4][kRowBytes];
-            float4 kp[kWarps4][kChunk4];
-            float4 vp[kWarps4][kChunk4];
-            float pw[kWarps4][kChunk4][G];
-        } loop;
-        float red_acc[kWarps4][G][kHD];
+            float acc[kWarps4][G][kHD];
+            float ml[kWarps4][G][2];
+        } red;
     } u;
-    float red_ml[kWarps4][G][2];
 };
 
-__device__ __forceinline__ float nib(uint32_t w, int shift) { return (float)((w >> shift) & 0xFu); }
+__device__ __forceinline__ void cp_async16_cg(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+
+// Copies chunk `cidx` of this warp's split into `buf` (one copy group; an
+// empty group when the chunk does not exist or its block id is invalid).
+__device__ __forceinline__ int int4_fetch_chunk(const Int4DecodeParams &p, int b, int h, int tok_begin,
+                                                int nchunks, int cidx, unsigned char *buf, int lane) {
+    int phys = -1;
+    if (cidx < nchunks) {
+        const int t0 = tok_begin + cidx * kChunk4;
+        phys = p.block_table[(size_t)b * p.max_blocks + t0 / kBS];
+        if (phys >= 0 && phys < p.num_blocks) {
+            const size_t row0 = ((size_t)phys * p.nkv + h) * kBS + t0 % kBS;
+            const uint8_t *kc = p.k_codes + row0 * kRowBytes;
+            const uint8_t *vc = p.v_codes + row0 * kRowBytes;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int q = lane + 32 * i, r = q >> 2, part = q & 3;
+                cp_async16_cg(buf + kStageKOff + r * kKPitch4 + 32 * kswz(r, part >> 1) + 16 * (part & 1),
+                              kc + r * kRowBytes + 16 * part);
+                cp_async16_cg(buf + kStageVOff + r * kVPitch4 + 16 * part, vc + r * kRowBytes + 16 * part);
+            }
+            cp_async16_cg(buf + kStageKpOff + 16 * lane, p.k_param + (row0 + lane) * 4);
+            cp_async16_cg(buf + kStageVpOff + 16 * lane, p.v_param + (row0 + lane) * 4);
+        } else {
+            if (lane == 0) flag_status(p.dev_status, KVQ8_DEV_BAD_BLOCK_ID);
+            phys = -1;
+        }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    return phys;
+}
 
 template <int G>
 __global__ void __launch_bounds__(kWarps4 * 32)
@@ -121,6 +226,7 @@ int4_decode_split_kernel(Int4DecodeParams p) {
     pdl_wait();
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t4 = lane & 3;
     const int cap = p.max_blocks * kBS;
     int L = p.ctx_lens[b];
     if (L < 0 || L > cap) {
@@ -137,166 +243,300 @@ int4_decode_split_kernel(Int4DecodeParams p) {
     if (tok_begin >= L) return;
     const int tok_end = min(L, tok_begin + p.split_tokens);
 
-    __shared__ __align__(16) Int4Smem<G> sm;
-    for (int i = threadIdx.x; i < G * kHD; i += kWarps4 * 32)
-        sm.q[i / kHD][i % kHD] = p.q[((size_t)b * p.nqh + (size_t)h * G) * kHD + i];
-    __syncthreads();
-    if (threadIdx.x < 2 * G) {
-        const int g = threadIdx.x >> 1, grp = threadIdx.x & 1;
-        float s = 0.0f;
-        for (int d = 0; d < 64; ++d) s += sm.q[g][grp * 64 + d];
-        sm.qsum[g][grp] = s;
-    }
-    __syncthreads();
-
-    float M[G], S[G], acc[G][4];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        M[g] = -INFINITY;
-        S[g] = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[g][j] = 0.0f;
-    }
-    const int vgrp = lane >> 4;  // group of this lane's four V dims
-
+    extern __shared__ __align__(16) unsigned char int4_smem_raw[];
+    Int4Smem<G> &sm = *reinterpret_cast<Int4Smem<G> *>(int4_smem_raw);
+    // this warp's chunks: cidx = warp, warp + 4, ...; two in flight
     const int nchunks = (tok_end - tok_begin + kChunk4 - 1) / kChunk4;
-    for (int cidx = warp; cidx < nchunks; cidx += kWarps4) {
-        const int t0 = tok_begin + cidx * kChunk4;
-        const int phys = p.block_table[(size_t)b * p.max_blocks + t0 / kBS];
-        if (phys < 0 || phys >= p.num_blocks) {
-            if (lane == 0) flag_status(p.dev_status, KVQ8_DEV_BAD_BLOCK_ID);
-            continue;
-        }
-        const size_t row0 = ((size_t)phys * p.nkv + h) * kBS + t0 % kBS;
-        // stage 32 K rows, 32 V rows (16-byte loads, coalesced) and their params
-        const uint8_t *kg = p.k_codes + row0 * kRowBytes;
-        const uint8_t *vg = p.v_codes + row0 * kRowBytes;
+    int valid_buf[kBufs4];
 #pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int r = it * 8 + (lane >> 2), ch = lane & 3;
-            *reinterpret_cast<int4 *>(&sm.u.loop.k[warp][r][ch * 16]) =
-                *reinterpret_cast<const int4 *>(kg + r * kRowBytes + ch * 16);
-            *reinterpret_cast<int4 *>(&sm.u.loop.v[warp][r][ch * 16]) =
-                *reinterpret_cast<const int4 *>(vg + r * kRowBytes + ch * 16);
-        }
-        sm.u.loop.kp[warp][lane] = reinterpret_cast<const float4 *>(p.k_param)[row0 + lane];
-        sm.u.loop.vp[warp][lane] = reinterpret_cast<const float4 *>(p.v_param)[row0 + lane];
-        __syncwarp();
+    for (int i = 0; i < kBufs4; ++i)
+        valid_buf[i] = int4_fetch_chunk(p, b, h, tok_begin, nchunks, warp + kWarps4 * i, sm.u.stage[warp][i], lane) >= 0;
 
-        // Q.K, lane = token
-        const bool valid = t0 + lane < tok_end;
-        float dot[G][2];
-#pragma unroll
-        for (int g = 0; g < G; ++g) dot[g][0] = dot[g][1] = 0.0f;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            const int4 kw = *reinterpret_cast<const int4 *>(&sm.u.loop.k[warp][lane][cc * 16]);
-            const uint32_t words[4] = {(uint32_t)kw.x, (uint32_t)kw.y, (uint32_t)kw.z, (uint32_t)kw.w};
-#pragma unroll
-            for (int wi = 0; wi < 4; ++wi) {
-                // 8 dims: byte k holds dims 2k (high nibble) and 2k+1 (low)
-                const uint32_t w = words[wi];
-                const float c[8] = {nib(w, 4), nib(w, 0), nib(w, 12), nib(w, 8),
-                                    nib(w, 20), nib(w, 16), nib(w, 28), nib(w, 24)};
-                const int d0 = cc * 32 + wi * 8;
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float4 qa = *reinterpret_cast<const float4 *>(&sm.q[g][d0]);
-                    const float4 qb = *reinterpret_cast<const float4 *>(&sm.q[g][d0 + 4]);
-                    float a = dot[g][cc >> 1];
-                    a = fmaf(qa.x, c[0], a); a = fmaf(qa.y, c[1], a);
-                    a = fmaf(qa.z, c[2], a); a = fmaf(qa.w, c[3], a);
-                    a = fmaf(qb.x, c[4], a); a = fmaf(qb.y, c[5], a);
-                    a = fmaf(qb.z, c[6], a); a = fmaf(qb.w, c[7], a);
-                    dot[g][cc >> 1] = a;
-                }
-            }
-        }
-        const float4 kp = sm.u.loop.kp[warp][lane];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float s = -INFINITY;
-            if (valid) {
-                const float a0 = kp.x * (dot[g][0] - kp.y * sm.qsum[g][0]);
-                const float a1 = kp.z * (dot[g][1] - kp.w * sm.qsum[g][1]);
-                s = (a0 + a1) * p.sm_scale_log2;
-            }
-            const float m_new = fmaxf(M[g], warp_max(s));  // finite: token t0 is valid
-            const float alpha = exp2f(M[g] - m_new);
-            const float w = valid ? exp2f(s - m_new) : 0.0f;
-            S[g] = S[g] * alpha + warp_sum(w);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[g][j] *= alpha;
-            M[g] = m_new;
-            sm.u.loop.pw[warp][lane][g] = w;
-        }
-        __syncwarp();
-
-        // P.V, lane = dims 4l..4l+3 (bytes 2l, 2l+1 of each V row)
-        const int ntok = min(kChunk4, tok_end - t0);
-        for (int t = 0; t < ntok; ++t) {
-            const uint32_t two = reinterpret_cast<const uint16_t *>(&sm.u.loop.v[warp][t][0])[lane];
-            const float4 vp = sm.u.loop.vp[warp][t];
-            const float vs = vgrp ? vp.z : vp.x, vz = vgrp ? vp.w : vp.y;
-            const float v0 = (nib(two, 4) - vz) * vs, v1 = (nib(two, 0) - vz) * vs;
-            const float v2 = (nib(two, 12) - vz) * vs, v3 = (nib(two, 8) - vz) * vs;
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float pw = sm.u.loop.pw[warp][t][g];
-                acc[g][0] = fmaf(pw, v0, acc[g][0]);
-                acc[g][1] = fmaf(pw, v1, acc[g][1]);
-                acc[g][2] = fmaf(pw, v2, acc[g][2]);
-                acc[g][3] = fmaf(pw, v3, acc[g][3]);
-            }
-        }
-        __syncwarp();
+    const float *qrow = p.q + ((size_t)b * p.nqh + (size_t)h * G) * kHD;
+    // power of two 2^k with max |q| * 2^k in [2^13, 2^14)
+    {
+        float m = 0.0f;
+        for (int i = threadIdx.x; i < G * kHD; i += kWarps4 * 32) m = fmaxf(m, fabsf(qrow[i]));
+        m = warp_max(m);
+        if (lane == 0) sm.qmax[warp] = m;
     }
-
-    // merge the warps' states into one record per query head
     __syncthreads();
+    float qmax = 0.0f;
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) sm.u.red_acc[warp][g][4 * lane + j] = acc[g][j];
-        if (lane == 0) {
-            sm.red_ml[warp][g][0] = M[g];
-            sm.red_ml[warp][g][1] = S[g];
+    for (int w = 0; w < kWarps4; ++w) qmax = fmaxf(qmax, sm.qmax[w]);
+    const int qexp = (qmax > 0.0f && isfinite(qmax)) ? 13 - ilogbf(qmax) : 0;
+    const float qscale = ldexpf(1.0f, max(-120, min(120, qexp)));
+    // A fragments of Q (high and low fp16 parts) in the Q.K k-order; the
+    // values facing high nibbles (k = 2*t4 + e) carry q / 16
+    for (int i = threadIdx.x; i < 8 * 32; i += kWarps4 * 32) {
+        const int ks = i >> 5, ln = i & 31, gg = ln >> 2, tt = ln & 3;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (gg < G) {
+            const float *qg = qrow + (size_t)gg * kHD;
+            const float x0 = qg[qk_dim(ks, 2 * tt)] * qscale * 0.0625f;
+            const float x1 = qg[qk_dim(ks, 2 * tt + 1)] * qscale * 0.0625f;
+            const float x8 = qg[qk_dim(ks, 2 * tt + 8)] * qscale, x9 = qg[qk_dim(ks, 2 * tt + 9)] * qscale;
+            const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+            const __half h8 = __float2half_rn(x8), h9 = __float2half_rn(x9);
+            v.x = pack_half2(__half2float(h0), __half2float(h1));
+            v.y = pack_half2(__half2float(h8), __half2float(h9));
+            v.z = pack_half2(x0 - __half2float(h0), x1 - __half2float(h1));
+            v.w = pack_half2(x8 - __half2float(h8), x9 - __half2float(h9));
         }
+        sm.qa[ks][ln] = v;
+    }
+    {
+        // Y_g, Q_g: 8 threads per (head, group), 8 dims each (even dims face
+        // high nibbles and are fed as q / 16)
+        const int gg = threadIdx.x >> 4, gr = (threadIdx.x >> 3) & 1, part = threadIdx.x & 7;
+        float ys = 0.0f, qs = 0.0f;
+        if (gg < G) {
+#pragma unroll
+            for (int d = 0; d < 8; ++d) {
+                const int dim = 64 * gr + 8 * part + d;
+                const float f = (dim & 1) ? 1.0f : 0.0625f;
+                const float x = qrow[(size_t)gg * kHD + dim] * qscale * f;
+                const float hf = __half2float(__float2half_rn(x));
+                const float y = hf + __half2float(__float2half_rn(x - hf));
+                ys += y;
+                qs += y / f;
+            }
+        }
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            ys += __shfl_xor_sync(0xffffffffu, ys, o);
+            qs += __shfl_xor_sync(0xffffffffu, qs, o);
+        }
+        if (part == 0) {
+            sm.qy[gg][gr] = ys;
+            sm.qq[gg][gr] = qs;
+        }
+    }
+    __syncthreads();
+    const float qy0 = 1024.0f * sm.qy[g][0], qy1 = 1024.0f * sm.qy[g][1];
+    const float qq0 = sm.qq[g][0], qq1 = sm.qq[g][1];
+    const float score_scale = p.sm_scale_log2 / qscale;
+
+    float M = -INFINITY, Sl = 0.0f, Zl[2] = {0.0f, 0.0f}, acc[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[mt][i] = 0.0f;
+    int e_cur = 1000;   // acc and Zl hold values in units of 2^e_cur
+
+    for (int it = 0, cidx = warp; cidx < nchunks; ++it, cidx += kWarps4) {
+        const int bi = it % kBufs4;
+        asm volatile("cp.async.wait_group %0;" ::"n"(kBufs4 - 1) : "memory");
+        __syncwarp();
+        const unsigned char *st = sm.u.stage[warp][bi];
+        const bool have = valid_buf[bi] != 0;
+        if (have) {
+        const int t0 = tok_begin + cidx * kChunk4;
+        const int ntok = min(kChunk4, tok_end - t0);
+        // K: token 8*nt + g, bytes 32*gr + 8*t4 .. +7
+        uint2 kw[4][2];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int gr = 0; gr < 2; ++gr)
+                kw[nt][gr] = *reinterpret_cast<const uint2 *>(st + kStageKOff + (8 * nt + g) * kKPitch4 +
+                                                              32 * kswz(8 * nt + g, gr) + 8 * t4);
+        // V: tokens 16*ks2 + 2*t4 + {0, 1, 8, 9}, bytes 32*gr + 4*g .. +3
+        uint32_t vw[2][4][2];
+#pragma unroll
+        for (int ks2 = 0; ks2 < 2; ++ks2)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int gr = 0; gr < 2; ++gr) {
+                    const int t = 16 * ks2 + 2 * t4 + (j & 1) + 8 * (j >> 1);
+                    vw[ks2][j][gr] = *reinterpret_cast<const uint32_t *>(st + kStageVOff + t * kVPitch4 + 32 * gr + 4 * g);
+                }
+        const float4 *kps = reinterpret_cast<const float4 *>(st + kStageKpOff);
+        const float4 *vps = reinterpret_cast<const float4 *>(st + kStageVpOff);
+        float4 vp[4][2];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) vp[nt][e] = vps[8 * nt + 2 * t4 + e];
+
+        // ---- scores: S^T = Q K^T, head g, tokens 8*nt + 2*t4 + e ----
+        float sc[4][2];
+        float mloc = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const int gr = ks >> 2, sub = ks & 3;
+                const uint32_t w0 = (sub >> 1) ? kw[nt][gr].y : kw[nt][gr].x;
+                const uint32_t w = (sub & 1) ? (w0 >> 8) : w0;
+                const uint32_t b0 = nib_pair(w, kHiNib), b1 = nib_pair(w, kLoNib);
+                const uint4 qa = sm.qa[ks][lane];
+                float(&d)[4] = gr ? d1 : d0;
+                mma_f16_16816(d, qa.x, 0u, qa.y, 0u, b0, b1);
+                mma_f16_16816(d, qa.z, 0u, qa.w, 0u, b0, b1);
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float4 k4 = kps[8 * nt + 2 * t4 + e];
+                const float s = k4.x * (d0[e] - qy0 - k4.y * qq0) + k4.z * (d1[e] - qy1 - k4.w * qq1);
+                const bool valid = 8 * nt + 2 * t4 + e < ntok;
+                sc[nt][e] = valid ? s * score_scale : -INFINITY;
+                mloc = fmaxf(mloc, sc[nt][e]);
+            }
+        }
+        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
+        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
+
+        // power-of-two unit of this chunk's P': 2^e > max V scale (see the q8 decode)
+        float vsmax = 0.0f;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                if (8 * nt + 2 * t4 + e >= ntok) vp[nt][e] = make_float4(0.f, 0.f, 0.f, 0.f);
+                vsmax = fmaxf(vsmax, fmaxf(vp[nt][e].x, vp[nt][e].z));
+            }
+        const int e_need = __reduce_max_sync(0xffffffffu, ((__float_as_int(vsmax) >> 23) & 0xff) - 126);
+        int e_new = e_cur;
+        if (e_need > e_cur || e_need < e_cur - 12) e_new = max(-120, min(120, e_need));
+        const float inv = __int_as_float((127 - e_new) << 23);
+
+        // online softmax per head g (the 4 lanes of row g agree), raised lazily
+        const bool grow = mloc > M + 8.0f;
+        float alpha = 1.0f;
+        bool rescale = e_new != e_cur;
+        if (__any_sync(0xffffffffu, grow)) {
+            rescale = true;
+            const float m_new = fmaxf(M, mloc);
+            alpha = exp2f(M - m_new);   // 0 while M is -inf
+            M = m_new;
+        }
+        const float two = __int_as_float((127 + max(-126, min(127, e_cur - e_new))) << 23);
+        float wsum = 0.0f, z0 = 0.0f, z1 = 0.0f;
+        uint32_t bh[2][2][2], bl[2][2][2];   // [group][k-step][b0, b1]
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            float p0[2], p1[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float w = exp2f(sc[nt][e] - M);    // 0 for invalid tokens (-inf)
+                wsum += w;
+                p0[e] = w * vp[nt][e].x * inv;
+                p1[e] = w * vp[nt][e].z * inv;
+                z0 = fmaf(p0[e], vp[nt][e].y, z0);
+                z1 = fmaf(p1[e], vp[nt][e].w, z1);
+            }
+            const __half h00 = __float2half_rn(p0[0]), h01 = __float2half_rn(p0[1]);
+            const __half h10 = __float2half_rn(p1[0]), h11 = __float2half_rn(p1[1]);
+            bh[0][nt >> 1][nt & 1] = pack_half2(__half2float(h00), __half2float(h01));
+            bh[1][nt >> 1][nt & 1] = pack_half2(__half2float(h10), __half2float(h11));
+            bl[0][nt >> 1][nt & 1] = pack_half2(p0[0] - __half2float(h00), p0[1] - __half2float(h01));
+            bl[1][nt >> 1][nt & 1] = pack_half2(p1[0] - __half2float(h10), p1[1] - __half2float(h11));
+        }
+        Sl = fmaf(Sl, alpha, wsum);
+        Zl[0] = fmaf(Zl[0], alpha * two, z0);
+        Zl[1] = fmaf(Zl[1], alpha * two, z1);
+        if (rescale) {  // warp-uniform; accumulator columns are heads 2*t4, 2*t4 + 1
+            const float f0 = __shfl_sync(0xffffffffu, alpha, 8 * t4) * two;
+            const float f1 = __shfl_sync(0xffffffffu, alpha, 8 * t4 + 4) * two;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                acc[mt][0] *= f0; acc[mt][1] *= f1;
+                acc[mt][2] *= f0; acc[mt][3] *= f1;
+            }
+        }
+        e_cur = e_new;
+
+        // ---- P.V: out^T += V^T P'_g ----
+#pragma unroll
+        for (int ks2 = 0; ks2 < 2; ++ks2) {
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                const int gr = mt >> 2, k = mt & 3;
+                const uint32_t sel = (uint32_t)(k | (k << 4) | ((4 + k) << 8) | ((4 + k) << 12));
+                const uint32_t r01 = __byte_perm(vw[ks2][0][gr], vw[ks2][1][gr], sel);
+                const uint32_t r89 = __byte_perm(vw[ks2][2][gr], vw[ks2][3][gr], sel);
+                const uint32_t a0 = nib_pair_exact(r01, kHiNib), a1 = nib_pair_exact(r01, kLoNib);
+                const uint32_t a2 = nib_pair_exact(r89, kHiNib), a3 = nib_pair_exact(r89, kLoNib);
+                mma_f16_16816(acc[mt], a0, a1, a2, a3, bh[gr][ks2][0], bh[gr][ks2][1]);
+                mma_f16_16816(acc[mt], a0, a1, a2, a3, bl[gr][ks2][0], bl[gr][ks2][1]);
+            }
+        }
+        }
+        __syncwarp();
+        valid_buf[bi] = int4_fetch_chunk(p, b, h, tok_begin, nchunks, cidx + kWarps4 * kBufs4,
+                                         sm.u.stage[warp][bi], lane) >= 0;
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+
+    // ---- this warp's state: head g owns (M, S, Z); accumulator columns are heads 2*t4, 2*t4+1 ----
+    Sl += __shfl_xor_sync(0xffffffffu, Sl, 1);
+    Sl += __shfl_xor_sync(0xffffffffu, Sl, 2);
+#pragma unroll
+    for (int gr = 0; gr < 2; ++gr) {
+        Zl[gr] += __shfl_xor_sync(0xffffffffu, Zl[gr], 1);
+        Zl[gr] += __shfl_xor_sync(0xffffffffu, Zl[gr], 2);
+    }
+    const float unit_scale = __int_as_float((127 + max(-126, min(127, e_cur))) << 23);
+    __syncthreads();   // every warp is done with its staging buffers
+    const float zc[2][2] = {{__shfl_sync(0xffffffffu, Zl[0], 8 * t4), __shfl_sync(0xffffffffu, Zl[1], 8 * t4)},
+                            {__shfl_sync(0xffffffffu, Zl[0], 8 * t4 + 4), __shfl_sync(0xffffffffu, Zl[1], 8 * t4 + 4)}};
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        const int gr = mt >> 2;
+        const int dim = 2 * (32 * gr + 4 * g + (mt & 3));
+        const int h0 = 2 * t4, h1 = 2 * t4 + 1;
+        // rows g carry 16 c (high nibbles: even dims)
+        if (h0 < G) {
+            sm.u.red.acc[warp][h0][dim] = (acc[mt][0] * 0.0625f - zc[0][gr]) * unit_scale;
+            sm.u.red.acc[warp][h0][dim + 1] = (acc[mt][2] - zc[0][gr]) * unit_scale;
+        }
+        if (h1 < G) {
+            sm.u.red.acc[warp][h1][dim] = (acc[mt][1] * 0.0625f - zc[1][gr]) * unit_scale;
+            sm.u.red.acc[warp][h1][dim + 1] = (acc[mt][3] - zc[1][gr]) * unit_scale;
+        }
+    }
+    if (t4 == 0 && g < G) {
+        sm.u.red.ml[warp][g][0] = M;
+        sm.u.red.ml[warp][g][1] = Sl;
     }
     __syncthreads();
     const int d = threadIdx.x;
     const size_t rec = u * p.nsplit + split;
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
+    for (int gq = 0; gq < G; ++gq) {
         float m = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kWarps4; ++w) m = fmaxf(m, sm.red_ml[w][g][0]);
+        for (int w = 0; w < kWarps4; ++w) m = fmaxf(m, sm.u.red.ml[w][gq][0]);
         float s_sum = 0.0f, a = 0.0f;
         if (m != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < kWarps4; ++w) {
-                const float f = exp2f(sm.red_ml[w][g][0] - m);
-                s_sum = fmaf(sm.red_ml[w][g][1], f, s_sum);
-                a = fmaf(sm.u.red_acc[w][g][d], f, a);
+                const float f = exp2f(sm.u.red.ml[w][gq][0] - m);
+                s_sum = fmaf(sm.u.red.ml[w][gq][1], f, s_sum);
+                a = fmaf(sm.u.red.acc[w][gq][d], f, a);
             }
         }
-        p.ws_acc[(rec * G + g) * kHD + d] = a;
+        p.ws_acc[(rec * G + gq) * kHD + d] = a;
         if (d == 0) {
-            p.ws_ml[(rec * G + g) * 2 + 0] = m;
-            p.ws_ml[(rec * G + g) * 2 + 1] = s_sum;
+            p.ws_ml[(rec * G + gq) * 2 + 0] = m;
+            p.ws_ml[(rec * G + gq) * 2 + 1] = s_sum;
         }
     }
 }
 
 }  // namespace
 
-// Splits: enough CTAs for several waves, within the record budget of the
-// decode workspace (kMaxCtas + units records).
-bool make_int4_plan(int batch, int nkv, int max_blocks, int *nsplit, int *split_tokens) {
+// Splits: as many CTAs as are resident at once (one wave; every split of a
+// unit has the same length), within the record budget of the decode
+// workspace (kMaxCtas + units records).
+bool make_int4_plan(int batch, int nkv, int max_blocks, int resident_ctas, int *nsplit, int *split_tokens) {
     const int64_t units = (int64_t)batch * nkv;
     if (units <= 0 || max_blocks <= 0) return false;
     const int64_t cap_tokens = (int64_t)max_blocks * kBS;
-    int64_t ns = (152 * 8 + units - 1) / units;
+    int64_t ns = resident_ctas > 0 ? resident_ctas / units : 1;
     ns = ns < 1 ? 1 : ns;
     ns = ns > 1 + kMaxCtas / units ? 1 + kMaxCtas / units : ns;
     int64_t st = (cap_tokens + ns - 1) / ns;
@@ -306,22 +546,62 @@ bool make_int4_plan(int batch, int nkv, int max_blocks, int *nsplit, int *split_
     return true;
 }
 
+template <int G>
+cudaError_t int4_occupancy(int *per) {
+    cudaError_t e = cudaFuncSetAttribute(int4_decode_split_kernel<G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Int4Smem<G>));
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per, int4_decode_split_kernel<G>, kWarps4 * 32,
+                                                         sizeof(Int4Smem<G>));
+}
+
+// CTAs of the decode kernel for G that the device holds at once.
+int int4_resident_ctas(int group) {
+    static int cached[64][9] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || group < 1 || group > 8) return 0;
+    if (cached[dev][group] == 0) {
+        int sms = 0, per = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cudaError_t e = cudaErrorInvalidValue;
+        switch (group) {
+            case 1: e = int4_occupancy<1>(&per); break;
+            case 2: e = int4_occupancy<2>(&per); break;
+            case 4: e = int4_occupancy<4>(&per); break;
+            case 8: e = int4_occupancy<8>(&per); break;
+            default: break;
+        }
+        if (e != cudaSuccess) return 0;
+        cached[dev][group] = sms * per;
+    }
+    return cached[dev][group];
+}
+
 cudaError_t launch_int4_append(const Int4AppendParams &p, cudaStream_t s) {
     dim3 grid((p.n_new + kAppendWarps4 - 1) / kAppendWarps4, p.nkv, p.batch);
     int4_append_kernel<<<grid, kAppendWarps4 * 32, 0, s>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_int4_decode_split(const Int4DecodeParams &p, int group, cudaStream_t s) {
+template <int G>
+cudaError_t launch_int4_split_g(const Int4DecodeParams &p, cudaStream_t s) {
+    const size_t smem = sizeof(Int4Smem<G>);
+    cudaError_t e = cudaFuncSetAttribute(int4_decode_split_kernel<G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     dim3 grid(p.nsplit, p.nkv, p.batch);
+    int4_decode_split_kernel<G><<<grid, kWarps4 * 32, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_int4_decode_split(const Int4DecodeParams &p, int group, cudaStream_t s) {
     switch (group) {
-        case 1: int4_decode_split_kernel<1><<<grid, kWarps4 * 32, 0, s>>>(p); break;
-        case 2: int4_decode_split_kernel<2><<<grid, kWarps4 * 32, 0, s>>>(p); break;
-        case 4: int4_decode_split_kernel<4><<<grid, kWarps4 * 32, 0, s>>>(p); break;
-        case 8: int4_decode_split_kernel<8><<<grid, kWarps4 * 32, 0, s>>>(p); break;
+        case 1: return launch_int4_split_g<1>(p, s);
+        case 2: return launch_int4_split_g<2>(p, s);
+        case 4: return launch_int4_split_g<4>(p, s);
+        case 8: return launch_int4_split_g<8>(p, s);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace kvq8

@@ -105,7 +105,8 @@ struct Int4DecodeParams {
     float *ws_ml, *ws_acc;        // same record format as DecodeParams
     uint32_t *dev_status;
 };
-bool make_int4_plan(int batch, int nkv, int max_blocks, int *nsplit, int *split_tokens);
+bool make_int4_plan(int batch, int nkv, int max_blocks, int resident_ctas, int *nsplit, int *split_tokens);
+int int4_resident_ctas(int group);
 cudaError_t launch_int4_append(const Int4AppendParams &p, cudaStream_t s);
 cudaError_t launch_int4_decode_split(const Int4DecodeParams &p, int group, cudaStream_t s);
 
