@@ -334,4 +334,63 @@ void orc_int4_dequantize_groups(const uint8_t *packed, const float *scale,
     }
 }
 
+/*
+ * Mixed precision by token age ([UltraQuant] §3.3, "practical note": tokens in
+ * time blocks share one precision; recent blocks stay 8-bit, the oldest are
+ * requantised to 4-bit).  One query head against a context whose first n4
+ * tokens are 4-bit (given here as their dequantised fp32 rows k4, v4) and
+ * whose remaining L8 tokens are int8 (codes and per-row scales).  Scores: the
+ * fp32 query against k4 for the old tokens ([UltraQuant] §4.1: dequantise,
+ * then standard attention); the [Day 9-2] integer block dots for the recent
+ * ones.  Then the same three passes as orc_decode_q8_three_pass over the
+ * concatenated sequence (old first), all in fp64.
+ */
+int orc_decode_mixed(const float *q, const int8_t *qi, const float *qsc, int hd,
+                     const float *k4, const float *v4, int64_t n4,
+                     const int8_t *kq, const float *ks, const int8_t *vq, const float *vs,
+                     int64_t L8, float sm_scale, double *out)
+{
+    for (int i = 0; i < hd; ++i)
+        out[i] = 0.0;
+    const int64_t L = n4 + L8;
+    if (L <= 0)
+        return 0;
+    double *s = (double *)malloc((size_t)L * sizeof(double));
+    if (!s)
+        return -1;
+    /* pass 1: scores */
+    for (int64_t t = 0; t < n4; ++t) {
+        double d = 0.0;
+        for (int i = 0; i < hd; ++i)
+            d += (double)q[i] * (double)k4[t * (int64_t)hd + i];
+        s[t] = d * (double)sm_scale;
+    }
+    if (L8 > 0)
+        scores_q8(qi, qsc, hd, kq, ks, L8, (double)sm_scale, s + n4);
+    double mu = s[0];
+    for (int64_t t = 1; t < L; ++t)
+        if (s[t] > mu)
+            mu = s[t];
+    /* pass 2: exponentials and their sum */
+    double S = 0.0;
+    for (int64_t t = 0; t < L; ++t) {
+        s[t] = exp(s[t] - mu);
+        S += s[t];
+    }
+    /* pass 3: weighted sum of the dequantised V rows */
+    for (int64_t t = 0; t < n4; ++t) {
+        const double w = s[t] / S;
+        for (int i = 0; i < hd; ++i)
+            out[i] += w * (double)v4[t * (int64_t)hd + i];
+    }
+    for (int64_t t = 0; t < L8; ++t) {
+        const double w = s[n4 + t] / S;
+        const int8_t *vt = vq + t * (int64_t)hd;
+        for (int i = 0; i < hd; ++i)
+            out[i] += w * ((double)vt[i] * (double)vs[t]);
+    }
+    free(s);
+    return 0;
+}
+
 int orc_version(void) { return 1; }

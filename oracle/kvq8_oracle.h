@@ -35,6 +35,10 @@ void orc_int4_quantize_groups(const float *x, int64_t n, int group,
 void orc_int4_dequantize_groups(const uint8_t *packed, const float *scale,
                                 const float *zero, int64_t n, int group,
                                 float *out);
+int orc_decode_mixed(const float *q, const int8_t *qi, const float *qsc, int hd,
+                     const float *k4, const float *v4, int64_t n4,
+                     const int8_t *kq, const float *ks, const int8_t *vq, const float *vs,
+                     int64_t L8, float sm_scale, double *out);
 int orc_version(void);
 
 #ifdef __cplusplus

@@ -66,6 +66,7 @@ def _load():
             "orc_attention_f64": (i32, [P, P, P, i64, i32, f32, P]),
             "orc_int4_quantize_groups": (None, [P, i64, i32, P, P, P]),
             "orc_int4_dequantize_groups": (None, [P, P, P, i64, i32, P]),
+            "orc_decode_mixed": (i32, [P, P, P, i32, P, P, i64, P, P, P, P, i64, f32, P]),
             "orc_version": (i32, []),
         }
         for name, (res, args) in sig.items():
@@ -230,6 +231,41 @@ def decode_quantized_unit(qi, qsc, kq, ks, vq, vs, sm_scale):
     out = np.empty((G, hd), np.float64)
     for g in range(G):
         out[g] = decode_q8_three_pass(qi[g], qsc[g], kq, ks, vq, vs, sm_scale)
+    return out
+
+
+def requantize_q8_to_q4(kq, ks, group=64):
+    """An int8 row's dequantised values requantised by the INT4 group rule
+    ([UltraQuant] §3.3: the oldest time blocks go from 8-bit to 4-bit).
+    Returns (packed, scale, zero)."""
+    return int4_quantize_groups(kv_dequantize_rows(kq, ks), group)
+
+
+def decode_mixed_unit(q_heads, k_rows, v_rows, n4, sm_scale):
+    """Mixed precision by token age for one (sequence, kv head): every token
+    is first cached as int8; the first n4 tokens (the old time blocks) are then
+    requantised to INT4 group-64; the decode reads the old tokens as 4-bit and
+    the recent ones as int8 (orc_decode_mixed).  Returns out fp64 [G][hd]."""
+    kq, ks = kv_quantize_rows(k_rows)
+    vq, vs = kv_quantize_rows(v_rows)
+    qi, qsc = q_quantize_blocks(q_heads)
+    n4 = int(n4)
+    k4 = int4_dequantize_groups(*requantize_q8_to_q4(kq[:n4], ks[:n4]))
+    v4 = int4_dequantize_groups(*requantize_q8_to_q4(vq[:n4], vs[:n4]))
+    G, hd = q_heads.shape
+    q_heads = _c(q_heads, np.float32)
+    k4, v4 = _c(k4, np.float32), _c(v4, np.float32)
+    kr, ksr = _c(kq[n4:], np.int8), _c(ks[n4:], np.float32)
+    vr, vsr = _c(vq[n4:], np.int8), _c(vs[n4:], np.float32)
+    out = np.empty((G, hd), np.float64)
+    for g in range(G):
+        row = np.empty(hd, np.float64)
+        qg, qig, qscg = _c(q_heads[g], np.float32), _c(qi[g], np.int8), _c(qsc[g], np.float32)
+        rc = _load().orc_decode_mixed(_p(qg), _p(qig), _p(qscg), hd, _p(k4), _p(v4), n4,
+                                      _p(kr), _p(ksr), _p(vr), _p(vsr), len(kr), float(sm_scale),
+                                      _p(row))
+        assert rc == 0
+        out[g] = row
     return out
 
 

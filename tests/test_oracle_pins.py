@@ -411,3 +411,56 @@ def test_int4_nibble_order_high_first():
     x[0], x[1] = 1.0, 0.0    # group min 0, max 1: scale 1/15, zero 0; codes 15 and 0
     packed, scale, zero = oracle.int4_quantize_groups(x, 64)
     assert zero[0] == 0.0 and packed[0] == 0xF0 and not packed[1:].any()
+
+
+# ---------------------------------------------------------------------------
+# mixed precision by token age (UltraQuant §3.3): old blocks 4-bit, recent int8
+# ---------------------------------------------------------------------------
+def test_mixed_with_no_old_tokens_is_the_q8_path():
+    q, k, v = _random_unit(31, 700, G=2)
+    mixed = oracle.decode_mixed_unit(q, k, v, 0, SM)
+    ref, _ = oracle.decode_unit_q8(q, k, v, SM)
+    assert np.max(np.abs(mixed - ref)) < 1e-15
+
+
+def test_mixed_with_only_old_tokens_is_attention_over_requantised_rows():
+    q, k, v = _random_unit(32, 512, G=2)
+    kq, ks = oracle.kv_quantize_rows(k)
+    vq, vs = oracle.kv_quantize_rows(v)
+    k4 = oracle.int4_dequantize_groups(*oracle.int4_quantize_groups(oracle.kv_dequantize_rows(kq, ks)))
+    v4 = oracle.int4_dequantize_groups(*oracle.int4_quantize_groups(oracle.kv_dequantize_rows(vq, vs)))
+    mixed = oracle.decode_mixed_unit(q, k, v, 512, SM)
+    ref = _sdpa64(q, k4[None], v4[None], float(SM))
+    assert np.max(np.abs(mixed - ref)) < 1e-12
+
+
+@pytest.mark.parametrize("n4", [256, 512, 768])
+def test_mixed_equals_one_softmax_over_both_parts(n4):
+    # an independent route with torch in fp64: the old tokens' logits from the
+    # fp32 query and the requantised rows, the recent tokens' logits from the
+    # dequantised query blocks and int8 rows (equal, exactly, to the integer
+    # block dots times their scales); one softmax over the concatenation
+    q, k, v = _random_unit(33, 1000, G=2)
+    kq, ks = oracle.kv_quantize_rows(k)
+    vq, vs = oracle.kv_quantize_rows(v)
+    qi, qsc = oracle.q_quantize_blocks(q)
+    T = lambda a: torch.from_numpy(np.asarray(a, np.float64))
+    k4 = oracle.int4_dequantize_groups(*oracle.int4_quantize_groups(oracle.kv_dequantize_rows(kq[:n4], ks[:n4])))
+    v4 = oracle.int4_dequantize_groups(*oracle.int4_quantize_groups(oracle.kv_dequantize_rows(vq[:n4], vs[:n4])))
+    qdeq = T(qi) * T(np.repeat(qsc, 32, axis=1))
+    k8 = T(kq[n4:]) * T(ks[n4:])[:, None]
+    v8 = T(vq[n4:]) * T(vs[n4:])[:, None]
+    logits = torch.cat([T(q) @ T(k4).T, qdeq @ k8.T], dim=1) * float(SM)
+    w = torch.softmax(logits, dim=1)
+    ref = (w @ torch.cat([T(v4), v8], dim=0)).numpy()
+    mixed = oracle.decode_mixed_unit(q, k, v, n4, SM)
+    assert np.max(np.abs(mixed - ref)) < 1e-12
+
+
+def test_requantised_rows_stay_within_both_half_steps():
+    x = _rows(34, 200, 3.0)
+    kq, ks = oracle.kv_quantize_rows(x)
+    packed, sc, zr = oracle.requantize_q8_to_q4(kq, ks)
+    y = oracle.int4_dequantize_groups(packed, sc, zr)
+    bound = 0.5 * ks[:, None] * 1.0001 + 0.5 * np.repeat(sc, 64, axis=1) * 1.0001
+    assert np.all(np.abs(y.astype(np.float64) - x) <= bound)
