@@ -659,6 +659,138 @@ def run_kvq4(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------ mixed precision by age ---
+def mixed_step_bytes(cfg, lens, n4):
+    """Algorithmic bytes of one mixed decode: 160 B per (token, kv head) for the
+    4-bit tokens, 264 B for the int8 tokens, the fp32 query and output."""
+    import numpy as np
+    lens = np.asarray(lens, np.int64)
+    old = np.minimum(lens, 256 * np.asarray(n4, np.int64))
+    t4, t8 = int(old.sum()), int((lens - old).sum())
+    return (t4 * cfg.nkv * 2 * (cfg.hd // 2 + 16) + t8 * cfg.nkv * (2 * cfg.hd + 8) +
+            2 * cfg.batch * cfg.nqh * cfg.hd * 4)
+
+
+def run_mixed(args, rank, world, local):
+    """Mixed precision by token age: every sequence's recent blocks in int8, the
+    older ones requantised to 4-bit; a step is one decode over both
+    (kvmix_decode_attn: 4-bit split, int8 split, one combine).  The
+    requantisation of a block runs once per 256 generated tokens and is not in
+    the step."""
+    import numpy as np
+    import torch
+    from int8_quantized_kv_gb300 import kvq8
+    from int8_quantized_kv_gb300 import workloads as wl
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist_init(world, "nccl")
+    kvq8.load()
+    cfg = wl.WORKLOADS[args.workload]
+    lens = wl.ctx_lens(cfg)
+    n4 = wl.mixed_old_blocks(lens)
+    table, num_blocks = wl.block_table(cfg, lens)
+    max_blocks = table.shape[1]
+    table4 = np.random.default_rng(1000 * cfg.config_id + 77).permutation(num_blocks)[:table.size]
+    table4 = table4.astype(np.int32).reshape(table.shape)
+    cache_bytes = num_blocks * 256 * (kvq8.cache_bytes_per_token(cfg.nkv) + kvq8.cache4_bytes_per_token(cfg.nkv))
+    copies = args.copies or max(2, math.ceil(8 * L2_BYTES / cache_bytes))
+    sm = 1.0 / math.sqrt(cfg.hd)
+    c8 = kvq8.alloc_cache(num_blocks, cfg.nkv, dev)
+    c4 = kvq8.alloc_cache4(num_blocks, cfg.nkv, dev)
+    table_d, table4_d = torch.from_numpy(table).to(dev), torch.from_numpy(table4).to(dev)
+    zero = torch.zeros(1, dtype=torch.int32, device=dev)
+    for b in range(cfg.batch):
+        L = int(lens[b])
+        k, v = wl.seq_kv(cfg, b, L)
+        kvq8.quantize_append(torch.from_numpy(k[None]).to(dev), torch.from_numpy(v[None]).to(dev), zero,
+                             table_d[b:b + 1], c8)
+    n4_d = torch.from_numpy(n4).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    kvq8.requantize_blocks(c8, table_d, c4, table4_d, torch.zeros_like(n4_d), n4_d, max(1, int(n4.max())),
+                           dev_status=status)
+    pairs = [(c8, c4)] + [(kvq8.KVCache(*[t.clone() for t in c8]), kvq8.KV4Cache(*[t.clone() for t in c4]))
+                          for _ in range(copies - 1)]
+    q_d = torch.from_numpy(wl.queries(cfg)).to(dev)
+    lens_d = torch.from_numpy(lens).to(dev)
+    ws = kvq8.alloc_mixed_workspace(cfg.batch, cfg.nqh, cfg.nkv, max_blocks, dev)
+    out = torch.empty_like(q_d)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        a, b4 = pairs[i % copies]
+        kvq8.decode_attn_mixed(q_d, a, table_d, b4, table4_d, lens_d, n4_d, out, ws, sm_scale=sm,
+                               dev_status=status, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item():#x} during warm-up")
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(i)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier()
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item():#x} in the timed region")
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    sbytes = mixed_step_bytes(cfg, lens, n4)
+    total_bytes, slowest = aggregate(sbytes * args.steps, elapsed, dev)
+    per_step = slowest / args.steps
+    value = total_bytes / slowest / 1e9
+
+    e2e_steps = args.e2e_steps or min(args.steps, 2000)
+    q_h = torch.from_numpy(wl.queries(cfg)).pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def e2e_step(i):
+        q_d.copy_(q_h, non_blocking=True)
+        step(i)
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for i in range(3):
+        e2e_step(i)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e2e_s = time.perf_counter() - t0
+    e_total, e_slowest = aggregate(sbytes * e2e_steps, e2e_s, dev)
+    peak, peak_kind = hbm_peak()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 5),
+        "us_per_step": round(per_step * 1e6, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8+int4", "data": "synthetic",
+        "config": dict(workload_config(cfg, lens, copies), parallelism=f"replicas{world}",
+                       bytes_per_step=sbytes, old_blocks_4bit=int(n4.max()),
+                       recent_blocks_int8=wl.MIXED_RECENT_BLOCKS,
+                       format="old 256-token blocks INT4 group-64 (requantised from int8), recent blocks int8",
+                       step="mixed decode (4-bit split + int8 split + combine); no append"),
+        "pct_of_hbm_peak": round(100 * (value / world) / peak, 2),
+        "roofline": {"bound": "hbm", "kernel": "kvmix_decode_attn (both splits + combine)",
+                     "achieved": round(value / world, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round((value / world) / peak, 4), "peak_kind": peak_kind, "traffic": None,
+                     "algorithmic_bytes_per_launch": sbytes, "us_per_launch": round(per_step * 1e6, 3)},
+        "e2e": {"value": round(e_total / e_slowest / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": q_h.numel() * 4, "d2h_bytes_per_step": out_h.numel() * 4,
+                "us_per_step": round(e_slowest / e2e_steps * 1e6, 2), "steps": e2e_steps},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------- bulk append ---
 def run_append(args, rank, world, local):
     """Quantise-append of n_new tokens per sequence (all kv heads) into the q8
@@ -753,7 +885,7 @@ def run_reference(args, rank, world):
         return
     import numpy as np
     from int8_quantized_kv_gb300 import workloads as wl
-    if args.workload.startswith(("int4", "append")):
+    if args.workload.startswith(("int4", "append", "mixed")):
         raise SystemExit("the reference arm times the q8 decode step; pick a decode workload")
     cfg = wl.WORKLOADS[args.workload]
     lens = wl.ctx_lens(cfg)
@@ -798,6 +930,8 @@ def main(argv=None):
         run_kvq4(args, rank, world, local)
     elif args.workload.startswith("append"):
         run_append(args, rank, world, local)
+    elif args.workload.startswith("mixed"):
+        run_mixed(args, rank, world, local)
     else:
         run_kvq8(args, rank, world, local)
 

@@ -274,6 +274,64 @@ kvq8_status kvq4_decode_attn(const float *q, int batch, int nqh, int nkv, int hd
                              float *out, void *workspace, size_t workspace_bytes,
                              uint32_t *dev_status, void *stream);
 
+/* ------------------------- mixed precision by token age (NEXT row) --- */
+
+/*
+ * [UltraQuant] §3.3 (time-adaptive quantisation, its practical note): tokens
+ * in a time block share one precision; recent blocks stay 8-bit and, as the
+ * sequence grows, the oldest blocks are requantised to 4-bit.  Here a time
+ * block is a cache block of 256 tokens: for sequence b the logical blocks
+ * [0, n4_blocks[b]) live in the 4-bit cache (tiles table4[b][j]) and the
+ * later ones in the int8 cache (tiles table8[b][j]); both tables have
+ * max_blocks columns and are indexed by the logical block.  The page's 2-bit
+ * tier is not defined there and is not built.
+ *
+ * kvmix_requantize -- for every sequence b, requantise the logical blocks
+ * [blk_from[b], blk_to[b]) (whole 256-token tiles, K and V) from the int8
+ * tiles to the 4-bit tiles: value = code * scale (fp32), then the 4-bit group
+ * rule of kvq4_quantize_append.  max_count >= max_b (blk_to[b] - blk_from[b])
+ * sizes the grid.  A range outside [0, max_blocks) or longer than max_count
+ * sets KVQ8_DEV_BAD_POSITION (the part inside is still done); a tile id
+ * outside its pool sets KVQ8_DEV_BAD_BLOCK_ID and is skipped.  The int8 tiles
+ * are left as they were.
+ */
+kvq8_status kvmix_requantize(int batch, int nkv, int hd,
+                             const int8_t *k_pool, const int8_t *v_pool,
+                             const float *k_scale, const float *v_scale,
+                             int num_blocks8, const int32_t *table8,
+                             uint8_t *k_codes, uint8_t *v_codes,
+                             float *k_param, float *v_param,
+                             int num_blocks4, const int32_t *table4,
+                             int max_blocks, int block_size,
+                             const int32_t *blk_from, const int32_t *blk_to, int max_count,
+                             uint32_t *dev_status, void *stream);
+
+/* Workspace of kvmix_decode_attn: twice kvq8_decode_workspace_bytes. */
+size_t kvmix_decode_workspace_bytes(int batch, int nqh, int nkv, int hd, int max_blocks,
+                                    int block_size);
+
+/*
+ * kvmix_decode_attn -- decode attention of sequence b over its tokens
+ * [0, 256 * n4_blocks[b]) in the 4-bit cache (fp32 query against the
+ * dequantised rows, as kvq4_decode_attn) and [256 * n4_blocks[b], ctx_lens[b])
+ * in the int8 cache (the q8 method of kvq8_decode_attn): both splits' partial
+ * results are merged by one combine, so the softmax is taken over the whole
+ * context.  n4_blocks: device int32 [batch] (values clamped to
+ * [0, max_blocks]).  Other arguments as kvq8_decode_attn and kvq4_decode_attn.
+ */
+kvq8_status kvmix_decode_attn(const float *q, int batch, int nqh, int nkv, int hd,
+                              const int8_t *k_pool, const int8_t *v_pool,
+                              const float *k_scale, const float *v_scale,
+                              int num_blocks8, const int32_t *table8,
+                              const uint8_t *k_codes, const uint8_t *v_codes,
+                              const float *k_param, const float *v_param,
+                              int num_blocks4, const int32_t *table4,
+                              int max_blocks, int block_size,
+                              const int32_t *ctx_lens, const int32_t *n4_blocks,
+                              float sm_scale, float *out,
+                              void *workspace, size_t workspace_bytes,
+                              uint32_t *dev_status, void *stream);
+
 /* --------------------------------------- fp32 cache (comparator row) --- */
 
 /*

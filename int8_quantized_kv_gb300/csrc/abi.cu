@@ -74,6 +74,10 @@ kvq8_status fill_decode_params(const float *q, int batch, int nqh, int nkv,
     p->ws_acc = (float *)(ws + plan->acc_offset);
     p->dev_status = dev_status;
     p->out = nullptr;
+    p->first_q8_block = nullptr;
+    p->ws_meta2 = nullptr;
+    p->ws_ml2 = nullptr;
+    p->ws_acc2 = nullptr;
     return KVQ8_OK;
 }
 
@@ -352,6 +356,7 @@ kvq8_status kvq4_decode_attn(const float *q, int batch, int nqh, int nkv, int hd
     c.out = out;
     Int4DecodeParams p;
     p.q = q;
+    p.n4_blocks = nullptr;
     p.batch = batch;
     p.nqh = nqh;
     p.nkv = nkv;
@@ -459,6 +464,123 @@ kvq8_status kvf32_decode_attn(const float *q, int batch, int nqh, int nkv, int h
     p.dev_status = dev_status;
     cudaStream_t s = (cudaStream_t)stream;
     if (launch_f32_decode_split(p, plan.group, s) != cudaSuccess) return KVQ8_ERR_CUDA;
+    if (launch_decode_combine(c, plan.group, s) != cudaSuccess) return KVQ8_ERR_CUDA;
+    return KVQ8_OK;
+}
+
+size_t kvmix_decode_workspace_bytes(int batch, int nqh, int nkv, int hd, int max_blocks,
+                                    int block_size) {
+    const size_t one = kvq8_decode_workspace_bytes(batch, nqh, nkv, hd, max_blocks, block_size);
+    return 2 * one;
+}
+
+kvq8_status kvmix_requantize(int batch, int nkv, int hd, const int8_t *k_pool, const int8_t *v_pool,
+                             const float *k_scale, const float *v_scale, int num_blocks8,
+                             const int32_t *table8, uint8_t *k_codes, uint8_t *v_codes,
+                             float *k_param, float *v_param, int num_blocks4, const int32_t *table4,
+                             int max_blocks, int block_size, const int32_t *blk_from,
+                             const int32_t *blk_to, int max_count, uint32_t *dev_status,
+                             void *stream) {
+    kvq8_status st = check_shape(hd, block_size);
+    if (st != KVQ8_OK) return st;
+    if (batch < 0 || nkv <= 0 || num_blocks8 <= 0 || num_blocks4 <= 0 || max_blocks <= 0 ||
+        max_count < 0)
+        return KVQ8_ERR_INVALID_ARG;
+    if (max_blocks > 2147483647 / kBS) return KVQ8_ERR_UNSUPPORTED;
+    if (batch > kMaxGridYZ || nkv > kMaxGridYZ) return KVQ8_ERR_UNSUPPORTED;
+    if (batch == 0 || max_count == 0) return KVQ8_OK;
+    if (!k_pool || !v_pool || !k_scale || !v_scale || !table8 || !k_codes || !v_codes ||
+        !k_param || !v_param || !table4 || !blk_from || !blk_to)
+        return KVQ8_ERR_INVALID_ARG;
+    if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(k_scale, 4) ||
+        !aligned(v_scale, 4) || !aligned(k_codes, 16) || !aligned(v_codes, 16) ||
+        !aligned(k_param, 16) || !aligned(v_param, 16) || !aligned(table8, 4) ||
+        !aligned(table4, 4) || !aligned(blk_from, 4) || !aligned(blk_to, 4))
+        return KVQ8_ERR_INVALID_ARG;
+    Int4RequantParams p;
+    p.batch = batch;
+    p.nkv = nkv;
+    p.k_pool = k_pool;
+    p.v_pool = v_pool;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.num_blocks8 = num_blocks8;
+    p.table8 = table8;
+    p.k_codes = k_codes;
+    p.v_codes = v_codes;
+    p.k_param = k_param;
+    p.v_param = v_param;
+    p.num_blocks4 = num_blocks4;
+    p.table4 = table4;
+    p.max_blocks = max_blocks;
+    p.blk_from = blk_from;
+    p.blk_to = blk_to;
+    p.max_count = max_count;
+    p.dev_status = dev_status;
+    if (launch_int4_requantize(p, (cudaStream_t)stream) != cudaSuccess) return KVQ8_ERR_CUDA;
+    return KVQ8_OK;
+}
+
+kvq8_status kvmix_decode_attn(const float *q, int batch, int nqh, int nkv, int hd,
+                              const int8_t *k_pool, const int8_t *v_pool, const float *k_scale,
+                              const float *v_scale, int num_blocks8, const int32_t *table8,
+                              const uint8_t *k_codes, const uint8_t *v_codes, const float *k_param,
+                              const float *v_param, int num_blocks4, const int32_t *table4,
+                              int max_blocks, int block_size, const int32_t *ctx_lens,
+                              const int32_t *n4_blocks, float sm_scale, float *out, void *workspace,
+                              size_t workspace_bytes, uint32_t *dev_status, void *stream) {
+    kvq8_status st = check_decode_args(q, batch, nqh, nkv, hd, k_pool, v_pool, k_scale, v_scale,
+                                       num_blocks8, table8, max_blocks, block_size, ctx_lens);
+    if (st != KVQ8_OK || batch == 0) return st;
+    st = check_decode_args(q, batch, nqh, nkv, hd, (const int8_t *)k_codes, (const int8_t *)v_codes,
+                           k_param, v_param, num_blocks4, table4, max_blocks, block_size, ctx_lens);
+    if (st != KVQ8_OK) return st;
+    if (!out || !aligned(out, 16) || !isfinite(sm_scale) || !n4_blocks || !aligned(n4_blocks, 4))
+        return KVQ8_ERR_INVALID_ARG;
+    DecodePlan plan;
+    if (!make_decode_plan(batch, nqh, nkv, max_blocks, &plan)) return KVQ8_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < 2 * plan.bytes)
+        return KVQ8_ERR_WORKSPACE;
+    // first half: the int8 split's records; second half: the 4-bit split's
+    DecodeParams c, c4;
+    st = fill_decode_params(q, batch, nqh, nkv, k_pool, v_pool, k_scale, v_scale, num_blocks8,
+                            table8, max_blocks, ctx_lens, sm_scale, workspace, plan.bytes,
+                            dev_status, &c, &plan);
+    if (st != KVQ8_OK) return st;
+    st = fill_decode_params(q, batch, nqh, nkv, nullptr, nullptr, nullptr, nullptr, num_blocks4,
+                            table4, max_blocks, ctx_lens, sm_scale, (char *)workspace + plan.bytes,
+                            plan.bytes, dev_status, &c4, &plan);
+    if (st != KVQ8_OK) return st;
+    c.out = out;
+    c.first_q8_block = n4_blocks;
+    c.ws_meta2 = c4.ws_meta;
+    c.ws_ml2 = c4.ws_ml;
+    c.ws_acc2 = c4.ws_acc;
+    Int4DecodeParams p;
+    p.q = q;
+    p.n4_blocks = n4_blocks;
+    p.batch = batch;
+    p.nqh = nqh;
+    p.nkv = nkv;
+    p.k_codes = k_codes;
+    p.v_codes = v_codes;
+    p.k_param = k_param;
+    p.v_param = v_param;
+    p.num_blocks = num_blocks4;
+    p.block_table = table4;
+    p.max_blocks = max_blocks;
+    p.ctx_lens = ctx_lens;
+    p.sm_scale_log2 = c.sm_scale_log2;
+    if (!make_int4_plan(batch, nkv, max_blocks, int4_resident_ctas(plan.group), &p.nsplit,
+                        &p.split_tokens))
+        return KVQ8_ERR_INVALID_ARG;
+    p.ws_meta = c4.ws_meta;
+    p.ws_ml = c4.ws_ml;
+    p.ws_acc = c4.ws_acc;
+    p.dev_status = dev_status;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (launch_int4_decode_split(p, plan.group, s) != cudaSuccess) return KVQ8_ERR_CUDA;
+    if (launch_decode_split(c, plan.group, s) != cudaSuccess) return KVQ8_ERR_CUDA;
     if (launch_decode_combine(c, plan.group, s) != cudaSuccess) return KVQ8_ERR_CUDA;
     return KVQ8_OK;
 }

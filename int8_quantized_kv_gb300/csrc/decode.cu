@@ -87,6 +87,16 @@ struct Misc {
 
 __device__ __forceinline__ int clamp_len(int L, int cap) { return max(0, min(L, cap)); }
 
+// The tokens [x, y) of sequence b that this launch decodes: [0, L) normally;
+// [256 * first_q8_block[b], L) when the older blocks of the sequence are held
+// in the 4-bit cache (mixed precision by token age).
+__device__ __forceinline__ int2 seq_span(const DecodeParams &p, int b, int cap) {
+    const int L = clamp_len(p.ctx_lens[b], cap);
+    const int s = p.first_q8_block ? min(L, max(0, min(p.first_q8_block[b], cap / kBS)) * kBS) : 0;
+    return make_int2(s, L);
+}
+__device__ __forceinline__ int span_stages(int2 sp) { return (sp.y - sp.x + kStageTok - 1) / kStageTok; }
+
 __device__ __forceinline__ uint32_t half2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 
 // int8 codes of 4 consecutive tokens -> two fp16 pairs (tokens 0,1 and 2,3),
@@ -164,7 +174,7 @@ decode_split_kernel(DecodeParams p) {
     for (int b = b_lo; b < b_hi; ++b) {
         const int L = p.ctx_lens[b];
         if (c == 0 && (L < 0 || L > cap)) flag_status(p.dev_status, KVQ8_DEV_BAD_CTX_LEN);
-        mine += (long long)p.nkv * ((clamp_len(L, cap) + kStageTok - 1) / kStageTok);
+        mine += (long long)p.nkv * span_stages(seq_span(p, b, cap));
     }
     long long incl = mine;
 #pragma unroll
@@ -194,8 +204,7 @@ decode_split_kernel(DecodeParams p) {
     if (mine > 0 && excl <= lo && lo < excl + mine) {
         long long acc = excl;
         for (int b = b_lo; b < b_hi; ++b) {
-            const long long n =
-                (long long)p.nkv * ((clamp_len(p.ctx_lens[b], cap) + kStageTok - 1) / kStageTok);
+            const long long n = (long long)p.nkv * span_stages(seq_span(p, b, cap));
             if (lo < acc + n) {
                 misc->b0 = b;
                 misc->base = acc;
@@ -209,7 +218,7 @@ decode_split_kernel(DecodeParams p) {
     int b = 0, h = 0, off = 0;
     if (hi > lo) {
         b = misc->b0;
-        const int nb = (clamp_len(p.ctx_lens[b], cap) + kStageTok - 1) / kStageTok;
+        const int nb = span_stages(seq_span(p, b, cap));
         const long long rel = lo - misc->base;
         h = (int)(rel / nb);
         off = (int)(rel % nb);
@@ -222,8 +231,8 @@ decode_split_kernel(DecodeParams p) {
         long long remaining = hi - lo;
         int kbase = 0;
         while (remaining > 0 && b < p.batch) {
-            const int L = clamp_len(p.ctx_lens[b], cap);
-            const int nb = (L + kStageTok - 1) / kStageTok;
+            const int2 sp = seq_span(p, b, cap);
+            const int nb = span_stages(sp);
             if (nb == 0) { ++b; h = 0; off = 0; continue; }
             const int seg_n = (int)min((long long)(nb - off), remaining);
             const int32_t *row = p.block_table + (size_t)b * p.max_blocks;
@@ -231,7 +240,7 @@ decode_split_kernel(DecodeParams p) {
             for (int j = 0; j < seg_n; ++j) {
                 const int k = kbase + j, slot = k % Lay::kStages;
                 const uint32_t par = ((k / Lay::kStages) & 1) ^ 1;
-                const int t0 = (off + j) * kStageTok;
+                const int t0 = sp.x + (off + j) * kStageTok;
                 const int lb = t0 / kBS, quarter = (t0 / kStageTok) & 3;
                 if (tbl_base < 0 || lb >= tbl_base + 32) {
                     tbl_base = lb;
@@ -291,8 +300,9 @@ decode_split_kernel(DecodeParams p) {
         long long remaining = hi - lo;
         int kbase = 0;
         while (remaining > 0 && b < p.batch) {
-            const int L = clamp_len(p.ctx_lens[b], cap);
-            const int nb = (L + kStageTok - 1) / kStageTok;
+            const int2 sp = seq_span(p, b, cap);
+            const int L = sp.y;
+            const int nb = span_stages(sp);
             if (nb == 0) { ++b; h = 0; off = 0; continue; }
             const int seg_n = (int)min((long long)(nb - off), remaining);
             const int u = b * p.nkv + h;
@@ -325,7 +335,7 @@ decode_split_kernel(DecodeParams p) {
                     const int8_t *vst = kst + kStageKBytes;
                     const float *ks_st = reinterpret_cast<const float *>(st + kStageKBytes + kStageVBytes);
                     const float *vs_st = ks_st + kStageTok;
-                    const int nvalid = min(kStageTok, L - (off + j) * kStageTok);
+                    const int nvalid = min(kStageTok, L - (sp.x + (off + j) * kStageTok));
                     const int ta = lane, tb = lane + 32;
                     const bool va = ta < nvalid, vb = tb < nvalid;
 
@@ -530,26 +540,39 @@ decode_split_kernel(DecodeParams p) {
 // Merge of the partial records of one (sequence, query head); thread = dim.
 // [Day 9-2] §2 segment 3 generalised to several partial states:
 // M = max_i M_i, S = sum_i S_i 2^(M_i - M), out = sum_i acc_i 2^(M_i - M) / S.
+// The records come from one split kernel, or from two (mixed precision by
+// token age: the 4-bit split over [0, x) and the int8 split over [x, L)).
 __global__ void __launch_bounds__(kHD)
 decode_combine_kernel(DecodeParams p, int G) {
     pdl_wait();  // the split kernel's records are visible after this
     const int qh = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
     const int h = qh / G, g = qh % G;
-    const int L = max(0, min(p.ctx_lens[b], p.max_blocks * kBS));
+    const int cap = p.max_blocks * kBS;
+    const int2 sp = seq_span(p, b, cap);
     float *o = p.out + ((size_t)b * p.nqh + qh) * kHD + d;
-    if (L == 0) { *o = 0.0f; return; }
+    if (sp.y == 0) { *o = 0.0f; return; }
     const size_t u = (size_t)b * p.nkv + h;
-    const int2 meta = p.ws_meta[u];
-    const size_t rec0 = (size_t)meta.x + u;
+    // source 0: this decode's records over [x, L); source 1: the 4-bit split's over [0, x)
+    const bool has0 = sp.y > sp.x, has1 = p.ws_meta2 != nullptr && sp.x > 0;
+    const int2 meta0 = has0 ? p.ws_meta[u] : make_int2(0, 0);
+    const int2 meta1 = has1 ? p.ws_meta2[u] : make_int2(0, 0);
+    const size_t r00 = (size_t)meta0.x + u, r10 = (size_t)meta1.x + u;
     float m = -INFINITY;
-    for (int j = 0; j < meta.y; ++j) m = fmaxf(m, p.ws_ml[((rec0 + j) * G + g) * 2]);
+    for (int j = 0; j < meta0.y; ++j) m = fmaxf(m, p.ws_ml[((r00 + j) * G + g) * 2]);
+    for (int j = 0; j < meta1.y; ++j) m = fmaxf(m, p.ws_ml2[((r10 + j) * G + g) * 2]);
     float s_sum = 0.0f, a = 0.0f;
     if (m != -INFINITY) {
-        for (int j = 0; j < meta.y; ++j) {
-            const size_t r = (rec0 + j) * G + g;
+        for (int j = 0; j < meta0.y; ++j) {
+            const size_t r = (r00 + j) * G + g;
             const float f = exp2f(p.ws_ml[r * 2] - m);
             s_sum = fmaf(p.ws_ml[r * 2 + 1], f, s_sum);
             a = fmaf(p.ws_acc[r * kHD + d], f, a);
+        }
+        for (int j = 0; j < meta1.y; ++j) {
+            const size_t r = (r10 + j) * G + g;
+            const float f = exp2f(p.ws_ml2[r * 2] - m);
+            s_sum = fmaf(p.ws_ml2[r * 2 + 1], f, s_sum);
+            a = fmaf(p.ws_acc2[r * kHD + d], f, a);
         }
     }
     *o = s_sum > 0.0f ? a / s_sum : 0.0f;

@@ -96,6 +96,66 @@ int4_append_kernel(Int4AppendParams p) {
                    p.v_param + row * 4, lane);
 }
 
+// ---- requantisation int8 -> INT4 of whole blocks (mixed precision by token age) ----
+// [UltraQuant] §3.3 ("practical note"): the oldest time blocks are requantised
+// from 8-bit to 4-bit.  Value of an int8 code: code * scale (fp32); then the
+// group-64 rule above.  One CTA per (block, kv head) tile of 256 tokens; K
+// rows are read chunk by chunk (undoing the slot-dependent chunk order), V
+// quarters ([128 dims][64 tokens]) are transposed through shared memory.
+constexpr int kReqWarps = 8;
+constexpr int kVtPitch = 65;   // odd byte pitch: lane l's rows fall in distinct banks
+
+__global__ void __launch_bounds__(kReqWarps * 32)
+int4_requantize_kernel(Int4RequantParams p) {
+    __shared__ uint8_t vt[kHD * kVtPitch];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int from = p.blk_from[b], to = p.blk_to[b];
+    if (blockIdx.x == 0 && threadIdx.x == 0 &&
+        (from < 0 || to > p.max_blocks || to - from > p.max_count))
+        flag_status(p.dev_status, KVQ8_DEV_BAD_POSITION);
+    const int j = max(0, from) + blockIdx.x;
+    if (j >= min(to, p.max_blocks)) return;
+    const int phys8 = p.table8[(size_t)b * p.max_blocks + j];
+    const int phys4 = p.table4[(size_t)b * p.max_blocks + j];
+    if (phys8 < 0 || phys8 >= p.num_blocks8 || phys4 < 0 || phys4 >= p.num_blocks4) {
+        if (threadIdx.x == 0) flag_status(p.dev_status, KVQ8_DEV_BAD_BLOCK_ID);
+        return;
+    }
+    const size_t tile8 = (size_t)phys8 * p.nkv + h, tile4 = (size_t)phys4 * p.nkv + h;
+    // K: lane l takes dims 4l..4l+3 (logical chunk l/4, stored at chunk (l/4) ^ (t & 7))
+    for (int t = warp; t < kBS; t += kReqWarps) {
+        const int8_t *row = p.k_pool + (tile8 * kBS + t) * kHD;
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(row + 16 * ((lane >> 2) ^ (t & 7)) + 4 * (lane & 3));
+        const float sc = p.k_scale[tile8 * kBS + t];
+        const float4 x = make_float4(__fmul_rn((float)(int8_t)(w & 0xff), sc), __fmul_rn((float)(int8_t)((w >> 8) & 0xff), sc),
+                                     __fmul_rn((float)(int8_t)((w >> 16) & 0xff), sc), __fmul_rn((float)(int8_t)(w >> 24), sc));
+        int4_store_row(x, p.k_codes + (tile4 * kBS + t) * kRowBytes, p.k_param + (tile4 * kBS + t) * 4, lane);
+    }
+    // V: one 64-token quarter at a time
+    for (int qd = 0; qd < kBS / kStageTok; ++qd) {
+        const uint8_t *src = reinterpret_cast<const uint8_t *>(p.v_pool) + tile8 * kHD * kBS + qd * kTileVQuarter;
+        __syncthreads();
+        for (int i = threadIdx.x; i < kHD * kStageTok / 16; i += kReqWarps * 32) {
+            const int4 v = reinterpret_cast<const int4 *>(src)[i];
+            const int r = (16 * i) / kStageTok, c0 = (16 * i) % kStageTok;
+            const uint32_t ws[4] = {(uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w};
+#pragma unroll
+            for (int k = 0; k < 16; ++k) vt[r * kVtPitch + c0 + k] = (uint8_t)(ws[k >> 2] >> (8 * (k & 3)));
+        }
+        __syncthreads();
+        for (int tq = warp; tq < kStageTok; tq += kReqWarps) {
+            const int t = qd * kStageTok + tq;
+            const float sc = p.v_scale[tile8 * kBS + t];
+            float xs[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xs[i] = __fmul_rn((float)(int8_t)vt[(4 * lane + i) * kVtPitch + tq], sc);
+            int4_store_row(make_float4(xs[0], xs[1], xs[2], xs[3]), p.v_codes + (tile4 * kBS + t) * kRowBytes,
+                           p.v_param + (tile4 * kBS + t) * 4, lane);
+        }
+    }
+}
+
 // ---- tensor-core decode ----
 // Both contractions run as mma.sync m16n8k16 (fp16 in, fp32 accumulate); codes
 // 0..15 are exact in fp16.
@@ -233,6 +293,7 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         if (threadIdx.x == 0 && split == 0 && h == 0) flag_status(p.dev_status, KVQ8_DEV_BAD_CTX_LEN);
         L = max(0, min(L, cap));
     }
+    if (p.n4_blocks) L = min(L, max(0, min(p.n4_blocks[b], p.max_blocks)) * kBS);   // the 4-bit part only
     const size_t u = (size_t)b * p.nkv + h;
     if (split == 0 && threadIdx.x == 0) {
         // records of unit u are u*nsplit + j; the combine reads first + u + j
@@ -575,6 +636,12 @@ int int4_resident_ctas(int group) {
         cached[dev][group] = sms * per;
     }
     return cached[dev][group];
+}
+
+cudaError_t launch_int4_requantize(const Int4RequantParams &p, cudaStream_t s) {
+    dim3 grid(p.max_count, p.nkv, p.batch);
+    int4_requantize_kernel<<<grid, kReqWarps * 32, 0, s>>>(p);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_int4_append(const Int4AppendParams &p, cudaStream_t s) {

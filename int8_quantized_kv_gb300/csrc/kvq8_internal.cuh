@@ -74,6 +74,11 @@ struct DecodeParams {
     float *ws_acc;                // [records][G][hd] (unnormalised V accumulator)
     uint32_t *dev_status;
     float *out;                   // [batch][nqh][hd] (combine only)
+    // mixed precision by token age (null otherwise): the int8 part starts at
+    // block first_q8_block[b]; the combine also merges the 4-bit split's records
+    const int32_t *first_q8_block;
+    const int2 *ws_meta2;
+    const float *ws_ml2, *ws_acc2;
 };
 cudaError_t launch_decode_split(const DecodeParams &p, int group, cudaStream_t s);
 cudaError_t launch_decode_combine(const DecodeParams &p, int group, cudaStream_t s);
@@ -92,6 +97,7 @@ struct Int4AppendParams {
 
 struct Int4DecodeParams {
     const float *q;               // [batch][nqh][hd]
+    const int32_t *n4_blocks;     // null, or: only tokens [0, 256 * n4_blocks[b]) (mixed precision)
     int batch, nqh, nkv;
     const uint8_t *k_codes, *v_codes;
     const float *k_param, *v_param;
@@ -105,6 +111,25 @@ struct Int4DecodeParams {
     float *ws_ml, *ws_acc;        // same record format as DecodeParams
     uint32_t *dev_status;
 };
+// Mixed precision by token age: logical blocks [blk_from[b], blk_to[b]) of
+// sequence b are requantised from the int8 tiles table8[b][j] into the 4-bit
+// tiles table4[b][j].
+struct Int4RequantParams {
+    int batch, nkv;
+    const int8_t *k_pool, *v_pool;
+    const float *k_scale, *v_scale;
+    int num_blocks8;
+    const int32_t *table8;
+    uint8_t *k_codes, *v_codes;
+    float *k_param, *v_param;
+    int num_blocks4;
+    const int32_t *table4;
+    int max_blocks;
+    const int32_t *blk_from, *blk_to;
+    int max_count;                // grid bound: blk_to - blk_from <= max_count
+    uint32_t *dev_status;
+};
+cudaError_t launch_int4_requantize(const Int4RequantParams &p, cudaStream_t s);
 bool make_int4_plan(int batch, int nkv, int max_blocks, int resident_ctas, int *nsplit, int *split_tokens);
 int int4_resident_ctas(int group);
 cudaError_t launch_int4_append(const Int4AppendParams &p, cudaStream_t s);

@@ -53,6 +53,11 @@ SIGNATURES = {
                                   _P, _P, _P, _P, _P, _P]),
     "kvq4_decode_attn": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _I,
                               _P, _F, _P, _P, _SZ, _P, _P]),
+    "kvmix_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "kvmix_requantize": (_I, [_I, _I, _I, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _P,
+                              _I, _I, _P, _P, _I, _P, _P]),
+    "kvmix_decode_attn": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _P,
+                               _I, _I, _P, _P, _F, _P, _P, _SZ, _P, _P]),
     "kvf32_pool_bytes": (_SZ, [_I, _I, _I, _I]),
     "kvf32_cache_bytes_per_token": (_SZ, [_I, _I]),
     "kvf32_append": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _I, _I, _I, _P, _P, _P, _P]),
@@ -388,3 +393,47 @@ def decode_attnf32(q, cache: KVF32Cache, block_table, ctx_lens, out, workspace,
         sm, _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(dev_status), _stream(stream))
     _check("kvf32_decode_attn", st)
+
+
+# ------------------------------------------ mixed precision by token age ---
+def mixed_workspace_bytes(batch: int, nqh: int, nkv: int, max_blocks: int) -> int:
+    return int(load().kvmix_decode_workspace_bytes(batch, nqh, nkv, HEAD_DIM, max_blocks, BLOCK_SIZE))
+
+
+def alloc_mixed_workspace(batch, nqh, nkv, max_blocks, device="cuda"):
+    import torch
+    n = mixed_workspace_bytes(batch, nqh, nkv, max_blocks)
+    if n == 0:
+        raise Kvq8Error("kvmix_decode_workspace_bytes", ERR_UNSUPPORTED)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def requantize_blocks(cache: KVCache, table8, cache4: KV4Cache, table4, blk_from, blk_to,
+                      max_count: int, dev_status=None, stream=None):
+    """Requantise logical blocks [blk_from[b], blk_to[b]) of every sequence from
+    the int8 cache (table8) into the 4-bit cache (table4)."""
+    _need_cuda(*cache, *cache4, table8, table4, blk_from, blk_to, dev_status)
+    batch, max_blocks = table8.shape
+    st = load().kvmix_requantize(
+        batch, cache.nkv, HEAD_DIM, _ptr(cache.k_pool), _ptr(cache.v_pool), _ptr(cache.k_scale),
+        _ptr(cache.v_scale), cache.num_blocks, _ptr(table8), _ptr(cache4.k_codes),
+        _ptr(cache4.v_codes), _ptr(cache4.k_param), _ptr(cache4.v_param), cache4.num_blocks,
+        _ptr(table4), max_blocks, BLOCK_SIZE, _ptr(blk_from), _ptr(blk_to), int(max_count),
+        _ptr(dev_status), _stream(stream))
+    _check("kvmix_requantize", st)
+
+
+def decode_attn_mixed(q, cache: KVCache, table8, cache4: KV4Cache, table4, ctx_lens, n4_blocks, out,
+                      workspace, sm_scale: Optional[float] = None, dev_status=None, stream=None):
+    """Decode over 4-bit old blocks [0, n4_blocks[b]) and int8 recent blocks."""
+    _need_cuda(q, table8, table4, ctx_lens, n4_blocks, out, workspace, *cache, *cache4, dev_status)
+    batch, nqh, hd = q.shape
+    sm = 1.0 / math.sqrt(hd) if sm_scale is None else sm_scale
+    st = load().kvmix_decode_attn(
+        _ptr(q), batch, nqh, cache.nkv, hd, _ptr(cache.k_pool), _ptr(cache.v_pool),
+        _ptr(cache.k_scale), _ptr(cache.v_scale), cache.num_blocks, _ptr(table8),
+        _ptr(cache4.k_codes), _ptr(cache4.v_codes), _ptr(cache4.k_param), _ptr(cache4.v_param),
+        cache4.num_blocks, _ptr(table4), table8.shape[1], BLOCK_SIZE, _ptr(ctx_lens),
+        _ptr(n4_blocks), sm, _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream))
+    _check("kvmix_decode_attn", st)

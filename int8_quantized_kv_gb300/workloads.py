@@ -166,9 +166,22 @@ LONG128K_OUTLIERS = Workload("batch4_ctx131072_outliers", 4, batch=4, nqh=32, nk
                              ctx=131072, outlier_channels=4)
 APPEND_8X4096 = Workload("append_batch8_4096tokens", 5, batch=8, nqh=32, nkv=8, ctx=4096)
 INT4_G64_32K = Workload("int4g64_batch8_ctx32768", 6, batch=8, nqh=32, nkv=8, ctx=32768)
+# Mixed precision by token age: the Qwen3-2B decode stack with the most recent
+# MIXED_RECENT_BLOCKS blocks (2048 tokens) of every sequence in int8 and the
+# older blocks requantised to 4-bit.
+MIXED_QWEN3_8K = Workload("mixed_qwen3_2b_28layers_ctx8192", 7, batch=28, nqh=16, nkv=8,
+                          ctx=8192, layers=28)
+MIXED_RECENT_BLOCKS = 8
+
+
+def mixed_old_blocks(lens, recent_blocks: int = MIXED_RECENT_BLOCKS) -> np.ndarray:
+    """Per sequence, the leading 256-token blocks held in 4-bit (int32 [batch])."""
+    nb = blocks_needed(lens)
+    return np.maximum(nb - recent_blocks, 0).astype(np.int32)
 
 WORKLOADS = {w.name: w for w in (SINGLE_HEAD_L256, QWEN3_2B_28L_8K, BATCH64_RAGGED,
-                                 LONG128K_OUTLIERS, APPEND_8X4096, INT4_G64_32K)}
+                                 LONG128K_OUTLIERS, APPEND_8X4096, INT4_G64_32K,
+                                 MIXED_QWEN3_8K)}
 
 
 def scaled(cfg: Workload, *, name=None, batch=None, ctx=None, ctx_range=None,

@@ -20,7 +20,7 @@ FAKE = 1 << 20   # a 256-aligned non-null address that is never dereferenced
 def _declared():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(kv(?:q8|q4|f32)_[a-z0-9_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(kv(?:q8|q4|f32|mix)_[a-z0-9_]+)\s*\(", src)))
 
 
 @pytest.fixture(scope="module")
@@ -34,7 +34,8 @@ def test_header_declares_expected_entry_points():
     for n in ("kvq8_quantize_append", "kvq8_quantize_q", "kvq8_decode_attn",
               "kvq8_decode_split", "kvq8_decode_combine", "kvq8_decode_workspace_bytes",
               "kvq8_decode_step", "kvq8_decode_attn_noalloc", "kvq4_quantize_append",
-              "kvq4_decode_attn", "kvf32_append", "kvf32_decode_attn"):
+              "kvq4_decode_attn", "kvf32_append", "kvf32_decode_attn", "kvmix_requantize",
+              "kvmix_decode_attn", "kvmix_decode_workspace_bytes"):
         assert n in names
 
 
@@ -180,6 +181,28 @@ def test_int4_cache_sizes_and_validation(lib):
                                 FAKE, 0.088, FAKE, FAKE, need - 1, None, None) == kvq8.ERR_WORKSPACE
     assert lib.kvq4_decode_attn(FAKE, 1, 8, 8, 128, FAKE, FAKE, FAKE, FAKE, 4, FAKE, 4, 256,
                                 FAKE, 0.088, None, FAKE, need, None, None) == kvq8.ERR_INVALID_ARG
+
+
+def test_mixed_precision_validation(lib):
+    one = kvq8.decode_workspace_bytes(1, 8, 8, 4)
+    assert kvq8.mixed_workspace_bytes(1, 8, 8, 4) == 2 * one
+    r = dict(batch=1, nkv=1, hd=128, kp=FAKE, vp=FAKE, ks=FAKE, vs=FAKE, nb8=2, t8=FAKE, kc=FAKE, vc=FAKE,
+             kpa=FAKE, vpa=FAKE, nb4=2, t4=FAKE, max_blocks=2, bs=256, bf=FAKE, bt=FAKE, max_count=1,
+             status=None, stream=None)
+    assert lib.kvmix_requantize(*dict(r, hd=64).values()) == kvq8.ERR_UNSUPPORTED
+    assert lib.kvmix_requantize(*dict(r, bt=None).values()) == kvq8.ERR_INVALID_ARG
+    assert lib.kvmix_requantize(*dict(r, kc=FAKE + 4).values()) == kvq8.ERR_INVALID_ARG
+    assert lib.kvmix_requantize(*dict(r, max_count=-1).values()) == kvq8.ERR_INVALID_ARG
+    assert lib.kvmix_requantize(*dict(r, max_count=0).values()) == kvq8.OK
+    d = dict(q=FAKE, batch=1, nqh=8, nkv=8, hd=128, kp=FAKE, vp=FAKE, ks=FAKE, vs=FAKE, nb8=4, t8=FAKE,
+             kc=FAKE, vc=FAKE, kpa=FAKE, vpa=FAKE, nb4=4, t4=FAKE, max_blocks=4, bs=256, lens=FAKE,
+             n4=FAKE, sm=0.088, out=FAKE, ws=FAKE, ws_bytes=2 * one, status=None, stream=None)
+    call = lambda **kw: lib.kvmix_decode_attn(*dict(d, **kw).values())
+    assert call(ws_bytes=2 * one - 1) == kvq8.ERR_WORKSPACE
+    assert call(n4=None) == kvq8.ERR_INVALID_ARG
+    assert call(t4=None) == kvq8.ERR_INVALID_ARG
+    assert call(nqh=24) == kvq8.ERR_UNSUPPORTED
+    assert call(batch=0) == kvq8.OK
 
 
 def test_library_is_built_for_sm103a():
