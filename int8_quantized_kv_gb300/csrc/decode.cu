@@ -89,10 +89,11 @@ __device__ __forceinline__ int clamp_len(int L, int cap) { return max(0, min(L, 
 
 // The tokens [x, y) of sequence b that this launch decodes: [0, L) normally;
 // [256 * first_q8_block[b], L) when the older blocks of the sequence are held
-// in the 4-bit cache (mixed precision by token age).
+// in the 4-bit cache (mixed precision by token age; kMixed).
+template <bool kMixed = true>
 __device__ __forceinline__ int2 seq_span(const DecodeParams &p, int b, int cap) {
     const int L = clamp_len(p.ctx_lens[b], cap);
-    const int s = p.first_q8_block ? min(L, max(0, min(p.first_q8_block[b], cap / kBS)) * kBS) : 0;
+    const int s = (kMixed && p.first_q8_block) ? min(L, max(0, min(p.first_q8_block[b], cap / kBS)) * kBS) : 0;
     return make_int2(s, L);
 }
 __device__ __forceinline__ int span_stages(int2 sp) { return (sp.y - sp.x + kStageTok - 1) / kStageTok; }
@@ -136,7 +137,7 @@ __device__ __forceinline__ bool slot_turn_bounded(volatile int *done, int round,
     return true;
 }
 
-template <int G>
+template <int G, bool kMixed>
 __global__ void __launch_bounds__(kSplitThreads, 1)
 decode_split_kernel(DecodeParams p) {
     using Lay = SplitLayout<G>;
@@ -174,7 +175,7 @@ decode_split_kernel(DecodeParams p) {
     for (int b = b_lo; b < b_hi; ++b) {
         const int L = p.ctx_lens[b];
         if (c == 0 && (L < 0 || L > cap)) flag_status(p.dev_status, KVQ8_DEV_BAD_CTX_LEN);
-        mine += (long long)p.nkv * span_stages(seq_span(p, b, cap));
+        mine += (long long)p.nkv * span_stages(seq_span<kMixed>(p, b, cap));
     }
     long long incl = mine;
 #pragma unroll
@@ -204,7 +205,7 @@ decode_split_kernel(DecodeParams p) {
     if (mine > 0 && excl <= lo && lo < excl + mine) {
         long long acc = excl;
         for (int b = b_lo; b < b_hi; ++b) {
-            const long long n = (long long)p.nkv * span_stages(seq_span(p, b, cap));
+            const long long n = (long long)p.nkv * span_stages(seq_span<kMixed>(p, b, cap));
             if (lo < acc + n) {
                 misc->b0 = b;
                 misc->base = acc;
@@ -218,7 +219,7 @@ decode_split_kernel(DecodeParams p) {
     int b = 0, h = 0, off = 0;
     if (hi > lo) {
         b = misc->b0;
-        const int nb = span_stages(seq_span(p, b, cap));
+        const int nb = span_stages(seq_span<kMixed>(p, b, cap));
         const long long rel = lo - misc->base;
         h = (int)(rel / nb);
         off = (int)(rel % nb);
@@ -231,7 +232,7 @@ decode_split_kernel(DecodeParams p) {
         long long remaining = hi - lo;
         int kbase = 0;
         while (remaining > 0 && b < p.batch) {
-            const int2 sp = seq_span(p, b, cap);
+            const int2 sp = seq_span<kMixed>(p, b, cap);
             const int nb = span_stages(sp);
             if (nb == 0) { ++b; h = 0; off = 0; continue; }
             const int seg_n = (int)min((long long)(nb - off), remaining);
@@ -300,7 +301,7 @@ decode_split_kernel(DecodeParams p) {
         long long remaining = hi - lo;
         int kbase = 0;
         while (remaining > 0 && b < p.batch) {
-            const int2 sp = seq_span(p, b, cap);
+            const int2 sp = seq_span<kMixed>(p, b, cap);
             const int L = sp.y;
             const int nb = span_stages(sp);
             if (nb == 0) { ++b; h = 0; off = 0; continue; }
@@ -590,10 +591,10 @@ int device_sm_count() {
     return cached[dev];
 }
 
-template <int G>
-cudaError_t launch_split_g(const DecodeParams &p, cudaStream_t s) {
+template <int G, bool kMixed>
+cudaError_t launch_split_gm(const DecodeParams &p, cudaStream_t s) {
     using Lay = SplitLayout<G>;
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<G>,
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<G, kMixed>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
     if (e != cudaSuccess) return e;
     const int sms = device_sm_count();
@@ -608,7 +609,12 @@ cudaError_t launch_split_g(const DecodeParams &p, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_split_kernel<G>, p);
+    return cudaLaunchKernelEx(&cfg, decode_split_kernel<G, kMixed>, p);
+}
+
+template <int G>
+cudaError_t launch_split_g(const DecodeParams &p, cudaStream_t s) {
+    return p.first_q8_block ? launch_split_gm<G, true>(p, s) : launch_split_gm<G, false>(p, s);
 }
 
 }  // namespace
