@@ -160,20 +160,21 @@ int4_requantize_kernel(Int4RequantParams p) {
 // Both contractions run as mma.sync m16n8k16 (fp16 in, fp32 accumulate); codes
 // 0..15 are exact in fp16.
 //
-// Q.K as S^T = Q K^T: A = the fp32 query split into fp16 high + low parts
-// (rows = heads, padded to 16), B = K codes (k = dims, n = 8 tokens).  The
-// S^T fragment (row = head, columns = tokens) is the B operand P.V needs, so
-// P never goes through shared memory.  K codes enter as fp16 by one
-// mask-and-or per two codes: a low nibble as 1024 + c, a high nibble in place
-// as 1024 + 16c (exact: fp16 steps are 1 on [1024, 2048)); the query values
-// facing high nibbles are divided by 16, so each code meets its own q.  The
-// 1024 is removed with the zero point:
+// Q.K as S = K Q^T: A = K codes (rows = 16 tokens, k = dims), B = the fp32
+// query split into fp16 high + low parts (columns = heads).  K codes enter as
+// fp16 by one mask-and-or per two codes: a low nibble as 1024 + c, a high
+// nibble in place as 1024 + 16c (exact: fp16 steps are 1 on [1024, 2048)); the
+// query values facing high nibbles are divided by 16, so each code meets its
+// own q.  The 1024 is removed with the zero point:
 //   s = sm * 2^-k * sum_g scale_g * (D'_g - 1024 Y_g - zero_g Q_g),
 //   D'_g = sum_{d in g} b_d y_d,  Y_g = sum_{d in g} y_d,  Q_g = sum_{d in g} q_d,
 // y = the fed query value (q or q/16, as high + low fp16 parts), q = the query
 // times a power of two 2^k that puts its largest element at 2^13..2^14 (fp16
 // keeps full precision for q/16).  Within a 64-dim group the bias costs at
-// most fp32 rounding of a 64-term sum.
+// most fp32 rounding of a 64-term sum.  The score fragment (row = token,
+// column = head) reaches P.V through shared memory: P' is stored as
+// [32 tokens][8 heads] fp16 tiles in the chunk's K area (free once K has been
+// read) and loaded back transposed (ldmatrix .trans) into the B fragments.
 //
 // P.V as out^T = V^T P: A = V codes (rows = dims, k = tokens, exact after one
 // fp16 subtract), B = P'_g = w * vscale_g(t) * 2^-e per dim group, split into
@@ -281,7 +282,7 @@ __device__ __forceinline__ int int4_fetch_chunk(const Int4DecodeParams &p, int b
 }
 
 template <int G>
-__global__ void __launch_bounds__(kWarps4 * 32)
+__global__ void __launch_bounds__(kWarps4 * 32, 3)
 int4_decode_split_kernel(Int4DecodeParams p) {
     pdl_wait();
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -374,11 +375,19 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         }
     }
     __syncthreads();
-    const float qy0 = 1024.0f * sm.qy[g][0], qy1 = 1024.0f * sm.qy[g][1];
-    const float qq0 = sm.qq[g][0], qq1 = sm.qq[g][1];
+    // this lane's heads are 2*t4 and 2*t4 + 1 (score and accumulator columns)
+    float qy[2][2], qq[2][2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int gr = 0; gr < 2; ++gr) {
+            qy[j][gr] = 1024.0f * sm.qy[2 * t4 + j][gr];
+            qq[j][gr] = sm.qq[2 * t4 + j][gr];
+        }
     const float score_scale = p.sm_scale_log2 / qscale;
 
-    float M = -INFINITY, Sl = 0.0f, Zl[2] = {0.0f, 0.0f}, acc[8][4];
+    float M[2] = {-INFINITY, -INFINITY}, Sl[2] = {0.0f, 0.0f}, Zl[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
+    float acc[8][4];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
@@ -395,113 +404,141 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         const int t0 = tok_begin + cidx * kChunk4;
         const int ntok = min(kChunk4, tok_end - t0);
         // K: token 8*nt + g, bytes 32*gr + 8*t4 .. +7
-        uint2 kw[4][2];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-            for (int gr = 0; gr < 2; ++gr)
-                kw[nt][gr] = *reinterpret_cast<const uint2 *>(st + kStageKOff + (8 * nt + g) * kKPitch4 +
-                                                              32 * kswz(8 * nt + g, gr) + 8 * t4);
-        // V: tokens 16*ks2 + 2*t4 + {0, 1, 8, 9}, bytes 32*gr + 4*g .. +3
-        uint32_t vw[2][4][2];
-#pragma unroll
-        for (int ks2 = 0; ks2 < 2; ++ks2)
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-#pragma unroll
-                for (int gr = 0; gr < 2; ++gr) {
-                    const int t = 16 * ks2 + 2 * t4 + (j & 1) + 8 * (j >> 1);
-                    vw[ks2][j][gr] = *reinterpret_cast<const uint32_t *>(st + kStageVOff + t * kVPitch4 + 32 * gr + 4 * g);
-                }
         const float4 *kps = reinterpret_cast<const float4 *>(st + kStageKpOff);
         const float4 *vps = reinterpret_cast<const float4 *>(st + kStageVpOff);
-        float4 vp[4][2];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) vp[nt][e] = vps[8 * nt + 2 * t4 + e];
+        // K rows, V words and parameters are read from the staging buffer just
+        // before their use (short register lifetimes)
+        const bool partial = ntok < kChunk4;   // only the split's last chunk
 
-        // ---- scores: S^T = Q K^T, head g, tokens 8*nt + 2*t4 + e ----
-        float sc[4][2];
-        float mloc = -INFINITY;
+        // ---- scores: S = K Q^T, tokens 16*mt + g + 8*r (rows), heads 2*t4 + j ----
+        float sc[2][2][2];
+        float mloc[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int mt = 0; mt < 2; ++mt) {
+            // K: tokens 16*mt + g + 8*r, bytes 32*gr + 8*t4 .. +7
+            uint2 kw[2][2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int gr = 0; gr < 2; ++gr) {
+                    const int t = 16 * mt + g + 8 * r;
+                    kw[r][gr] = *reinterpret_cast<const uint2 *>(st + kStageKOff + t * kKPitch4 +
+                                                                 32 * kswz(t, gr) + 8 * t4);
+                }
+            float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};   // per group
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const int gr = ks >> 2, sub = ks & 3;
-                const uint32_t w0 = (sub >> 1) ? kw[nt][gr].y : kw[nt][gr].x;
-                const uint32_t w = (sub & 1) ? (w0 >> 8) : w0;
-                const uint32_t b0 = nib_pair(w, kHiNib), b1 = nib_pair(w, kLoNib);
+                uint32_t a[4];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const uint32_t w0 = (sub >> 1) ? kw[r][gr].y : kw[r][gr].x;
+                    const uint32_t w = (sub & 1) ? (w0 >> 8) : w0;
+                    a[r] = nib_pair(w, kHiNib);       // rows g / g+8, k = 2*t4 + e
+                    a[2 + r] = nib_pair(w, kLoNib);   // rows g / g+8, k = 2*t4 + 8 + e
+                }
                 const uint4 qa = sm.qa[ks][lane];
-                float(&d)[4] = gr ? d1 : d0;
-                mma_f16_16816(d, qa.x, 0u, qa.y, 0u, b0, b1);
-                mma_f16_16816(d, qa.z, 0u, qa.w, 0u, b0, b1);
+                mma_f16_16816(d[gr], a[0], a[1], a[2], a[3], qa.x, qa.y);
+                mma_f16_16816(d[gr], a[0], a[1], a[2], a[3], qa.z, qa.w);
             }
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const float4 k4 = kps[8 * nt + 2 * t4 + e];
-                const float s = k4.x * (d0[e] - qy0 - k4.y * qq0) + k4.z * (d1[e] - qy1 - k4.w * qq1);
-                const bool valid = 8 * nt + 2 * t4 + e < ntok;
-                sc[nt][e] = valid ? s * score_scale : -INFINITY;
-                mloc = fmaxf(mloc, sc[nt][e]);
+            for (int r = 0; r < 2; ++r) {
+                const float4 k4 = kps[16 * mt + g + 8 * r];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float x = k4.x * (d[0][2 * r + j] - qy[j][0] - k4.y * qq[j][0]) +
+                                    k4.z * (d[1][2 * r + j] - qy[j][1] - k4.w * qq[j][1]);
+                    sc[mt][r][j] = x * score_scale;
+                }
             }
         }
-        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
-        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
+        if (partial) {
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+                    if (16 * mt + g + 8 * r >= ntok) sc[mt][r][0] = sc[mt][r][1] = -INFINITY;
+        }
+        // this lane's score tokens' V parameters (zero past the end: stale slots)
+        float4 vp[2][2];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                vp[mt][r] = vps[16 * mt + g + 8 * r];
+                if (partial && 16 * mt + g + 8 * r >= ntok) vp[mt][r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+                mloc[j] = fmaxf(mloc[j], fmaxf(sc[mt][0][j], sc[mt][1][j]));
+            mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 4));
+            mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 8));
+            mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 16));
+        }
 
         // power-of-two unit of this chunk's P': 2^e > max V scale (see the q8 decode)
         float vsmax = 0.0f;
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                if (8 * nt + 2 * t4 + e >= ntok) vp[nt][e] = make_float4(0.f, 0.f, 0.f, 0.f);
-                vsmax = fmaxf(vsmax, fmaxf(vp[nt][e].x, vp[nt][e].z));
-            }
+            for (int r = 0; r < 2; ++r) vsmax = fmaxf(vsmax, fmaxf(vp[mt][r].x, vp[mt][r].z));
         const int e_need = __reduce_max_sync(0xffffffffu, ((__float_as_int(vsmax) >> 23) & 0xff) - 126);
         int e_new = e_cur;
         if (e_need > e_cur || e_need < e_cur - 12) e_new = max(-120, min(120, e_need));
         const float inv = __int_as_float((127 - e_new) << 23);
 
-        // online softmax per head g (the 4 lanes of row g agree), raised lazily
-        const bool grow = mloc > M + 8.0f;
-        float alpha = 1.0f;
+        // online softmax per head (the 8 lanes of a column agree), raised lazily
+        const bool grow = mloc[0] > M[0] + 8.0f || mloc[1] > M[1] + 8.0f;
+        float alpha[2] = {1.0f, 1.0f};
         bool rescale = e_new != e_cur;
         if (__any_sync(0xffffffffu, grow)) {
             rescale = true;
-            const float m_new = fmaxf(M, mloc);
-            alpha = exp2f(M - m_new);   // 0 while M is -inf
-            M = m_new;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float m_new = fmaxf(M[j], mloc[j]);
+                alpha[j] = exp2f(M[j] - m_new);   // 0 while M is -inf
+                M[j] = m_new;
+            }
         }
         const float two = __int_as_float((127 + max(-126, min(127, e_cur - e_new))) << 23);
-        float wsum = 0.0f, z0 = 0.0f, z1 = 0.0f;
-        uint32_t bh[2][2][2], bl[2][2][2];   // [group][k-step][b0, b1]
+        // P'_g = w * vscale_g * 2^-e, high and low fp16 parts, into the freed K
+        // area as [group][part][32 tokens][8 heads] for the transposing loads
+        uint32_t *ptile = reinterpret_cast<uint32_t *>(const_cast<unsigned char *>(st) + kStageKOff);
+        __syncwarp();   // every lane is done reading the K rows
+        float wsum[2] = {0.f, 0.f}, zs[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            float p0[2], p1[2];
+        for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const float w = exp2f(sc[nt][e] - M);    // 0 for invalid tokens (-inf)
-                wsum += w;
-                p0[e] = w * vp[nt][e].x * inv;
-                p1[e] = w * vp[nt][e].z * inv;
-                z0 = fmaf(p0[e], vp[nt][e].y, z0);
-                z1 = fmaf(p1[e], vp[nt][e].w, z1);
+            for (int r = 0; r < 2; ++r) {
+                const int t = 16 * mt + g + 8 * r;
+                float pg[2][2];   // [group][head j]
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float w = exp2f(sc[mt][r][j] - M[j]);   // 0 for invalid tokens (-inf)
+                    wsum[j] += w;
+                    pg[0][j] = w * vp[mt][r].x * inv;
+                    pg[1][j] = w * vp[mt][r].z * inv;
+                    zs[j][0] = fmaf(pg[0][j], vp[mt][r].y, zs[j][0]);
+                    zs[j][1] = fmaf(pg[1][j], vp[mt][r].w, zs[j][1]);
+                }
+#pragma unroll
+                for (int gr = 0; gr < 2; ++gr) {
+                    const __half h0 = __float2half_rn(pg[gr][0]), h1 = __float2half_rn(pg[gr][1]);
+                    ptile[((gr * 2 + 0) * kChunk4 + t) * 4 + t4] = pack_half2(__half2float(h0), __half2float(h1));
+                    ptile[((gr * 2 + 1) * kChunk4 + t) * 4 + t4] =
+                        pack_half2(pg[gr][0] - __half2float(h0), pg[gr][1] - __half2float(h1));
+                }
             }
-            const __half h00 = __float2half_rn(p0[0]), h01 = __float2half_rn(p0[1]);
-            const __half h10 = __float2half_rn(p1[0]), h11 = __float2half_rn(p1[1]);
-            bh[0][nt >> 1][nt & 1] = pack_half2(__half2float(h00), __half2float(h01));
-            bh[1][nt >> 1][nt & 1] = pack_half2(__half2float(h10), __half2float(h11));
-            bl[0][nt >> 1][nt & 1] = pack_half2(p0[0] - __half2float(h00), p0[1] - __half2float(h01));
-            bl[1][nt >> 1][nt & 1] = pack_half2(p1[0] - __half2float(h10), p1[1] - __half2float(h11));
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            Sl[j] = fmaf(Sl[j], alpha[j], wsum[j]);
+            Zl[j][0] = fmaf(Zl[j][0], alpha[j] * two, zs[j][0]);
+            Zl[j][1] = fmaf(Zl[j][1], alpha[j] * two, zs[j][1]);
         }
-        Sl = fmaf(Sl, alpha, wsum);
-        Zl[0] = fmaf(Zl[0], alpha * two, z0);
-        Zl[1] = fmaf(Zl[1], alpha * two, z1);
-        if (rescale) {  // warp-uniform; accumulator columns are heads 2*t4, 2*t4 + 1
-            const float f0 = __shfl_sync(0xffffffffu, alpha, 8 * t4) * two;
-            const float f1 = __shfl_sync(0xffffffffu, alpha, 8 * t4 + 4) * two;
+        if (rescale) {  // warp-uniform; accumulator columns are this lane's heads
+            const float f0 = alpha[0] * two, f1 = alpha[1] * two;
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
                 acc[mt][0] *= f0; acc[mt][1] *= f1;
@@ -509,16 +546,41 @@ int4_decode_split_kernel(Int4DecodeParams p) {
             }
         }
         e_cur = e_new;
+        __syncwarp();
+        // B fragments of P.V: matrix i of an x4 transposing load = tokens 8i..8i+7,
+        // so lane (g, t4) receives {P[8i + 2*t4][g], P[8i + 2*t4 + 1][g]}
+        uint32_t bh[2][2][2], bl[2][2][2];   // [group][k-step][b0, b1]
+#pragma unroll
+        for (int gr = 0; gr < 2; ++gr)
+#pragma unroll
+            for (int hl = 0; hl < 2; ++hl) {
+                const uint32_t addr = (uint32_t)__cvta_generic_to_shared(ptile + ((gr * 2 + hl) * kChunk4 + lane) * 4);
+                uint32_t r0, r1, r2, r3;
+                asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                             : "r"(addr));
+                uint32_t(&bb)[2][2] = hl ? bl[gr] : bh[gr];
+                bb[0][0] = r0; bb[0][1] = r1; bb[1][0] = r2; bb[1][1] = r3;
+            }
 
         // ---- P.V: out^T += V^T P'_g ----
 #pragma unroll
         for (int ks2 = 0; ks2 < 2; ++ks2) {
+            // V: tokens 16*ks2 + 2*t4 + {0, 1, 8, 9}, bytes 32*gr + 4*g .. +3
+            uint32_t vw[4][2];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int gr = 0; gr < 2; ++gr) {
+                    const int t = 16 * ks2 + 2 * t4 + (j & 1) + 8 * (j >> 1);
+                    vw[j][gr] = *reinterpret_cast<const uint32_t *>(st + kStageVOff + t * kVPitch4 + 32 * gr + 4 * g);
+                }
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
                 const int gr = mt >> 2, k = mt & 3;
                 const uint32_t sel = (uint32_t)(k | (k << 4) | ((4 + k) << 8) | ((4 + k) << 12));
-                const uint32_t r01 = __byte_perm(vw[ks2][0][gr], vw[ks2][1][gr], sel);
-                const uint32_t r89 = __byte_perm(vw[ks2][2][gr], vw[ks2][3][gr], sel);
+                const uint32_t r01 = __byte_perm(vw[0][gr], vw[1][gr], sel);
+                const uint32_t r89 = __byte_perm(vw[2][gr], vw[3][gr], sel);
                 const uint32_t a0 = nib_pair_exact(r01, kHiNib), a1 = nib_pair_exact(r01, kLoNib);
                 const uint32_t a2 = nib_pair_exact(r89, kHiNib), a3 = nib_pair_exact(r89, kLoNib);
                 mma_f16_16816(acc[mt], a0, a1, a2, a3, bh[gr][ks2][0], bh[gr][ks2][1]);
@@ -532,18 +594,18 @@ int4_decode_split_kernel(Int4DecodeParams p) {
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 
-    // ---- this warp's state: head g owns (M, S, Z); accumulator columns are heads 2*t4, 2*t4+1 ----
-    Sl += __shfl_xor_sync(0xffffffffu, Sl, 1);
-    Sl += __shfl_xor_sync(0xffffffffu, Sl, 2);
+    // ---- this warp's state: lanes of column t4 hold heads 2*t4, 2*t4+1 ----
 #pragma unroll
-    for (int gr = 0; gr < 2; ++gr) {
-        Zl[gr] += __shfl_xor_sync(0xffffffffu, Zl[gr], 1);
-        Zl[gr] += __shfl_xor_sync(0xffffffffu, Zl[gr], 2);
+    for (int j = 0; j < 2; ++j) {
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            Sl[j] += __shfl_xor_sync(0xffffffffu, Sl[j], o);
+            Zl[j][0] += __shfl_xor_sync(0xffffffffu, Zl[j][0], o);
+            Zl[j][1] += __shfl_xor_sync(0xffffffffu, Zl[j][1], o);
+        }
     }
     const float unit_scale = __int_as_float((127 + max(-126, min(127, e_cur))) << 23);
     __syncthreads();   // every warp is done with its staging buffers
-    const float zc[2][2] = {{__shfl_sync(0xffffffffu, Zl[0], 8 * t4), __shfl_sync(0xffffffffu, Zl[1], 8 * t4)},
-                            {__shfl_sync(0xffffffffu, Zl[0], 8 * t4 + 4), __shfl_sync(0xffffffffu, Zl[1], 8 * t4 + 4)}};
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
         const int gr = mt >> 2;
@@ -551,17 +613,21 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         const int h0 = 2 * t4, h1 = 2 * t4 + 1;
         // rows g carry 16 c (high nibbles: even dims)
         if (h0 < G) {
-            sm.u.red.acc[warp][h0][dim] = (acc[mt][0] * 0.0625f - zc[0][gr]) * unit_scale;
-            sm.u.red.acc[warp][h0][dim + 1] = (acc[mt][2] - zc[0][gr]) * unit_scale;
+            sm.u.red.acc[warp][h0][dim] = (acc[mt][0] * 0.0625f - Zl[0][gr]) * unit_scale;
+            sm.u.red.acc[warp][h0][dim + 1] = (acc[mt][2] - Zl[0][gr]) * unit_scale;
         }
         if (h1 < G) {
-            sm.u.red.acc[warp][h1][dim] = (acc[mt][1] * 0.0625f - zc[1][gr]) * unit_scale;
-            sm.u.red.acc[warp][h1][dim + 1] = (acc[mt][3] - zc[1][gr]) * unit_scale;
+            sm.u.red.acc[warp][h1][dim] = (acc[mt][1] * 0.0625f - Zl[1][gr]) * unit_scale;
+            sm.u.red.acc[warp][h1][dim + 1] = (acc[mt][3] - Zl[1][gr]) * unit_scale;
         }
     }
-    if (t4 == 0 && g < G) {
-        sm.u.red.ml[warp][g][0] = M;
-        sm.u.red.ml[warp][g][1] = Sl;
+    if (g == 0) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            if (2 * t4 + j < G) {
+                sm.u.red.ml[warp][2 * t4 + j][0] = M[j];
+                sm.u.red.ml[warp][2 * t4 + j][1] = Sl[j];
+            }
     }
     __syncthreads();
     const int d = threadIdx.x;
