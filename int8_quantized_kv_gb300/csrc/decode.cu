@@ -34,8 +34,9 @@
 //    and written as one record per query head.
 // All waits are bounded: a wait that times out sets KVQ8_DEV_TIMEOUT and the
 // CTA unwinds without leaving copies in flight.  The kernel is launched as a
-// programmatic dependent of the previous kernel in its stream, so its launch
-// overlaps that kernel; it waits for that kernel's results before reading.
+// programmatic dependent of the previous kernel in its stream, so its launch,
+// prologue and query quantisation overlap that kernel; the producer waits for
+// that kernel's results before its first copy from the pools.
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -145,9 +146,11 @@ decode_split_kernel(DecodeParams p) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
     const int cap = p.max_blocks * kBS;
-    // launched as a programmatic dependent of the previous kernel in the stream
-    // (the step's append): its results are visible after this wait
-    pdl_wait();
+    // Launched as a programmatic dependent of the previous kernel in the stream
+    // (the step's append), which writes the pools and scales only.  The
+    // prologue and the query quantisation (ctx_lens, block table, q) run before
+    // that kernel ends; the producer waits for its results before the first
+    // copy from the pools.
     Misc *misc = reinterpret_cast<Misc *>(smem + Lay::oMisc);
     int8_t *q_codes = reinterpret_cast<int8_t *>(smem + Lay::oQCodes);
     float *q_scale = reinterpret_cast<float *>(smem + Lay::oQScale);
@@ -227,6 +230,7 @@ decode_split_kernel(DecodeParams p) {
 
     if (warp == kConsumerWarps) {
         // =========================== producer warp ===========================
+        pdl_wait();   // the previous kernel's writes to the pools are visible after this
         const uint64_t pol = l2_evict_first_policy();
         bool aborted = false;
         long long remaining = hi - lo;
