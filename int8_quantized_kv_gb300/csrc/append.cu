@@ -27,6 +27,32 @@ constexpr int kRowsPerWarp = kQTok / kQWarps;
 constexpr int kVStride = kQTok + 4;              // staged V dim row: 17 words, conflict-free
 constexpr int kNoAppend = INT_MIN;               // this sequence appends nothing
 
+// kv_code of four values of one row whose scale is sc = fl(max|row| / 127),
+// with one reciprocal per row in place of a division per value.  For |v| <=
+// max|row|, |v / sc| < 127.0001; p = fl(v * fl(1 / sc)) carries two roundings,
+// so |p - v / sc| < 127.0001 * (2^-23 + 2^-46) < 2^-16, and fl(v / sc) lies
+// within half an ulp below 128 (2^-18) of v / sc: |p - fl(v / sc)| < 2^-15.
+// Where p is at least 2^-15 from every half-integer, p and fl(v / sc) round
+// to the same integer (|p| < 127.5, so no clamp is needed); the four values
+// are divided exactly when one of them is closer (about 6e-5 of values) or
+// when sc lies outside [2^-120, 2^120] (a zero row, a subnormal or non-finite
+// scale), which gives kv_code's result in every case.
+__device__ __forceinline__ int4 kv_codes4(float4 x, float sc) {
+    if (sc >= 0x1p-120f && sc <= 0x1p120f) {
+        const float inv = __frcp_rn(sc);
+        const float p0 = __fmul_rn(x.x, inv), p1 = __fmul_rn(x.y, inv);
+        const float p2 = __fmul_rn(x.z, inv), p3 = __fmul_rn(x.w, inv);
+        const float r0 = rintf(p0), r1 = rintf(p1), r2 = rintf(p2), r3 = rintf(p3);
+        constexpr float kLim = 0.5f - 0x1p-15f;
+        const float d = fmaxf(fmaxf(fabsf(p0 - r0), fabsf(p1 - r1)),
+                              fmaxf(fabsf(p2 - r2), fabsf(p3 - r3)));
+        if (d <= kLim)
+            return make_int4(__float2int_rn(r0), __float2int_rn(r1), __float2int_rn(r2),
+                             __float2int_rn(r3));
+    }
+    return make_int4(kv_code(x.x, sc), kv_code(x.y, sc), kv_code(x.z, sc), kv_code(x.w, sc));
+}
+
 // Position of the first new token of sequence b: start_pos[b], or in a decode
 // step ctx_lens[b] - 1 (nothing for an empty or out-of-table context, which
 // the decode flags).
@@ -96,8 +122,8 @@ quantize_append_kernel(AppendParams p) {
             float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
             m = warp_max(m);
             const float sc = kv_row_scale(m);
-            const uint32_t w = pack4(kv_code(x.x, sc), kv_code(x.y, sc), kv_code(x.z, sc),
-                                     kv_code(x.w, sc));
+            const int4 c = kv_codes4(x, sc);
+            const uint32_t w = pack4(c.x, c.y, c.z, c.w);
             // 16-byte chunk lane/4 of the row goes to chunk position (lane/4) ^ (slot & 7)
             unsigned char *row = reinterpret_cast<unsigned char *>(p.k_pool) + (tile * kBS + slot) * kHD;
             reinterpret_cast<uint32_t *>(row + (((lane >> 2) ^ (slot & 7)) << 4))[lane & 3] = w;
@@ -108,10 +134,11 @@ quantize_append_kernel(AppendParams p) {
             float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
             m = warp_max(m);
             const float sc = kv_row_scale(m);
-            v_stage[lane + 0][r] = (int8_t)kv_code(x.x, sc);
-            v_stage[lane + 32][r] = (int8_t)kv_code(x.y, sc);
-            v_stage[lane + 64][r] = (int8_t)kv_code(x.z, sc);
-            v_stage[lane + 96][r] = (int8_t)kv_code(x.w, sc);
+            const int4 c = kv_codes4(x, sc);
+            v_stage[lane + 0][r] = (int8_t)c.x;
+            v_stage[lane + 32][r] = (int8_t)c.y;
+            v_stage[lane + 64][r] = (int8_t)c.z;
+            v_stage[lane + 96][r] = (int8_t)c.w;
             if (lane == 0) v_sc[r] = sc;
         }
     }
@@ -169,7 +196,8 @@ quantize_append_token_kernel(AppendParams p) {
     {
         const float m = warp_max(fmaxf(fmaxf(fabsf(xk.x), fabsf(xk.y)), fmaxf(fabsf(xk.z), fabsf(xk.w))));
         const float s = kv_row_scale(m);
-        const uint32_t w = pack4(kv_code(xk.x, s), kv_code(xk.y, s), kv_code(xk.z, s), kv_code(xk.w, s));
+        const int4 c = kv_codes4(xk, s);
+        const uint32_t w = pack4(c.x, c.y, c.z, c.w);
         unsigned char *row = reinterpret_cast<unsigned char *>(p.k_pool) + (tile * kBS + slot) * kHD;
         reinterpret_cast<uint32_t *>(row + (((lane >> 2) ^ (slot & 7)) << 4))[lane & 3] = w;
         if (lane == 0) p.k_scale[tile * kBS + slot] = s;
@@ -178,10 +206,11 @@ quantize_append_token_kernel(AppendParams p) {
         const float m = warp_max(fmaxf(fmaxf(fabsf(xv.x), fabsf(xv.y)), fmaxf(fabsf(xv.z), fabsf(xv.w))));
         const float s = kv_row_scale(m);
         int8_t *vg = p.v_pool + tile * kHD * kBS + (size_t)(slot / kStageTok) * kTileVQuarter + slot % kStageTok;
-        vg[(size_t)(4 * lane + 0) * kStageTok] = (int8_t)kv_code(xv.x, s);
-        vg[(size_t)(4 * lane + 1) * kStageTok] = (int8_t)kv_code(xv.y, s);
-        vg[(size_t)(4 * lane + 2) * kStageTok] = (int8_t)kv_code(xv.z, s);
-        vg[(size_t)(4 * lane + 3) * kStageTok] = (int8_t)kv_code(xv.w, s);
+        const int4 c = kv_codes4(xv, s);
+        vg[(size_t)(4 * lane + 0) * kStageTok] = (int8_t)c.x;
+        vg[(size_t)(4 * lane + 1) * kStageTok] = (int8_t)c.y;
+        vg[(size_t)(4 * lane + 2) * kStageTok] = (int8_t)c.z;
+        vg[(size_t)(4 * lane + 3) * kStageTok] = (int8_t)c.w;
         if (lane == 0) p.v_scale[tile * kBS + slot] = s;
     }
 }

@@ -112,6 +112,65 @@ def test_quantize_append_bit_exact(gpu_lib, start, n_new):
     assert np.all(kp.transpose(0, 1, 2, 3)[~written] == 0x55)
 
 
+def _near_half_rows(n_rows, seed):
+    """Rows whose quotients v / scale sit within a few ulps of half-integers:
+    row max m (so scale = m/127 in fp32), then values fl((k + 0.5) * scale)
+    moved by -3..3 ulps.  Multiplying by the rounded reciprocal instead of
+    dividing rounds some of these to the other integer."""
+    rng = np.random.default_rng(seed)
+    rows = np.empty((n_rows, HD), np.float32)
+    for i in range(n_rows):
+        m = np.float32(rng.uniform(0.3, 700.0))
+        sc = m / np.float32(127.0)
+        k = rng.integers(-126, 126, HD).astype(np.float32)
+        v = ((k + np.float32(0.5)) * sc).astype(np.float32)
+        for j, steps in enumerate(rng.integers(-3, 4, HD)):
+            for _ in range(abs(int(steps))):
+                v[j] = np.nextafter(v[j], np.float32(np.inf if steps > 0 else -np.inf))
+        v[rng.integers(HD)] = m if rng.random() < 0.5 else -m
+        rows[i] = v
+    return rows
+
+
+def _multiply_rounds_differently(rows):
+    """How many values of the rows a plain v * (1/scale) would code differently
+    from round_half_even(fl(v / scale))."""
+    m = np.abs(rows).max(axis=1, keepdims=True)
+    sc = (m / np.float32(127.0)).astype(np.float32)
+    inv = (np.float32(1.0) / sc).astype(np.float32)
+    return int(np.sum(np.rint(rows * inv) != np.rint(rows / sc)))
+
+
+@pytest.mark.parametrize("n_new", [1, 64, 200])
+def test_quantize_append_quotients_near_half_integers(gpu_lib, n_new):
+    """K/V codes stay bit-exact where the quotient is within ulps of a rounding
+    boundary: the kernels multiply by the reciprocal only where that provably
+    rounds like the division, and divide elsewhere."""
+    batch, nkv = (48, 2) if n_new == 1 else (2, 2)
+    rows = _near_half_rows(batch * n_new * nkv * 2, seed=n_new)
+    assert _multiply_rounds_differently(rows) > 0
+    k = rows[: batch * n_new * nkv].reshape(batch, n_new, nkv, HD)
+    v = rows[batch * n_new * nkv:].reshape(batch, n_new, nkv, HD)
+    max_blocks = (n_new + 255) // 256
+    table = np.arange(batch * max_blocks, dtype=np.int32).reshape(batch, max_blocks)
+    cache = kvq8.alloc_cache(batch * max_blocks, nkv)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvq8.quantize_append(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(),
+                         torch.zeros(batch, dtype=torch.int32, device="cuda"),
+                         torch.from_numpy(table).cuda(), cache, dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    kp, vp = cache.k_pool.cpu().numpy(), cache.v_pool.cpu().numpy()
+    pos = np.arange(n_new)
+    for b in range(batch):
+        phys, slot = table[b, pos // 256], pos % 256
+        for h in range(nkv):
+            kq, _ = oracle.kv_quantize_rows(k[b, :, h])
+            vq, _ = oracle.kv_quantize_rows(v[b, :, h])
+            assert np.array_equal(k_rows_logical(kp, phys, h, slot), kq), (b, h)
+            assert np.array_equal(v_rows_logical(vp, phys, h, slot), vq), (b, h)
+
+
 def test_byte_count_of_allocated_cache(gpu_lib):
     # 2112 bytes per token per layer for 8 kv heads of 128 ([Day 9-1] §2)
     nb = 5
