@@ -5,12 +5,15 @@
 // one fp32 scale = max|v|/127 per (token, kv head) row of 128 values, codes
 // round_half_even(v/scale) in [-127, 127].
 //
-// One CTA takes 32 consecutive new tokens of one (sequence, kv head); each of
-// its 8 warps quantises 4 tokens, one row per warp-iteration with a float4 per
-// lane (a row is one coalesced 512-byte read).  K codes go straight to the
-// token-major K tile (one 128-byte row, its 16-byte chunks permuted by slot);
-// V codes are transposed through shared memory so that the dim-major V
-// quarters are written as runs of consecutive slots.
+// Bulk append: one warp per run of 16 consecutive new tokens of one (sequence,
+// kv head), with no shared memory and no block barrier, so that warps stream
+// independently.  A row is one coalesced 512-byte read, a float4 per lane
+// (lane l holds dims 4l..4l+3), and the warp keeps the loads of the next rows
+// in flight while it quantises.  K codes go straight to the token-major K tile
+// (one 128-byte row, its 16-byte chunks permuted by slot).  For V each lane
+// gathers the codes of its 4 dims over the 16 tokens in registers and writes
+// them as one 16-byte piece of each dim-major row of the quarter.  A decode
+// step's single token per sequence takes a warp per (sequence, kv head).
 #include <limits.h>
 
 #include "kvq8_device.cuh"
@@ -21,36 +24,59 @@ namespace kvq8 {
 namespace {
 
 constexpr int kAppendWarps = 8;                  // one-token kernel: warps per CTA
-constexpr int kQWarps = 16;                      // quarter kernel: warps per CTA
-constexpr int kQTok = kStageTok;                 // tokens per CTA: one 64-token quarter
-constexpr int kRowsPerWarp = kQTok / kQWarps;
-constexpr int kVStride = kQTok + 4;              // staged V dim row: 17 words, conflict-free
+constexpr int kBulkWarps = 8;                    // bulk kernel: warps per CTA
+constexpr int kQTok = kStageTok;                 // the V layout's 64-token quarter
+constexpr int kRunTok = 16;                      // tokens per bulk warp
+constexpr int kRunsPerQuarter = kQTok / kRunTok;
+constexpr int kLoadAhead = 2;                    // rows in flight ahead of the one quantised
 constexpr int kNoAppend = INT_MIN;               // this sequence appends nothing
+static_assert(4 % kLoadAhead == 0, "row r of a run uses load buffer r % kLoadAhead = (r % 4) % kLoadAhead");
 
 // kv_code of four values of one row whose scale is sc = fl(max|row| / 127),
-// with one reciprocal per row in place of a division per value.  For |v| <=
-// max|row|, |v / sc| < 127.0001; p = fl(v * fl(1 / sc)) carries two roundings,
-// so |p - v / sc| < 127.0001 * (2^-23 + 2^-46) < 2^-16, and fl(v / sc) lies
-// within half an ulp below 128 (2^-18) of v / sc: |p - fl(v / sc)| < 2^-15.
-// Where p is at least 2^-15 from every half-integer, p and fl(v / sc) round
-// to the same integer (|p| < 127.5, so no clamp is needed); the four values
-// are divided exactly when one of them is closer (about 6e-5 of values) or
-// when sc lies outside [2^-120, 2^120] (a zero row, a subnormal or non-finite
-// scale), which gives kv_code's result in every case.
-__device__ __forceinline__ int4 kv_codes4(float4 x, float sc) {
+// each in the low byte of a word, with one reciprocal per row in place of a
+// division per value.  With inv = fl(1 / sc), t = fl(v * inv + 1.5 * 2^23)
+// holds round_half_even(v * inv) in its low mantissa bits (the sum lies where
+// the fp32 spacing is 1, and 1.5 * 2^23 is even), so its low byte is the code
+// as a two's complement byte; e = fl(v * inv - r), r = t - 1.5 * 2^23, is the
+// residual of that rounding to within 2^-26.  For |v| <= max|row|,
+// |v / sc| < 127.0001, so v * inv lies within 127.0001 * 2^-24 < 2^-17 of
+// v / sc, and fl(v / sc) within half an ulp below 128 (2^-18) of v / sc.
+// When |e| <= 1/2 - 2^-15, fl(v / sc) is therefore strictly closer than 1/2
+// to r, and round_half_even(fl(v / sc)) = r, which is within [-127, 127] (no
+// clamp needed).  The four values are divided exactly when one residual is
+// larger (about 6e-5 of values) or not a number, or when sc lies outside
+// [2^-120, 2^120] (a zero row, a subnormal or non-finite scale); the result
+// equals kv_code's in every case.
+__device__ __forceinline__ uint4 kv_code_bytes4(float4 x, float sc) {
     if (sc >= 0x1p-120f && sc <= 0x1p120f) {
-        const float inv = __frcp_rn(sc);
-        const float p0 = __fmul_rn(x.x, inv), p1 = __fmul_rn(x.y, inv);
-        const float p2 = __fmul_rn(x.z, inv), p3 = __fmul_rn(x.w, inv);
-        const float r0 = rintf(p0), r1 = rintf(p1), r2 = rintf(p2), r3 = rintf(p3);
+        constexpr float kShift = 0x1.8p23f;
         constexpr float kLim = 0.5f - 0x1p-15f;
-        const float d = fmaxf(fmaxf(fabsf(p0 - r0), fabsf(p1 - r1)),
-                              fmaxf(fabsf(p2 - r2), fabsf(p3 - r3)));
-        if (d <= kLim)
-            return make_int4(__float2int_rn(r0), __float2int_rn(r1), __float2int_rn(r2),
-                             __float2int_rn(r3));
+        const float inv = __frcp_rn(sc);
+        const float t0 = __fmaf_rn(x.x, inv, kShift), t1 = __fmaf_rn(x.y, inv, kShift);
+        const float t2 = __fmaf_rn(x.z, inv, kShift), t3 = __fmaf_rn(x.w, inv, kShift);
+        const float e0 = __fmaf_rn(x.x, inv, -__fsub_rn(t0, kShift));
+        const float e1 = __fmaf_rn(x.y, inv, -__fsub_rn(t1, kShift));
+        const float e2 = __fmaf_rn(x.z, inv, -__fsub_rn(t2, kShift));
+        const float e3 = __fmaf_rn(x.w, inv, -__fsub_rn(t3, kShift));
+        if ((fabsf(e0) <= kLim) & (fabsf(e1) <= kLim) & (fabsf(e2) <= kLim) & (fabsf(e3) <= kLim))
+            return make_uint4(__float_as_uint(t0), __float_as_uint(t1), __float_as_uint(t2),
+                              __float_as_uint(t3));
     }
-    return make_int4(kv_code(x.x, sc), kv_code(x.y, sc), kv_code(x.z, sc), kv_code(x.w, sc));
+    return make_uint4((uint32_t)kv_code(x.x, sc), (uint32_t)kv_code(x.y, sc),
+                      (uint32_t)kv_code(x.z, sc), (uint32_t)kv_code(x.w, sc));
+}
+
+// The low bytes of four words as one little-endian word.
+__device__ __forceinline__ uint32_t low_bytes4(uint4 c) {
+    return __byte_perm(__byte_perm(c.x, c.y, 0x0040), __byte_perm(c.z, c.w, 0x0040), 0x5410);
+}
+
+// Max |v| of a row held as a float4 per lane, not-a-number values left out
+// (0 for a row of them).  Non-negative floats order like their bit patterns,
+// so one unsigned warp reduction takes the maximum.
+__device__ __forceinline__ float row_max_abs(float4 x) {
+    const float a = fmaxf(fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))), 0.0f);
+    return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(a)));
 }
 
 // Position of the first new token of sequence b: start_pos[b], or in a decode
@@ -62,108 +88,154 @@ __device__ __forceinline__ int start_position(const AppendParams &p, int b, int 
     return (L >= 1 && L <= cap) ? L - 1 : kNoAppend;
 }
 
-// One CTA per 64-token quarter of the cache touched by the new tokens of one
-// (sequence, kv head): CTA x takes quarter floor(start/64) + x.  Every warp
-// first issues the loads of its 4 rows (K and V), then quantises them; K rows
-// go to the token-major tile, V codes through shared memory to the dim-major
-// quarter, which a full quarter writes as one contiguous 8 KiB run.
-__global__ void __launch_bounds__(kQWarps * 32)
-quantize_append_kernel(AppendParams p) {
-    const int h = blockIdx.y, b = blockIdx.z;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    __shared__ __align__(16) int8_t v_stage[kHD][kVStride];
-    __shared__ __align__(16) float v_sc[kQTok];
-
-    pdl_launch_dependents();  // let the next kernel of the step be scheduled now
-    const int cap = p.max_blocks * kBS;
-    const int start = start_position(p, b, cap);
-    if (start == kNoAppend) return;
-    const long long q0 = ((long long)start >= 0 ? start / kQTok : -(((long long)-start + kQTok - 1) / kQTok));
-    const long long qpos = (q0 + blockIdx.x) * kQTok;          // first position of this quarter
-    const long long lo = max((long long)start, qpos);
-    const long long hi = min((long long)start + p.n_new, qpos + kQTok);
-    if (lo >= hi) return;                                        // block-uniform
+// Rows [vlo, vhi) of quarter x (counted from the quarter of start) of
+// sequence b that the append writes, with qpos the quarter's first position;
+// false when there are none.  Positions outside the table are left out, and
+// flagged by the threads that pass `flag`.
+__device__ __forceinline__ bool quarter_rows(const AppendParams &p, int b, long long x, int cap,
+                                             bool flag, long long &start, long long &qpos,
+                                             long long &vlo, long long &vhi) {
+    const int s0 = start_position(p, b, cap);
+    if (s0 == kNoAppend) return false;
+    start = s0;
+    const long long q0 = start >= 0 ? start / kQTok : -((-start + kQTok - 1) / kQTok);
+    qpos = (q0 + x) * kQTok;
+    const long long lo = max(start, qpos);
+    const long long hi = min(start + p.n_new, qpos + kQTok);
+    if (lo >= hi) return false;
     if (lo < 0 || hi > cap) {
-        if (threadIdx.x == 0) flag_status(p.dev_status, KVQ8_DEV_BAD_POSITION);
-        if (hi <= 0 || lo >= cap) return;
+        if (flag) flag_status(p.dev_status, KVQ8_DEV_BAD_POSITION);
+        if (hi <= 0 || lo >= cap) return false;
     }
-    const long long vlo = max(lo, 0LL), vhi = min(hi, (long long)cap);  // positions inside the table
+    vlo = max(lo, 0LL);
+    vhi = min(hi, (long long)cap);
+    return true;
+}
+
+// Source offset (in floats) of the new row at position pos of (b, h).
+__device__ __forceinline__ size_t new_row_offset(const AppendParams &p, int b, int h,
+                                                 long long pos, long long start) {
+    return (((size_t)b * p.n_new + (size_t)(pos - start)) * p.nkv + h) * kHD;
+}
+
+// Bulk append, one warp per task w = ((b * quarters + x) * nkv + h) * 4 + j:
+// tokens 16j..16j+15 of quarter x (counted from the quarter of the first new
+// token) of sequence b, kv head h.  The four runs of a quarter sit in one CTA,
+// so that the 16-byte pieces of each V row are all written at about the same
+// time.
+__global__ void __launch_bounds__(kBulkWarps * 32, 4)
+quantize_append_kernel(AppendParams p, int quarters, long long tasks) {
+    pdl_launch_dependents();  // let the next kernel of the stream be scheduled now
+    const int lane = threadIdx.x & 31;
+    const long long task = (long long)blockIdx.x * kBulkWarps + (threadIdx.x >> 5);
+    if (task >= tasks) return;
+    const int j = (int)(task % kRunsPerQuarter);
+    long long t = task / kRunsPerQuarter;
+    const int h = (int)(t % p.nkv);
+    t /= p.nkv;
+    const long long x = t % quarters;
+    const int b = (int)(t / quarters);
+    const int cap = p.max_blocks * kBS;
+    long long start, qpos, vlo, vhi;
+    if (!quarter_rows(p, b, x, cap, lane == 0 && j == 0, start, qpos, vlo, vhi)) return;
+    const long long r0 = qpos + kRunTok * j;                    // first position of the run
+    const long long lo = max(vlo, r0), hi = min(vhi, r0 + kRunTok);
+    if (lo >= hi) return;                                        // warp-uniform
     const int phys = p.block_table[(size_t)b * p.max_blocks + (int)(qpos / kBS)];
     if (phys < 0 || phys >= p.num_blocks) {
-        if (threadIdx.x == 0) flag_status(p.dev_status, KVQ8_DEV_BAD_BLOCK_ID);
+        if (lane == 0) flag_status(p.dev_status, KVQ8_DEV_BAD_BLOCK_ID);
         return;
     }
     const size_t tile = (size_t)phys * p.nkv + h;
-    const int slot0 = (int)(qpos % kBS);                         // first slot of the quarter
+    const int slot0 = (int)(qpos % kBS) + kRunTok * j;          // a multiple of 16
+    // K row of slot slot0 + r: its 16-byte chunk c sits at chunk position c ^ (r & 7)
+    unsigned char *krow = reinterpret_cast<unsigned char *>(p.k_pool) + (tile * kBS + slot0) * kHD;
+    // V: dim d of the run at vrun[d * 64 + r]
+    int8_t *vrun = p.v_pool + tile * kHD * kBS + (size_t)(slot0 / kQTok) * kTileVQuarter + slot0 % kQTok;
+    const int kchunk = lane >> 2, kword = lane & 3;
 
-    // this warp's rows: quarter offsets r = warp + 16j.  K: lane l holds dims
-    // 4l..4l+3 (one packed word of codes); V: lane l holds dims l + 32k, so that
-    // the transposing writes below hit 32 different banks
-    float4 xk[kRowsPerWarp], xv[kRowsPerWarp];
+    if (lo == r0 && hi == r0 + kRunTok) {
+        // the whole run: rows r0 .. r0 + 15, kLoadAhead of them in flight
+        const size_t src = new_row_offset(p, b, h, r0, start);
+        const float4 *kp = reinterpret_cast<const float4 *>(p.k_new + src) + lane;  // next row to load
+        const float4 *vp = reinterpret_cast<const float4 *>(p.v_new + src) + lane;
+        const size_t step = (size_t)p.nkv * (kHD / 4);           // one row, in float4
+        float4 kb[kLoadAhead], vb[kLoadAhead];
 #pragma unroll
-    for (int j = 0; j < kRowsPerWarp; ++j) {
-        const long long pos = qpos + warp + kQWarps * j;
-        if (pos >= vlo && pos < vhi) {
-            const size_t src = (((size_t)b * p.n_new + (size_t)(pos - start)) * p.nkv + h) * kHD;
-            xk[j] = reinterpret_cast<const float4 *>(p.k_new + src)[lane];
-            const float *vr = p.v_new + src;
-            xv[j] = make_float4(vr[lane], vr[lane + 32], vr[lane + 64], vr[lane + 96]);
+        for (int r = 0; r < kLoadAhead; ++r) {
+            kb[r] = __ldcs(kp);
+            vb[r] = __ldcs(vp);
+            kp += step;
+            vp += step;
         }
-    }
+        // groups of 4 rows; after group g, vw[i][3] holds its tokens of dim
+        // 4 * lane + i and vw[i][0..2] the three groups before
+        uint32_t vw[4][kRunTok / 4];
+        float sc_keep = 0.0f;          // lane r < 16: K scale of row r; lane 16 + r: V scale
+#pragma unroll 1
+        for (int g = 0; g < kRunTok / 4; ++g) {
+            uint32_t wg[4];
 #pragma unroll
-    for (int j = 0; j < kRowsPerWarp; ++j) {
-        const int r = warp + kQWarps * j;
-        const long long pos = qpos + r;
-        if (pos < vlo || pos >= vhi) continue;                   // warp-uniform
-        const int slot = slot0 + r;
-        {
-            const float4 x = xk[j];
-            float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
-            m = warp_max(m);
-            const float sc = kv_row_scale(m);
-            const int4 c = kv_codes4(x, sc);
-            const uint32_t w = pack4(c.x, c.y, c.z, c.w);
-            // 16-byte chunk lane/4 of the row goes to chunk position (lane/4) ^ (slot & 7)
-            unsigned char *row = reinterpret_cast<unsigned char *>(p.k_pool) + (tile * kBS + slot) * kHD;
-            reinterpret_cast<uint32_t *>(row + (((lane >> 2) ^ (slot & 7)) << 4))[lane & 3] = w;
-            if (lane == 0) p.k_scale[tile * kBS + slot] = sc;
+            for (int u = 0; u < 4; ++u) {
+                const int r = 4 * g + u;
+                const float4 xk = kb[u % kLoadAhead], xv = vb[u % kLoadAhead];
+                if (r + kLoadAhead < kRunTok) {
+                    kb[u % kLoadAhead] = __ldcs(kp);
+                    vb[u % kLoadAhead] = __ldcs(vp);
+                    kp += step;
+                    vp += step;
+                }
+                const float sk = kv_row_scale(row_max_abs(xk));
+                const float sv = kv_row_scale(row_max_abs(xv));
+                const uint32_t wk = low_bytes4(kv_code_bytes4(xk, sk));
+                const uint4 cv = kv_code_bytes4(xv, sv);
+                reinterpret_cast<uint32_t *>(krow + r * kHD + ((kchunk ^ (r & 7)) << 4))[kword] = wk;
+                if (lane == r) sc_keep = sk;
+                if (lane == 16 + r) sc_keep = sv;
+                // byte u of the group's word of each of the lane's dims
+                constexpr uint32_t kIns[4] = {0x3210, 0x3240, 0x3410, 0x4210};
+                if (u == 0) {
+                    wg[0] = cv.x; wg[1] = cv.y; wg[2] = cv.z; wg[3] = cv.w;
+                } else {
+                    wg[0] = __byte_perm(wg[0], cv.x, kIns[u]);
+                    wg[1] = __byte_perm(wg[1], cv.y, kIns[u]);
+                    wg[2] = __byte_perm(wg[2], cv.z, kIns[u]);
+                    wg[3] = __byte_perm(wg[3], cv.w, kIns[u]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                vw[i][0] = vw[i][1];
+                vw[i][1] = vw[i][2];
+                vw[i][2] = vw[i][3];
+                vw[i][3] = wg[i];
+            }
         }
-        {
-            const float4 x = xv[j];
-            float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
-            m = warp_max(m);
-            const float sc = kv_row_scale(m);
-            const int4 c = kv_codes4(x, sc);
-            v_stage[lane + 0][r] = (int8_t)c.x;
-            v_stage[lane + 32][r] = (int8_t)c.y;
-            v_stage[lane + 64][r] = (int8_t)c.z;
-            v_stage[lane + 96][r] = (int8_t)c.w;
-            if (lane == 0) v_sc[r] = sc;
-        }
-    }
-    __syncthreads();
-
-    int8_t *vq = p.v_pool + tile * kHD * kBS + (size_t)(slot0 / kQTok) * kTileVQuarter;
-    if (vlo == qpos && vhi == qpos + kQTok) {
-        // the whole quarter: 128 dim rows of 64 bytes, one 8 KiB run, 16-byte stores
-        for (int e = threadIdx.x; e < kHD * (kQTok / 16); e += kQWarps * 32) {
-            const int d = e / (kQTok / 16), c16 = e % (kQTok / 16);
-            const uint32_t *w = reinterpret_cast<const uint32_t *>(&v_stage[d][16 * c16]);
-            reinterpret_cast<int4 *>(vq + (size_t)d * kQTok)[c16] =
-                make_int4((int)w[0], (int)w[1], (int)w[2], (int)w[3]);
-        }
-        if (threadIdx.x < kQTok / 4)
-            reinterpret_cast<float4 *>(p.v_scale + tile * kBS + slot0)[threadIdx.x] =
-                reinterpret_cast<const float4 *>(v_sc)[threadIdx.x];
+        (lane < 16 ? p.k_scale : p.v_scale)[tile * kBS + slot0 + (lane & 15)] = sc_keep;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4 *>(vrun + (size_t)(4 * lane + i) * kQTok) =
+                make_uint4(vw[i][0], vw[i][1], vw[i][2], vw[i][3]);
     } else {
-        // part of a quarter: one byte per (dim, new token)
-        const int r0 = (int)(vlo - qpos), r1 = (int)(vhi - qpos);
-        for (int e = threadIdx.x; e < kHD * kQTok; e += kQWarps * 32) {
-            const int d = e / kQTok, r = e % kQTok;
-            if (r >= r0 && r < r1) vq[(size_t)d * kQTok + r] = v_stage[d][r];
+        // part of a run (the ends of the appended range): row by row
+        for (int r = (int)(lo - r0); r < (int)(hi - r0); ++r) {
+            const size_t src = new_row_offset(p, b, h, r0 + r, start);
+            const float4 xk = reinterpret_cast<const float4 *>(p.k_new + src)[lane];
+            const float4 xv = reinterpret_cast<const float4 *>(p.v_new + src)[lane];
+            const float sk = kv_row_scale(row_max_abs(xk));
+            const float sv = kv_row_scale(row_max_abs(xv));
+            reinterpret_cast<uint32_t *>(krow + r * kHD + ((kchunk ^ (r & 7)) << 4))[kword] =
+                low_bytes4(kv_code_bytes4(xk, sk));
+            const uint4 cv = kv_code_bytes4(xv, sv);
+            vrun[(size_t)(4 * lane + 0) * kQTok + r] = (int8_t)cv.x;
+            vrun[(size_t)(4 * lane + 1) * kQTok + r] = (int8_t)cv.y;
+            vrun[(size_t)(4 * lane + 2) * kQTok + r] = (int8_t)cv.z;
+            vrun[(size_t)(4 * lane + 3) * kQTok + r] = (int8_t)cv.w;
+            if (lane == 0) {
+                p.k_scale[tile * kBS + slot0 + r] = sk;
+                p.v_scale[tile * kBS + slot0 + r] = sv;
+            }
         }
-        if (threadIdx.x >= r0 && threadIdx.x < r1) p.v_scale[tile * kBS + slot0 + threadIdx.x] = v_sc[threadIdx.x];
     }
 }
 
@@ -194,19 +266,16 @@ quantize_append_token_kernel(AppendParams p) {
     const float4 xk = reinterpret_cast<const float4 *>(p.k_new + src)[lane];
     const float4 xv = reinterpret_cast<const float4 *>(p.v_new + src)[lane];
     {
-        const float m = warp_max(fmaxf(fmaxf(fabsf(xk.x), fabsf(xk.y)), fmaxf(fabsf(xk.z), fabsf(xk.w))));
-        const float s = kv_row_scale(m);
-        const int4 c = kv_codes4(xk, s);
-        const uint32_t w = pack4(c.x, c.y, c.z, c.w);
+        const float s = kv_row_scale(row_max_abs(xk));
         unsigned char *row = reinterpret_cast<unsigned char *>(p.k_pool) + (tile * kBS + slot) * kHD;
-        reinterpret_cast<uint32_t *>(row + (((lane >> 2) ^ (slot & 7)) << 4))[lane & 3] = w;
+        reinterpret_cast<uint32_t *>(row + (((lane >> 2) ^ (slot & 7)) << 4))[lane & 3] =
+            low_bytes4(kv_code_bytes4(xk, s));
         if (lane == 0) p.k_scale[tile * kBS + slot] = s;
     }
     {
-        const float m = warp_max(fmaxf(fmaxf(fabsf(xv.x), fabsf(xv.y)), fmaxf(fabsf(xv.z), fabsf(xv.w))));
-        const float s = kv_row_scale(m);
+        const float s = kv_row_scale(row_max_abs(xv));
         int8_t *vg = p.v_pool + tile * kHD * kBS + (size_t)(slot / kStageTok) * kTileVQuarter + slot % kStageTok;
-        const int4 c = kv_codes4(xv, s);
+        const uint4 c = kv_code_bytes4(xv, s);
         vg[(size_t)(4 * lane + 0) * kStageTok] = (int8_t)c.x;
         vg[(size_t)(4 * lane + 1) * kStageTok] = (int8_t)c.y;
         vg[(size_t)(4 * lane + 2) * kStageTok] = (int8_t)c.z;
@@ -232,8 +301,11 @@ cudaError_t launch_quantize_append(const AppendParams &p, cudaStream_t s) {
                                        kAppendWarps * 32, 0, s>>>(p);
     } else {
         // quarters touched by n_new consecutive positions: at most n_new/64 + 1
-        dim3 grid(p.n_new / kQTok + (p.n_new % kQTok ? 2 : 1), p.nkv, p.batch);
-        quantize_append_kernel<<<grid, kQWarps * 32, 0, s>>>(p);
+        const int quarters = p.n_new / kQTok + (p.n_new % kQTok ? 2 : 1);
+        const long long tasks = (long long)kRunsPerQuarter * quarters * p.nkv * p.batch;
+        const long long blocks = (tasks + kBulkWarps - 1) / kBulkWarps;
+        if (blocks > INT_MAX) return cudaErrorInvalidConfiguration;
+        quantize_append_kernel<<<(unsigned)blocks, kBulkWarps * 32, 0, s>>>(p, quarters, tasks);
     }
     return cudaGetLastError();
 }
