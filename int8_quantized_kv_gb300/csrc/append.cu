@@ -8,8 +8,8 @@
 // Bulk append: one warp per run of 16 consecutive new tokens of one (sequence,
 // kv head), with no shared memory and no block barrier, so that warps stream
 // independently.  A row is one coalesced 512-byte read, a float4 per lane
-// (lane l holds dims 4l..4l+3), and the warp keeps the loads of the next rows
-// in flight while it quantises.  K codes go straight to the token-major K tile
+// (lane l holds dims 4l..4l+3); the warp keeps the copies of its next five
+// rows in flight to a shared-memory ring while it quantises.  K codes go straight to the token-major K tile
 // (one 128-byte row, its 16-byte chunks permuted by slot).  For V each lane
 // gathers the codes of its 4 dims over the 16 tokens in registers and writes
 // them as one 16-byte piece of each dim-major row of the quarter.  A decode
@@ -28,9 +28,8 @@ constexpr int kBulkWarps = 8;                    // bulk kernel: warps per CTA
 constexpr int kQTok = kStageTok;                 // the V layout's 64-token quarter
 constexpr int kRunTok = 16;                      // tokens per bulk warp
 constexpr int kRunsPerQuarter = kQTok / kRunTok;
-constexpr int kLoadAhead = 2;                    // rows in flight ahead of the one quantised
+constexpr int kRing = 6;                         // rows per bulk warp staged in shared memory
 constexpr int kNoAppend = INT_MIN;               // this sequence appends nothing
-static_assert(4 % kLoadAhead == 0, "row r of a run uses load buffer r % kLoadAhead = (r % 4) % kLoadAhead");
 
 // kv_code of four values of one row whose scale is sc = fl(max|row| / 127),
 // each in the low byte of a word, with one reciprocal per row in place of a
@@ -125,6 +124,8 @@ __device__ __forceinline__ size_t new_row_offset(const AppendParams &p, int b, i
 // time.
 __global__ void __launch_bounds__(kBulkWarps * 32, 4)
 quantize_append_kernel(AppendParams p, int quarters, long long tasks) {
+    __shared__ __align__(16) float4 ring[kBulkWarps][kRing][2][32];   // [warp][slot][K, V][lane]
+
     pdl_launch_dependents();  // let the next kernel of the stream be scheduled now
     const int lane = threadIdx.x & 31;
     const long long task = (long long)blockIdx.x * kBulkWarps + (threadIdx.x >> 5);
@@ -155,19 +156,24 @@ quantize_append_kernel(AppendParams p, int quarters, long long tasks) {
     const int kchunk = lane >> 2, kword = lane & 3;
 
     if (lo == r0 && hi == r0 + kRunTok) {
-        // the whole run: rows r0 .. r0 + 15, kLoadAhead of them in flight
+        // the whole run: rows r0 .. r0 + 15 through a ring of kRing row slots in
+        // shared memory, kRing - 1 rows in flight; each lane copies and later
+        // reads back only its own 16 bytes of a row, so its own copy groups
+        // order everything and the warp needs no barrier
         const size_t src = new_row_offset(p, b, h, r0, start);
-        const float4 *kp = reinterpret_cast<const float4 *>(p.k_new + src) + lane;  // next row to load
+        const float4 *kp = reinterpret_cast<const float4 *>(p.k_new + src) + lane;  // next row to copy
         const float4 *vp = reinterpret_cast<const float4 *>(p.v_new + src) + lane;
         const size_t step = (size_t)p.nkv * (kHD / 4);           // one row, in float4
-        float4 kb[kLoadAhead], vb[kLoadAhead];
+        float4 (*slots)[2][32] = ring[threadIdx.x >> 5];
 #pragma unroll
-        for (int r = 0; r < kLoadAhead; ++r) {
-            kb[r] = __ldcs(kp);
-            vb[r] = __ldcs(vp);
+        for (int r = 0; r < kRing - 1; ++r) {
+            cp_async16_cg(&slots[r][0][lane], kp);
+            cp_async16_cg(&slots[r][1][lane], vp);
+            cp_async_commit();
             kp += step;
             vp += step;
         }
+        int rd = 0, wr = kRing - 1;    // slots of the row read next and the row copied next
         // groups of 4 rows; after group g, vw[i][3] holds its tokens of dim
         // 4 * lane + i and vw[i][0..2] the three groups before
         uint32_t vw[4][kRunTok / 4];
@@ -178,13 +184,17 @@ quantize_append_kernel(AppendParams p, int quarters, long long tasks) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int r = 4 * g + u;
-                const float4 xk = kb[u % kLoadAhead], xv = vb[u % kLoadAhead];
-                if (r + kLoadAhead < kRunTok) {
-                    kb[u % kLoadAhead] = __ldcs(kp);
-                    vb[u % kLoadAhead] = __ldcs(vp);
+                cp_async_wait<kRing - 2>();   // row r has landed (rows r + 1 .. r + kRing - 2 may not)
+                const float4 xk = slots[rd][0][lane], xv = slots[rd][1][lane];
+                rd = rd + 1 == kRing ? 0 : rd + 1;
+                if (r + kRing - 1 < kRunTok) {   // into the slot of row r - 1, read before
+                    cp_async16_cg(&slots[wr][0][lane], kp);
+                    cp_async16_cg(&slots[wr][1][lane], vp);
                     kp += step;
                     vp += step;
+                    wr = wr + 1 == kRing ? 0 : wr + 1;
                 }
+                cp_async_commit();               // possibly empty: one group per row
                 const float sk = kv_row_scale(row_max_abs(xk));
                 const float sv = kv_row_scale(row_max_abs(xv));
                 const uint32_t wk = low_bytes4(kv_code_bytes4(xk, sk));

@@ -245,12 +245,6 @@ struct Int4Smem {
     } u;
 };
 
-__device__ __forceinline__ void cp_async16_cg(void *dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
-                 "l"(src)
-                 : "memory");
-}
-
 // Copies chunk `cidx` of this warp's split into `buf` (one copy group; an
 // empty group when the chunk does not exist or its block id is invalid).
 __device__ __forceinline__ int int4_fetch_chunk(const Int4DecodeParams &p, int b, int h, int tok_begin,

@@ -77,6 +77,20 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (cached in L2 only); dst and
+// src 16-byte aligned.  Completion through commit / wait groups.
+__device__ __forceinline__ void cp_async16_cg(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Waits until at most N of this thread's copy groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // Hint: bring `bytes` of global memory at src into L2 (no completion to wait
 // for).  src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
