@@ -24,7 +24,7 @@ namespace kvq8 {
 namespace {
 
 constexpr int kAppendWarps = 8;                  // one-token kernel: warps per CTA
-constexpr int kBulkWarps = 8;                    // bulk kernel: warps per CTA
+constexpr int kBulkWarps = 4;                    // bulk kernel: warps per CTA (one quarter)
 constexpr int kQTok = kStageTok;                 // the V layout's 64-token quarter
 constexpr int kRunTok = 16;                      // tokens per bulk warp
 constexpr int kRunsPerQuarter = kQTok / kRunTok;
@@ -33,24 +33,27 @@ constexpr int kNoAppend = INT_MIN;               // this sequence appends nothin
 
 // kv_code of four values of one row whose scale is sc = fl(max|row| / 127),
 // each in the low byte of a word, with one reciprocal per row in place of a
-// division per value.  With inv = fl(1 / sc), t = fl(v * inv + 1.5 * 2^23)
-// holds round_half_even(v * inv) in its low mantissa bits (the sum lies where
-// the fp32 spacing is 1, and 1.5 * 2^23 is even), so its low byte is the code
-// as a two's complement byte; e = fl(v * inv - r), r = t - 1.5 * 2^23, is the
-// residual of that rounding to within 2^-26.  For |v| <= max|row|,
-// |v / sc| < 127.0001, so v * inv lies within 127.0001 * 2^-24 < 2^-17 of
-// v / sc, and fl(v / sc) within half an ulp below 128 (2^-18) of v / sc.
-// When |e| <= 1/2 - 2^-15, fl(v / sc) is therefore strictly closer than 1/2
+// division per value.  inv approximates 1 / sc (the hardware reciprocal, which
+// the PTX ISA bounds by one ulp; the argument below allows three).  t =
+// fl(v * inv + 1.5 * 2^23) holds round_half_even(v * inv) in its low mantissa
+// bits (the sum lies where the fp32 spacing is 1, and 1.5 * 2^23 is even), so
+// its low byte is the code as a two's complement byte; e = fl(v * inv - r),
+// r = t - 1.5 * 2^23, is the residual of that rounding to within 2^-26.  For
+// |v| <= max|row|, |v / sc| < 127.0001, so v * inv lies within
+// 127.0001 * 3 * 2^-23 < 4.6e-5 of v / sc, and fl(v / sc) within half an ulp
+// below 128 (2^-18) of v / sc.  When |e| <= 1/2 - 2^-14 (2^-14 > 6.1e-5 >
+// 4.6e-5 + 2^-18 + 2^-26), fl(v / sc) is therefore strictly closer than 1/2
 // to r, and round_half_even(fl(v / sc)) = r, which is within [-127, 127] (no
 // clamp needed).  The four values are divided exactly when one residual is
-// larger (about 6e-5 of values) or not a number, or when sc lies outside
+// larger (about 1.2e-4 of values) or not a number, or when sc lies outside
 // [2^-120, 2^120] (a zero row, a subnormal or non-finite scale); the result
 // equals kv_code's in every case.
 __device__ __forceinline__ uint4 kv_code_bytes4(float4 x, float sc) {
     if (sc >= 0x1p-120f && sc <= 0x1p120f) {
         constexpr float kShift = 0x1.8p23f;
-        constexpr float kLim = 0.5f - 0x1p-15f;
-        const float inv = __frcp_rn(sc);
+        constexpr float kLim = 0.5f - 0x1p-14f;
+        float inv;
+        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(sc));
         const float t0 = __fmaf_rn(x.x, inv, kShift), t1 = __fmaf_rn(x.y, inv, kShift);
         const float t2 = __fmaf_rn(x.z, inv, kShift), t3 = __fmaf_rn(x.w, inv, kShift);
         const float e0 = __fmaf_rn(x.x, inv, -__fsub_rn(t0, kShift));
@@ -122,7 +125,7 @@ __device__ __forceinline__ size_t new_row_offset(const AppendParams &p, int b, i
 // token) of sequence b, kv head h.  The four runs of a quarter sit in one CTA,
 // so that the 16-byte pieces of each V row are all written at about the same
 // time.
-__global__ void __launch_bounds__(kBulkWarps * 32, 4)
+__global__ void __launch_bounds__(kBulkWarps * 32, 8)
 quantize_append_kernel(AppendParams p, int quarters, long long tasks) {
     __shared__ __align__(16) float4 ring[kBulkWarps][kRing][2][32];   // [warp][slot][K, V][lane]
 
