@@ -154,24 +154,35 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+# Sources that decide each timed kernel's code (the .cu and every header it
+# includes); a DRAM-traffic record is used only while their hash matches.
+_HEADERS = ("kvq8_device.cuh", "kvq8_internal.cuh", "kvq8_ptx.cuh", "../../include/kvq8.h")
+KERNEL_SOURCES = {
+    "decode_split_kernel": ("decode.cu",) + _HEADERS,
+    "quantize_append_kernel": ("append.cu",) + _HEADERS,
+    "kvq4_decode_attn": ("int4.cu", "decode.cu") + _HEADERS,
+    "kvmix_decode_attn": ("int4.cu", "decode.cu") + _HEADERS,
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for name in ("decode.cu", "kvq8_device.cuh", "kvq8_internal.cuh"):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "int8_quantized_kv_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per decode-split launch from a committed ncu summary, if it was
-    taken on the current kernel source; else None."""
-    p = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes (read + written) per launch of `kernel` on `workload`, from the
+    committed ncu summary, if it was taken on the current source; else None."""
+    p = os.path.join(ROOT, "profiles", "kernel_traffic.json")
     try:
         with open(p) as f:
-            rec = json.load(f)
-    except (OSError, ValueError):
+            rec = json.load(f)["records"][kernel]
+    except (OSError, ValueError, KeyError):
         return None
-    if rec.get("source_hash") != kernel_source_hash():
+    if rec.get("source_hash") != kernel_source_hash(kernel):
         return None
     return rec.get("per_launch_bytes", {}).get(workload)
 
@@ -450,7 +461,7 @@ def run_kvq8(args, rank, world, local):
     peak, peak_kind = hbm_peak()
     split_bytes = split_kernel_bytes(cfg, lens)
     achieved = split_bytes / split_s / 1e9
-    traffic = recorded_traffic(cfg.name)
+    traffic = recorded_traffic("decode_split_kernel", cfg.name)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 5),
@@ -646,7 +657,8 @@ def run_kvq4(args, rank, world, local):
         "pct_of_hbm_peak": round(100 * (value / world) / peak, 2),
         "roofline": {"bound": "hbm", "kernel": "kvq4_decode_attn (int4 split + combine)",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind, "traffic": None,
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "traffic": recorded_traffic("kvq4_decode_attn", cfg.name),
                      "algorithmic_bytes_per_launch": dec_bytes, "us_per_launch": round(dec_s * 1e6, 3)},
         "e2e": {"value": round(e_total / e_slowest / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": (q_h.numel() + nk_h.numel() + nv_h.numel()) * 4,
@@ -779,7 +791,8 @@ def run_mixed(args, rank, world, local):
         "pct_of_hbm_peak": round(100 * (value / world) / peak, 2),
         "roofline": {"bound": "hbm", "kernel": "kvmix_decode_attn (both splits + combine)",
                      "achieved": round(value / world, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round((value / world) / peak, 4), "peak_kind": peak_kind, "traffic": None,
+                     "frac": round((value / world) / peak, 4), "peak_kind": peak_kind,
+                     "traffic": recorded_traffic("kvmix_decode_attn", cfg.name),
                      "algorithmic_bytes_per_launch": sbytes, "us_per_launch": round(per_step * 1e6, 3)},
         "e2e": {"value": round(e_total / e_slowest / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": q_h.numel() * 4, "d2h_bytes_per_step": out_h.numel() * 4,
@@ -865,7 +878,8 @@ def run_append(args, rank, world, local):
         "pct_of_hbm_peak": round(100 * (value / world) / peak, 2),
         "roofline": {"bound": "hbm", "kernel": "quantize_append_kernel", "achieved": round(value / world, 2),
                      "peak": peak, "unit": "GB/s", "frac": round(value / world / peak, 4),
-                     "peak_kind": peak_kind, "traffic": None, "algorithmic_bytes_per_launch": sbytes,
+                     "peak_kind": peak_kind, "traffic": recorded_traffic("quantize_append_kernel", cfg.name),
+                     "algorithmic_bytes_per_launch": sbytes,
                      "us_per_launch": round(per_step * 1e6, 3)},
         "e2e": {"value": round(e_total / e_slowest / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": 2 * k.nbytes, "d2h_bytes_per_step": 0,
