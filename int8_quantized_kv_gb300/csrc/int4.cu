@@ -278,6 +278,14 @@ __device__ __forceinline__ int int4_fetch_chunk(const Int4DecodeParams &p, int b
 template <int G>
 __global__ void __launch_bounds__(kWarps4 * 32, 3)
 int4_decode_split_kernel(Int4DecodeParams p) {
+    // kPack (G <= 4): the 8 MMA columns carry the high fp16 parts of the
+    // operand facing the heads in columns 0-3 and the low parts in 4-7, so one
+    // MMA does both halves; lane (g, t4) then owns token 16*mt + g + 8*(t4/2)
+    // and heads 2*(t4%2) + j of the scores, and its accumulator columns hold
+    // the high (t4 < 2) or low (t4 >= 2) parts for those heads, added at the
+    // end.  Otherwise (G = 8) the columns are the 8 heads and each product
+    // takes two MMAs.
+    constexpr bool kPack = G <= 4;
     pdl_wait();
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -301,12 +309,13 @@ int4_decode_split_kernel(Int4DecodeParams p) {
 
     extern __shared__ __align__(16) unsigned char int4_smem_raw[];
     Int4Smem<G> &sm = *reinterpret_cast<Int4Smem<G> *>(int4_smem_raw);
-    // this warp's chunks: cidx = warp, warp + 4, ...; two in flight
+    // this warp's chunks: cidx = warp, warp + 4, ...; two in flight; bit i of
+    // `valid` says whether buffer i holds a chunk
     const int nchunks = (tok_end - tok_begin + kChunk4 - 1) / kChunk4;
-    int valid_buf[kBufs4];
+    unsigned valid = 0;
 #pragma unroll
     for (int i = 0; i < kBufs4; ++i)
-        valid_buf[i] = int4_fetch_chunk(p, b, h, tok_begin, nchunks, warp + kWarps4 * i, sm.u.stage[warp][i], lane) >= 0;
+        valid |= (unsigned)(int4_fetch_chunk(p, b, h, tok_begin, nchunks, warp + kWarps4 * i, sm.u.stage[warp][i], lane) >= 0) << i;
 
     const float *qrow = p.q + ((size_t)b * p.nqh + (size_t)h * G) * kHD;
     // power of two 2^k with max |q| * 2^k in [2^13, 2^14)
@@ -322,24 +331,51 @@ int4_decode_split_kernel(Int4DecodeParams p) {
     for (int w = 0; w < kWarps4; ++w) qmax = fmaxf(qmax, sm.qmax[w]);
     const int qexp = (qmax > 0.0f && isfinite(qmax)) ? 13 - ilogbf(qmax) : 0;
     const float qscale = ldexpf(1.0f, max(-120, min(120, qexp)));
-    // A fragments of Q (high and low fp16 parts) in the Q.K k-order; the
-    // values facing high nibbles (k = 2*t4 + e) carry q / 16
-    for (int i = threadIdx.x; i < 8 * 32; i += kWarps4 * 32) {
-        const int ks = i >> 5, ln = i & 31, gg = ln >> 2, tt = ln & 3;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (gg < G) {
-            const float *qg = qrow + (size_t)gg * kHD;
-            const float x0 = qg[qk_dim(ks, 2 * tt)] * qscale * 0.0625f;
-            const float x1 = qg[qk_dim(ks, 2 * tt + 1)] * qscale * 0.0625f;
-            const float x8 = qg[qk_dim(ks, 2 * tt + 8)] * qscale, x9 = qg[qk_dim(ks, 2 * tt + 9)] * qscale;
-            const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-            const __half h8 = __float2half_rn(x8), h9 = __float2half_rn(x9);
-            v.x = pack_half2(__half2float(h0), __half2float(h1));
-            v.y = pack_half2(__half2float(h8), __half2float(h9));
-            v.z = pack_half2(x0 - __half2float(h0), x1 - __half2float(h1));
-            v.w = pack_half2(x8 - __half2float(h8), x9 - __half2float(h9));
+    // B fragments of Q in the Q.K k-order (column gg of lane (gg, tt); the
+    // values facing high nibbles, k = 2*tt + e, carry q / 16).  kPack: kept in
+    // registers, column gg = head gg % 4, high part for gg < 4, low part else;
+    // otherwise staged in shared memory as high and low parts of head gg.
+    uint32_t qb[8][2];
+    if constexpr (kPack) {
+        const int hq = g & 3;
+        const bool low = g >= 4;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            float x[4] = {0.f, 0.f, 0.f, 0.f};
+            if (hq < G) {
+                const float *qg = qrow + (size_t)hq * kHD;
+                x[0] = qg[qk_dim(ks, 2 * t4)] * qscale * 0.0625f;
+                x[1] = qg[qk_dim(ks, 2 * t4 + 1)] * qscale * 0.0625f;
+                x[2] = qg[qk_dim(ks, 2 * t4 + 8)] * qscale;
+                x[3] = qg[qk_dim(ks, 2 * t4 + 9)] * qscale;
+            }
+            float y[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float hi = __half2float(__float2half_rn(x[e]));
+                y[e] = low ? x[e] - hi : hi;
+            }
+            qb[ks][0] = pack_half2(y[0], y[1]);
+            qb[ks][1] = pack_half2(y[2], y[3]);
         }
-        sm.qa[ks][ln] = v;
+    } else {
+        for (int i = threadIdx.x; i < 8 * 32; i += kWarps4 * 32) {
+            const int ks = i >> 5, ln = i & 31, gg = ln >> 2, tt = ln & 3;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (gg < G) {
+                const float *qg = qrow + (size_t)gg * kHD;
+                const float x0 = qg[qk_dim(ks, 2 * tt)] * qscale * 0.0625f;
+                const float x1 = qg[qk_dim(ks, 2 * tt + 1)] * qscale * 0.0625f;
+                const float x8 = qg[qk_dim(ks, 2 * tt + 8)] * qscale, x9 = qg[qk_dim(ks, 2 * tt + 9)] * qscale;
+                const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+                const __half h8 = __float2half_rn(x8), h9 = __float2half_rn(x9);
+                v.x = pack_half2(__half2float(h0), __half2float(h1));
+                v.y = pack_half2(__half2float(h8), __half2float(h9));
+                v.z = pack_half2(x0 - __half2float(h0), x1 - __half2float(h1));
+                v.w = pack_half2(x8 - __half2float(h8), x9 - __half2float(h9));
+            }
+            sm.qa[ks][ln] = v;
+        }
     }
     {
         // Y_g, Q_g: 8 threads per (head, group), 8 dims each (even dims face
@@ -369,17 +405,23 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         }
     }
     __syncthreads();
-    // this lane's heads are 2*t4 and 2*t4 + 1 (score and accumulator columns)
+    // this lane's heads (score and accumulator columns): 2*(t4 % 2) + j when
+    // packed, 2*t4 + j otherwise
+    const int hbase = kPack ? 2 * (t4 & 1) : 2 * t4;
     float qy[2][2], qq[2][2];
 #pragma unroll
     for (int j = 0; j < 2; ++j)
 #pragma unroll
         for (int gr = 0; gr < 2; ++gr) {
-            qy[j][gr] = 1024.0f * sm.qy[2 * t4 + j][gr];
-            qq[j][gr] = sm.qq[2 * t4 + j][gr];
+            qy[j][gr] = 1024.0f * sm.qy[hbase + j][gr];
+            qq[j][gr] = sm.qq[hbase + j][gr];
         }
     const float score_scale = p.sm_scale_log2 / qscale;
 
+    // scores per lane: kPack 1 token x 2 heads per m-tile, else 2 tokens (rows
+    // g, g + 8) x 2 heads
+    constexpr int kR = kPack ? 1 : 2;
+    const int tsel = kPack ? 8 * (t4 >> 1) : 0;   // this lane's token offset when packed
     float M[2] = {-INFINITY, -INFINITY}, Sl[2] = {0.0f, 0.0f}, Zl[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
     float acc[8][4];
 #pragma unroll
@@ -393,19 +435,17 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         asm volatile("cp.async.wait_group %0;" ::"n"(kBufs4 - 1) : "memory");
         __syncwarp();
         const unsigned char *st = sm.u.stage[warp][bi];
-        const bool have = valid_buf[bi] != 0;
-        if (have) {
+        if ((valid >> bi) & 1u) {
         const int t0 = tok_begin + cidx * kChunk4;
         const int ntok = min(kChunk4, tok_end - t0);
-        // K: token 8*nt + g, bytes 32*gr + 8*t4 .. +7
         const float4 *kps = reinterpret_cast<const float4 *>(st + kStageKpOff);
         const float4 *vps = reinterpret_cast<const float4 *>(st + kStageVpOff);
         // K rows, V words and parameters are read from the staging buffer just
         // before their use (short register lifetimes)
         const bool partial = ntok < kChunk4;   // only the split's last chunk
 
-        // ---- scores: S = K Q^T, tokens 16*mt + g + 8*r (rows), heads 2*t4 + j ----
-        float sc[2][2][2];
+        // ---- scores: S = K Q^T, tokens 16*mt + g + 8*r (rows) ----
+        float sc[2][kR][2];
         float mloc[2] = {-INFINITY, -INFINITY};
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
@@ -431,42 +471,71 @@ int4_decode_split_kernel(Int4DecodeParams p) {
                     a[r] = nib_pair(w, kHiNib);       // rows g / g+8, k = 2*t4 + e
                     a[2 + r] = nib_pair(w, kLoNib);   // rows g / g+8, k = 2*t4 + 8 + e
                 }
-                const uint4 qa = sm.qa[ks][lane];
-                mma_f16_16816(d[gr], a[0], a[1], a[2], a[3], qa.x, qa.y);
-                mma_f16_16816(d[gr], a[0], a[1], a[2], a[3], qa.z, qa.w);
+                if constexpr (kPack) {
+                    mma_f16_16816(d[gr], a[0], a[1], a[2], a[3], qb[ks][0], qb[ks][1]);
+                } else {
+                    const uint4 qa = sm.qa[ks][lane];
+                    mma_f16_16816(d[gr], a[0], a[1], a[2], a[3], qa.x, qa.y);
+                    mma_f16_16816(d[gr], a[0], a[1], a[2], a[3], qa.z, qa.w);
+                }
             }
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const float4 k4 = kps[16 * mt + g + 8 * r];
+            if constexpr (kPack) {
+                // lane t4 < 2 holds the high parts of rows g and g + 8, lane t4 ^ 2
+                // the low parts: each keeps one row and receives the other part
+                const bool lo_lane = t4 >= 2;
+                const float4 k4 = kps[16 * mt + g + tsel];
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
-                    const float x = k4.x * (d[0][2 * r + j] - qy[j][0] - k4.y * qq[j][0]) +
-                                    k4.z * (d[1][2 * r + j] - qy[j][1] - k4.w * qq[j][1]);
-                    sc[mt][r][j] = x * score_scale;
+                    float dt[2];
+#pragma unroll
+                    for (int gr = 0; gr < 2; ++gr) {
+                        const float send = lo_lane ? d[gr][j] : d[gr][2 + j];
+                        const float keep = lo_lane ? d[gr][2 + j] : d[gr][j];
+                        dt[gr] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+                    }
+                    const float x = k4.x * (dt[0] - qy[j][0] - k4.y * qq[j][0]) +
+                                    k4.z * (dt[1] - qy[j][1] - k4.w * qq[j][1]);
+                    sc[mt][0][j] = x * score_scale;
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < kR; ++r) {
+                    const float4 k4 = kps[16 * mt + g + 8 * r];
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const float x = k4.x * (d[0][2 * r + j] - qy[j][0] - k4.y * qq[j][0]) +
+                                        k4.z * (d[1][2 * r + j] - qy[j][1] - k4.w * qq[j][1]);
+                        sc[mt][r][j] = x * score_scale;
+                    }
                 }
             }
         }
+        // token of score (mt, r) of this lane
+        auto tok_of = [&](int mt, int r) { return 16 * mt + g + (kPack ? tsel : 8 * r); };
         if (partial) {
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-                for (int r = 0; r < 2; ++r)
-                    if (16 * mt + g + 8 * r >= ntok) sc[mt][r][0] = sc[mt][r][1] = -INFINITY;
+                for (int r = 0; r < kR; ++r)
+                    if (tok_of(mt, r) >= ntok) sc[mt][r][0] = sc[mt][r][1] = -INFINITY;
         }
         // this lane's score tokens' V parameters (zero past the end: stale slots)
-        float4 vp[2][2];
+        float4 vp[2][kR];
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                vp[mt][r] = vps[16 * mt + g + 8 * r];
-                if (partial && 16 * mt + g + 8 * r >= ntok) vp[mt][r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int r = 0; r < kR; ++r) {
+                vp[mt][r] = vps[tok_of(mt, r)];
+                if (partial && tok_of(mt, r) >= ntok) vp[mt][r] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt)
-                mloc[j] = fmaxf(mloc[j], fmaxf(sc[mt][0][j], sc[mt][1][j]));
+#pragma unroll
+                for (int r = 0; r < kR; ++r) mloc[j] = fmaxf(mloc[j], sc[mt][r][j]);
+            // lanes sharing this lane's heads: all g, and t4 ^ 2 when packed
+            if constexpr (kPack) mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 2));
             mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 4));
             mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 8));
             mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 16));
@@ -477,13 +546,13 @@ int4_decode_split_kernel(Int4DecodeParams p) {
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-            for (int r = 0; r < 2; ++r) vsmax = fmaxf(vsmax, fmaxf(vp[mt][r].x, vp[mt][r].z));
+            for (int r = 0; r < kR; ++r) vsmax = fmaxf(vsmax, fmaxf(vp[mt][r].x, vp[mt][r].z));
         const int e_need = __reduce_max_sync(0xffffffffu, ((__float_as_int(vsmax) >> 23) & 0xff) - 126);
         int e_new = e_cur;
         if (e_need > e_cur || e_need < e_cur - 12) e_new = max(-120, min(120, e_need));
         const float inv = __int_as_float((127 - e_new) << 23);
 
-        // online softmax per head (the 8 lanes of a column agree), raised lazily
+        // online softmax per head (the lanes of a head agree), raised lazily
         const bool grow = mloc[0] > M[0] + 8.0f || mloc[1] > M[1] + 8.0f;
         float alpha[2] = {1.0f, 1.0f};
         bool rescale = e_new != e_cur;
@@ -498,15 +567,16 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         }
         const float two = __int_as_float((127 + max(-126, min(127, e_cur - e_new))) << 23);
         // P'_g = w * vscale_g * 2^-e, high and low fp16 parts, into the freed K
-        // area as [group][part][32 tokens][8 heads] for the transposing loads
+        // area for the transposing loads: kPack [group][32 tokens][high parts of
+        // heads 0-3 | low parts], else [group][part][32 tokens][8 heads]
         uint32_t *ptile = reinterpret_cast<uint32_t *>(const_cast<unsigned char *>(st) + kStageKOff);
         __syncwarp();   // every lane is done reading the K rows
         float wsum[2] = {0.f, 0.f}, zs[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int t = 16 * mt + g + 8 * r;
+            for (int r = 0; r < kR; ++r) {
+                const int t = tok_of(mt, r);
                 float pg[2][2];   // [group][head j]
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
@@ -520,9 +590,17 @@ int4_decode_split_kernel(Int4DecodeParams p) {
 #pragma unroll
                 for (int gr = 0; gr < 2; ++gr) {
                     const __half h0 = __float2half_rn(pg[gr][0]), h1 = __float2half_rn(pg[gr][1]);
-                    ptile[((gr * 2 + 0) * kChunk4 + t) * 4 + t4] = pack_half2(__half2float(h0), __half2float(h1));
-                    ptile[((gr * 2 + 1) * kChunk4 + t) * 4 + t4] =
-                        pack_half2(pg[gr][0] - __half2float(h0), pg[gr][1] - __half2float(h1));
+                    const uint32_t hi = pack_half2(__half2float(h0), __half2float(h1));
+                    const uint32_t lo = pack_half2(pg[gr][0] - __half2float(h0), pg[gr][1] - __half2float(h1));
+                    if constexpr (kPack) {
+                        // words 4t + t4 and 4t + (t4 ^ 2): 32 distinct banks per store
+                        const bool lo_lane = t4 >= 2;
+                        ptile[(gr * kChunk4 + t) * 4 + t4] = lo_lane ? lo : hi;
+                        ptile[(gr * kChunk4 + t) * 4 + (t4 ^ 2)] = lo_lane ? hi : lo;
+                    } else {
+                        ptile[((gr * 2 + 0) * kChunk4 + t) * 4 + t4] = hi;
+                        ptile[((gr * 2 + 1) * kChunk4 + t) * 4 + t4] = lo;
+                    }
                 }
             }
 #pragma unroll
@@ -543,18 +621,18 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         __syncwarp();
         // B fragments of P.V: matrix i of an x4 transposing load = tokens 8i..8i+7,
         // so lane (g, t4) receives {P[8i + 2*t4][g], P[8i + 2*t4 + 1][g]}
-        uint32_t bh[2][2][2], bl[2][2][2];   // [group][k-step][b0, b1]
+        constexpr int kParts = kPack ? 1 : 2;
+        uint32_t bf[2][kParts][2][2];   // [group][part][k-step][b0, b1]
 #pragma unroll
         for (int gr = 0; gr < 2; ++gr)
 #pragma unroll
-            for (int hl = 0; hl < 2; ++hl) {
-                const uint32_t addr = (uint32_t)__cvta_generic_to_shared(ptile + ((gr * 2 + hl) * kChunk4 + lane) * 4);
+            for (int hl = 0; hl < kParts; ++hl) {
+                const uint32_t addr = (uint32_t)__cvta_generic_to_shared(ptile + ((gr * kParts + hl) * kChunk4 + lane) * 4);
                 uint32_t r0, r1, r2, r3;
                 asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                              : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                              : "r"(addr));
-                uint32_t(&bb)[2][2] = hl ? bl[gr] : bh[gr];
-                bb[0][0] = r0; bb[0][1] = r1; bb[1][0] = r2; bb[1][1] = r3;
+                bf[gr][hl][0][0] = r0; bf[gr][hl][0][1] = r1; bf[gr][hl][1][0] = r2; bf[gr][hl][1][1] = r3;
             }
 
         // ---- P.V: out^T += V^T P'_g ----
@@ -577,50 +655,60 @@ int4_decode_split_kernel(Int4DecodeParams p) {
                 const uint32_t r89 = __byte_perm(vw[2][gr], vw[3][gr], sel);
                 const uint32_t a0 = nib_pair_exact(r01, kHiNib), a1 = nib_pair_exact(r01, kLoNib);
                 const uint32_t a2 = nib_pair_exact(r89, kHiNib), a3 = nib_pair_exact(r89, kLoNib);
-                mma_f16_16816(acc[mt], a0, a1, a2, a3, bh[gr][ks2][0], bh[gr][ks2][1]);
-                mma_f16_16816(acc[mt], a0, a1, a2, a3, bl[gr][ks2][0], bl[gr][ks2][1]);
+#pragma unroll
+                for (int hl = 0; hl < kParts; ++hl)
+                    mma_f16_16816(acc[mt], a0, a1, a2, a3, bf[gr][hl][ks2][0], bf[gr][hl][ks2][1]);
             }
         }
         }
         __syncwarp();
-        valid_buf[bi] = int4_fetch_chunk(p, b, h, tok_begin, nchunks, cidx + kWarps4 * kBufs4,
+        const bool ok = int4_fetch_chunk(p, b, h, tok_begin, nchunks, cidx + kWarps4 * kBufs4,
                                          sm.u.stage[warp][bi], lane) >= 0;
+        valid = (valid & ~(1u << bi)) | ((unsigned)ok << bi);
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 
-    // ---- this warp's state: lanes of column t4 hold heads 2*t4, 2*t4+1 ----
+    // ---- this warp's state: the lanes of this lane's heads ----
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
+        for (int o = kPack ? 2 : 4; o < 32; o <<= 1) {
             Sl[j] += __shfl_xor_sync(0xffffffffu, Sl[j], o);
             Zl[j][0] += __shfl_xor_sync(0xffffffffu, Zl[j][0], o);
             Zl[j][1] += __shfl_xor_sync(0xffffffffu, Zl[j][1], o);
         }
     }
+    if constexpr (kPack) {
+        // add the low parts' columns (lane t4 ^ 2) into the high parts'
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[mt][i] += __shfl_xor_sync(0xffffffffu, acc[mt][i], 2);
+    }
     const float unit_scale = __int_as_float((127 + max(-126, min(127, e_cur))) << 23);
     __syncthreads();   // every warp is done with its staging buffers
+    const bool writer = !kPack || t4 < 2;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
         const int gr = mt >> 2;
         const int dim = 2 * (32 * gr + 4 * g + (mt & 3));
-        const int h0 = 2 * t4, h1 = 2 * t4 + 1;
+        const int h0 = hbase, h1 = hbase + 1;
         // rows g carry 16 c (high nibbles: even dims)
-        if (h0 < G) {
+        if (writer && h0 < G) {
             sm.u.red.acc[warp][h0][dim] = (acc[mt][0] * 0.0625f - Zl[0][gr]) * unit_scale;
             sm.u.red.acc[warp][h0][dim + 1] = (acc[mt][2] - Zl[0][gr]) * unit_scale;
         }
-        if (h1 < G) {
+        if (writer && h1 < G) {
             sm.u.red.acc[warp][h1][dim] = (acc[mt][1] * 0.0625f - Zl[1][gr]) * unit_scale;
             sm.u.red.acc[warp][h1][dim + 1] = (acc[mt][3] - Zl[1][gr]) * unit_scale;
         }
     }
-    if (g == 0) {
+    if (g == 0 && writer) {
 #pragma unroll
         for (int j = 0; j < 2; ++j)
-            if (2 * t4 + j < G) {
-                sm.u.red.ml[warp][2 * t4 + j][0] = M[j];
-                sm.u.red.ml[warp][2 * t4 + j][1] = Sl[j];
+            if (hbase + j < G) {
+                sm.u.red.ml[warp][hbase + j][0] = M[j];
+                sm.u.red.ml[warp][hbase + j][1] = Sl[j];
             }
     }
     __syncthreads();
