@@ -157,31 +157,29 @@ int4_requantize_kernel(Int4RequantParams p) {
 }
 
 // ---- tensor-core decode ----
-// Both contractions run as mma.sync m16n8k16 (fp16 in, fp32 accumulate); codes
-// 0..15 are exact in fp16.
+// Both contractions run as mma.sync m16n8k16 (fp16 in, fp32 accumulate).
+// Codes enter as fp16 by one mask per two codes, with no conversion: the
+// masked bits of a low nibble are the fp16 subnormal c * 2^-24, those of a
+// high nibble, in place, 16c * 2^-24 (exact); the sums are scaled back by 2^24.
 //
 // Q.K as S = K Q^T: A = K codes (rows = 16 tokens, k = dims), B = the fp32
-// query split into fp16 high + low parts (columns = heads).  K codes enter as
-// fp16 by one mask-and-or per two codes: a low nibble as 1024 + c, a high
-// nibble in place as 1024 + 16c (exact: fp16 steps are 1 on [1024, 2048)); the
-// query values facing high nibbles are divided by 16, so each code meets its
-// own q.  The 1024 is removed with the zero point:
-//   s = sm * 2^-k * sum_g scale_g * (D'_g - 1024 Y_g - zero_g Q_g),
-//   D'_g = sum_{d in g} b_d y_d,  Y_g = sum_{d in g} y_d,  Q_g = sum_{d in g} q_d,
-// y = the fed query value (q or q/16, as high + low fp16 parts), q = the query
-// times a power of two 2^k that puts its largest element at 2^13..2^14 (fp16
-// keeps full precision for q/16).  Within a 64-dim group the bias costs at
-// most fp32 rounding of a 64-term sum.  The score fragment (row = token,
-// column = head) reaches P.V through shared memory: P' is stored as
-// [32 tokens][8 heads] fp16 tiles in the chunk's K area (free once K has been
-// read) and loaded back transposed (ldmatrix .trans) into the B fragments.
+// query split into fp16 high + low parts (columns = heads).  The query values
+// facing high nibbles are divided by 16, so each code meets its own q:
+//   s = sm * 2^-k * sum_g scale_g * (2^24 D'_g - zero_g Q_g),
+//   D'_g = sum_{d in g} a_d y_d,  Q_g = sum_{d in g} q_d,
+// a = the fed code value, y = the fed query value (q or q/16, as high + low
+// fp16 parts), q = the query times a power of two 2^k that puts its largest
+// element at 2^13..2^14 (fp16 keeps full precision for q/16).  The score
+// fragment (row = token, column = head) reaches P.V through shared memory: P'
+// is stored as fp16 tiles of 32 tokens x 8 columns in the chunk's K area
+// (free once K has been read) and loaded back transposed (ldmatrix .trans)
+// into the B fragments.
 //
-// P.V as out^T = V^T P: A = V codes (rows = dims, k = tokens, exact after one
-// fp16 subtract), B = P'_g = w * vscale_g(t) * 2^-e per dim group, split into
-// fp16 high + low; V codes enter as exact fp16 (c, or 16c for the high nibble
-// of a byte, which the epilogue divides by 16); the zero point enters as a
-// correction per (head, group),
-//   out[d][h] = sum_t P'_g c_{t,d} - Z[h][g],  Z[h][g] = sum_t P'_g zero_g(t),
+// P.V as out^T = V^T P: A = V codes (rows = dims, k = tokens), B = P'_g = w *
+// vscale_g(t) * 2^-e per dim group, split into fp16 high + low; the high
+// nibble of a byte enters as 16c, which the epilogue divides by 16; the zero
+// point enters as a correction per (head, group),
+//   out[d][h] = 2^24 sum_t P'_g a_{t,d} - Z[h][g],  Z[h][g] = sum_t P'_g zero_g(t),
 // rescaled with the accumulator.  Row r of m-tile mt is dim 2*B + (r >= 8)
 // with byte B = 32*(mt/4) + 4*(r%8) + mt%4, so a lane reads one 32-bit word
 // per token and dim group.
@@ -189,20 +187,11 @@ int4_requantize_kernel(Int4RequantParams p) {
 // k-order of Q.K (k-step ks: group ks/4, sub = ks%4; lane t4 supplies the
 // nibbles of the word at byte 32*(ks/4) + 8*t4 + 4*(sub/2)): k = 2*t4 + e ->
 // the high nibble of byte (sub%2) + 2e, k = 2*t4 + 8 + e -> its low nibble.
-constexpr uint32_t kFp16x2_1024 = 0x64006400u;
-
-// {1024 + n0, 1024 + n2} of the low nibbles of bytes 0 and 2 of w (mask
-// 0x000F000F), or {1024 + 16 n0', 1024 + 16 n2'} of their high nibbles (mask
-// 0x00F000F0)
-__device__ __forceinline__ uint32_t nib_pair(uint32_t w, uint32_t mask) { return (w & mask) | kFp16x2_1024; }
-
-// the same without the 1024: {n0, n2} or {16 n0', 16 n2'}, exact
-__device__ __forceinline__ uint32_t nib_pair_exact(uint32_t w, uint32_t mask) {
-    uint32_t x = nib_pair(w, mask);
-    const __half2 r = __hsub2(*reinterpret_cast<__half2 *>(&x),
-                              __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
-    return *reinterpret_cast<const uint32_t *>(&r);
-}
+// The fp16 pair {n0 * 2^-24, n2 * 2^-24} of the low nibbles of bytes 0 and 2
+// of w (mask 0x000F000F), or {16 n0' * 2^-24, 16 n2' * 2^-24} of their high
+// nibbles (mask 0x00F000F0): the masked bits are fp16 subnormals, exact.
+__device__ __forceinline__ uint32_t nib_pair(uint32_t w, uint32_t mask) { return w & mask; }
+constexpr float kNibUnit = 0x1p24f;   // 1 / the value of one code step in nib_pair
 constexpr uint32_t kLoNib = 0x000F000Fu, kHiNib = 0x00F000F0u;
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
@@ -233,7 +222,6 @@ constexpr int kBufs4 = 2;
 template <int G>
 struct Int4Smem {
     uint4 qa[8][32];                 // per k-step and lane: a0 high, a2 high, a0 low, a2 low
-    float qy[8][2];                  // Y_g per head (rows >= G: 0)
     float qq[8][2];                  // Q_g per head
     float qmax[kWarps4];
     union {
@@ -245,24 +233,34 @@ struct Int4Smem {
     } u;
 };
 
+// Per-lane shared-memory offsets of the chunk copies: the chunk's 32 code rows
+// are 2 KiB contiguous in the cache, lane l copying bytes 16l + 512i (row
+// l/4 + 8i, part l%4); the staged K row keeps its 32-byte halves swapped on
+// rows 2, 3 (mod 4), which row + 8 does not change.
+struct Int4FetchLane {
+    int kdst, vdst;
+    __device__ __forceinline__ explicit Int4FetchLane(int lane)
+        : kdst((lane >> 2) * kKPitch4 + 32 * kswz(lane >> 2, (lane & 3) >> 1) + 16 * (lane & 1)),
+          vdst((lane >> 2) * kVPitch4 + 16 * (lane & 3)) {}
+};
+
 // Copies chunk `cidx` of this warp's split into `buf` (one copy group; an
 // empty group when the chunk does not exist or its block id is invalid).
 __device__ __forceinline__ int int4_fetch_chunk(const Int4DecodeParams &p, int b, int h, int tok_begin,
-                                                int nchunks, int cidx, unsigned char *buf, int lane) {
+                                                int nchunks, int cidx, unsigned char *buf, int lane,
+                                                const Int4FetchLane &fl) {
     int phys = -1;
     if (cidx < nchunks) {
         const int t0 = tok_begin + cidx * kChunk4;
         phys = p.block_table[(size_t)b * p.max_blocks + t0 / kBS];
         if (phys >= 0 && phys < p.num_blocks) {
             const size_t row0 = ((size_t)phys * p.nkv + h) * kBS + t0 % kBS;
-            const uint8_t *kc = p.k_codes + row0 * kRowBytes;
-            const uint8_t *vc = p.v_codes + row0 * kRowBytes;
+            const uint8_t *kc = p.k_codes + row0 * kRowBytes + 16 * lane;
+            const uint8_t *vc = p.v_codes + row0 * kRowBytes + 16 * lane;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int q = lane + 32 * i, r = q >> 2, part = q & 3;
-                cp_async16_cg(buf + kStageKOff + r * kKPitch4 + 32 * kswz(r, part >> 1) + 16 * (part & 1),
-                              kc + r * kRowBytes + 16 * part);
-                cp_async16_cg(buf + kStageVOff + r * kVPitch4 + 16 * part, vc + r * kRowBytes + 16 * part);
+                cp_async16_cg(buf + kStageKOff + fl.kdst + 8 * kKPitch4 * i, kc + 512 * i);
+                cp_async16_cg(buf + kStageVOff + fl.vdst + 8 * kVPitch4 * i, vc + 512 * i);
             }
             cp_async16_cg(buf + kStageKpOff + 16 * lane, p.k_param + (row0 + lane) * 4);
             cp_async16_cg(buf + kStageVpOff + 16 * lane, p.v_param + (row0 + lane) * 4);
@@ -271,7 +269,7 @@ __device__ __forceinline__ int int4_fetch_chunk(const Int4DecodeParams &p, int b
             phys = -1;
         }
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
+    cp_async_commit();
     return phys;
 }
 
@@ -312,10 +310,12 @@ int4_decode_split_kernel(Int4DecodeParams p) {
     // this warp's chunks: cidx = warp, warp + 4, ...; two in flight; bit i of
     // `valid` says whether buffer i holds a chunk
     const int nchunks = (tok_end - tok_begin + kChunk4 - 1) / kChunk4;
+    const Int4FetchLane fl(lane);
     unsigned valid = 0;
 #pragma unroll
     for (int i = 0; i < kBufs4; ++i)
-        valid |= (unsigned)(int4_fetch_chunk(p, b, h, tok_begin, nchunks, warp + kWarps4 * i, sm.u.stage[warp][i], lane) >= 0) << i;
+        valid |= (unsigned)(int4_fetch_chunk(p, b, h, tok_begin, nchunks, warp + kWarps4 * i, sm.u.stage[warp][i],
+                                             lane, fl) >= 0) << i;
 
     const float *qrow = p.q + ((size_t)b * p.nqh + (size_t)h * G) * kHD;
     // power of two 2^k with max |q| * 2^k in [2^13, 2^14)
@@ -378,10 +378,11 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         }
     }
     {
-        // Y_g, Q_g: 8 threads per (head, group), 8 dims each (even dims face
-        // high nibbles and are fed as q / 16)
+        // Q_g: 8 threads per (head, group), 8 dims each, summing the query as
+        // the MMAs see it (even dims face high nibbles and are fed as q / 16,
+        // as high + low fp16 parts)
         const int gg = threadIdx.x >> 4, gr = (threadIdx.x >> 3) & 1, part = threadIdx.x & 7;
-        float ys = 0.0f, qs = 0.0f;
+        float qs = 0.0f;
         if (gg < G) {
 #pragma unroll
             for (int d = 0; d < 8; ++d) {
@@ -390,32 +391,22 @@ int4_decode_split_kernel(Int4DecodeParams p) {
                 const float x = qrow[(size_t)gg * kHD + dim] * qscale * f;
                 const float hf = __half2float(__float2half_rn(x));
                 const float y = hf + __half2float(__float2half_rn(x - hf));
-                ys += y;
                 qs += y / f;
             }
         }
 #pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {
-            ys += __shfl_xor_sync(0xffffffffu, ys, o);
-            qs += __shfl_xor_sync(0xffffffffu, qs, o);
-        }
-        if (part == 0) {
-            sm.qy[gg][gr] = ys;
-            sm.qq[gg][gr] = qs;
-        }
+        for (int o = 1; o < 8; o <<= 1) qs += __shfl_xor_sync(0xffffffffu, qs, o);
+        if (part == 0) sm.qq[gg][gr] = qs;
     }
     __syncthreads();
     // this lane's heads (score and accumulator columns): 2*(t4 % 2) + j when
     // packed, 2*t4 + j otherwise
     const int hbase = kPack ? 2 * (t4 & 1) : 2 * t4;
-    float qy[2][2], qq[2][2];
+    float qq[2][2];
 #pragma unroll
     for (int j = 0; j < 2; ++j)
 #pragma unroll
-        for (int gr = 0; gr < 2; ++gr) {
-            qy[j][gr] = 1024.0f * sm.qy[hbase + j][gr];
-            qq[j][gr] = sm.qq[hbase + j][gr];
-        }
+        for (int gr = 0; gr < 2; ++gr) qq[j][gr] = sm.qq[hbase + j][gr];
     const float score_scale = p.sm_scale_log2 / qscale;
 
     // scores per lane: kPack 1 token x 2 heads per m-tile, else 2 tokens (rows
@@ -432,7 +423,7 @@ int4_decode_split_kernel(Int4DecodeParams p) {
 
     for (int it = 0, cidx = warp; cidx < nchunks; ++it, cidx += kWarps4) {
         const int bi = it % kBufs4;
-        asm volatile("cp.async.wait_group %0;" ::"n"(kBufs4 - 1) : "memory");
+        cp_async_wait<kBufs4 - 1>();
         __syncwarp();
         const unsigned char *st = sm.u.stage[warp][bi];
         if ((valid >> bi) & 1u) {
@@ -493,8 +484,8 @@ int4_decode_split_kernel(Int4DecodeParams p) {
                         const float keep = lo_lane ? d[gr][2 + j] : d[gr][j];
                         dt[gr] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
                     }
-                    const float x = k4.x * (dt[0] - qy[j][0] - k4.y * qq[j][0]) +
-                                    k4.z * (dt[1] - qy[j][1] - k4.w * qq[j][1]);
+                    const float x = k4.x * fmaf(dt[0], kNibUnit, -k4.y * qq[j][0]) +
+                                    k4.z * fmaf(dt[1], kNibUnit, -k4.w * qq[j][1]);
                     sc[mt][0][j] = x * score_scale;
                 }
             } else {
@@ -503,8 +494,8 @@ int4_decode_split_kernel(Int4DecodeParams p) {
                     const float4 k4 = kps[16 * mt + g + 8 * r];
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
-                        const float x = k4.x * (d[0][2 * r + j] - qy[j][0] - k4.y * qq[j][0]) +
-                                        k4.z * (d[1][2 * r + j] - qy[j][1] - k4.w * qq[j][1]);
+                        const float x = k4.x * fmaf(d[0][2 * r + j], kNibUnit, -k4.y * qq[j][0]) +
+                                        k4.z * fmaf(d[1][2 * r + j], kNibUnit, -k4.w * qq[j][1]);
                         sc[mt][r][j] = x * score_scale;
                     }
                 }
@@ -653,8 +644,8 @@ int4_decode_split_kernel(Int4DecodeParams p) {
                 const uint32_t sel = (uint32_t)(k | (k << 4) | ((4 + k) << 8) | ((4 + k) << 12));
                 const uint32_t r01 = __byte_perm(vw[0][gr], vw[1][gr], sel);
                 const uint32_t r89 = __byte_perm(vw[2][gr], vw[3][gr], sel);
-                const uint32_t a0 = nib_pair_exact(r01, kHiNib), a1 = nib_pair_exact(r01, kLoNib);
-                const uint32_t a2 = nib_pair_exact(r89, kHiNib), a3 = nib_pair_exact(r89, kLoNib);
+                const uint32_t a0 = nib_pair(r01, kHiNib), a1 = nib_pair(r01, kLoNib);
+                const uint32_t a2 = nib_pair(r89, kHiNib), a3 = nib_pair(r89, kLoNib);
 #pragma unroll
                 for (int hl = 0; hl < kParts; ++hl)
                     mma_f16_16816(acc[mt], a0, a1, a2, a3, bf[gr][hl][ks2][0], bf[gr][hl][ks2][1]);
@@ -663,7 +654,7 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         }
         __syncwarp();
         const bool ok = int4_fetch_chunk(p, b, h, tok_begin, nchunks, cidx + kWarps4 * kBufs4,
-                                         sm.u.stage[warp][bi], lane) >= 0;
+                                         sm.u.stage[warp][bi], lane, fl) >= 0;
         valid = (valid & ~(1u << bi)) | ((unsigned)ok << bi);
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -693,14 +684,14 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         const int gr = mt >> 2;
         const int dim = 2 * (32 * gr + 4 * g + (mt & 3));
         const int h0 = hbase, h1 = hbase + 1;
-        // rows g carry 16 c (high nibbles: even dims)
+        // rows g carry 16 c (high nibbles: even dims), in code steps of 2^-24
         if (writer && h0 < G) {
-            sm.u.red.acc[warp][h0][dim] = (acc[mt][0] * 0.0625f - Zl[0][gr]) * unit_scale;
-            sm.u.red.acc[warp][h0][dim + 1] = (acc[mt][2] - Zl[0][gr]) * unit_scale;
+            sm.u.red.acc[warp][h0][dim] = fmaf(acc[mt][0], kNibUnit * 0.0625f, -Zl[0][gr]) * unit_scale;
+            sm.u.red.acc[warp][h0][dim + 1] = fmaf(acc[mt][2], kNibUnit, -Zl[0][gr]) * unit_scale;
         }
         if (writer && h1 < G) {
-            sm.u.red.acc[warp][h1][dim] = (acc[mt][1] * 0.0625f - Zl[1][gr]) * unit_scale;
-            sm.u.red.acc[warp][h1][dim + 1] = (acc[mt][3] - Zl[1][gr]) * unit_scale;
+            sm.u.red.acc[warp][h1][dim] = fmaf(acc[mt][1], kNibUnit * 0.0625f, -Zl[1][gr]) * unit_scale;
+            sm.u.red.acc[warp][h1][dim + 1] = fmaf(acc[mt][3], kNibUnit, -Zl[1][gr]) * unit_scale;
         }
     }
     if (g == 0 && writer) {
