@@ -296,14 +296,18 @@ int4_decode_split_kernel(Int4DecodeParams p) {
     }
     if (p.n4_blocks) L = min(L, max(0, min(p.n4_blocks[b], p.max_blocks)) * kBS);   // the 4-bit part only
     const size_t u = (size_t)b * p.nkv + h;
+    // this unit's nsplit splits share its L tokens evenly (whole chunks), so
+    // that a unit shorter than the table (a short context, or the 4-bit part
+    // of a mixed-precision sequence) still keeps every CTA of the grid busy
+    const int st = max(kChunk4, ((L + p.nsplit - 1) / p.nsplit + kChunk4 - 1) / kChunk4 * kChunk4);
     if (split == 0 && threadIdx.x == 0) {
         // records of unit u are u*nsplit + j; the combine reads first + u + j
-        const int nvalid = (L + p.split_tokens - 1) / p.split_tokens;
+        const int nvalid = (L + st - 1) / st;
         p.ws_meta[u] = make_int2((int)(u * (p.nsplit - 1)), nvalid);
     }
-    const int tok_begin = split * p.split_tokens;
+    const int tok_begin = split * st;
     if (tok_begin >= L) return;
-    const int tok_end = min(L, tok_begin + p.split_tokens);
+    const int tok_end = min(L, tok_begin + st);
 
     extern __shared__ __align__(16) unsigned char int4_smem_raw[];
     Int4Smem<G> &sm = *reinterpret_cast<Int4Smem<G> *>(int4_smem_raw);
@@ -729,9 +733,10 @@ int4_decode_split_kernel(Int4DecodeParams p) {
 
 }  // namespace
 
-// Splits: as many CTAs as are resident at once (one wave; every split of a
-// unit has the same length), within the record budget of the decode
-// workspace (kMaxCtas + units records).
+// Splits: as many CTAs as are resident at once (one wave), within the record
+// budget of the decode workspace (kMaxCtas + units records).  The kernel
+// divides each unit's own length among its nsplit splits; split_tokens is
+// the split length of a unit that fills the table.
 bool make_int4_plan(int batch, int nkv, int max_blocks, int resident_ctas, int *nsplit, int *split_tokens) {
     const int64_t units = (int64_t)batch * nkv;
     if (units <= 0 || max_blocks <= 0) return false;
