@@ -487,10 +487,61 @@ def run_kvq8(args, rank, world, local):
     }
     if comparator is not None:
         line["fp32_kv_comparator"] = comparator
+    if cfg.layers > 1 and cfg.batch == cfg.layers:
+        line["per_layer_graph"] = per_layer_graph(args, cfg, sbytes, caches[0], q_d, nk1, nv1, table_d,
+                                                  lens_d, out, status, sm, max_blocks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, lens, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def per_layer_graph(args, cfg, sbytes, cache, q_d, nk1, nv1, table_d, lens_d, out_folded, status, sm,
+                    max_blocks):
+    """The same step as cfg.layers separate kvq8_decode_step calls, one per
+    layer (batch 1 each, its own workspace), captured once in a CUDA graph and
+    replayed: the launch form of an engine that runs one layer at a time.  One
+    replay streams every layer's cache (the sum is far above L2), so replays
+    read from HBM like the folded step."""
+    import torch
+    from int8_quantized_kv_gb300 import kvq8
+    dev = q_d.device
+    n_layers = cfg.batch
+    outs = torch.empty_like(q_d)
+    wss = [kvq8.alloc_workspace(1, cfg.nqh, cfg.nkv, max_blocks, dev) for _ in range(n_layers)]
+    s = torch.cuda.Stream(dev)
+
+    def calls():
+        for b in range(n_layers):
+            kvq8.decode_step(q_d[b:b + 1], nk1[b:b + 1], nv1[b:b + 1], cache, table_d[b:b + 1],
+                             lens_d[b:b + 1], outs[b:b + 1], wss[b], sm_scale=sm, dev_status=status,
+                             stream=s)
+
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        calls()                       # once outside the graph
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        calls()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    n = max(10, min(args.steps, 200))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item():#x} in the per-layer calls")
+    t = e0.elapsed_time(e1) / 1e3 / n
+    d = (outs.double() - out_folded.double()).abs()
+    return {"us_per_step": round(t * 1e6, 2), "value": round(sbytes / t / 1e9, 2), "unit": "GB/s",
+            "calls_per_step": n_layers, "launches_per_step": 3 * n_layers, "replays": n,
+            "path": f"{n_layers} kvq8_decode_step calls (one layer each) in one CUDA graph",
+            "max_abs_diff_vs_folded": float(d.max())}
 
 
 def f32_comparator(args, cfg, lens, cf, q_d, table_d, lens_d, ws, out_q8, status, stream, split_s):
