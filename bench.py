@@ -433,13 +433,14 @@ def run_kvq8(args, rank, world, local):
     nk_h, nv_h = torch.from_numpy(new_k).pin_memory(), torch.from_numpy(new_v).pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
 
+    nk1_h, nv1_h = nk_h[:, 0], nv_h[:, 0]
+
     def e2e_step(i):
+        # one C call: host Q and the step's token copied in, the step, the result
+        # copied out; then the host waits for it
         c = caches[i % copies]
-        q_d.copy_(q_h, non_blocking=True)
-        nk_d.copy_(nk_h, non_blocking=True)
-        nv_d.copy_(nv_h, non_blocking=True)
-        kvq8.decode_step(q_d, nk1, nv1, c, table_d, lens_d, out, ws, sm_scale=sm, stream=stream)
-        out_h.copy_(out, non_blocking=True)
+        kvq8.decode_step_host(q_h, nk1_h, nv1_h, out_h, q_d, nk1, nv1, c, table_d, lens_d, out, ws,
+                              sm_scale=sm, stream=stream)
         stream.synchronize()
 
     for i in range(3):
@@ -912,9 +913,9 @@ def run_append(args, rank, world, local):
     e2e_steps = args.e2e_steps or min(args.steps, 50)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        k_d.copy_(k_h, non_blocking=True)
-        v_d.copy_(v_h, non_blocking=True)
-        step()
+        # one C call: the host rows copied in and appended; then the host waits
+        kvq8.quantize_append_host(k_h, v_h, k_d, v_d, start_d, table_d, cache, dev_status=status,
+                                  stream=stream)
         stream.synchronize()
     e2e_s = time.perf_counter() - t0
     e_total, e_slowest = aggregate(sbytes * e2e_steps, e2e_s, dev)

@@ -125,6 +125,27 @@ kvq8_status kvq8_quantize_append(const float *k_new, const float *v_new,
                                  float *k_scale, float *v_scale,
                                  uint32_t *dev_status, void *stream);
 
+/*
+ * kvq8_quantize_append_host -- kvq8_quantize_append with the new rows in host
+ * memory: k_new_host and v_new_host (fp32 [batch][n_new][nkv][hd]) are copied
+ * into the caller's device buffers k_new and v_new of the same size (one
+ * cudaMemcpyAsync each, on `stream`), then appended.  Asynchronous like every
+ * call here: the host buffers must not change until the stream has passed
+ * this point; page-locked host memory lets the copies run at full speed.
+ * Returns as kvq8_quantize_append (all arguments are checked before anything
+ * is queued); KVQ8_ERR_INVALID_ARG also for a null host pointer when there is
+ * something to append; KVQ8_ERR_CUDA when a copy cannot be queued.
+ */
+kvq8_status kvq8_quantize_append_host(const float *k_new_host, const float *v_new_host,
+                                      float *k_new, float *v_new,
+                                      int batch, int n_new, int nkv, int hd,
+                                      const int32_t *start_pos,
+                                      const int32_t *block_table, int max_blocks,
+                                      int block_size, int num_blocks,
+                                      int8_t *k_pool, int8_t *v_pool,
+                                      float *k_scale, float *v_scale,
+                                      uint32_t *dev_status, void *stream);
+
 /* ------------------------------------------------------- query quantize --- */
 
 /*
@@ -226,6 +247,31 @@ kvq8_status kvq8_decode_step(const float *q, const float *k_new, const float *v_
                              const int32_t *ctx_lens, float sm_scale, float *out,
                              void *workspace, size_t workspace_bytes,
                              uint32_t *dev_status, void *stream);
+
+/*
+ * kvq8_decode_step_host -- kvq8_decode_step from host memory and back, the
+ * call a serving loop makes each step: q_host (fp32 [batch][nqh][hd]),
+ * k_new_host and v_new_host (fp32 [batch][nkv][hd]) are copied into the
+ * caller's device buffers q, k_new and v_new, the step runs, and its result is
+ * copied from the device buffer out into out_host ([batch][nqh][hd]); one
+ * cudaMemcpyAsync per copy, all on `stream`.  The caller synchronises the
+ * stream before reading out_host; the input host buffers must not change until
+ * then.  Page-locked host memory lets the copies run at full speed.  Returns as
+ * kvq8_decode_step (all arguments are checked before anything is queued);
+ * KVQ8_ERR_INVALID_ARG also for a null host pointer when batch > 0;
+ * KVQ8_ERR_CUDA when a copy cannot be queued.
+ */
+kvq8_status kvq8_decode_step_host(const float *q_host, const float *k_new_host,
+                                  const float *v_new_host, float *out_host,
+                                  float *q, float *k_new, float *v_new,
+                                  int batch, int nqh, int nkv, int hd,
+                                  int8_t *k_pool, int8_t *v_pool,
+                                  float *k_scale, float *v_scale,
+                                  int num_blocks, const int32_t *block_table,
+                                  int max_blocks, int block_size,
+                                  const int32_t *ctx_lens, float sm_scale,
+                                  float *out, void *workspace, size_t workspace_bytes,
+                                  uint32_t *dev_status, void *stream);
 
 /* -------------------------------------------- 4-bit cache (NEXT row) --- */
 

@@ -113,11 +113,14 @@ size_t kvq8_cache_bytes_per_token(int nkv, int hd) {
     return (size_t)nkv * (2 * (size_t)hd + 2 * sizeof(float));
 }
 
-kvq8_status kvq8_quantize_append(const float *k_new, const float *v_new, int batch, int n_new,
-                                 int nkv, int hd, const int32_t *start_pos,
-                                 const int32_t *block_table, int max_blocks, int block_size,
-                                 int num_blocks, int8_t *k_pool, int8_t *v_pool, float *k_scale,
-                                 float *v_scale, uint32_t *dev_status, void *stream) {
+// Checks the arguments of kvq8_quantize_append and fills p; *noop when there
+// is nothing to append.
+static kvq8_status prepare_append(const float *k_new, const float *v_new, int batch, int n_new, int nkv,
+                                  int hd, const int32_t *start_pos, const int32_t *block_table,
+                                  int max_blocks, int block_size, int num_blocks, int8_t *k_pool,
+                                  int8_t *v_pool, float *k_scale, float *v_scale, uint32_t *dev_status,
+                                  AppendParams *p, bool *noop) {
+    *noop = true;
     kvq8_status st = check_shape(hd, block_size);
     if (st != KVQ8_OK) return st;
     if (batch < 0 || n_new < 0 || nkv <= 0 || num_blocks <= 0 || max_blocks <= 0)
@@ -132,23 +135,64 @@ kvq8_status kvq8_quantize_append(const float *k_new, const float *v_new, int bat
         !aligned(v_pool, 16) || !aligned(k_scale, 16) || !aligned(v_scale, 16) ||
         !aligned(start_pos, 4) || !aligned(block_table, 4))
         return KVQ8_ERR_INVALID_ARG;
+    p->k_new = k_new;
+    p->v_new = v_new;
+    p->batch = batch;
+    p->n_new = n_new;
+    p->nkv = nkv;
+    p->start_pos = start_pos;
+    p->block_table = block_table;
+    p->max_blocks = max_blocks;
+    p->num_blocks = num_blocks;
+    p->k_pool = k_pool;
+    p->v_pool = v_pool;
+    p->k_scale = k_scale;
+    p->v_scale = v_scale;
+    p->dev_status = dev_status;
+    p->ctx_lens = nullptr;
+    *noop = false;
+    return KVQ8_OK;
+}
+
+// One asynchronous copy (a no-op for 0 bytes).
+static bool copy_async(void *dst, const void *src, size_t bytes, cudaMemcpyKind kind, cudaStream_t s) {
+    return bytes == 0 || cudaMemcpyAsync(dst, src, bytes, kind, s) == cudaSuccess;
+}
+
+kvq8_status kvq8_quantize_append(const float *k_new, const float *v_new, int batch, int n_new,
+                                 int nkv, int hd, const int32_t *start_pos,
+                                 const int32_t *block_table, int max_blocks, int block_size,
+                                 int num_blocks, int8_t *k_pool, int8_t *v_pool, float *k_scale,
+                                 float *v_scale, uint32_t *dev_status, void *stream) {
     AppendParams p;
-    p.k_new = k_new;
-    p.v_new = v_new;
-    p.batch = batch;
-    p.n_new = n_new;
-    p.nkv = nkv;
-    p.start_pos = start_pos;
-    p.block_table = block_table;
-    p.max_blocks = max_blocks;
-    p.num_blocks = num_blocks;
-    p.k_pool = k_pool;
-    p.v_pool = v_pool;
-    p.k_scale = k_scale;
-    p.v_scale = v_scale;
-    p.dev_status = dev_status;
-    p.ctx_lens = nullptr;
+    bool noop;
+    const kvq8_status st = prepare_append(k_new, v_new, batch, n_new, nkv, hd, start_pos, block_table,
+                                          max_blocks, block_size, num_blocks, k_pool, v_pool, k_scale,
+                                          v_scale, dev_status, &p, &noop);
+    if (st != KVQ8_OK || noop) return st;
     if (launch_quantize_append(p, (cudaStream_t)stream) != cudaSuccess) return KVQ8_ERR_CUDA;
+    return KVQ8_OK;
+}
+
+kvq8_status kvq8_quantize_append_host(const float *k_new_host, const float *v_new_host,
+                                      float *k_new, float *v_new, int batch, int n_new, int nkv,
+                                      int hd, const int32_t *start_pos, const int32_t *block_table,
+                                      int max_blocks, int block_size, int num_blocks, int8_t *k_pool,
+                                      int8_t *v_pool, float *k_scale, float *v_scale,
+                                      uint32_t *dev_status, void *stream) {
+    AppendParams p;
+    bool noop;
+    const kvq8_status st = prepare_append(k_new, v_new, batch, n_new, nkv, hd, start_pos, block_table,
+                                          max_blocks, block_size, num_blocks, k_pool, v_pool, k_scale,
+                                          v_scale, dev_status, &p, &noop);
+    if (st != KVQ8_OK || noop) return st;
+    if (!k_new_host || !v_new_host) return KVQ8_ERR_INVALID_ARG;
+    const size_t bytes = (size_t)batch * n_new * nkv * hd * sizeof(float);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (!copy_async(k_new, k_new_host, bytes, cudaMemcpyHostToDevice, s) ||
+        !copy_async(v_new, v_new_host, bytes, cudaMemcpyHostToDevice, s))
+        return KVQ8_ERR_CUDA;
+    if (launch_quantize_append(p, s) != cudaSuccess) return KVQ8_ERR_CUDA;
     return KVQ8_OK;
 }
 
@@ -241,44 +285,94 @@ kvq8_status kvq8_decode_attn(const float *q, int batch, int nqh, int nkv, int hd
     return KVQ8_OK;
 }
 
+// Checks the arguments of kvq8_decode_step and fills the parameters of its
+// three launches.
+static kvq8_status prepare_decode_step(const float *q, const float *k_new, const float *v_new, int batch,
+                                       int nqh, int nkv, int hd, int8_t *k_pool, int8_t *v_pool,
+                                       float *k_scale, float *v_scale, int num_blocks,
+                                       const int32_t *block_table, int max_blocks, int block_size,
+                                       const int32_t *ctx_lens, float sm_scale, float *out,
+                                       void *workspace, size_t workspace_bytes, uint32_t *dev_status,
+                                       DecodeParams *p, DecodePlan *plan, AppendParams *a) {
+    kvq8_status st = check_decode_args(q, batch, nqh, nkv, hd, k_pool, v_pool, k_scale, v_scale,
+                                       num_blocks, block_table, max_blocks, block_size, ctx_lens);
+    if (st != KVQ8_OK || batch == 0) return st;
+    if (!out || !aligned(out, 16) || !isfinite(sm_scale)) return KVQ8_ERR_INVALID_ARG;
+    if (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)) return KVQ8_ERR_INVALID_ARG;
+    st = fill_decode_params(q, batch, nqh, nkv, k_pool, v_pool, k_scale, v_scale, num_blocks,
+                            block_table, max_blocks, ctx_lens, sm_scale, workspace,
+                            workspace_bytes, dev_status, p, plan);
+    if (st != KVQ8_OK) return st;
+    p->out = out;
+    a->k_new = k_new;
+    a->v_new = v_new;
+    a->batch = batch;
+    a->n_new = 1;
+    a->nkv = nkv;
+    a->start_pos = nullptr;   // the new token goes to ctx_lens[b] - 1
+    a->ctx_lens = ctx_lens;
+    a->block_table = block_table;
+    a->max_blocks = max_blocks;
+    a->num_blocks = num_blocks;
+    a->k_pool = k_pool;
+    a->v_pool = v_pool;
+    a->k_scale = k_scale;
+    a->v_scale = v_scale;
+    a->dev_status = dev_status;
+    return KVQ8_OK;
+}
+
+static kvq8_status launch_decode_step(const DecodeParams &p, const DecodePlan &plan, const AppendParams &a,
+                                      cudaStream_t s) {
+    if (launch_quantize_append(a, s) != cudaSuccess) return KVQ8_ERR_CUDA;
+    if (launch_decode_split(p, plan.group, s) != cudaSuccess) return KVQ8_ERR_CUDA;
+    if (launch_decode_combine(p, plan.group, s) != cudaSuccess) return KVQ8_ERR_CUDA;
+    return KVQ8_OK;
+}
+
 kvq8_status kvq8_decode_step(const float *q, const float *k_new, const float *v_new, int batch,
                              int nqh, int nkv, int hd, int8_t *k_pool, int8_t *v_pool,
                              float *k_scale, float *v_scale, int num_blocks,
                              const int32_t *block_table, int max_blocks, int block_size,
                              const int32_t *ctx_lens, float sm_scale, float *out, void *workspace,
                              size_t workspace_bytes, uint32_t *dev_status, void *stream) {
-    kvq8_status st = check_decode_args(q, batch, nqh, nkv, hd, k_pool, v_pool, k_scale, v_scale,
-                                       num_blocks, block_table, max_blocks, block_size, ctx_lens);
-    if (st != KVQ8_OK || batch == 0) return st;
-    if (!out || !aligned(out, 16) || !isfinite(sm_scale)) return KVQ8_ERR_INVALID_ARG;
-    if (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)) return KVQ8_ERR_INVALID_ARG;
     DecodeParams p;
     DecodePlan plan;
-    st = fill_decode_params(q, batch, nqh, nkv, k_pool, v_pool, k_scale, v_scale, num_blocks,
-                            block_table, max_blocks, ctx_lens, sm_scale, workspace,
-                            workspace_bytes, dev_status, &p, &plan);
-    if (st != KVQ8_OK) return st;
-    p.out = out;
     AppendParams a;
-    a.k_new = k_new;
-    a.v_new = v_new;
-    a.batch = batch;
-    a.n_new = 1;
-    a.nkv = nkv;
-    a.start_pos = nullptr;   // the new token goes to ctx_lens[b] - 1
-    a.ctx_lens = ctx_lens;
-    a.block_table = block_table;
-    a.max_blocks = max_blocks;
-    a.num_blocks = num_blocks;
-    a.k_pool = k_pool;
-    a.v_pool = v_pool;
-    a.k_scale = k_scale;
-    a.v_scale = v_scale;
-    a.dev_status = dev_status;
+    const kvq8_status st = prepare_decode_step(q, k_new, v_new, batch, nqh, nkv, hd, k_pool, v_pool, k_scale,
+                                               v_scale, num_blocks, block_table, max_blocks, block_size,
+                                               ctx_lens, sm_scale, out, workspace, workspace_bytes,
+                                               dev_status, &p, &plan, &a);
+    if (st != KVQ8_OK || batch == 0) return st;
+    return launch_decode_step(p, plan, a, (cudaStream_t)stream);
+}
+
+kvq8_status kvq8_decode_step_host(const float *q_host, const float *k_new_host, const float *v_new_host,
+                                  float *out_host, float *q, float *k_new, float *v_new, int batch,
+                                  int nqh, int nkv, int hd, int8_t *k_pool, int8_t *v_pool,
+                                  float *k_scale, float *v_scale, int num_blocks,
+                                  const int32_t *block_table, int max_blocks, int block_size,
+                                  const int32_t *ctx_lens, float sm_scale, float *out, void *workspace,
+                                  size_t workspace_bytes, uint32_t *dev_status, void *stream) {
+    DecodeParams p;
+    DecodePlan plan;
+    AppendParams a;
+    kvq8_status st = prepare_decode_step(q, k_new, v_new, batch, nqh, nkv, hd, k_pool, v_pool, k_scale,
+                                         v_scale, num_blocks, block_table, max_blocks, block_size,
+                                         ctx_lens, sm_scale, out, workspace, workspace_bytes, dev_status,
+                                         &p, &plan, &a);
+    if (st != KVQ8_OK || batch == 0) return st;
+    if (!q_host || !k_new_host || !v_new_host || !out_host) return KVQ8_ERR_INVALID_ARG;
+    const size_t qbytes = (size_t)batch * nqh * hd * sizeof(float);
+    const size_t kvbytes = (size_t)batch * nkv * hd * sizeof(float);
     cudaStream_t s = (cudaStream_t)stream;
-    if (launch_quantize_append(a, s) != cudaSuccess) return KVQ8_ERR_CUDA;
-    if (launch_decode_split(p, plan.group, s) != cudaSuccess) return KVQ8_ERR_CUDA;
-    if (launch_decode_combine(p, plan.group, s) != cudaSuccess) return KVQ8_ERR_CUDA;
+    if (!copy_async(q, q_host, qbytes, cudaMemcpyHostToDevice, s) ||
+        !copy_async(k_new, k_new_host, kvbytes, cudaMemcpyHostToDevice, s) ||
+        !copy_async(v_new, v_new_host, kvbytes, cudaMemcpyHostToDevice, s))
+        return KVQ8_ERR_CUDA;
+    st = launch_decode_step(p, plan, a, s);
+    if (st != KVQ8_OK) return st;
+    if (!copy_async(out_host, out, qbytes, cudaMemcpyDeviceToHost, s)) return KVQ8_ERR_CUDA;
     return KVQ8_OK;
 }
 

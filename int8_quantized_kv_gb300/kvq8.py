@@ -37,6 +37,8 @@ SIGNATURES = {
     "kvq8_cache_bytes_per_token": (_SZ, [_I, _I]),
     "kvq8_quantize_append": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _I, _I, _I,
                                   _P, _P, _P, _P, _P, _P]),
+    "kvq8_quantize_append_host": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _I, _I,
+                                       _P, _P, _P, _P, _P, _P]),
     "kvq8_quantize_q": (_I, [_P, _I64, _I, _P, _P, _P]),
     "kvq8_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "kvq8_decode_attn": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _I,
@@ -46,6 +48,8 @@ SIGNATURES = {
     "kvq8_decode_combine": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
     "kvq8_decode_step": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _I,
                               _P, _F, _P, _P, _SZ, _P, _P]),
+    "kvq8_decode_step_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I,
+                                   _P, _I, _I, _P, _F, _P, _P, _SZ, _P, _P]),
     "kvq4_code_pool_bytes": (_SZ, [_I, _I, _I, _I]),
     "kvq4_param_pool_bytes": (_SZ, [_I, _I, _I]),
     "kvq4_cache_bytes_per_token": (_SZ, [_I, _I]),
@@ -125,6 +129,21 @@ def _stream(stream, device=None) -> Optional[int]:
     return stream.cuda_stream
 
 
+def _need_host(*tensors):
+    for t in tensors:
+        if t.is_cuda:
+            raise ValueError("expected a host tensor; got one on " + str(t.device))
+        if not t.is_contiguous():
+            raise ValueError("kvq8 takes contiguous tensors")
+        if t.dtype != _torch().float32:
+            raise ValueError("host buffers are fp32")
+
+
+def _torch():
+    import torch
+    return torch
+
+
 def _need_cuda(*tensors):
     for t in tensors:
         if t is None or isinstance(t, int):
@@ -202,6 +221,24 @@ def quantize_append(k_new, v_new, start_pos, block_table, cache: KVCache,
     _check("kvq8_quantize_append", st)
 
 
+def quantize_append_host(k_host, v_host, k_new, v_new, start_pos, block_table, cache: KVCache,
+                         dev_status=None, stream=None):
+    """quantize_append with the new rows in host memory (page-locked for full
+    speed): k_host, v_host are copied into the device buffers k_new, v_new
+    (fp32 [batch][n_new][nkv][128]) on the stream, then appended."""
+    _need_host(k_host, v_host)
+    _need_cuda(k_new, v_new, start_pos, block_table, *cache, dev_status)
+    if k_host.shape != k_new.shape or v_host.shape != v_new.shape or k_new.shape != v_new.shape:
+        raise ValueError("host and device row buffers differ in shape")
+    batch, n_new, nkv, hd = k_new.shape
+    st = load().kvq8_quantize_append_host(
+        _ptr(k_host), _ptr(v_host), _ptr(k_new), _ptr(v_new), batch, n_new, nkv, hd, _ptr(start_pos),
+        _ptr(block_table), block_table.shape[1], BLOCK_SIZE, cache.num_blocks,
+        _ptr(cache.k_pool), _ptr(cache.v_pool), _ptr(cache.k_scale), _ptr(cache.v_scale),
+        _ptr(dev_status), _stream(stream))
+    _check("kvq8_quantize_append_host", st)
+
+
 def quantize_q(q, q_codes, q_scales, stream=None):
     """q fp32 [..., 128] -> q_codes int8 [..., 128], q_scales fp32 [..., 4]."""
     _need_cuda(q, q_codes, q_scales)
@@ -245,6 +282,29 @@ def decode_step(q, k_new, v_new, cache: KVCache, block_table, ctx_lens, out, wor
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status),
         _stream(stream))
     _check("kvq8_decode_step", st)
+
+
+def decode_step_host(q_host, k_host, v_host, out_host, q, k_new, v_new, cache: KVCache, block_table,
+                     ctx_lens, out, workspace, sm_scale: Optional[float] = None, dev_status=None,
+                     stream=None):
+    """decode_step from host memory and back: q_host, k_host, v_host are copied
+    into the device buffers q, k_new, v_new, the step runs, and out is copied
+    into out_host, all queued on the stream; synchronise it before reading
+    out_host.  Host buffers page-locked for full speed."""
+    _need_host(q_host, k_host, v_host, out_host)
+    _need_cuda(q, k_new, v_new, block_table, ctx_lens, out, workspace, *cache, dev_status)
+    if (q_host.shape != q.shape or out_host.shape != out.shape or q.shape != out.shape or
+            k_host.shape != k_new.shape or v_host.shape != v_new.shape):
+        raise ValueError("host and device buffers differ in shape")
+    batch, nqh, nkv, hd, max_blocks = _decode_common(q, cache, block_table, ctx_lens)
+    sm = 1.0 / math.sqrt(hd) if sm_scale is None else sm_scale
+    st = load().kvq8_decode_step_host(
+        _ptr(q_host), _ptr(k_host), _ptr(v_host), _ptr(out_host), _ptr(q), _ptr(k_new), _ptr(v_new),
+        batch, nqh, nkv, hd, _ptr(cache.k_pool), _ptr(cache.v_pool), _ptr(cache.k_scale),
+        _ptr(cache.v_scale), cache.num_blocks, _ptr(block_table), max_blocks, BLOCK_SIZE,
+        _ptr(ctx_lens), sm, _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(dev_status), _stream(stream))
+    _check("kvq8_decode_step_host", st)
 
 
 def decode_split(q, cache: KVCache, block_table, ctx_lens, workspace,

@@ -35,7 +35,8 @@ def test_header_declares_expected_entry_points():
               "kvq8_decode_split", "kvq8_decode_combine", "kvq8_decode_workspace_bytes",
               "kvq8_decode_step", "kvq8_decode_attn_noalloc", "kvq4_quantize_append",
               "kvq4_decode_attn", "kvf32_append", "kvf32_decode_attn", "kvmix_requantize",
-              "kvmix_decode_attn", "kvmix_decode_workspace_bytes"):
+              "kvmix_decode_attn", "kvmix_decode_workspace_bytes", "kvq8_decode_step_host",
+              "kvq8_quantize_append_host"):
         assert n in names
 
 
@@ -135,6 +136,40 @@ def test_decode_validation(lib):
         == kvq8.ERR_WORKSPACE
     assert lib.kvq8_decode_combine(1, 8, 8, 128, 4, 256, None, FAKE, need, FAKE, None) \
         == kvq8.ERR_INVALID_ARG
+
+
+def test_host_buffer_entry_validation(lib):
+    """The host-buffer entries check every argument before queueing a copy."""
+    def app(**kw):
+        a = dict(kh=FAKE, vh=FAKE, k=FAKE, v=FAKE, batch=1, n_new=2, nkv=1, hd=128, start=FAKE,
+                 table=FAKE, max_blocks=1, bs=256, num_blocks=1, kp=FAKE, vp=FAKE, ks=FAKE, vs=FAKE,
+                 status=None, stream=None)
+        a.update(kw)
+        return lib.kvq8_quantize_append_host(*a.values())
+    assert app(kh=None) == kvq8.ERR_INVALID_ARG
+    assert app(vh=None) == kvq8.ERR_INVALID_ARG
+    assert app(k=None) == kvq8.ERR_INVALID_ARG                      # device staging buffer
+    assert app(v=FAKE + 4) == kvq8.ERR_INVALID_ARG
+    assert app(hd=64) == kvq8.ERR_UNSUPPORTED
+    assert app(kh=None, batch=0) == kvq8.OK                         # nothing to append
+    assert app(kh=None, n_new=0) == kvq8.OK
+
+    need = kvq8.decode_workspace_bytes(1, 8, 8, 4)
+
+    def step(**kw):
+        a = dict(qh=FAKE, kh=FAKE, vh=FAKE, oh=FAKE, q=FAKE, k=FAKE, v=FAKE, batch=1, nqh=8, nkv=8,
+                 hd=128, kp=FAKE, vp=FAKE, ks=FAKE, vs=FAKE, num_blocks=4, table=FAKE, max_blocks=4,
+                 bs=256, lens=FAKE, sm=0.088, out=FAKE, ws=FAKE, ws_bytes=need, status=None, stream=None)
+        a.update(kw)
+        return lib.kvq8_decode_step_host(*a.values())
+    for host in ("qh", "kh", "vh", "oh"):
+        assert step(**{host: None}) == kvq8.ERR_INVALID_ARG
+    assert step(q=None) == kvq8.ERR_INVALID_ARG
+    assert step(k=FAKE + 8) == kvq8.ERR_INVALID_ARG
+    assert step(out=None) == kvq8.ERR_INVALID_ARG
+    assert step(nqh=24) == kvq8.ERR_UNSUPPORTED
+    assert step(ws_bytes=need - 1) == kvq8.ERR_WORKSPACE
+    assert step(qh=None, batch=0) == kvq8.OK
 
 
 def test_quantize_q_validation(lib):

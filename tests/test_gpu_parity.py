@@ -455,6 +455,58 @@ def test_decode_step_equals_append_then_decode(gpu_lib):
                 assert np.array_equal(x, y)
 
 
+def test_decode_step_host_buffers_equal_device_call(gpu_lib):
+    """kvq8_decode_step_host (host q and new rows in, host result out) gives the
+    device call's results bit for bit, pools included, and the oracle's."""
+    cfg = wl.scaled(wl.QWEN3_2B_28L_8K, batch=3, ctx=1300)
+    a = StepCase(cfg)
+    dev_out = a.step()
+    b = StepCase(cfg)
+    q_h = torch.from_numpy(wl.queries(cfg)).pin_memory()
+    k_h = torch.from_numpy(b.k_new).pin_memory()
+    v_h = torch.from_numpy(b.v_new).pin_memory()
+    out_h = torch.full(tuple(q_h.shape), float("nan")).pin_memory()
+    q_d, k_d, v_d = torch.zeros_like(b.q_d), torch.zeros_like(b.k_new_d), torch.zeros_like(b.v_new_d)
+    out_d = torch.empty_like(b.q_d)
+    ws = kvq8.alloc_workspace(cfg.batch, cfg.nqh, cfg.nkv, b.max_blocks)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()          # the cache was filled on the default stream
+    kvq8.decode_step_host(q_h, k_h, v_h, out_h, q_d, k_d, v_d, b.cache, b.table_d, b.lens_d, out_d, ws,
+                          sm_scale=SM_SCALE, dev_status=b.status, stream=stream)
+    stream.synchronize()
+    assert b.status.item() == 0
+    assert np.array_equal(out_h.numpy(), dev_out)
+    pa, pb = a.host_pools(), b.host_pools()
+    for bb in range(cfg.batch):
+        for h in range(cfg.nkv):
+            for x, y in zip(a.gather_unit(pa, bb, h), b.gather_unit(pb, bb, h)):
+                assert np.array_equal(x, y)
+    _check_step(b, out_h.numpy())
+
+
+def test_quantize_append_host_buffers_equal_device_call(gpu_lib):
+    nkv, n_new, batch = 2, 300, 2
+    rng = np.random.default_rng(77)
+    k = rng.standard_normal((batch, n_new, nkv, HD)).astype(np.float32)
+    v = (rng.standard_normal((batch, n_new, nkv, HD)) * 2).astype(np.float32)
+    table = np.arange(2 * batch, dtype=np.int32).reshape(batch, 2)
+    start = torch.tensor([5, 100], dtype=torch.int32, device="cuda")
+    td = torch.from_numpy(table).cuda()
+    c1, c2 = kvq8.alloc_cache(2 * batch, nkv), kvq8.alloc_cache(2 * batch, nkv)
+    for c in (c1, c2):
+        for t in c:
+            t.zero_()
+    kvq8.quantize_append(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(), start, td, c1)
+    k_stage, v_stage = torch.empty(k.shape, device="cuda"), torch.empty(v.shape, device="cuda")
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    kvq8.quantize_append_host(torch.from_numpy(k).pin_memory(), torch.from_numpy(v).pin_memory(),
+                              k_stage, v_stage, start, td, c2, stream=stream)
+    stream.synchronize()
+    for x, y in zip(c1, c2):
+        assert torch.equal(x, y)
+
+
 @pytest.mark.slow
 def test_decode_step_full_size_qwen3_2b(gpu_lib):
     cfg = wl.QWEN3_2B_28L_8K
