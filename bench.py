@@ -187,6 +187,25 @@ def recorded_traffic(kernel: str, workload: str):
     return rec.get("per_launch_bytes", {}).get(workload)
 
 
+def cross_check_traffic(line):
+    """Traffic measured by ncu against the algorithmic bytes of the same launch:
+    the ratio, and a flag when they differ by more than 5 %: above, bytes read
+    more than once; below, bytes served from L2 or writes still in L2 (not yet
+    written back) when the kernel ended."""
+    r = line.get("roofline", {})
+    if r.get("traffic") and r.get("algorithmic_bytes_per_launch"):
+        ratio = r["traffic"] / r["algorithmic_bytes_per_launch"]
+        r["traffic_over_algorithmic"] = round(ratio, 4)
+        if ratio > 1.05:
+            r["traffic_check"] = "more than 5 % above the algorithmic bytes: re-reads"
+        elif ratio < 0.95:
+            r["traffic_check"] = ("more than 5 % below the algorithmic bytes: served from L2, or writes "
+                                  "still in L2 at the kernel's end")
+        else:
+            r["traffic_check"] = "within 5 % of the algorithmic bytes"
+    return line
+
+
 # ------------------------------------------------------------- workloads ---
 def step_bytes(cfg, lens):
     """Algorithmic bytes of one step: the decode pass plus the append of one
@@ -513,7 +532,7 @@ def run_kvq8(args, rank, world, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, lens, args.cpu_seconds)
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        print(json.dumps(cross_check_traffic(line)), flush=True)
 
 
 def per_layer_graph(args, cfg, sbytes, cache, q_d, nk1, nv1, table_d, lens_d, out_folded, status, sm,
@@ -739,7 +758,7 @@ def run_kvq4(args, rank, world, local):
         "clocks": clocks,
     }
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        print(json.dumps(cross_check_traffic(line)), flush=True)
 
 
 # ------------------------------------------------ mixed precision by age ---
@@ -872,7 +891,7 @@ def run_mixed(args, rank, world, local):
         "clocks": clocks,
     }
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        print(json.dumps(cross_check_traffic(line)), flush=True)
 
 
 # ------------------------------------------------------------- bulk append ---
@@ -959,7 +978,7 @@ def run_append(args, rank, world, local):
         "clocks": clocks,
     }
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        print(json.dumps(cross_check_traffic(line)), flush=True)
 
 
 # ----------------------------------------------------------- reference arm ---
