@@ -416,8 +416,8 @@ decode_split_kernel(DecodeParams p) {
                     }
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
-                        const float wa = va ? exp2f(sa[g] - M[g]) : 0.0f;
-                        const float wb = vb ? exp2f(sb[g] - M[g]) : 0.0f;
+                        const float wa = va ? ex2_approx(sa[g] - M[g]) : 0.0f;
+                        const float wb = vb ? ex2_approx(sb[g] - M[g]) : 0.0f;
                         Sl[g] = fmaf(Sl[g], alpha[g], wa + wb);
                         const float pa = wa * vsa * inv, pb = wb * vsb * inv;
                         const __half ha = __float2half_rn(pa), hb = __float2half_rn(pb);

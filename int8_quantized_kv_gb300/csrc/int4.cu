@@ -206,15 +206,6 @@ __device__ __forceinline__ int qk_dim(int ks, int kk) {
     return 2 * byte + lo;
 }
 
-// 2^x by the hardware's approximate base-2 exponential (relative error about
-// 2^-22, far inside the output tolerance; results below 2^-126, which weigh
-// nothing next to the running maximum's 1, flush to 0; -inf gives 0).
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 // Per-warp staging of one 32-token chunk: K and V code rows and the K and V
 // parameter rows; two buffers per warp, filled by 16-byte cp.async.  The
 // fragment reads are conflict-free: K rows keep 64 B with the two 32-byte

@@ -97,6 +97,15 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// 2^x by the hardware's approximate base-2 exponential (relative error about
+// 2^-22, far inside the decode's output tolerance; results below 2^-126, which
+// weigh nothing next to a running maximum's 1, flush to 0; -inf gives 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // D (16x8 fp32) += A (16x16 fp16, row) * B (16x8 fp16, col).
 __device__ __forceinline__ void mma_f16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                               uint32_t a3, uint32_t b0, uint32_t b1) {
