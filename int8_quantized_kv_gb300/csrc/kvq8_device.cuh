@@ -41,12 +41,6 @@ __device__ __forceinline__ int kv_code(float v, float scale) {
     return max(-127, min(127, c));
 }
 
-// Packs the codes of four consecutive values into one little-endian word.
-__device__ __forceinline__ uint32_t pack4(int c0, int c1, int c2, int c3) {
-    return (uint32_t)(c0 & 0xff) | ((uint32_t)(c1 & 0xff) << 8) |
-           ((uint32_t)(c2 & 0xff) << 16) | ((uint32_t)(c3 & 0xff) << 24);
-}
-
 // 32-block query rule ([Day 9-2] §2 segment 1) for one row of 128 values,
 // executed by one full warp: lane l handles element 32*k + l of block k.
 // qm = max |x| over the block (1 when below 1e-6); block scale = qm * (1/127);
