@@ -301,6 +301,13 @@ decode_split_kernel(DecodeParams p) {
         float *red_m = red_acc + G * kHD;
         float *red_s = red_m + G;
         const int n = lane >> 2, t4 = lane & 3;  // MMA fragment coordinates
+        // P.V for G <= 4 packs P's high fp16 parts into columns 0..G-1 and its
+        // low parts into G..2G-1 of one MMA (half the MMAs); the columns' sums
+        // are added at the segment's end.  Accumulator columns 2*t4, 2*t4 + 1
+        // then belong to heads col_head0, col_head1 (for their rescaling).
+        constexpr bool kPackPV = G <= 4;
+        const int col_head0 = kPackPV ? (2 * t4) % G : 2 * t4;
+        const int col_head1 = kPackPV ? (2 * t4 + 1) % G : 2 * t4 + 1;
         bool aborted = false;
         long long remaining = hi - lo;
         int kbase = 0;
@@ -431,8 +438,8 @@ decode_split_kernel(DecodeParams p) {
                         float f0 = 0.0f, f1 = 0.0f;
 #pragma unroll
                         for (int g = 0; g < G; ++g) {
-                            if (g == 2 * t4) f0 = alpha[g] * two;
-                            if (g == 2 * t4 + 1) f1 = alpha[g] * two;
+                            if (g == col_head0) f0 = alpha[g] * two;
+                            if (g == col_head1) f1 = alpha[g] * two;
                         }
 #pragma unroll
                         for (int mt = 0; mt < 8; ++mt) {
@@ -444,19 +451,30 @@ decode_split_kernel(DecodeParams p) {
                     __syncwarp();
 
                     // ---- segment 2c: acc += V . P on the tensor cores ----
+                    // B columns: kPackPV, head n's high part (n < G) or head n - G's
+                    // low part (G <= n < 2G); else the high part of head n in
+                    // bh and its low part in bl (two MMAs)
                     uint32_t bh[8], bl[8];
-                    if (n < G) {
-                        const int4 h0 = lds128(p_hi + n * kPRowHalves + t4 * 16);
-                        const int4 h1 = lds128(p_hi + n * kPRowHalves + t4 * 16 + 8);
-                        const int4 l0 = lds128(p_lo + n * kPRowHalves + t4 * 16);
-                        const int4 l1 = lds128(p_lo + n * kPRowHalves + t4 * 16 + 8);
+                    const __half *rh = kPackPV ? (n < G ? p_hi + n * kPRowHalves
+                                                        : (n < 2 * G ? p_lo + (n - G) * kPRowHalves : nullptr))
+                                               : (n < G ? p_hi + n * kPRowHalves : nullptr);
+                    if (rh) {
+                        const int4 h0 = lds128(rh + t4 * 16);
+                        const int4 h1 = lds128(rh + t4 * 16 + 8);
                         bh[0] = h0.x; bh[1] = h0.y; bh[2] = h0.z; bh[3] = h0.w;
                         bh[4] = h1.x; bh[5] = h1.y; bh[6] = h1.z; bh[7] = h1.w;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) bh[i] = 0u;
+                    }
+                    if (!kPackPV && n < G) {
+                        const int4 l0 = lds128(p_lo + n * kPRowHalves + t4 * 16);
+                        const int4 l1 = lds128(p_lo + n * kPRowHalves + t4 * 16 + 8);
                         bl[0] = l0.x; bl[1] = l0.y; bl[2] = l0.z; bl[3] = l0.w;
                         bl[4] = l1.x; bl[5] = l1.y; bl[6] = l1.z; bl[7] = l1.w;
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) { bh[i] = 0u; bl[i] = 0u; }
+                        for (int i = 0; i < 8; ++i) bl[i] = 0u;
                     }
 #pragma unroll
                     for (int mt = 0; mt < 8; ++mt) {
@@ -471,7 +489,7 @@ decode_split_kernel(DecodeParams p) {
                             codes_to_half2(w0[s], a0, a2);
                             codes_to_half2(w1[s], a1, a3);
                             mma_f16_16816(acc[mt], a0, a1, a2, a3, bh[2 * s], bh[2 * s + 1]);
-                            mma_f16_16816(acc[mt], a0, a1, a2, a3, bl[2 * s], bl[2 * s + 1]);
+                            if (!kPackPV) mma_f16_16816(acc[mt], a0, a1, a2, a3, bl[2 * s], bl[2 * s + 1]);
                         }
                     }
                 }
@@ -483,6 +501,20 @@ decode_split_kernel(DecodeParams p) {
             }
 
             // ---- merge the 7 warp states of this segment into one record ----
+            if (kPackPV) {
+                // add the low parts' columns into the high parts' (the lanes
+                // that hold columns 2*t4 < G, which the record write below reads)
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    if (G == 1) {
+                        acc[mt][0] += acc[mt][1];
+                        acc[mt][2] += acc[mt][3];
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc[mt][i] += __shfl_xor_sync(0xffffffffu, acc[mt][i], G / 2);
+                    }
+                }
+            }
             const float unit_scale = __int_as_float((127 + max(-126, min(127, e_cur))) << 23);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
