@@ -281,9 +281,14 @@ int4_decode_split_kernel(Int4DecodeParams p) {
     // MMA does both halves; lane (g, t4) then owns token 16*mt + g + 8*(t4/2)
     // and heads 2*(t4%2) + j of the scores, and its accumulator columns hold
     // the high (t4 < 2) or low (t4 >= 2) parts for those heads, added at the
-    // end.  Otherwise (G = 8) the columns are the 8 heads and each product
-    // takes two MMAs.
+    // end.  kPack2 (G <= 2): columns 0-1 high parts, 2-3 low parts, 4-7 zero;
+    // one shuffle joins the halves (lanes t4 = 0, 1 keep rows g, g + 8) and a
+    // second moves the second m-tile's scores to lanes t4 = 2, 3, so that lane
+    // (g, t4) owns token 16*(t4/2) + g + 8*(t4%2) and both heads: no lane
+    // works on padding heads.  Otherwise (G = 8) the columns are the 8 heads
+    // and each product takes two MMAs.
     constexpr bool kPack = G <= 4;
+    constexpr bool kPack2 = G <= 2;
     pdl_wait();
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -341,8 +346,10 @@ int4_decode_split_kernel(Int4DecodeParams p) {
     // otherwise staged in shared memory as high and low parts of head gg.
     uint32_t qb[8][2];
     if constexpr (kPack) {
-        const int hq = g & 3;
-        const bool low = g >= 4;
+        // kPack2: column gg = head gg % 2 (gg < 4; high part for gg < 2), zero
+        // for gg >= 4; kPack: head gg % 4, high part for gg < 4
+        const int hq = kPack2 ? (g < 4 ? (g & 1) : G) : (g & 3);
+        const bool low = kPack2 ? (g & 2) != 0 : g >= 4;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             float x[4] = {0.f, 0.f, 0.f, 0.f};
@@ -405,7 +412,7 @@ int4_decode_split_kernel(Int4DecodeParams p) {
     __syncthreads();
     // this lane's heads (score and accumulator columns): 2*(t4 % 2) + j when
     // packed, 2*t4 + j otherwise
-    const int hbase = kPack ? 2 * (t4 & 1) : 2 * t4;
+    const int hbase = kPack2 ? 0 : (kPack ? 2 * (t4 & 1) : 2 * t4);
     float qq[2][2];
 #pragma unroll
     for (int j = 0; j < 2; ++j)
@@ -416,7 +423,9 @@ int4_decode_split_kernel(Int4DecodeParams p) {
     // scores per lane: kPack 1 token x 2 heads per m-tile, else 2 tokens (rows
     // g, g + 8) x 2 heads
     constexpr int kR = kPack ? 1 : 2;
+    constexpr int kM = kPack2 ? 1 : 2;   // score m-slots per lane
     const int tsel = kPack ? 8 * (t4 >> 1) : 0;   // this lane's token offset when packed
+    const int tok2 = 16 * (t4 >> 1) + g + 8 * (t4 & 1);   // kPack2: this lane's token
     float M[2] = {-INFINITY, -INFINITY}, Sl[2] = {0.0f, 0.0f}, Zl[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
     float acc[8][4];
 #pragma unroll
@@ -440,8 +449,9 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         const bool partial = ntok < kChunk4;   // only the split's last chunk
 
         // ---- scores: S = K Q^T, tokens 16*mt + g + 8*r (rows) ----
-        float sc[2][kR][2];
+        float sc[kM][kR][2];
         float mloc[2] = {-INFINITY, -INFINITY};
+        float dtm[2][2][2];   // kPack2: [m-tile][group][head] sums of this lane's row
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
             // K: tokens 16*mt + g + 8*r, bytes 32*gr + 8*t4 .. +7
@@ -474,7 +484,20 @@ int4_decode_split_kernel(Int4DecodeParams p) {
                     mma_f16_16816(d[gr], a[0], a[1], a[2], a[3], qa.z, qa.w);
                 }
             }
-            if constexpr (kPack) {
+            if constexpr (kPack2) {
+                // lane t4 = 0 holds the high parts of rows g and g + 8, lane 1 the
+                // low parts: each keeps one row (t4 = 0: g) and receives the other
+                // part; lanes t4 = 2, 3 hold the zero columns
+                const bool lo_lane = (t4 & 1) != 0;
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int gr = 0; gr < 2; ++gr) {
+                        const float send = lo_lane ? d[gr][j] : d[gr][2 + j];
+                        const float keep = lo_lane ? d[gr][2 + j] : d[gr][j];
+                        dtm[mt][gr][j] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+                    }
+            } else if constexpr (kPack) {
                 // lane t4 < 2 holds the high parts of rows g and g + 8, lane t4 ^ 2
                 // the low parts: each keeps one row and receives the other part
                 const bool lo_lane = t4 >= 2;
@@ -505,19 +528,37 @@ int4_decode_split_kernel(Int4DecodeParams p) {
                 }
             }
         }
+        if constexpr (kPack2) {
+            // the second m-tile's rows go to lanes t4 = 2, 3
+            const float4 k4 = kps[tok2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float dt[2];
+#pragma unroll
+                for (int gr = 0; gr < 2; ++gr) {
+                    const float m1 = __shfl_xor_sync(0xffffffffu, dtm[1][gr][j], 2);
+                    dt[gr] = t4 < 2 ? dtm[0][gr][j] : m1;
+                }
+                const float x = k4.x * fmaf(dt[0], kNibUnit, -k4.y * qq[j][0]) +
+                                k4.z * fmaf(dt[1], kNibUnit, -k4.w * qq[j][1]);
+                sc[0][0][j] = x * score_scale;
+            }
+        }
         // token of score (mt, r) of this lane
-        auto tok_of = [&](int mt, int r) { return 16 * mt + g + (kPack ? tsel : 8 * r); };
+        auto tok_of = [&](int mt, int r) {
+            return kPack2 ? tok2 : 16 * mt + g + (kPack ? tsel : 8 * r);
+        };
         if (partial) {
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
+            for (int mt = 0; mt < kM; ++mt)
 #pragma unroll
                 for (int r = 0; r < kR; ++r)
                     if (tok_of(mt, r) >= ntok) sc[mt][r][0] = sc[mt][r][1] = -INFINITY;
         }
         // this lane's score tokens' V parameters (zero past the end: stale slots)
-        float4 vp[2][kR];
+        float4 vp[kM][kR];
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+        for (int mt = 0; mt < kM; ++mt)
 #pragma unroll
             for (int r = 0; r < kR; ++r) {
                 vp[mt][r] = vps[tok_of(mt, r)];
@@ -526,10 +567,12 @@ int4_decode_split_kernel(Int4DecodeParams p) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
+            for (int mt = 0; mt < kM; ++mt)
 #pragma unroll
                 for (int r = 0; r < kR; ++r) mloc[j] = fmaxf(mloc[j], sc[mt][r][j]);
-            // lanes sharing this lane's heads: all g, and t4 ^ 2 when packed
+            // lanes sharing this lane's heads: all g, and t4 ^ 2 when packed, all
+            // lanes when kPack2
+            if constexpr (kPack2) mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 1));
             if constexpr (kPack) mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 2));
             mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 4));
             mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 8));
@@ -539,7 +582,7 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         // power-of-two unit of this chunk's P': 2^e > max V scale (see the q8 decode)
         float vsmax = 0.0f;
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+        for (int mt = 0; mt < kM; ++mt)
 #pragma unroll
             for (int r = 0; r < kR; ++r) vsmax = fmaxf(vsmax, fmaxf(vp[mt][r].x, vp[mt][r].z));
         const int e_need = __reduce_max_sync(0xffffffffu, ((__float_as_int(vsmax) >> 23) & 0xff) - 126);
@@ -563,12 +606,14 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         const float two = __int_as_float((127 + max(-126, min(127, e_cur - e_new))) << 23);
         // P'_g = w * vscale_g * 2^-e, high and low fp16 parts, into the freed K
         // area for the transposing loads: kPack [group][32 tokens][high parts of
-        // heads 0-3 | low parts], else [group][part][32 tokens][8 heads]
+        // heads 0-3 | low parts] (kPack2: words 0, 1 = high and low parts of heads
+        // 0-1; words 2, 3 unwritten, their B columns zeroed after the load), else
+        // [group][part][32 tokens][8 heads]
         uint32_t *ptile = reinterpret_cast<uint32_t *>(const_cast<unsigned char *>(st) + kStageKOff);
         __syncwarp();   // every lane is done reading the K rows
         float wsum[2] = {0.f, 0.f}, zs[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+        for (int mt = 0; mt < kM; ++mt)
 #pragma unroll
             for (int r = 0; r < kR; ++r) {
                 const int t = tok_of(mt, r);
@@ -589,7 +634,12 @@ int4_decode_split_kernel(Int4DecodeParams p) {
                     const __half h0 = __float2half_rn(pg[gr][0]), h1 = __float2half_rn(pg[gr][1]);
                     const uint32_t hi = pack_half2(__half2float(h0), __half2float(h1));
                     const uint32_t lo = pack_half2(pg[gr][0] - __half2float(h0), pg[gr][1] - __half2float(h1));
-                    if constexpr (kPack) {
+                    if constexpr (kPack2) {
+                        // lanes t4 = 1, 3 store in the other order: two banks per g
+                        const int w0 = t4 & 1;
+                        ptile[(gr * kChunk4 + t) * 4 + w0] = w0 ? lo : hi;
+                        ptile[(gr * kChunk4 + t) * 4 + (w0 ^ 1)] = w0 ? hi : lo;
+                    } else if constexpr (kPack) {
                         // words 4t + t4 and 4t + (t4 ^ 2): 32 distinct banks per store
                         const bool lo_lane = t4 >= 2;
                         ptile[(gr * kChunk4 + t) * 4 + t4] = lo_lane ? lo : hi;
@@ -630,6 +680,9 @@ int4_decode_split_kernel(Int4DecodeParams p) {
                              : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                              : "r"(addr));
                 bf[gr][hl][0][0] = r0; bf[gr][hl][0][1] = r1; bf[gr][hl][1][0] = r2; bf[gr][hl][1][1] = r3;
+                if (kPack2 && g >= 4) {   // columns 4-7: zero (the tile's words 2, 3 are stale)
+                    bf[gr][hl][0][0] = 0u; bf[gr][hl][0][1] = 0u; bf[gr][hl][1][0] = 0u; bf[gr][hl][1][1] = 0u;
+                }
             }
 
         // ---- P.V: out^T += V^T P'_g ----
@@ -669,22 +722,23 @@ int4_decode_split_kernel(Int4DecodeParams p) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
 #pragma unroll
-        for (int o = kPack ? 2 : 4; o < 32; o <<= 1) {
+        for (int o = kPack2 ? 1 : (kPack ? 2 : 4); o < 32; o <<= 1) {
             Sl[j] += __shfl_xor_sync(0xffffffffu, Sl[j], o);
             Zl[j][0] += __shfl_xor_sync(0xffffffffu, Zl[j][0], o);
             Zl[j][1] += __shfl_xor_sync(0xffffffffu, Zl[j][1], o);
         }
     }
     if constexpr (kPack) {
-        // add the low parts' columns (lane t4 ^ 2) into the high parts'
+        // add the low parts' columns (lane t4 ^ 1 when kPack2, else t4 ^ 2) into
+        // the high parts'
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[mt][i] += __shfl_xor_sync(0xffffffffu, acc[mt][i], 2);
+            for (int i = 0; i < 4; ++i) acc[mt][i] += __shfl_xor_sync(0xffffffffu, acc[mt][i], kPack2 ? 1 : 2);
     }
     const float unit_scale = __int_as_float((127 + max(-126, min(127, e_cur))) << 23);
     __syncthreads();   // every warp is done with its staging buffers
-    const bool writer = !kPack || t4 < 2;
+    const bool writer = kPack2 ? t4 == 0 : (!kPack || t4 < 2);
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
         const int gr = mt >> 2;
