@@ -230,7 +230,9 @@ kvq8_status kvq8_decode_combine(int batch, int nqh, int nkv, int hd,
  * context including it.  Same results as kvq8_quantize_append (n_new = 1,
  * start_pos[b] = ctx_lens[b] - 1) followed by kvq8_decode_attn; the three
  * kernels are launched back to back, each as a programmatic dependent of the
- * previous one so that their launches overlap.
+ * kernel before it in the stream (the first of whatever the caller queued
+ * last), so that their launches overlap; each waits for that kernel's results
+ * before it reads them.
  *
  *   k_new, v_new  fp32 [batch][nkv][hd]: the step's token ([Day 9-3] §2 rule)
  *                 (sequences with ctx_lens[b] == 0 append nothing and yield 0;

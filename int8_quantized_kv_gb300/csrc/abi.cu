@@ -69,6 +69,7 @@ kvq8_status fill_decode_params(const float *q, int batch, int nqh, int nkv,
     p->max_blocks = max_blocks;
     p->ctx_lens = ctx_lens;
     p->sm_scale_log2 = sm_scale * 1.4426950408889634f;
+    p->early_prologue = 0;
     p->ws_meta = (int2 *)(ws + plan->meta_offset);
     p->ws_ml = (float *)(ws + plan->ml_offset);
     p->ws_acc = (float *)(ws + plan->acc_offset);
@@ -304,6 +305,7 @@ static kvq8_status prepare_decode_step(const float *q, const float *k_new, const
                             workspace_bytes, dev_status, p, plan);
     if (st != KVQ8_OK) return st;
     p->out = out;
+    p->early_prologue = 1;   // the split follows this step's own append
     a->k_new = k_new;
     a->v_new = v_new;
     a->batch = batch;

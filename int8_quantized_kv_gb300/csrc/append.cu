@@ -256,7 +256,11 @@ quantize_append_kernel(AppendParams p, int quarters, long long tasks) {
 // K row and V row quantised from one float4 per lane; no staging needed.
 __global__ void __launch_bounds__(kAppendWarps * 32)
 quantize_append_token_kernel(AppendParams p) {
-    pdl_launch_dependents();  // let the next kernel of the step be scheduled now
+    // Launched as a programmatic dependent: wait for the previous kernel in the
+    // stream (which may have produced the new token's K and V), then let the
+    // next kernel of the step be scheduled.
+    pdl_wait();
+    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wid = blockIdx.x * kAppendWarps + warp;
     if (wid >= p.batch * p.nkv) return;
@@ -310,8 +314,17 @@ quantize_q_kernel(const float *__restrict__ q, int64_t n_rows, int8_t *__restric
 cudaError_t launch_quantize_append(const AppendParams &p, cudaStream_t s) {
     if (p.n_new == 1) {
         const int64_t warps = (int64_t)p.batch * p.nkv;
-        quantize_append_token_kernel<<<(unsigned)((warps + kAppendWarps - 1) / kAppendWarps),
-                                       kAppendWarps * 32, 0, s>>>(p);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)((warps + kAppendWarps - 1) / kAppendWarps));
+        cfg.blockDim = dim3(kAppendWarps * 32);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, quantize_append_token_kernel, p);
     } else {
         // quarters touched by n_new consecutive positions: at most n_new/64 + 1
         const int quarters = p.n_new / kQTok + (p.n_new % kQTok ? 2 : 1);

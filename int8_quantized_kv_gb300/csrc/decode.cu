@@ -34,9 +34,12 @@
 //    and written as one record per query head.
 // All waits are bounded: a wait that times out sets KVQ8_DEV_TIMEOUT and the
 // CTA unwinds without leaving copies in flight.  The kernel is launched as a
-// programmatic dependent of the previous kernel in its stream, so its launch,
-// prologue and query quantisation overlap that kernel; the producer waits for
-// that kernel's results before its first copy from the pools.
+// programmatic dependent of the previous kernel in its stream, so that its
+// launch overlaps that kernel.  Inside a decode step (after the step's own
+// append) its prologue and query quantisation overlap the append too and only
+// the producer waits, before its first copy from the pools; after any other
+// kernel every thread waits first.  The combine releases the next kernel of
+// the stream as soon as the split's records are visible to it.
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -146,11 +149,14 @@ decode_split_kernel(DecodeParams p) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
     const int cap = p.max_blocks * kBS;
-    // Launched as a programmatic dependent of the previous kernel in the stream
-    // (the step's append), which writes the pools and scales only.  The
-    // prologue and the query quantisation (ctx_lens, block table, q) run before
-    // that kernel ends; the producer waits for its results before the first
-    // copy from the pools.
+    // Launched as a programmatic dependent of the previous kernel in the stream.
+    // Inside a decode step that kernel is the step's append, which writes only
+    // the pools and scales: the prologue and the query quantisation (ctx_lens,
+    // block table, q) then run before it ends, and only the producer waits for
+    // its results, before the first copy from the pools.  After any other
+    // kernel (whose outputs may be this kernel's inputs) every thread waits
+    // here first.
+    if (!p.early_prologue) pdl_wait();
     Misc *misc = reinterpret_cast<Misc *>(smem + Lay::oMisc);
     int8_t *q_codes = reinterpret_cast<int8_t *>(smem + Lay::oQCodes);
     float *q_scale = reinterpret_cast<float *>(smem + Lay::oQScale);
@@ -162,21 +168,21 @@ decode_split_kernel(DecodeParams p) {
     volatile int *done = reinterpret_cast<volatile int *>(smem + Lay::oDone);
     const uint32_t full0 = smem_addr(smem + Lay::oFull), empty0 = smem_addr(smem + Lay::oEmpty);
 
-    if (tid == 0) {
-        for (int i = 0; i < Lay::kStages; ++i) {
-            mbar_init(full0 + 8 * i, 1);
-            mbar_init(empty0 + 8 * i, 1);
-            done[i] = 0;
-        }
-        fence_mbar_init();
-    }
-
     // ---- prologue: total stage count T and where this CTA's range starts ----
     const int per = (p.batch + kSplitThreads - 1) / kSplitThreads;
     const int b_lo = min(p.batch, tid * per), b_hi = min(p.batch, b_lo + per);
+    // the first context length is loaded before the barriers are initialised,
+    // so that its latency covers them
+    const int L_first = b_lo < b_hi ? p.ctx_lens[b_lo] : 0;
+    if (tid < Lay::kStages) {
+        mbar_init(full0 + 8 * tid, 1);
+        mbar_init(empty0 + 8 * tid, 1);
+        done[tid] = 0;
+        fence_mbar_init();
+    }
     long long mine = 0;
     for (int b = b_lo; b < b_hi; ++b) {
-        const int L = p.ctx_lens[b];
+        const int L = b == b_lo ? L_first : p.ctx_lens[b];
         if (c == 0 && (L < 0 || L > cap)) flag_status(p.dev_status, KVQ8_DEV_BAD_CTX_LEN);
         mine += (long long)p.nkv * span_stages(seq_span<kMixed>(p, b, cap));
     }
@@ -203,7 +209,15 @@ decode_split_kernel(DecodeParams p) {
     // the stages are shared by min(gridDim.x, T) CTAs so that every active CTA
     // owns at least one stage and the CTAs covering a unit are consecutive
     const int C = (int)min((long long)gridDim.x, T);
-    const long long lo = c < C ? (long long)c * T / C : 0, hi = c < C ? (long long)(c + 1) * T / C : 0;
+    // lo = c*T/C and hi = (c+1)*T/C from one 64-bit division: with T = Tq*C + Tr,
+    // k*T/C = k*Tq + (k*Tr)/C exactly, and k*Tr < C*C fits 32 bits
+    long long lo = 0, hi = 0;
+    if (c < C) {
+        const long long Tq = T / C;
+        const int Tr = (int)(T - Tq * C);
+        lo = (long long)c * Tq + (c * Tr) / C;
+        hi = (long long)(c + 1) * Tq + ((c + 1) * Tr) / C;
+    }
     __syncthreads();
     if (mine > 0 && excl <= lo && lo < excl + mine) {
         long long acc = excl;
@@ -223,9 +237,14 @@ decode_split_kernel(DecodeParams p) {
     if (hi > lo) {
         b = misc->b0;
         const int nb = span_stages(seq_span<kMixed>(p, b, cap));
-        const long long rel = lo - misc->base;
-        h = (int)(rel / nb);
-        off = (int)(rel % nb);
+        const long long rel = lo - misc->base;   // < nkv * nb
+        if (rel <= 0x7fffffffLL) {
+            h = (int)rel / nb;
+            off = (int)rel - h * nb;
+        } else {
+            h = (int)(rel / nb);
+            off = (int)(rel % nb);
+        }
     }
 
     if (warp == kConsumerWarps) {
@@ -582,6 +601,10 @@ decode_split_kernel(DecodeParams p) {
 __global__ void __launch_bounds__(kHD)
 decode_combine_kernel(DecodeParams p, int G) {
     pdl_wait();  // the split kernel's records are visible after this
+    // the next kernel may be scheduled now: a kernel of this library that
+    // follows (the next step's append, a split) waits for this grid to
+    // complete before it reads anything
+    pdl_launch_dependents();
     const int qh = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
     const int h = qh / G, g = qh % G;
     const int cap = p.max_blocks * kBS;

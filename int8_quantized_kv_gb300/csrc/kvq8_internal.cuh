@@ -69,6 +69,11 @@ struct DecodeParams {
     int max_blocks;
     const int32_t *ctx_lens;
     float sm_scale_log2;          // sm_scale * log2(e): softmax runs in base 2
+    // 1: the split kernel reads q, ctx_lens and the block table before its
+    // dependency wait (only when the kernel before it in the stream is this
+    // library's own one-token append of the same step, which writes nothing
+    // but the pools and scales); 0: every thread waits first
+    int early_prologue;
     int2 *ws_meta;                // [units]: (first CTA, CTA count)
     float *ws_ml;                 // [records][G][2]  (running max M, sum S)
     float *ws_acc;                // [records][G][hd] (unnormalised V accumulator)

@@ -439,6 +439,46 @@ def test_decode_step_twice_on_one_workspace(gpu_lib):
     _check_step(case, second)
 
 
+def _chain(call, q0, n, sync_between):
+    """n calls, each taking the previous call's output as its query."""
+    outs, x = [], q0
+    for _ in range(n):
+        o = torch.full_like(q0, float("nan"))
+        call(x, o)
+        if sync_between:
+            torch.cuda.synchronize()
+        outs.append(o)
+        x = o
+    torch.cuda.synchronize()
+    return [o.cpu().numpy() for o in outs]
+
+
+def test_output_fed_back_as_query_without_sync(gpu_lib):
+    """The combine lets the next kernel launch early, and the decode and the
+    step launch as programmatic dependents: a call that reads, as its query,
+    the output the call just before it is still writing must see that output
+    complete (the same results as with a full synchronisation in between)."""
+    cfg = wl.scaled(wl.BATCH64_RAGGED, batch=6, ctx_range=(300, 5000))
+    case = StepCase(cfg)
+    ws = kvq8.alloc_workspace(cfg.batch, cfg.nqh, cfg.nkv, case.max_blocks)
+
+    def attn(x, o):
+        kvq8.decode_attn(x, case.cache, case.table_d, case.lens_d, o, ws, dev_status=case.status)
+
+    def step(x, o):
+        kvq8.decode_step(x, case.k_new_d, case.v_new_d, case.cache, case.table_d, case.lens_d, o, ws,
+                         dev_status=case.status)
+
+    step(case.q_d, torch.empty_like(case.q_d))   # the appended token is in place from here on
+    for call in (attn, step):
+        fast = _chain(call, case.q_d, 6, sync_between=False)
+        slow = _chain(call, case.q_d, 6, sync_between=True)
+        for a, b in zip(fast, slow):
+            assert np.isfinite(a).all()
+            assert np.array_equal(a, b)
+    assert case.status_bits() == 0
+
+
 def test_decode_step_equals_append_then_decode(gpu_lib):
     cfg = wl.scaled(wl.BATCH64_RAGGED, batch=5, ctx_range=(512, 3000))
     a = StepCase(cfg)
