@@ -330,6 +330,25 @@ decode_split_kernel(DecodeParams p) {
         bool aborted = false;
         long long remaining = hi - lo;
         int kbase = 0;
+        // This warp's query rows (heads g = warp, warp + 7 of the unit) of the
+        // unit (qb, qh), loaded one segment ahead so that the quantisation at
+        // a segment's start waits for no global load.
+        constexpr int kQRows = (G + kConsumerWarps - 1) / kConsumerWarps;
+        float qx[kQRows][4];
+        int qb = -1, qh = -1;
+        auto load_q_rows = [&](int bb, int hh) {
+#pragma unroll
+            for (int i = 0; i < kQRows; ++i) {
+                const int g = warp + i * kConsumerWarps;
+                if (g < G) {
+                    const float *r = p.q + ((size_t)bb * p.nqh + (size_t)hh * G + g) * kHD;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) qx[i][k] = r[32 * k + lane];
+                }
+            }
+            qb = bb;
+            qh = hh;
+        };
         while (remaining > 0 && b < p.batch) {
             const int2 sp = seq_span<kMixed>(p, b, cap);
             const int L = sp.y;
@@ -339,11 +358,19 @@ decode_split_kernel(DecodeParams p) {
             const int u = b * p.nkv + h;
 
             // segment 1: quantise this unit's G query heads once
+            if (qb != b || qh != h) load_q_rows(b, h);   // not loaded ahead
             named_barrier_sync(1, kConsumerWarps * 32);
-            for (int g = warp; g < G; g += kConsumerWarps)
-                quantize_q_row_warp(p.q + ((size_t)b * p.nqh + (size_t)h * G + g) * kHD, lane,
-                                    q_codes + g * kHD, q_scale + g * kNQB);
+#pragma unroll
+            for (int i = 0; i < kQRows; ++i) {
+                const int g = warp + i * kConsumerWarps;
+                if (g < G) quantize_q_vals_warp(qx[i], lane, q_codes + g * kHD, q_scale + g * kNQB);
+            }
             named_barrier_sync(1, kConsumerWarps * 32);
+            if (remaining > seg_n) {   // the next segment's unit follows this one
+                const int nh = h + 1 == p.nkv ? 0 : h + 1;
+                const int nbq = h + 1 == p.nkv ? b + 1 : b;
+                if (nbq < p.batch) load_q_rows(nbq, nh);
+            }
 
             float M[G], Sl[G], acc[8][4];
 #pragma unroll

@@ -42,14 +42,14 @@ __device__ __forceinline__ int kv_code(float v, float scale) {
 }
 
 // 32-block query rule ([Day 9-2] §2 segment 1) for one row of 128 values,
-// executed by one full warp: lane l handles element 32*k + l of block k.
+// executed by one full warp: lane l holds element 32*k + l of block k in x[k].
 // qm = max |x| over the block (1 when below 1e-6); block scale = qm * (1/127);
 // code = round_half_even(x * (127/qm)) clamped to [-128, 127].
-__device__ __forceinline__ void quantize_q_row_warp(const float *__restrict__ row, int lane,
-                                                    int8_t *codes, float *scales) {
+__device__ __forceinline__ void quantize_q_vals_warp(const float (&xs)[4], int lane, int8_t *codes,
+                                                     float *scales) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const float x = row[32 * k + lane];
+        const float x = xs[k];
         float qm = warp_max(fabsf(x));
         if (qm < 1e-6f) qm = 1.0f;
         const float iq = __fdiv_rn(127.0f, qm);
@@ -58,6 +58,15 @@ __device__ __forceinline__ void quantize_q_row_warp(const float *__restrict__ ro
         codes[32 * k + lane] = (int8_t)c;
         if (lane == 0) scales[k] = __fmul_rn(qm, KVQ8_INV127);
     }
+}
+
+// The same for a row in global memory.
+__device__ __forceinline__ void quantize_q_row_warp(const float *__restrict__ row, int lane,
+                                                    int8_t *codes, float *scales) {
+    float xs[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) xs[k] = row[32 * k + lane];
+    quantize_q_vals_warp(xs, lane, codes, scales);
 }
 
 }  // namespace kvq8
