@@ -26,10 +26,11 @@
 //    online-softmax state (two warps per SM sub-partition leave room for 255
 //    registers a thread).  Q.K: lane = token (two tokens per lane), dp4a on
 //    int8 codes, exact int32 per 32-block.  P.V: tensor-core MMA m16n8k16 with
-//    A = V (int8 codes -> fp16, exact) and B = P, the weights times the V
-//    scale, split into fp16 high + low parts (two MMAs) and scaled per stage
-//    by a power of two so that fp16 range and precision lose nothing that
-//    fp32 accumulation keeps; D accumulates in fp32.
+//    A = V (int8 codes + 128 as exact fp16 subnormals, the offset removed
+//    once per stage by a correction tile) and B = P, the weights times the V
+//    scale, split into fp16 high + low parts and scaled per stage by a power
+//    of two so that fp16 range and precision lose nothing that fp32
+//    accumulation keeps; D accumulates in fp32.
 //  * At the end of a segment the 7 warp states are merged in shared memory
 //    and written as one record per query head.
 // All waits are bounded: a wait that times out sets KVQ8_DEV_TIMEOUT and the
@@ -102,18 +103,20 @@ __device__ __forceinline__ int2 seq_span(const DecodeParams &p, int b, int cap) 
 }
 __device__ __forceinline__ int span_stages(int2 sp) { return (sp.y - sp.x + kStageTok - 1) / kStageTok; }
 
-__device__ __forceinline__ uint32_t half2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
-
-// int8 codes of 4 consecutive tokens -> two fp16 pairs (tokens 0,1 and 2,3),
-// exact: (1024 + (v + 128)) - 1152 = v.
-__device__ __forceinline__ void codes_to_half2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+// int8 codes v of 4 consecutive tokens -> two fp16 pairs (tokens 0,1 and 2,3)
+// holding (v + 128) * 2^-24: the offset byte in the low bits of a half is the
+// fp16 subnormal of that value (exact; the tensor cores take subnormals as
+// they are).  The offset is removed by kNegOffset below.
+__device__ __forceinline__ void codes_to_sub2(uint32_t w, uint32_t &lo, uint32_t &hi) {
     const uint32_t x = w ^ 0x80808080u;
-    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
-    uint32_t l = __byte_perm(x, 0x64646464u, 0x4140);
-    uint32_t h = __byte_perm(x, 0x64646464u, 0x4342);
-    lo = half2_bits(__hsub2(*reinterpret_cast<__half2 *>(&l), bias));
-    hi = half2_bits(__hsub2(*reinterpret_cast<__half2 *>(&h), bias));
+    lo = __byte_perm(x, 0u, 0x4140);
+    hi = __byte_perm(x, 0u, 0x4342);
 }
+// fp16 pair (-2^-17, -2^-17) = -128 code steps of 2^-24: an A operand of these
+// times P gives -128 * 2^-24 * sum_t P[t][col] in every row, the offset's
+// share of the accumulator for that stage.
+constexpr uint32_t kNegOffset = 0x80808080u;
+constexpr float kCodeUnit = 16777216.0f;   // 2^24: one code step of codes_to_sub2
 
 __device__ __forceinline__ int4 lds128(const void *p) { return *reinterpret_cast<const int4 *>(p); }
 
@@ -522,6 +525,14 @@ decode_split_kernel(DecodeParams p) {
 #pragma unroll
                         for (int i = 0; i < 8; ++i) bl[i] = 0u;
                     }
+                    // the stage's offset correction, one tile shared by all dims
+                    float corr[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        mma_f16_16816(corr, kNegOffset, kNegOffset, kNegOffset, kNegOffset, bh[2 * s], bh[2 * s + 1]);
+                        if (!kPackPV)
+                            mma_f16_16816(corr, kNegOffset, kNegOffset, kNegOffset, kNegOffset, bl[2 * s], bl[2 * s + 1]);
+                    }
 #pragma unroll
                     for (int mt = 0; mt < 8; ++mt) {
                         const int d = mt * 16 + n;
@@ -532,12 +543,19 @@ decode_split_kernel(DecodeParams p) {
 #pragma unroll
                         for (int s = 0; s < 4; ++s) {
                             uint32_t a0, a2, a1, a3;
-                            codes_to_half2(w0[s], a0, a2);
-                            codes_to_half2(w1[s], a1, a3);
+                            codes_to_sub2(w0[s], a0, a2);
+                            codes_to_sub2(w1[s], a1, a3);
                             mma_f16_16816(acc[mt], a0, a1, a2, a3, bh[2 * s], bh[2 * s + 1]);
                             if (!kPackPV) mma_f16_16816(acc[mt], a0, a1, a2, a3, bl[2 * s], bl[2 * s + 1]);
                         }
                     }
+                    // remove the stage's offset now, so that the accumulator never
+                    // carries more than one stage of it (its rounding stays at the
+                    // scale of the result)
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc[mt][i] += corr[i];
                 }
                 __syncwarp();
                 if (lane == 0) {
@@ -571,12 +589,12 @@ decode_split_kernel(DecodeParams p) {
             for (int mt = 0; mt < 8; ++mt) {
                 const int d0 = mt * 16 + n, h0 = 2 * t4, h1 = 2 * t4 + 1;
                 if (h0 < G) {
-                    red_acc[h0 * kHD + d0] = acc[mt][0] * unit_scale;
-                    red_acc[h0 * kHD + d0 + 8] = acc[mt][2] * unit_scale;
+                    red_acc[h0 * kHD + d0] = acc[mt][0] * kCodeUnit * unit_scale;
+                    red_acc[h0 * kHD + d0 + 8] = acc[mt][2] * kCodeUnit * unit_scale;
                 }
                 if (h1 < G) {
-                    red_acc[h1 * kHD + d0] = acc[mt][1] * unit_scale;
-                    red_acc[h1 * kHD + d0 + 8] = acc[mt][3] * unit_scale;
+                    red_acc[h1 * kHD + d0] = acc[mt][1] * kCodeUnit * unit_scale;
+                    red_acc[h1 * kHD + d0 + 8] = acc[mt][3] * kCodeUnit * unit_scale;
                 }
             }
             named_barrier_sync(1, kConsumerWarps * 32);
