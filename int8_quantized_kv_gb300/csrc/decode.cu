@@ -643,6 +643,8 @@ decode_split_kernel(DecodeParams p) {
 // M = max_i M_i, S = sum_i S_i 2^(M_i - M), out = sum_i acc_i 2^(M_i - M) / S.
 // The records come from one split kernel, or from two (mixed precision by
 // token age: the 4-bit split over [0, x) and the int8 split over [x, L)).
+constexpr int kCombineRegs = 8;   // records merged from registers (more: the loop below)
+
 __global__ void __launch_bounds__(kHD)
 decode_combine_kernel(DecodeParams p, int G) {
     pdl_wait();  // the split kernel's records are visible after this
@@ -662,6 +664,38 @@ decode_combine_kernel(DecodeParams p, int G) {
     const int2 meta0 = has0 ? p.ws_meta[u] : make_int2(0, 0);
     const int2 meta1 = has1 ? p.ws_meta2[u] : make_int2(0, 0);
     const size_t r00 = (size_t)meta0.x + u, r10 = (size_t)meta1.x + u;
+    if (meta1.y == 0 && meta0.y <= kCombineRegs) {
+        // the usual case: every record's (M, S) and accumulator loaded at once,
+        // then merged in the same order as below
+        float mr[kCombineRegs], sr[kCombineRegs], ar[kCombineRegs];
+#pragma unroll
+        for (int j = 0; j < kCombineRegs; ++j) {
+            if (j < meta0.y) {
+                const size_t r = (r00 + j) * G + g;
+                const float2 ml = *reinterpret_cast<const float2 *>(p.ws_ml + r * 2);
+                mr[j] = ml.x;
+                sr[j] = ml.y;
+                ar[j] = p.ws_acc[r * kHD + d];
+            }
+        }
+        float m = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kCombineRegs; ++j)
+            if (j < meta0.y) m = fmaxf(m, mr[j]);
+        float s_sum = 0.0f, a = 0.0f;
+        if (m != -INFINITY) {
+#pragma unroll
+            for (int j = 0; j < kCombineRegs; ++j) {
+                if (j < meta0.y) {
+                    const float f = exp2f(mr[j] - m);
+                    s_sum = fmaf(sr[j], f, s_sum);
+                    a = fmaf(ar[j], f, a);
+                }
+            }
+        }
+        *o = s_sum > 0.0f ? a / s_sum : 0.0f;
+        return;
+    }
     float m = -INFINITY;
     for (int j = 0; j < meta0.y; ++j) m = fmaxf(m, p.ws_ml[((r00 + j) * G + g) * 2]);
     for (int j = 0; j < meta1.y; ++j) m = fmaxf(m, p.ws_ml2[((r10 + j) * G + g) * 2]);
