@@ -4,9 +4,11 @@
 One step = the whole hot path over one batch: quantise-append of the step's
 new K/V token for every (layer, kv head), split-KV decode attention of every
 query head over its paged int8 context, and the split merge: one
-kvq8_decode_step call (three launches, each overlapping the previous one's
-tail through programmatic dependent launch; the same three kernels called one
-by one through their own entry points are timed beside it as `unfused`).  The default workload is the 28-layer
+kvq8_decode_step call (two launches: the split kernel, which also appends the
+step's new token, and the merge, whose launch overlaps the split's tail
+through programmatic dependent launch; the three separate entry points --
+append, split, merge -- called one by one are timed beside it as `unfused`).
+The default workload is the 28-layer
 Qwen3-2B-shaped decode stack (16 query / 8 kv heads, hd 128, context 8192,
 batch 1), its layers folded into the batch dimension of one call.
 
@@ -399,8 +401,9 @@ def run_kvq8(args, rank, world, local):
             kvq8.decode_step(q_d, nk1, nv1, c, table_d, lens_d, out, ws, sm_scale=sm,
                              dev_status=status, stream=stream)
         else:
-            # the same three kernels through their own entry points, with events
-            # around the split kernel (the roofline's dominant kernel)
+            # the step's work as three calls through their own entry points
+            # (append, split, combine), with events around the split kernel
+            # (the roofline's dominant kernel)
             kvq8.quantize_append(nk_d, nv_d, start_d, table_d, c, dev_status=status, stream=stream)
             ev[0].record(stream)
             kvq8.decode_split(q_d, c, table_d, lens_d, ws, sm_scale=sm, dev_status=status,
@@ -441,7 +444,7 @@ def run_kvq8(args, rank, world, local):
     barrier()
     elapsed = t_start.elapsed_time(t_end) / 1e3
     split_s = sum(a.elapsed_time(b) for a, b in split_ev) / 1e3 / len(split_ev)
-    launches = 3 * args.steps
+    launches = 2 * args.steps + len(split_ev)   # sampled steps run three calls
 
     # the same step as three launches (append, split, combine), for comparison
     n_unf = min(args.steps, 1000)
@@ -578,7 +581,7 @@ def per_layer_graph(args, cfg, sbytes, cache, q_d, nk1, nv1, table_d, lens_d, ou
     t = e0.elapsed_time(e1) / 1e3 / n
     d = (outs.double() - out_folded.double()).abs()
     return {"us_per_step": round(t * 1e6, 2), "value": round(sbytes / t / 1e9, 2), "unit": "GB/s",
-            "calls_per_step": n_layers, "launches_per_step": 3 * n_layers, "replays": n,
+            "calls_per_step": n_layers, "launches_per_step": 2 * n_layers, "replays": n,
             "path": f"{n_layers} kvq8_decode_step calls (one layer each) in one CUDA graph",
             "max_abs_diff_vs_folded": float(d.max())}
 

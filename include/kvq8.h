@@ -228,11 +228,14 @@ kvq8_status kvq8_decode_combine(int batch, int nqh, int nkv, int hd,
  * kvq8_decode_step -- one decode step in one call: append the step's new
  * token of every sequence at position ctx_lens[b] - 1 and attend over the
  * context including it.  Same results as kvq8_quantize_append (n_new = 1,
- * start_pos[b] = ctx_lens[b] - 1) followed by kvq8_decode_attn; the three
- * kernels are launched back to back, each as a programmatic dependent of the
- * kernel before it in the stream (the first of whatever the caller queued
- * last), so that their launches overlap; each waits for that kernel's results
- * before it reads them.
+ * start_pos[b] = ctx_lens[b] - 1) followed by kvq8_decode_attn, in two
+ * launches: the split kernel also appends the new token (the CTA that decodes
+ * a unit's last 64-token stage quantises the token into that stage and into
+ * the pools), then the merge.  Both are programmatic dependents of the kernel
+ * before them in the stream, so that their launches overlap it; each waits
+ * for that kernel's results before it reads anything.  The block holding a
+ * sequence's new position must belong to that sequence alone (no other
+ * sequence of the call may read it in the same call).
  *
  *   k_new, v_new  fp32 [batch][nkv][hd]: the step's token ([Day 9-3] §2 rule)
  *                 (sequences with ctx_lens[b] == 0 append nothing and yield 0;

@@ -69,7 +69,8 @@ kvq8_status fill_decode_params(const float *q, int batch, int nqh, int nkv,
     p->max_blocks = max_blocks;
     p->ctx_lens = ctx_lens;
     p->sm_scale_log2 = sm_scale * 1.4426950408889634f;
-    p->early_prologue = 0;
+    p->k_new = nullptr;
+    p->v_new = nullptr;
     p->ws_meta = (int2 *)(ws + plan->meta_offset);
     p->ws_ml = (float *)(ws + plan->ml_offset);
     p->ws_acc = (float *)(ws + plan->acc_offset);
@@ -150,7 +151,6 @@ static kvq8_status prepare_append(const float *k_new, const float *v_new, int ba
     p->k_scale = k_scale;
     p->v_scale = v_scale;
     p->dev_status = dev_status;
-    p->ctx_lens = nullptr;
     *noop = false;
     return KVQ8_OK;
 }
@@ -287,14 +287,14 @@ kvq8_status kvq8_decode_attn(const float *q, int batch, int nqh, int nkv, int hd
 }
 
 // Checks the arguments of kvq8_decode_step and fills the parameters of its
-// three launches.
+// two launches (the split kernel also appends the step's new token).
 static kvq8_status prepare_decode_step(const float *q, const float *k_new, const float *v_new, int batch,
                                        int nqh, int nkv, int hd, int8_t *k_pool, int8_t *v_pool,
                                        float *k_scale, float *v_scale, int num_blocks,
                                        const int32_t *block_table, int max_blocks, int block_size,
                                        const int32_t *ctx_lens, float sm_scale, float *out,
                                        void *workspace, size_t workspace_bytes, uint32_t *dev_status,
-                                       DecodeParams *p, DecodePlan *plan, AppendParams *a) {
+                                       DecodeParams *p, DecodePlan *plan) {
     kvq8_status st = check_decode_args(q, batch, nqh, nkv, hd, k_pool, v_pool, k_scale, v_scale,
                                        num_blocks, block_table, max_blocks, block_size, ctx_lens);
     if (st != KVQ8_OK || batch == 0) return st;
@@ -305,28 +305,12 @@ static kvq8_status prepare_decode_step(const float *q, const float *k_new, const
                             workspace_bytes, dev_status, p, plan);
     if (st != KVQ8_OK) return st;
     p->out = out;
-    p->early_prologue = 1;   // the split follows this step's own append
-    a->k_new = k_new;
-    a->v_new = v_new;
-    a->batch = batch;
-    a->n_new = 1;
-    a->nkv = nkv;
-    a->start_pos = nullptr;   // the new token goes to ctx_lens[b] - 1
-    a->ctx_lens = ctx_lens;
-    a->block_table = block_table;
-    a->max_blocks = max_blocks;
-    a->num_blocks = num_blocks;
-    a->k_pool = k_pool;
-    a->v_pool = v_pool;
-    a->k_scale = k_scale;
-    a->v_scale = v_scale;
-    a->dev_status = dev_status;
+    p->k_new = k_new;   // appended at ctx_lens[b] - 1 by the split kernel
+    p->v_new = v_new;
     return KVQ8_OK;
 }
 
-static kvq8_status launch_decode_step(const DecodeParams &p, const DecodePlan &plan, const AppendParams &a,
-                                      cudaStream_t s) {
-    if (launch_quantize_append(a, s) != cudaSuccess) return KVQ8_ERR_CUDA;
+static kvq8_status launch_decode_step(const DecodeParams &p, const DecodePlan &plan, cudaStream_t s) {
     if (launch_decode_split(p, plan.group, s) != cudaSuccess) return KVQ8_ERR_CUDA;
     if (launch_decode_combine(p, plan.group, s) != cudaSuccess) return KVQ8_ERR_CUDA;
     return KVQ8_OK;
@@ -340,13 +324,12 @@ kvq8_status kvq8_decode_step(const float *q, const float *k_new, const float *v_
                              size_t workspace_bytes, uint32_t *dev_status, void *stream) {
     DecodeParams p;
     DecodePlan plan;
-    AppendParams a;
     const kvq8_status st = prepare_decode_step(q, k_new, v_new, batch, nqh, nkv, hd, k_pool, v_pool, k_scale,
                                                v_scale, num_blocks, block_table, max_blocks, block_size,
                                                ctx_lens, sm_scale, out, workspace, workspace_bytes,
-                                               dev_status, &p, &plan, &a);
+                                               dev_status, &p, &plan);
     if (st != KVQ8_OK || batch == 0) return st;
-    return launch_decode_step(p, plan, a, (cudaStream_t)stream);
+    return launch_decode_step(p, plan, (cudaStream_t)stream);
 }
 
 kvq8_status kvq8_decode_step_host(const float *q_host, const float *k_new_host, const float *v_new_host,
@@ -358,11 +341,10 @@ kvq8_status kvq8_decode_step_host(const float *q_host, const float *k_new_host, 
                                   size_t workspace_bytes, uint32_t *dev_status, void *stream) {
     DecodeParams p;
     DecodePlan plan;
-    AppendParams a;
     kvq8_status st = prepare_decode_step(q, k_new, v_new, batch, nqh, nkv, hd, k_pool, v_pool, k_scale,
                                          v_scale, num_blocks, block_table, max_blocks, block_size,
                                          ctx_lens, sm_scale, out, workspace, workspace_bytes, dev_status,
-                                         &p, &plan, &a);
+                                         &p, &plan);
     if (st != KVQ8_OK || batch == 0) return st;
     if (!q_host || !k_new_host || !v_new_host || !out_host) return KVQ8_ERR_INVALID_ARG;
     const size_t qbytes = (size_t)batch * nqh * hd * sizeof(float);
@@ -372,7 +354,7 @@ kvq8_status kvq8_decode_step_host(const float *q_host, const float *k_new_host, 
         !copy_async(k_new, k_new_host, kvbytes, cudaMemcpyHostToDevice, s) ||
         !copy_async(v_new, v_new_host, kvbytes, cudaMemcpyHostToDevice, s))
         return KVQ8_ERR_CUDA;
-    st = launch_decode_step(p, plan, a, s);
+    st = launch_decode_step(p, plan, s);
     if (st != KVQ8_OK) return st;
     if (!copy_async(out_host, out, qbytes, cudaMemcpyDeviceToHost, s)) return KVQ8_ERR_CUDA;
     return KVQ8_OK;

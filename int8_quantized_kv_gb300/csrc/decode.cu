@@ -36,11 +36,12 @@
 // All waits are bounded: a wait that times out sets KVQ8_DEV_TIMEOUT and the
 // CTA unwinds without leaving copies in flight.  The kernel is launched as a
 // programmatic dependent of the previous kernel in its stream, so that its
-// launch overlaps that kernel.  Inside a decode step (after the step's own
-// append) its prologue and query quantisation overlap the append too and only
-// the producer waits, before its first copy from the pools; after any other
-// kernel every thread waits first.  The combine releases the next kernel of
-// the stream as soon as the split's records are visible to it.
+// launch overlaps that kernel; every thread waits for that kernel's results
+// first.  The combine releases the next kernel of the stream as soon as the
+// split's records are visible to it.  In a decode step the split kernel also
+// appends the step's new token: the consumer that decodes the stage holding
+// position ctx_lens[b] - 1 quantises the token into that staged stage and
+// into the pools (no separate append launch).
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -144,6 +145,49 @@ __device__ __forceinline__ bool slot_turn_bounded(volatile int *done, int round,
     return true;
 }
 
+// A decode step's new token of unit (b, h), position pos = ctx_lens[b] - 1,
+// which is row t of the stage staged at st: quantised by the warp ([Day 9-3]
+// §2 rule, the same functions as the append kernels; lane l holds dims
+// 4l..4l+3), written over the row the copy brought in (K row with its chunk
+// order, V column of the dim-major quarter, both scales) and into the pools
+// and scale arrays.  Only this CTA reads that position in this launch.
+__device__ __noinline__ void append_new_token(const DecodeParams &p, int b, int h, int pos, int t,
+                                                 int lane, unsigned char *st) {
+    const size_t src = ((size_t)b * p.nkv + h) * kHD;
+    const float4 xk = reinterpret_cast<const float4 *>(p.k_new + src)[lane];
+    const float4 xv = reinterpret_cast<const float4 *>(p.v_new + src)[lane];
+    const int phys = p.block_table[(size_t)b * p.max_blocks + pos / kBS];   // valid: the stage was copied
+    const float sk = kv_row_scale(row_max_abs(xk)), sv = kv_row_scale(row_max_abs(xv));
+    const uint32_t wk = low_bytes4(kv_code_bytes4(xk, sk));
+    const uint4 cv = kv_code_bytes4(xv, sv);
+    const int slot = pos % kBS;   // slot & 7 == t & 7: stages start at multiples of 64
+    const int kpos = ((((lane >> 2) ^ (slot & 7)) << 4) + (lane & 3) * 4);
+    // the staged stage
+    *reinterpret_cast<uint32_t *>(st + t * kHD + kpos) = wk;
+    unsigned char *vs = st + kStageKBytes + t;
+    vs[(4 * lane + 0) * kStageTok] = (unsigned char)cv.x;
+    vs[(4 * lane + 1) * kStageTok] = (unsigned char)cv.y;
+    vs[(4 * lane + 2) * kStageTok] = (unsigned char)cv.z;
+    vs[(4 * lane + 3) * kStageTok] = (unsigned char)cv.w;
+    float *scl = reinterpret_cast<float *>(st + kStageKBytes + kStageVBytes);
+    // the cache (the pools of a decode step are the caller's writable buffers)
+    const size_t tile = (size_t)phys * p.nkv + h;
+    int8_t *kp = const_cast<int8_t *>(p.k_pool), *vp = const_cast<int8_t *>(p.v_pool);
+    *reinterpret_cast<uint32_t *>(kp + (tile * kBS + slot) * kHD + kpos) = wk;
+    int8_t *vg = vp + tile * kHD * kBS + (size_t)(slot / kStageTok) * kTileVQuarter + slot % kStageTok;
+    vg[(size_t)(4 * lane + 0) * kStageTok] = (int8_t)cv.x;
+    vg[(size_t)(4 * lane + 1) * kStageTok] = (int8_t)cv.y;
+    vg[(size_t)(4 * lane + 2) * kStageTok] = (int8_t)cv.z;
+    vg[(size_t)(4 * lane + 3) * kStageTok] = (int8_t)cv.w;
+    if (lane == 0) {
+        scl[t] = sk;
+        scl[kStageTok + t] = sv;
+        const_cast<float *>(p.k_scale)[tile * kBS + slot] = sk;
+        const_cast<float *>(p.v_scale)[tile * kBS + slot] = sv;
+    }
+    __syncwarp();   // the patched rows are read by every lane below
+}
+
 template <int G, bool kMixed>
 __global__ void __launch_bounds__(kSplitThreads, 1)
 decode_split_kernel(DecodeParams p) {
@@ -152,14 +196,10 @@ decode_split_kernel(DecodeParams p) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
     const int cap = p.max_blocks * kBS;
-    // Launched as a programmatic dependent of the previous kernel in the stream.
-    // Inside a decode step that kernel is the step's append, which writes only
-    // the pools and scales: the prologue and the query quantisation (ctx_lens,
-    // block table, q) then run before it ends, and only the producer waits for
-    // its results, before the first copy from the pools.  After any other
-    // kernel (whose outputs may be this kernel's inputs) every thread waits
-    // here first.
-    if (!p.early_prologue) pdl_wait();
+    // Launched as a programmatic dependent of the previous kernel in the stream
+    // (its launch overlaps that kernel's end), whose outputs may be this
+    // kernel's inputs: every thread waits for it here first.
+    pdl_wait();
     Misc *misc = reinterpret_cast<Misc *>(smem + Lay::oMisc);
     int8_t *q_codes = reinterpret_cast<int8_t *>(smem + Lay::oQCodes);
     float *q_scale = reinterpret_cast<float *>(smem + Lay::oQScale);
@@ -252,7 +292,6 @@ decode_split_kernel(DecodeParams p) {
 
     if (warp == kConsumerWarps) {
         // =========================== producer warp ===========================
-        pdl_wait();   // the previous kernel's writes to the pools are visible after this
         const uint64_t pol = l2_evict_first_policy();
         bool aborted = false;
         long long remaining = hi - lo;
@@ -359,6 +398,13 @@ decode_split_kernel(DecodeParams p) {
             if (nb == 0) { ++b; h = 0; off = 0; continue; }
             const int seg_n = (int)min((long long)(nb - off), remaining);
             const int u = b * p.nkv + h;
+            // a decode step appends its new token at position ctx_lens[b] - 1
+            // (none for an empty context or one beyond the table)
+            int app_pos = -1;
+            if (p.k_new) {
+                const int Lraw = p.ctx_lens[b];
+                if (Lraw >= 1 && Lraw <= cap) app_pos = Lraw - 1;
+            }
 
             // segment 1: quantise this unit's G query heads once
             if (qb != b || qh != h) load_q_rows(b, h);   // not loaded ahead
@@ -397,6 +443,9 @@ decode_split_kernel(DecodeParams p) {
                     const float *ks_st = reinterpret_cast<const float *>(st + kStageKBytes + kStageVBytes);
                     const float *vs_st = ks_st + kStageTok;
                     const int nvalid = min(kStageTok, L - (sp.x + (off + j) * kStageTok));
+                    const int tnew = app_pos - (sp.x + (off + j) * kStageTok);
+                    if (tnew >= 0 && tnew < kStageTok)
+                        append_new_token(p, b, h, app_pos, tnew, lane, const_cast<unsigned char *>(st));
                     const int ta = lane, tb = lane + 32;
                     const bool va = ta < nvalid, vb = tb < nvalid;
 

@@ -41,6 +41,56 @@ __device__ __forceinline__ int kv_code(float v, float scale) {
     return max(-127, min(127, c));
 }
 
+// kv_code of four values of one row whose scale is sc = fl(max|row| / 127),
+// each in the low byte of a word, with one reciprocal per row in place of a
+// division per value.  inv approximates 1 / sc (the hardware reciprocal, which
+// the PTX ISA bounds by one ulp; the argument below allows three).  t =
+// fl(v * inv + 1.5 * 2^23) holds round_half_even(v * inv) in its low mantissa
+// bits (the sum lies where the fp32 spacing is 1, and 1.5 * 2^23 is even), so
+// its low byte is the code as a two's complement byte; e = fl(v * inv - r),
+// r = t - 1.5 * 2^23, is the residual of that rounding to within 2^-26.  For
+// |v| <= max|row|, |v / sc| < 127.0001, so v * inv lies within
+// 127.0001 * 3 * 2^-23 < 4.6e-5 of v / sc, and fl(v / sc) within half an ulp
+// below 128 (2^-18) of v / sc.  When |e| <= 1/2 - 2^-14 (2^-14 > 6.1e-5 >
+// 4.6e-5 + 2^-18 + 2^-26), fl(v / sc) is therefore strictly closer than 1/2
+// to r, and round_half_even(fl(v / sc)) = r, which is within [-127, 127] (no
+// clamp needed).  The four values are divided exactly when one residual is
+// larger (about 1.2e-4 of values) or not a number, or when sc lies outside
+// [2^-120, 2^120] (a zero row, a subnormal or non-finite scale); the result
+// equals kv_code's in every case.
+__device__ __forceinline__ uint4 kv_code_bytes4(float4 x, float sc) {
+    if (sc >= 0x1p-120f && sc <= 0x1p120f) {
+        constexpr float kShift = 0x1.8p23f;
+        constexpr float kLim = 0.5f - 0x1p-14f;
+        float inv;
+        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(sc));
+        const float t0 = __fmaf_rn(x.x, inv, kShift), t1 = __fmaf_rn(x.y, inv, kShift);
+        const float t2 = __fmaf_rn(x.z, inv, kShift), t3 = __fmaf_rn(x.w, inv, kShift);
+        const float e0 = __fmaf_rn(x.x, inv, -__fsub_rn(t0, kShift));
+        const float e1 = __fmaf_rn(x.y, inv, -__fsub_rn(t1, kShift));
+        const float e2 = __fmaf_rn(x.z, inv, -__fsub_rn(t2, kShift));
+        const float e3 = __fmaf_rn(x.w, inv, -__fsub_rn(t3, kShift));
+        if ((fabsf(e0) <= kLim) & (fabsf(e1) <= kLim) & (fabsf(e2) <= kLim) & (fabsf(e3) <= kLim))
+            return make_uint4(__float_as_uint(t0), __float_as_uint(t1), __float_as_uint(t2),
+                              __float_as_uint(t3));
+    }
+    return make_uint4((uint32_t)kv_code(x.x, sc), (uint32_t)kv_code(x.y, sc),
+                      (uint32_t)kv_code(x.z, sc), (uint32_t)kv_code(x.w, sc));
+}
+
+// The low bytes of four words as one little-endian word.
+__device__ __forceinline__ uint32_t low_bytes4(uint4 c) {
+    return __byte_perm(__byte_perm(c.x, c.y, 0x0040), __byte_perm(c.z, c.w, 0x0040), 0x5410);
+}
+
+// Max |v| of a row held as a float4 per lane, not-a-number values left out
+// (0 for a row of them).  Non-negative floats order like their bit patterns,
+// so one unsigned warp reduction takes the maximum.
+__device__ __forceinline__ float row_max_abs(float4 x) {
+    const float a = fmaxf(fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))), 0.0f);
+    return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(a)));
+}
+
 // 32-block query rule ([Day 9-2] §2 segment 1) for one row of 128 values,
 // executed by one full warp: lane l holds element 32*k + l of block k in x[k].
 // qm = max |x| over the block (1 when below 1e-6); block scale = qm * (1/127);

@@ -19,8 +19,7 @@ constexpr int kMaxGridYZ = 65535;  // launch limit on gridDim.y / gridDim.z
 struct AppendParams {
     const float *k_new, *v_new;   // [batch][n_new][nkv][hd]
     int batch, n_new, nkv;
-    const int32_t *start_pos;     // [batch]; null: position ctx_lens[b] - 1 (decode step)
-    const int32_t *ctx_lens;      // decode step only: [batch]
+    const int32_t *start_pos;     // [batch]: position of each sequence's first new token
     const int32_t *block_table;   // [batch][max_blocks]
     int max_blocks, num_blocks;
     int8_t *k_pool, *v_pool;
@@ -69,11 +68,10 @@ struct DecodeParams {
     int max_blocks;
     const int32_t *ctx_lens;
     float sm_scale_log2;          // sm_scale * log2(e): softmax runs in base 2
-    // 1: the split kernel reads q, ctx_lens and the block table before its
-    // dependency wait (only when the kernel before it in the stream is this
-    // library's own one-token append of the same step, which writes nothing
-    // but the pools and scales); 0: every thread waits first
-    int early_prologue;
+    // A decode step's new token ([batch][nkv][hd] each; null otherwise): the
+    // split kernel quantises it into position ctx_lens[b] - 1, in the stage it
+    // copies and in the pools, which are then the caller's writable buffers
+    const float *k_new, *v_new;
     int2 *ws_meta;                // [units]: (first CTA, CTA count)
     float *ws_ml;                 // [records][G][2]  (running max M, sum S)
     float *ws_acc;                // [records][G][hd] (unnormalised V accumulator)
