@@ -255,16 +255,21 @@ kvq8_status kvq8_decode_step(const float *q, const float *k_new, const float *v_
 
 /*
  * kvq8_decode_step_host -- kvq8_decode_step from host memory and back, the
- * call a serving loop makes each step: q_host (fp32 [batch][nqh][hd]),
- * k_new_host and v_new_host (fp32 [batch][nkv][hd]) are copied into the
- * caller's device buffers q, k_new and v_new, the step runs, and its result is
- * copied from the device buffer out into out_host ([batch][nqh][hd]); one
- * cudaMemcpyAsync per copy, all on `stream`.  The caller synchronises the
- * stream before reading out_host; the input host buffers must not change until
- * then.  Page-locked host memory lets the copies run at full speed.  Returns as
- * kvq8_decode_step (all arguments are checked before anything is queued);
- * KVQ8_ERR_INVALID_ARG also for a null host pointer when batch > 0;
- * KVQ8_ERR_CUDA when a copy cannot be queued.
+ * call a serving loop makes each step: the inputs q_host (fp32
+ * [batch][nqh][hd]), k_new_host and v_new_host (fp32 [batch][nkv][hd]) and the
+ * result out_host ([batch][nqh][hd]) are in host memory.  When all four are
+ * page-locked and mapped into the device's address space (every page-locked
+ * allocation, on a system with unified addressing) and 16-byte aligned, the
+ * kernels read the inputs from host memory and write the result there
+ * themselves: nothing is copied and the device buffers q, k_new, v_new and
+ * out are left untouched.  Otherwise the inputs are copied into the caller's
+ * device buffers q, k_new and v_new, the step runs, and its result is copied
+ * from the device buffer out into out_host (one cudaMemcpyAsync per copy).
+ * Everything is queued on `stream`; the caller synchronises the stream before
+ * reading out_host, and the input host buffers must not change until then.
+ * Returns as kvq8_decode_step (all arguments, the device buffers included, are
+ * checked before anything is queued); KVQ8_ERR_INVALID_ARG also for a null
+ * host pointer when batch > 0; KVQ8_ERR_CUDA when a copy cannot be queued.
  */
 kvq8_status kvq8_decode_step_host(const float *q_host, const float *k_new_host,
                                   const float *v_new_host, float *out_host,

@@ -155,6 +155,23 @@ static kvq8_status prepare_append(const float *k_new, const float *v_new, int ba
     return KVQ8_OK;
 }
 
+// The device address of host memory that the GPU can access directly and that
+// is 16-byte aligned there: page-locked memory mapped into the device's
+// address space (with unified addressing, every page-locked allocation);
+// null for anything else (pageable or device memory), which the caller then
+// copies.
+static const void *mapped_host(const void *h) {
+    if (!h || !aligned(h, 16)) return nullptr;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, h) != cudaSuccess) {
+        (void)cudaGetLastError();   // an unknown pointer: not mapped
+        return nullptr;
+    }
+    if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr || !aligned(a.devicePointer, 16))
+        return nullptr;
+    return a.devicePointer;
+}
+
 // One asynchronous copy (a no-op for 0 bytes).
 static bool copy_async(void *dst, const void *src, size_t bytes, cudaMemcpyKind kind, cudaStream_t s) {
     return bytes == 0 || cudaMemcpyAsync(dst, src, bytes, kind, s) == cudaSuccess;
@@ -350,6 +367,18 @@ kvq8_status kvq8_decode_step_host(const float *q_host, const float *k_new_host, 
     const size_t qbytes = (size_t)batch * nqh * hd * sizeof(float);
     const size_t kvbytes = (size_t)batch * nkv * hd * sizeof(float);
     cudaStream_t s = (cudaStream_t)stream;
+    // Host buffers that the GPU can address (page-locked memory mapped into the
+    // device's address space) are read and written by the kernels themselves:
+    // no copy is queued and the step's two launches stay chained.
+    const void *qm = mapped_host(q_host), *km = mapped_host(k_new_host), *vm = mapped_host(v_new_host);
+    const void *om = mapped_host(out_host);
+    if (qm && km && vm && om) {
+        p.q = static_cast<const float *>(qm);
+        p.k_new = static_cast<const float *>(km);
+        p.v_new = static_cast<const float *>(vm);
+        p.out = static_cast<float *>(const_cast<void *>(om));
+        return launch_decode_step(p, plan, s);
+    }
     if (!copy_async(q, q_host, qbytes, cudaMemcpyHostToDevice, s) ||
         !copy_async(k_new, k_new_host, kvbytes, cudaMemcpyHostToDevice, s) ||
         !copy_async(v_new, v_new_host, kvbytes, cudaMemcpyHostToDevice, s))

@@ -287,10 +287,10 @@ def decode_step(q, k_new, v_new, cache: KVCache, block_table, ctx_lens, out, wor
 def decode_step_host(q_host, k_host, v_host, out_host, q, k_new, v_new, cache: KVCache, block_table,
                      ctx_lens, out, workspace, sm_scale: Optional[float] = None, dev_status=None,
                      stream=None):
-    """decode_step from host memory and back: q_host, k_host, v_host are copied
-    into the device buffers q, k_new, v_new, the step runs, and out is copied
-    into out_host, all queued on the stream; synchronise it before reading
-    out_host.  Host buffers page-locked for full speed."""
+    """decode_step from host memory and back, queued on the stream (synchronise
+    it before reading out_host).  Page-locked host buffers are read and written
+    by the kernels directly; other host buffers are copied through the device
+    buffers q, k_new, v_new and out."""
     _need_host(q_host, k_host, v_host, out_host)
     _need_cuda(q, k_new, v_new, block_table, ctx_lens, out, workspace, *cache, dev_status)
     if (q_host.shape != q.shape or out_host.shape != out.shape or q.shape != out.shape or

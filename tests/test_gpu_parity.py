@@ -495,17 +495,22 @@ def test_decode_step_equals_append_then_decode(gpu_lib):
                 assert np.array_equal(x, y)
 
 
-def test_decode_step_host_buffers_equal_device_call(gpu_lib):
+@pytest.mark.parametrize("pinned", [True, False])
+def test_decode_step_host_buffers_equal_device_call(gpu_lib, pinned):
     """kvq8_decode_step_host (host q and new rows in, host result out) gives the
-    device call's results bit for bit, pools included, and the oracle's."""
+    device call's results bit for bit, pools included, and the oracle's: with
+    page-locked buffers (read and written by the kernels themselves) and with
+    pageable ones (copied through the device buffers)."""
     cfg = wl.scaled(wl.QWEN3_2B_28L_8K, batch=3, ctx=1300)
     a = StepCase(cfg)
     dev_out = a.step()
     b = StepCase(cfg)
-    q_h = torch.from_numpy(wl.queries(cfg)).pin_memory()
-    k_h = torch.from_numpy(b.k_new).pin_memory()
-    v_h = torch.from_numpy(b.v_new).pin_memory()
-    out_h = torch.full(tuple(q_h.shape), float("nan")).pin_memory()
+    host = (lambda t: t.pin_memory()) if pinned else (lambda t: t.clone())
+    q_h = host(torch.from_numpy(wl.queries(cfg)))
+    k_h = host(torch.from_numpy(b.k_new))
+    v_h = host(torch.from_numpy(b.v_new))
+    out_h = host(torch.full(tuple(q_h.shape), float("nan")))
+    assert q_h.is_pinned() == pinned and out_h.is_pinned() == pinned
     q_d, k_d, v_d = torch.zeros_like(b.q_d), torch.zeros_like(b.k_new_d), torch.zeros_like(b.v_new_d)
     out_d = torch.empty_like(b.q_d)
     ws = kvq8.alloc_workspace(cfg.batch, cfg.nqh, cfg.nkv, b.max_blocks)
