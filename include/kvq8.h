@@ -17,7 +17,12 @@
  *   `stream` (a cudaStream_t, NULL = legacy default stream).  The library
  *   allocates no memory, never synchronises the device or the stream, and
  *   keeps no state between calls apart from a per-device cache of device
- *   attributes.
+ *   attributes.  A device pointer may also be the device address of
+ *   page-locked host memory mapped into the device's address space
+ *   (kvq8_host_device_pointer): the kernels then read or write that host
+ *   memory themselves over the host link, which pays for the small per-step
+ *   buffers (q, the new token's k_new and v_new, out), not for the pools or
+ *   the workspace.
  * - Work is enqueued asynchronously on `stream`.  Argument errors are
  *   detected on the host and returned before anything is enqueued.  A
  *   failed launch returns KVQ8_ERR_CUDA (the CUDA error is left for
@@ -282,6 +287,18 @@ kvq8_status kvq8_decode_step_host(const float *q_host, const float *k_new_host,
                                   const int32_t *ctx_lens, float sm_scale,
                                   float *out, void *workspace, size_t workspace_bytes,
                                   uint32_t *dev_status, void *stream);
+
+/*
+ * kvq8_host_device_pointer -- not part of the pages' method: the device
+ * address of host memory that the current device can access directly
+ * (page-locked memory mapped into its address space; with unified addressing
+ * every page-locked allocation is), provided it is 16-byte aligned there;
+ * NULL for pageable, device, unknown or misaligned memory.  The result can be
+ * passed wherever a call takes q, k_new, v_new or out.  Looked up once for
+ * buffers that are reused every step, it saves kvq8_decode_step_host's
+ * per-call lookup.
+ */
+const void *kvq8_host_device_pointer(const void *host_ptr);
 
 /* -------------------------------------------- 4-bit cache (NEXT row) --- */
 

@@ -389,6 +389,8 @@ kvq8_status kvq8_decode_step_host(const float *q_host, const float *k_new_host, 
     return KVQ8_OK;
 }
 
+const void *kvq8_host_device_pointer(const void *host_ptr) { return mapped_host(host_ptr); }
+
 size_t kvq4_code_pool_bytes(int num_blocks, int nkv, int hd, int block_size) {
     if (num_blocks < 0 || nkv < 0 || hd < 0 || block_size < 0) return 0;
     return (size_t)num_blocks * nkv * block_size * (hd / 2);

@@ -781,9 +781,7 @@ int device_sm_count() {
 template <int G, bool kMixed>
 cudaError_t launch_split_gm(const DecodeParams &p, cudaStream_t s) {
     using Lay = SplitLayout<G>;
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<G, kMixed>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
-    if (e != cudaSuccess) return e;
+    static std::atomic<uint64_t> configured{0};
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     cudaLaunchConfig_t cfg = {};
@@ -796,7 +794,13 @@ cudaError_t launch_split_gm(const DecodeParams &p, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_split_kernel<G, kMixed>, p);
+    return launch_after_setting(
+        configured,
+        [] {
+            return cudaFuncSetAttribute(decode_split_kernel<G, kMixed>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
+        },
+        [&] { return cudaLaunchKernelEx(&cfg, decode_split_kernel<G, kMixed>, p); });
 }
 
 template <int G>

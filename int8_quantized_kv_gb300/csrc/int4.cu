@@ -852,13 +852,22 @@ cudaError_t launch_int4_append(const Int4AppendParams &p, cudaStream_t s) {
 
 template <int G>
 cudaError_t launch_int4_split_g(const Int4DecodeParams &p, cudaStream_t s) {
-    const size_t smem = sizeof(Int4Smem<G>);
-    cudaError_t e = cudaFuncSetAttribute(int4_decode_split_kernel<G>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    dim3 grid(p.nsplit, p.nkv, p.batch);
-    int4_decode_split_kernel<G><<<grid, kWarps4 * 32, smem, s>>>(p);
-    return cudaGetLastError();
+    constexpr size_t smem = sizeof(Int4Smem<G>);
+    static std::atomic<uint64_t> configured{0};
+    return launch_after_setting(
+        configured,
+        [] {
+            return cudaFuncSetAttribute(int4_decode_split_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)smem);
+        },
+        [&] {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(p.nsplit, p.nkv, p.batch);
+            cfg.blockDim = dim3(kWarps4 * 32);
+            cfg.dynamicSmemBytes = smem;
+            cfg.stream = s;
+            return cudaLaunchKernelEx(&cfg, int4_decode_split_kernel<G>, p);
+        });
 }
 
 cudaError_t launch_int4_decode_split(const Int4DecodeParams &p, int group, cudaStream_t s) {

@@ -5,9 +5,36 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "kvq8.h"
 
 namespace kvq8 {
+
+// Runs `launch` after `set` (a kernel attribute such as its dynamic shared-
+// memory limit) has been applied once on the current device: the setting
+// belongs to the device's context, and applying it on every launch costs a
+// driver call per launch.  `configured` holds one bit per device.  Should a
+// launch be refused as an invalid configuration although the bit is set (the
+// context was re-created since), the attribute is applied again and the
+// launch repeated once.  `launch` returns that launch's own status
+// (cudaLaunchKernelEx), so nothing runs twice.
+template <typename SetFn, typename LaunchFn>
+cudaError_t launch_after_setting(std::atomic<uint64_t> &configured, SetFn set, LaunchFn launch) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
+    cudaError_t e;
+    if (bit == 0 || !(configured.load(std::memory_order_relaxed) & bit)) {
+        if ((e = set()) != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_relaxed);
+        return launch();
+    }
+    if ((e = launch()) != cudaErrorInvalidValue) return e;
+    (void)cudaGetLastError();
+    if ((e = set()) != cudaSuccess) return e;
+    return launch();
+}
 
 constexpr int kHD = 128;           // head dimension
 constexpr int kBS = 256;           // tokens per cache block

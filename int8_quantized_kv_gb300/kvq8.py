@@ -50,6 +50,7 @@ SIGNATURES = {
                               _P, _F, _P, _P, _SZ, _P, _P]),
     "kvq8_decode_step_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I,
                                    _P, _I, _I, _P, _F, _P, _P, _SZ, _P, _P]),
+    "kvq8_host_device_pointer": (_P, [_P]),
     "kvq4_code_pool_bytes": (_SZ, [_I, _I, _I, _I]),
     "kvq4_param_pool_bytes": (_SZ, [_I, _I, _I]),
     "kvq4_cache_bytes_per_token": (_SZ, [_I, _I]),
@@ -305,6 +306,65 @@ def decode_step_host(q_host, k_host, v_host, out_host, q, k_new, v_new, cache: K
         _ptr(ctx_lens), sm, _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(dev_status), _stream(stream))
     _check("kvq8_decode_step_host", st)
+
+
+class DecodeStep:
+    """A decode step bound to fixed buffers: the arguments are checked and
+    converted once, and each step is then one C call (bind once, run every
+    step, as a serving loop does with its reused buffers).
+
+    run() is kvq8_decode_step on the bound device buffers.  With host buffers
+    bound as well (q_host, k_host, v_host, out_host), run_host() is the same
+    step reading the inputs from and writing the result to them: page-locked
+    host buffers are handed to the kernels directly (their device addresses
+    are looked up here, once), others go through kvq8_decode_step_host and the
+    bound device buffers.  Refill the bound inputs between steps; the stream
+    (the current one when None) is bound too.  Synchronise it before reading
+    the result."""
+
+    def __init__(self, q, k_new, v_new, cache: KVCache, block_table, ctx_lens, out, workspace,
+                 sm_scale: Optional[float] = None, dev_status=None, stream=None,
+                 q_host=None, k_host=None, v_host=None, out_host=None):
+        _need_cuda(q, k_new, v_new, block_table, ctx_lens, out, workspace, *cache, dev_status)
+        batch, nqh, nkv, hd, max_blocks = _decode_common(q, cache, block_table, ctx_lens)
+        sm = 1.0 / math.sqrt(hd) if sm_scale is None else sm_scale
+        lib = load()
+        self._lib = lib
+        st = _P(_stream(stream))
+        common = [_I(batch), _I(nqh), _I(nkv), _I(hd), _P(_ptr(cache.k_pool)), _P(_ptr(cache.v_pool)),
+                  _P(_ptr(cache.k_scale)), _P(_ptr(cache.v_scale)), _I(cache.num_blocks),
+                  _P(_ptr(block_table)), _I(max_blocks), _I(BLOCK_SIZE), _P(_ptr(ctx_lens)), _F(sm)]
+        tail = [_P(_ptr(workspace)), _SZ(workspace.numel() * workspace.element_size()), _P(_ptr(dev_status)), st]
+        self._dev_args = tuple([_P(_ptr(q)), _P(_ptr(k_new)), _P(_ptr(v_new))] + common + [_P(_ptr(out))] + tail)
+        self._keep = (q, k_new, v_new, cache, block_table, ctx_lens, out, workspace, dev_status, stream)
+        self._host_fn = None
+        hosts = (q_host, k_host, v_host, out_host)
+        if any(h is not None for h in hosts):
+            if any(h is None for h in hosts):
+                raise ValueError("bind all four host buffers or none")
+            _need_host(*hosts)
+            if (q_host.shape != q.shape or out_host.shape != out.shape or q.shape != out.shape or
+                    k_host.shape != k_new.shape or v_host.shape != v_new.shape):
+                raise ValueError("host and device buffers differ in shape")
+            mapped = [lib.kvq8_host_device_pointer(_ptr(h)) for h in hosts]
+            if all(mapped):
+                self._host_fn = lib.kvq8_decode_step
+                self._host_args = tuple([_P(mapped[0]), _P(mapped[1]), _P(mapped[2])] + common +
+                                        [_P(mapped[3])] + tail)
+            else:
+                self._host_fn = lib.kvq8_decode_step_host
+                self._host_args = tuple([_P(_ptr(h)) for h in hosts] + list(self._dev_args[:3]) + common +
+                                        [self._dev_args[3 + len(common)]] + tail)
+            self._keep = self._keep + hosts
+        self.host_direct = self._host_fn is not None and self._host_fn is lib.kvq8_decode_step
+
+    def run(self):
+        _check("kvq8_decode_step", self._lib.kvq8_decode_step(*self._dev_args))
+
+    def run_host(self):
+        if self._host_fn is None:
+            raise ValueError("no host buffers bound")
+        _check("kvq8_decode_step", self._host_fn(*self._host_args))
 
 
 def decode_split(q, cache: KVCache, block_table, ctx_lens, workspace,

@@ -529,6 +529,54 @@ def test_decode_step_host_buffers_equal_device_call(gpu_lib, pinned):
     _check_step(b, out_h.numpy())
 
 
+@pytest.mark.parametrize("pinned", [True, False])
+def test_bound_decode_step_equals_the_calls(gpu_lib, pinned):
+    """kvq8.DecodeStep (arguments checked and converted once): run() gives
+    kvq8_decode_step's results and run_host() those of the host-buffer call,
+    bit for bit, over several steps with the inputs refilled in between."""
+    cfg = wl.scaled(wl.QWEN3_2B_28L_8K, batch=3, ctx=1300)
+    a = StepCase(cfg)
+    b = StepCase(cfg)
+    host = (lambda t: t.pin_memory()) if pinned else (lambda t: t.clone())
+    q_h = host(torch.from_numpy(wl.queries(cfg)))
+    k_h = host(torch.from_numpy(b.k_new))
+    v_h = host(torch.from_numpy(b.v_new))
+    out_h = host(torch.full(tuple(q_h.shape), float("nan")))
+    q_d, k_d, v_d = torch.zeros_like(b.q_d), torch.zeros_like(b.k_new_d), torch.zeros_like(b.v_new_d)
+    out_d = torch.empty_like(b.q_d)
+    ws_a = kvq8.alloc_workspace(cfg.batch, cfg.nqh, cfg.nkv, a.max_blocks)
+    ws_b = kvq8.alloc_workspace(cfg.batch, cfg.nqh, cfg.nkv, b.max_blocks)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    dev_step = kvq8.DecodeStep(a.q_d, a.k_new_d, a.v_new_d, a.cache, a.table_d, a.lens_d, out_d, ws_a,
+                               sm_scale=SM_SCALE, dev_status=a.status, stream=stream)
+    host_step = kvq8.DecodeStep(q_d, k_d, v_d, b.cache, b.table_d, b.lens_d, torch.empty_like(out_d), ws_b,
+                                sm_scale=SM_SCALE, dev_status=b.status, stream=stream,
+                                q_host=q_h, k_host=k_h, v_host=v_h, out_host=out_h)
+    assert host_step.host_direct == pinned
+    rng = np.random.default_rng(7)
+    for it in range(3):
+        qn = rng.standard_normal(tuple(q_h.shape)).astype(np.float32)
+        q_h.copy_(torch.from_numpy(qn))
+        a.q_d.copy_(torch.from_numpy(qn))
+        torch.cuda.synchronize()
+        dev_step.run()
+        host_step.run_host()
+        stream.synchronize()
+        assert np.array_equal(out_h.numpy(), out_d.cpu().numpy()), f"step {it}"
+        ref = out_d.cpu().numpy().copy()
+        kvq8.decode_step(a.q_d, a.k_new_d, a.v_new_d, a.cache, a.table_d, a.lens_d, out_d, ws_a,
+                         sm_scale=SM_SCALE, dev_status=a.status, stream=stream)
+        stream.synchronize()
+        assert np.array_equal(ref, out_d.cpu().numpy())
+    assert a.status.item() == 0 and b.status.item() == 0
+    pa, pb = a.host_pools(), b.host_pools()
+    for bb in range(cfg.batch):
+        for h in range(cfg.nkv):
+            for x, y in zip(a.gather_unit(pa, bb, h), b.gather_unit(pb, bb, h)):
+                assert np.array_equal(x, y)
+
+
 def test_quantize_append_host_buffers_equal_device_call(gpu_lib):
     nkv, n_new, batch = 2, 300, 2
     rng = np.random.default_rng(77)
