@@ -529,6 +529,19 @@ def test_decode_step_host_buffers_equal_device_call(gpu_lib, pinned):
     _check_step(b, out_h.numpy())
 
 
+def test_host_device_pointer(gpu_lib):
+    """kvq8_host_device_pointer: a device address for page-locked host memory
+    (16-byte aligned there), NULL for pageable, device or misaligned memory."""
+    lib = kvq8.load()
+    pinned = torch.zeros(64).pin_memory()
+    addr = lib.kvq8_host_device_pointer(pinned.data_ptr())
+    assert addr is not None and addr % 16 == 0
+    assert lib.kvq8_host_device_pointer(pinned.data_ptr() + 4) is None
+    assert lib.kvq8_host_device_pointer(torch.zeros(64).data_ptr()) is None
+    assert lib.kvq8_host_device_pointer(torch.zeros(64, device="cuda").data_ptr()) is None
+    assert lib.kvq8_host_device_pointer(None) is None
+
+
 @pytest.mark.parametrize("pinned", [True, False])
 def test_bound_decode_step_equals_the_calls(gpu_lib, pinned):
     """kvq8.DecodeStep (arguments checked and converted once): run() gives
