@@ -308,6 +308,39 @@ def decode_step_host(q_host, k_host, v_host, out_host, q, k_new, v_new, cache: K
     _check("kvq8_decode_step_host", st)
 
 
+class HostMapped:
+    """A page-locked host tensor presented to this binding's calls as device
+    memory: data_ptr() is its device address (kvq8_host_device_pointer), so the
+    kernels read (q, new rows) or write (out) the host memory themselves over
+    the host link, with no copy.  Meant for the small per-step buffers; raises
+    if the tensor is not a contiguous page-locked fp32 host tensor that the
+    device can address at a 16-byte boundary."""
+
+    is_cuda = True
+
+    def __init__(self, t):
+        _need_host(t)
+        if not t.is_pinned():
+            raise ValueError("HostMapped needs a page-locked (pinned) tensor")
+        addr = load().kvq8_host_device_pointer(t.data_ptr())
+        if not addr:
+            raise ValueError("the device cannot address this host memory (or not 16-byte aligned)")
+        self._t, self._addr = t, addr
+        self.shape, self.dtype = t.shape, t.dtype
+
+    def data_ptr(self) -> int:
+        return self._addr
+
+    def is_contiguous(self) -> bool:
+        return True
+
+    def numel(self) -> int:
+        return self._t.numel()
+
+    def element_size(self) -> int:
+        return self._t.element_size()
+
+
 class DecodeStep:
     """A decode step bound to fixed buffers: the arguments are checked and
     converted once, and each step is then one C call (bind once, run every

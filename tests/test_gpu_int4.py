@@ -166,3 +166,22 @@ def test_int4_workload_full_size_sampled(gpu_lib):
     G = cfg.group
     for b, h in {(int(rng.integers(cfg.batch)), int(rng.integers(cfg.nkv))) for _ in range(4)}:
         assert_close(out[b, h * G:(h + 1) * G], case.oracle_unit(b, h), f"full int4 b={b} h={h}")
+
+
+def test_int4_decode_on_host_mapped_buffers(gpu_lib):
+    """The same call with the query read from, and the result written to,
+    page-locked host memory (kvq8.HostMapped) gives the device call's output
+    bit for bit."""
+    cfg = wl.Workload("int4_host", 690, batch=3, nqh=8, nkv=2, ctx_range=(100, 1500))
+    case = Int4Case(cfg)
+    dev_out = case.decode()
+    q_h = torch.from_numpy(case.q).pin_memory()
+    out_h = torch.full(tuple(q_h.shape), float("nan")).pin_memory()
+    ws = kvq8.alloc_workspace(cfg.batch, cfg.nqh, cfg.nkv, case.max_blocks)
+    kvq8.decode_attn4(kvq8.HostMapped(q_h), case.cache, case.table_d, case.lens_d, kvq8.HostMapped(out_h), ws,
+                      sm_scale=SM_SCALE, dev_status=case.status)
+    torch.cuda.synchronize()
+    assert case.status.item() == 0
+    assert np.array_equal(out_h.numpy(), dev_out)
+    with pytest.raises(ValueError):
+        kvq8.HostMapped(torch.zeros(4))          # pageable: not addressable by the device

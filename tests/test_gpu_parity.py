@@ -529,6 +529,22 @@ def test_decode_step_host_buffers_equal_device_call(gpu_lib, pinned):
     _check_step(b, out_h.numpy())
 
 
+def test_decode_attn_on_host_mapped_buffers(gpu_lib):
+    """decode_attn reading the query from and writing the result to page-locked
+    host memory (kvq8.HostMapped) equals the device call bit for bit."""
+    cfg = _unit_cfg(4, nkv=2, batch=3, ctx_range=(100, 3000), cid=470)
+    case = Case(cfg)
+    dev_out = case.decode()
+    q_h = torch.from_numpy(case.q).pin_memory()
+    out_h = torch.full(tuple(q_h.shape), float("nan")).pin_memory()
+    ws = kvq8.alloc_workspace(cfg.batch, cfg.nqh, cfg.nkv, case.max_blocks)
+    kvq8.decode_attn(kvq8.HostMapped(q_h), case.cache, case.table_d, case.lens_d, kvq8.HostMapped(out_h), ws,
+                     sm_scale=SM_SCALE, dev_status=case.status)
+    torch.cuda.synchronize()
+    assert case.status_bits() == 0
+    assert np.array_equal(out_h.numpy(), dev_out)
+
+
 def test_host_device_pointer(gpu_lib):
     """kvq8_host_device_pointer: a device address for page-locked host memory
     (16-byte aligned there), NULL for pageable, device or misaligned memory."""
