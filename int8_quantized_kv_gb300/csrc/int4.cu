@@ -213,10 +213,10 @@ __device__ __forceinline__ int qk_dim(int ks, int kk) {
 constexpr int kKPitch4 = 64, kVPitch4 = 80;
 __device__ __forceinline__ int kswz(int r, int seg) { return seg ^ ((r >> 1) & 1); }
 constexpr int kStageKOff = 0;
-constexpr int kStageVOff = kChunk4 * kKPitch4;                    // 3072
-constexpr int kStageKpOff = kStageVOff + kChunk4 * kVPitch4;      // 5632
-constexpr int kStageVpOff = kStageKpOff + kChunk4 * 16;           // 6144
-constexpr int kStageBytes4 = kStageVpOff + kChunk4 * 16;          // 6656
+constexpr int kStageVOff = kChunk4 * kKPitch4;                    // 2048
+constexpr int kStageKpOff = kStageVOff + kChunk4 * kVPitch4;      // 4608
+constexpr int kStageVpOff = kStageKpOff + kChunk4 * 16;           // 5120
+constexpr int kStageBytes4 = kStageVpOff + kChunk4 * 16;          // 5632
 constexpr int kBufs4 = 2;
 
 template <int G>
@@ -564,20 +564,14 @@ int4_decode_split_kernel(Int4DecodeParams p) {
                 vp[mt][r] = vps[tok_of(mt, r)];
                 if (partial && tok_of(mt, r) >= ntok) vp[mt][r] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
+        // this lane's own maxima; the warp reduces them only when some lane's
+        // score passes its head's running maximum by more than 2^8 (below)
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < 2; ++j)
 #pragma unroll
             for (int mt = 0; mt < kM; ++mt)
 #pragma unroll
                 for (int r = 0; r < kR; ++r) mloc[j] = fmaxf(mloc[j], sc[mt][r][j]);
-            // lanes sharing this lane's heads: all g, and t4 ^ 2 when packed, all
-            // lanes when kPack2
-            if constexpr (kPack2) mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 1));
-            if constexpr (kPack) mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 2));
-            mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 4));
-            mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 8));
-            mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 16));
-        }
 
         // power-of-two unit of this chunk's P': 2^e > max V scale (see the q8 decode)
         float vsmax = 0.0f;
@@ -590,7 +584,11 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         if (e_need > e_cur || e_need < e_cur - 12) e_new = max(-120, min(120, e_need));
         const float inv = __int_as_float((127 - e_new) << 23);
 
-        // online softmax per head (the lanes of a head agree), raised lazily
+        // online softmax per head (the lanes of a head agree), raised lazily:
+        // some lane's score of a head is above M + 8 exactly when the head's
+        // maximum over the chunk is, so the lanes' own maxima decide whether
+        // to raise, and the maxima are reduced over the lanes sharing the head
+        // (all g, and t4 ^ 2 when packed, all lanes when kPack2) only then
         const bool grow = mloc[0] > M[0] + 8.0f || mloc[1] > M[1] + 8.0f;
         float alpha[2] = {1.0f, 1.0f};
         bool rescale = e_new != e_cur;
@@ -598,6 +596,11 @@ int4_decode_split_kernel(Int4DecodeParams p) {
             rescale = true;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
+                if constexpr (kPack2) mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 1));
+                if constexpr (kPack) mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 2));
+                mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 4));
+                mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 8));
+                mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 16));
                 const float m_new = fmaxf(M[j], mloc[j]);
                 alpha[j] = exp2f(M[j] - m_new);   // 0 while M is -inf
                 M[j] = m_new;

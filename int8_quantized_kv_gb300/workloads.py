@@ -179,6 +179,34 @@ def mixed_old_blocks(lens, recent_blocks: int = MIXED_RECENT_BLOCKS) -> np.ndarr
     nb = blocks_needed(lens)
     return np.maximum(nb - recent_blocks, 0).astype(np.int32)
 
+def steered_unit(seed: int, L: int, G: int, shape: str, peak: float = 150.0,
+                 hd: int = HEAD_DIM):
+    """Queries and K/V rows of one (sequence, kv head) whose scores are steered.
+
+    Every query head is a common unit direction c times 4 plus N(0, 0.3^2)
+    noise; every K row is N(0, 1) noise plus a_t * c, so that a head's score
+    of token t grows with a_t.  shape "ramp": a_t rises linearly from 0 to
+    `peak` over the sequence (the running maximum of the softmax keeps
+    rising, stage after stage); "spike": a_t = 0 except one token at 2L/3
+    with a_t = `peak` (one late jump far above every earlier score).  V rows
+    are N(0, 1).  Returns float32 q [G][hd], k [L][hd], v [L][hd].
+    """
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([90_000, seed, L, G])))
+    c = rng.standard_normal(hd)
+    c /= np.linalg.norm(c)
+    q = 4.0 * c[None, :] + 0.3 * rng.standard_normal((G, hd))
+    if shape == "ramp":
+        a = peak * np.arange(L) / max(L - 1, 1)
+    elif shape == "spike":
+        a = np.zeros(L)
+        a[(2 * L) // 3] = peak
+    else:
+        raise ValueError(f"unknown shape {shape!r}")
+    k = rng.standard_normal((L, hd)) + a[:, None] * c[None, :]
+    v = rng.standard_normal((L, hd))
+    return q.astype(np.float32), k.astype(np.float32), v.astype(np.float32)
+
+
 WORKLOADS = {w.name: w for w in (SINGLE_HEAD_L256, QWEN3_2B_28L_8K, BATCH64_RAGGED,
                                  LONG128K_OUTLIERS, APPEND_8X4096, INT4_G64_32K,
                                  MIXED_QWEN3_8K)}

@@ -1,0 +1,99 @@
+"""Decode parity on inputs whose scores move the softmax's running maximum late.
+
+On N(0, 1) workloads the running maximum settles within the first stages, so
+the path that raises it later (reducing the maxima over the lanes of a head,
+rescaling the running sum and the accumulator) runs rarely.  Here the keys are
+steered ([Day 9-2] §2, the online softmax: when a score exceeds the running
+maximum M, the running sum and the V accumulator are rescaled by exp(M_old -
+M_new)): "ramp" raises every head's score steadily over the whole sequence,
+so the maximum is raised stage after stage in every split; "spike" puts one
+token far above all others two thirds of the way in, so everything
+accumulated before it is rescaled to almost nothing.  Each path (int8, INT4,
+fp32 K/V) is compared with the oracle on the same inputs, within
+1e-4 + 1e-3 * |oracle|, for every GQA group size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from int8_quantized_kv_gb300 import kvq8
+from int8_quantized_kv_gb300 import workloads as wl
+from kvq8_harness import SM_SCALE, assert_close
+
+pytestmark = pytest.mark.gpu
+HD = 128
+NKV = 2
+L = 3000
+
+
+def _inputs(G, shape):
+    """q [1][NKV*G][HD], k/v [1][L][NKV][HD] (device), the per-head arrays
+    for the oracle, and the cache's block table."""
+    units = [wl.steered_unit(h, L, G, shape) for h in range(NKV)]
+    q = np.concatenate([u[0] for u in units])[None]
+    k = np.stack([u[1] for u in units], axis=1)[None]
+    v = np.stack([u[2] for u in units], axis=1)[None]
+    cfg = wl.Workload("steered", 90, batch=1, nqh=NKV * G, nkv=NKV, ctx=L)
+    table, num_blocks = wl.block_table(cfg, np.array([L], np.int32), spare_blocks=1)
+    dev = {n: torch.from_numpy(np.ascontiguousarray(a)).cuda() for n, a in
+           (("q", q), ("k", k), ("v", v), ("table", table))}
+    dev["lens"] = torch.tensor([L], dtype=torch.int32, device="cuda")
+    dev["start"] = torch.zeros(1, dtype=torch.int32, device="cuda")
+    return units, dev, num_blocks, table.shape[1]
+
+
+@pytest.mark.parametrize("shape", ["ramp", "spike"])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_int8_decode_steered(gpu_lib, G, shape):
+    units, d, num_blocks, max_blocks = _inputs(G, shape)
+    cache = kvq8.alloc_cache(num_blocks, NKV)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvq8.quantize_append(d["k"], d["v"], d["start"], d["table"], cache, dev_status=status)
+    out = torch.full_like(d["q"], float("nan"))
+    ws = kvq8.alloc_workspace(1, NKV * G, NKV, max_blocks)
+    kvq8.decode_attn(d["q"], cache, d["table"], d["lens"], out, ws, sm_scale=SM_SCALE, dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    out = out.cpu().numpy()[0]
+    for h, (q, k, v) in enumerate(units):
+        ref, _ = oracle.decode_unit_q8(q, k, v, SM_SCALE)
+        assert_close(out[h * G:(h + 1) * G], ref, f"int8 {shape} G={G} h={h}")
+
+
+@pytest.mark.parametrize("shape", ["ramp", "spike"])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_int4_decode_steered(gpu_lib, G, shape):
+    units, d, num_blocks, max_blocks = _inputs(G, shape)
+    cache = kvq8.alloc_cache4(num_blocks, NKV)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvq8.quantize_append4(d["k"], d["v"], d["start"], d["table"], cache, dev_status=status)
+    out = torch.full_like(d["q"], float("nan"))
+    ws = kvq8.alloc_workspace(1, NKV * G, NKV, max_blocks)
+    kvq8.decode_attn4(d["q"], cache, d["table"], d["lens"], out, ws, sm_scale=SM_SCALE, dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    out = out.cpu().numpy()[0]
+    for h, (q, k, v) in enumerate(units):
+        kd = oracle.int4_dequantize_groups(*oracle.int4_quantize_groups(k, 64), 64)
+        vd = oracle.int4_dequantize_groups(*oracle.int4_quantize_groups(v, 64), 64)
+        ref = np.stack([oracle.attention_f64(q[g], kd, vd, SM_SCALE) for g in range(G)])
+        assert_close(out[h * G:(h + 1) * G], ref, f"int4 {shape} G={G} h={h}")
+
+
+@pytest.mark.parametrize("shape", ["ramp", "spike"])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_f32_decode_steered(gpu_lib, G, shape):
+    units, d, num_blocks, max_blocks = _inputs(G, shape)
+    cache = kvq8.alloc_cachef32(num_blocks, NKV)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvq8.appendf32(d["k"], d["v"], d["start"], d["table"], cache, dev_status=status)
+    out = torch.full_like(d["q"], float("nan"))
+    ws = kvq8.alloc_workspace(1, NKV * G, NKV, max_blocks)
+    kvq8.decode_attnf32(d["q"], cache, d["table"], d["lens"], out, ws, sm_scale=SM_SCALE, dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    out = out.cpu().numpy()[0]
+    for h, (q, k, v) in enumerate(units):
+        ref = np.stack([oracle.attention_f64(q[g], k, v, SM_SCALE) for g in range(G)])
+        assert_close(out[h * G:(h + 1) * G], ref, f"f32 {shape} G={G} h={h}")
