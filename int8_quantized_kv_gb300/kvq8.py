@@ -271,8 +271,9 @@ def decode_attn(q, cache: KVCache, block_table, ctx_lens, out, workspace,
 def decode_step(q, k_new, v_new, cache: KVCache, block_table, ctx_lens, out, workspace,
                 sm_scale: Optional[float] = None, dev_status=None, stream=None):
     """One decode step: append k_new/v_new (fp32 [batch][nkv][128]) at position
-    ctx_lens-1 and attend over ctx_lens tokens (three launches: append, split,
-    combine, each a programmatic dependent of the one before)."""
+    ctx_lens-1 and attend over ctx_lens tokens (two launches: the split kernel,
+    which also appends the token, and the combine, a programmatic dependent of
+    the split)."""
     _need_cuda(q, k_new, v_new, block_table, ctx_lens, out, workspace, *cache, dev_status)
     batch, nqh, nkv, hd, max_blocks = _decode_common(q, cache, block_table, ctx_lens)
     sm = 1.0 / math.sqrt(hd) if sm_scale is None else sm_scale

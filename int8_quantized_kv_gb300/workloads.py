@@ -12,7 +12,8 @@ full-size workloads that way).
 
 Streams: 0 = K/V of a unit, 1 = queries of a sequence, 2 = block-table
 permutation, 3 = per-sequence context lengths, 4 = outlier channel choice,
-5 = tokens appended by a decode step.
+5 = tokens appended by a decode step, 6 = rows a whole batch appends in one
+call.
 """
 from __future__ import annotations
 
@@ -144,6 +145,15 @@ def seq_kv(cfg: Workload, b: int, L: Optional[int] = None, threads: Optional[int
         with ThreadPoolExecutor(n) as ex:
             list(ex.map(one, range(cfg.nkv)))
     return k, v
+
+
+def batch_new_kv(cfg: Workload, n_new: int):
+    """fp32 K and V [batch][n_new][nkv][hd] from one stream: the rows that every
+    sequence of a batch appends in one call (cheap to draw for large batches)."""
+    rng = _rng(cfg, 6, n_new)
+    shape = (cfg.batch, n_new, cfg.nkv, cfg.hd)
+    return (rng.standard_normal(shape, dtype=np.float32),
+            rng.standard_normal(shape, dtype=np.float32))
 
 
 def queries(cfg: Workload) -> np.ndarray:

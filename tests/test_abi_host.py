@@ -131,6 +131,8 @@ def test_decode_validation(lib):
         assert _decode(lib, fn, ws=FAKE + 16, ws_bytes=need) == kvq8.ERR_WORKSPACE
         assert _decode(lib, fn, ws_bytes=need - 1) == kvq8.ERR_WORKSPACE
         assert _decode(lib, fn, batch=0) == kvq8.OK
+        assert _decode(lib, fn, batch=65536) == kvq8.ERR_UNSUPPORTED     # beyond the grid's y/z limit
+        assert _decode(lib, fn, max_blocks=(2**31 - 1) // 256 + 1) == kvq8.ERR_UNSUPPORTED   # positions past int32
     assert _decode(lib, out=None, ws_bytes=need) == kvq8.ERR_INVALID_ARG
     assert lib.kvq8_decode_combine(1, 8, 8, 128, 4, 256, FAKE, FAKE, need - 1, FAKE, None) \
         == kvq8.ERR_WORKSPACE
