@@ -206,24 +206,27 @@ __device__ __forceinline__ int qk_dim(int ks, int kk) {
     return 2 * byte + lo;
 }
 
-// Per-warp staging of one 32-token chunk: K and V code rows and the K and V
-// parameter rows; two buffers per warp, filled by 16-byte cp.async.  The
-// fragment reads are conflict-free: K rows keep 64 B with the two 32-byte
-// halves of rows 2, 3 (mod 4) swapped; V rows are padded to 80 B.
-constexpr int kKPitch4 = 64, kVPitch4 = 80;
-__device__ __forceinline__ int kswz(int r, int seg) { return seg ^ ((r >> 1) & 1); }
+// Per-warp staging of one 32-token chunk: its K codes (2 KiB), V codes (2 KiB)
+// and K and V parameter rows (512 B each) are contiguous in the cache (a chunk
+// starts at a multiple of 32 slots), so one lane brings each in with a 1-D
+// bulk copy, completing on the buffer's mbarrier; two buffers per warp.  The
+// staged rows keep the cache's 64-byte pitch; the fragment loads then meet
+// 2-way bank conflicts, which cost nothing measurable (a cache layout that
+// removed them, with the rows' 32-byte pieces permuted, ran at the same speed).
 constexpr int kStageKOff = 0;
-constexpr int kStageVOff = kChunk4 * kKPitch4;                    // 2048
-constexpr int kStageKpOff = kStageVOff + kChunk4 * kVPitch4;      // 4608
-constexpr int kStageVpOff = kStageKpOff + kChunk4 * 16;           // 5120
-constexpr int kStageBytes4 = kStageVpOff + kChunk4 * 16;          // 5632
+constexpr int kStageVOff = kChunk4 * kRowBytes;                   // 2048
+constexpr int kStageKpOff = kStageVOff + kChunk4 * kRowBytes;     // 4096
+constexpr int kStageVpOff = kStageKpOff + kChunk4 * 16;           // 4608
+constexpr int kStageBytes4 = kStageVpOff + kChunk4 * 16;          // 5120
 constexpr int kBufs4 = 2;
+constexpr uint64_t kWait4Ns = 2000000000ull;                      // bound of every copy wait
 
 template <int G>
 struct Int4Smem {
     uint4 qa[8][32];                 // per k-step and lane: a0 high, a2 high, a0 low, a2 low
     float qq[8][2];                  // Q_g per head
     float qmax[kWarps4];
+    unsigned long long bar[kWarps4][kBufs4];   // per warp and buffer: copies complete
     union {
         unsigned char stage[kWarps4][kBufs4][kStageBytes4];
         struct {
@@ -233,43 +236,34 @@ struct Int4Smem {
     } u;
 };
 
-// Per-lane shared-memory offsets of the chunk copies: the chunk's 32 code rows
-// are 2 KiB contiguous in the cache, lane l copying bytes 16l + 512i (row
-// l/4 + 8i, part l%4); the staged K row keeps its 32-byte halves swapped on
-// rows 2, 3 (mod 4), which row + 8 does not change.
-struct Int4FetchLane {
-    int kdst, vdst;
-    __device__ __forceinline__ explicit Int4FetchLane(int lane)
-        : kdst((lane >> 2) * kKPitch4 + 32 * kswz(lane >> 2, (lane & 3) >> 1) + 16 * (lane & 1)),
-          vdst((lane >> 2) * kVPitch4 + 16 * (lane & 3)) {}
-};
-
-// Copies chunk `cidx` of this warp's split into `buf` (one copy group; an
-// empty group when the chunk does not exist or its block id is invalid).
+// Fills `buf` (its mbarrier `bar`) with chunk `cidx` of this warp's split:
+// lane 0 issues the four bulk copies, or, when the chunk does not exist or its
+// block id is invalid, completes the barrier's phase with a plain arrival.
+// Every call completes exactly one phase of `bar`.  Returns the block id (-1
+// for no data).  The buffer's earlier contents were read and written through
+// the generic proxy; the proxy fence orders those accesses (of every lane: the
+// caller synchronises the warp first) before the copies' writes.
 __device__ __forceinline__ int int4_fetch_chunk(const Int4DecodeParams &p, int b, int h, int tok_begin,
-                                                int nchunks, int cidx, unsigned char *buf, int lane,
-                                                const Int4FetchLane &fl) {
+                                                int nchunks, int cidx, unsigned char *buf, uint32_t bar,
+                                                uint64_t pol, int lane) {
     int phys = -1;
     if (cidx < nchunks) {
         const int t0 = tok_begin + cidx * kChunk4;
         phys = p.block_table[(size_t)b * p.max_blocks + t0 / kBS];
-        if (phys >= 0 && phys < p.num_blocks) {
-            const size_t row0 = ((size_t)phys * p.nkv + h) * kBS + t0 % kBS;
-            const uint8_t *kc = p.k_codes + row0 * kRowBytes + 16 * lane;
-            const uint8_t *vc = p.v_codes + row0 * kRowBytes + 16 * lane;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                cp_async16_cg(buf + kStageKOff + fl.kdst + 8 * kKPitch4 * i, kc + 512 * i);
-                cp_async16_cg(buf + kStageVOff + fl.vdst + 8 * kVPitch4 * i, vc + 512 * i);
-            }
-            cp_async16_cg(buf + kStageKpOff + 16 * lane, p.k_param + (row0 + lane) * 4);
-            cp_async16_cg(buf + kStageVpOff + 16 * lane, p.v_param + (row0 + lane) * 4);
-        } else {
+        if (phys < 0 || phys >= p.num_blocks) {
             if (lane == 0) flag_status(p.dev_status, KVQ8_DEV_BAD_BLOCK_ID);
             phys = -1;
+        } else if (lane == 0) {
+            const size_t row0 = ((size_t)phys * p.nkv + h) * kBS + t0 % kBS;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive_expect_tx(bar, kStageBytes4);
+            bulk_copy_g2s(smem_addr(buf + kStageKOff), p.k_codes + row0 * kRowBytes, kChunk4 * kRowBytes, bar, pol);
+            bulk_copy_g2s(smem_addr(buf + kStageVOff), p.v_codes + row0 * kRowBytes, kChunk4 * kRowBytes, bar, pol);
+            bulk_copy_g2s(smem_addr(buf + kStageKpOff), p.k_param + row0 * 4, kChunk4 * 16, bar, pol);
+            bulk_copy_g2s(smem_addr(buf + kStageVpOff), p.v_param + row0 * 4, kChunk4 * 16, bar, pol);
         }
     }
-    cp_async_commit();
+    if (phys < 0 && lane == 0) mbar_arrive(bar);
     return phys;
 }
 
@@ -316,15 +310,24 @@ int4_decode_split_kernel(Int4DecodeParams p) {
 
     extern __shared__ __align__(16) unsigned char int4_smem_raw[];
     Int4Smem<G> &sm = *reinterpret_cast<Int4Smem<G> *>(int4_smem_raw);
-    // this warp's chunks: cidx = warp, warp + 4, ...; two in flight; bit i of
-    // `valid` says whether buffer i holds a chunk
+    // this warp's chunks: cidx = warp, warp + 4, ...; two in flight.  Bit i of
+    // `valid`: buffer i holds a chunk; of `fill_par`: parity of the phase of
+    // buffer i's latest fill; of `pending`: that phase is not waited for yet
     const int nchunks = (tok_end - tok_begin + kChunk4 - 1) / kChunk4;
-    const Int4FetchLane fl(lane);
-    unsigned valid = 0;
+    const uint64_t pol = l2_evict_first_policy();
+    const uint32_t bar0 = smem_addr(&sm.bar[warp][0]);
+    if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < kBufs4; ++i) mbar_init(bar0 + 8 * i, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    unsigned valid = 0, fill_par = 0, pending = (1u << kBufs4) - 1;
 #pragma unroll
     for (int i = 0; i < kBufs4; ++i)
         valid |= (unsigned)(int4_fetch_chunk(p, b, h, tok_begin, nchunks, warp + kWarps4 * i, sm.u.stage[warp][i],
-                                             lane, fl) >= 0) << i;
+                                             bar0 + 8 * i, pol, lane) >= 0) << i;
+    bool aborted = false;
 
     const float *qrow = p.q + ((size_t)b * p.nqh + (size_t)h * G) * kHD;
     // power of two 2^k with max |q| * 2^k in [2^13, 2^14)
@@ -436,7 +439,12 @@ int4_decode_split_kernel(Int4DecodeParams p) {
 
     for (int it = 0, cidx = warp; cidx < nchunks; ++it, cidx += kWarps4) {
         const int bi = it % kBufs4;
-        cp_async_wait<kBufs4 - 1>();
+        if (!mbar_wait_bounded(bar0 + 8 * bi, (fill_par >> bi) & 1u, kWait4Ns)) {
+            if (lane == 0) flag_status(p.dev_status, KVQ8_DEV_TIMEOUT);
+            aborted = true;
+            break;
+        }
+        pending &= ~(1u << bi);
         __syncwarp();
         const unsigned char *st = sm.u.stage[warp][bi];
         if ((valid >> bi) & 1u) {
@@ -461,8 +469,7 @@ int4_decode_split_kernel(Int4DecodeParams p) {
 #pragma unroll
                 for (int gr = 0; gr < 2; ++gr) {
                     const int t = 16 * mt + g + 8 * r;
-                    kw[r][gr] = *reinterpret_cast<const uint2 *>(st + kStageKOff + t * kKPitch4 +
-                                                                 32 * kswz(t, gr) + 8 * t4);
+                    kw[r][gr] = *reinterpret_cast<const uint2 *>(st + kStageKOff + t * kRowBytes + 32 * gr + 8 * t4);
                 }
             float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};   // per group
 #pragma unroll
@@ -698,7 +705,7 @@ int4_decode_split_kernel(Int4DecodeParams p) {
 #pragma unroll
                 for (int gr = 0; gr < 2; ++gr) {
                     const int t = 16 * ks2 + 2 * t4 + (j & 1) + 8 * (j >> 1);
-                    vw[j][gr] = *reinterpret_cast<const uint32_t *>(st + kStageVOff + t * kVPitch4 + 32 * gr + 4 * g);
+                    vw[j][gr] = *reinterpret_cast<const uint32_t *>(st + kStageVOff + t * kRowBytes + 32 * gr + 4 * g);
                 }
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
@@ -716,10 +723,17 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         }
         __syncwarp();
         const bool ok = int4_fetch_chunk(p, b, h, tok_begin, nchunks, cidx + kWarps4 * kBufs4,
-                                         sm.u.stage[warp][bi], lane, fl) >= 0;
+                                         sm.u.stage[warp][bi], bar0 + 8 * bi, pol, lane) >= 0;
         valid = (valid & ~(1u << bi)) | ((unsigned)ok << bi);
+        fill_par ^= 1u << bi;
+        pending |= 1u << bi;
     }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    if (aborted) {
+        // no copy of this warp may still be in flight when the CTA exits
+#pragma unroll
+        for (int i = 0; i < kBufs4; ++i)
+            if ((pending >> i) & 1u) mbar_wait_bounded(bar0 + 8 * i, (fill_par >> i) & 1u, kWait4Ns);
+    }
 
     // ---- this warp's state: the lanes of this lane's heads ----
 #pragma unroll
