@@ -300,6 +300,22 @@ kvq8_status kvq8_decode_step_host(const float *q_host, const float *k_new_host,
  */
 const void *kvq8_host_device_pointer(const void *host_ptr);
 
+/*
+ * kvq8_selftest_bounded_wait -- not part of the pages' method: a check that
+ * the kernels' bounded waits end.  Every wait of the decode kernels on a copy
+ * or a shared-memory slot gives up after a bound, ORs KVQ8_DEV_TIMEOUT into
+ * *dev_status and unwinds rather than spin forever.  This call launches one
+ * warp that runs the same wait routine on an mbarrier phase that nothing
+ * completes, bounded by timeout_ns (1 us .. 10 s), so the bound passes on
+ * purpose: the warp then ORs KVQ8_DEV_TIMEOUT into *dev_status, writes the
+ * nanoseconds it waited to *waited_ns (when non-NULL) and exits, leaving the
+ * context usable.  dev_status (4-byte aligned) and waited_ns (8-byte aligned)
+ * are device pointers; enqueued on `stream`.  KVQ8_ERR_INVALID_ARG for a NULL
+ * or misaligned status word or a bound outside the range.
+ */
+kvq8_status kvq8_selftest_bounded_wait(uint32_t *dev_status, uint64_t timeout_ns,
+                                       unsigned long long *waited_ns, void *stream);
+
 /* -------------------------------------------- 4-bit cache (NEXT row) --- */
 
 /*

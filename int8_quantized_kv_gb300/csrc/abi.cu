@@ -391,6 +391,16 @@ kvq8_status kvq8_decode_step_host(const float *q_host, const float *k_new_host, 
 
 const void *kvq8_host_device_pointer(const void *host_ptr) { return mapped_host(host_ptr); }
 
+kvq8_status kvq8_selftest_bounded_wait(uint32_t *dev_status, uint64_t timeout_ns,
+                                       unsigned long long *waited_ns, void *stream) {
+    if (!dev_status || !aligned(dev_status, 4) || (waited_ns && !aligned(waited_ns, 8)))
+        return KVQ8_ERR_INVALID_ARG;
+    if (timeout_ns < 1000ull || timeout_ns > 10000000000ull) return KVQ8_ERR_INVALID_ARG;
+    if (launch_bounded_wait_selftest(dev_status, timeout_ns, waited_ns, (cudaStream_t)stream) != cudaSuccess)
+        return KVQ8_ERR_CUDA;
+    return KVQ8_OK;
+}
+
 size_t kvq4_code_pool_bytes(int num_blocks, int nkv, int hd, int block_size) {
     if (num_blocks < 0 || nkv < 0 || hd < 0 || block_size < 0) return 0;
     return (size_t)num_blocks * nkv * block_size * (hd / 2);

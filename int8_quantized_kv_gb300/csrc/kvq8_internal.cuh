@@ -194,4 +194,9 @@ bool make_f32_plan(int batch, int nkv, int max_blocks, int *nsplit, int *split_t
 cudaError_t launch_f32_append(const F32AppendParams &p, cudaStream_t s);
 cudaError_t launch_f32_decode_split(const F32DecodeParams &p, int group, cudaStream_t s);
 
+// One warp waiting, bounded by timeout_ns, on an mbarrier phase that nothing
+// completes (kvq8_selftest_bounded_wait).
+cudaError_t launch_bounded_wait_selftest(uint32_t *dev_status, uint64_t timeout_ns, unsigned long long *waited_ns,
+                                         cudaStream_t s);
+
 }  // namespace kvq8

@@ -51,6 +51,7 @@ SIGNATURES = {
     "kvq8_decode_step_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I,
                                    _P, _I, _I, _P, _F, _P, _P, _SZ, _P, _P]),
     "kvq8_host_device_pointer": (_P, [_P]),
+    "kvq8_selftest_bounded_wait": (_I, [_P, ctypes.c_uint64, _P, _P]),
     "kvq4_code_pool_bytes": (_SZ, [_I, _I, _I, _I]),
     "kvq4_param_pool_bytes": (_SZ, [_I, _I, _I]),
     "kvq4_cache_bytes_per_token": (_SZ, [_I, _I]),
@@ -437,6 +438,16 @@ def decode_attn_noalloc(q, cache: KVCache, block_table, ctx_lens, out,
         max_blocks, BLOCK_SIZE, _ptr(ctx_lens), sm, _ptr(out), _ptr(dev_status),
         _stream(stream))
     _check("kvq8_decode_attn_noalloc", st)
+
+
+def selftest_bounded_wait(timeout_ns: int, dev_status, waited_ns=None, stream=None):
+    """One warp waits, bounded by timeout_ns, on a barrier phase that nothing
+    completes (the decode kernels' wait routine): it ORs KVQ8_DEV_TIMEOUT into
+    dev_status (int32 [1], device) and writes the nanoseconds it waited into
+    waited_ns (int64 [1], device, optional)."""
+    _need_cuda(dev_status, waited_ns)
+    _check("kvq8_selftest_bounded_wait",
+           load().kvq8_selftest_bounded_wait(_ptr(dev_status), int(timeout_ns), _ptr(waited_ns), _stream(stream)))
 
 
 # ------------------------------------------------------------ 4-bit cache ---

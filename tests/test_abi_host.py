@@ -36,7 +36,7 @@ def test_header_declares_expected_entry_points():
               "kvq8_decode_step", "kvq8_decode_attn_noalloc", "kvq4_quantize_append",
               "kvq4_decode_attn", "kvf32_append", "kvf32_decode_attn", "kvmix_requantize",
               "kvmix_decode_attn", "kvmix_decode_workspace_bytes", "kvq8_decode_step_host",
-              "kvq8_quantize_append_host"):
+              "kvq8_quantize_append_host", "kvq8_selftest_bounded_wait"):
         assert n in names
 
 
@@ -172,6 +172,15 @@ def test_host_buffer_entry_validation(lib):
     assert step(nqh=24) == kvq8.ERR_UNSUPPORTED
     assert step(ws_bytes=need - 1) == kvq8.ERR_WORKSPACE
     assert step(qh=None, batch=0) == kvq8.OK
+
+
+def test_selftest_bounded_wait_validation(lib):
+    f = lib.kvq8_selftest_bounded_wait
+    assert f(None, 10**6, None, None) == kvq8.ERR_INVALID_ARG           # no status word
+    assert f(FAKE + 2, 10**6, None, None) == kvq8.ERR_INVALID_ARG       # misaligned status word
+    assert f(FAKE, 10**6, FAKE + 4, None) == kvq8.ERR_INVALID_ARG       # misaligned time word
+    assert f(FAKE, 999, None, None) == kvq8.ERR_INVALID_ARG             # bound below 1 us
+    assert f(FAKE, 10**10 + 1, None, None) == kvq8.ERR_INVALID_ARG      # bound above 10 s
 
 
 def test_quantize_q_validation(lib):

@@ -303,6 +303,24 @@ def test_bad_ctx_len_is_flagged_and_clamped(gpu_lib):
     assert_close(out[0], case.oracle_unit(0, 0))
 
 
+def test_bounded_wait_gives_up_and_the_context_stays_usable(gpu_lib):
+    # the decode kernels' wait routine on a barrier phase that nothing completes:
+    # it must give up after its bound, flag the timeout and return
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    waited = torch.zeros(1, dtype=torch.int64, device="cuda")
+    kvq8.selftest_bounded_wait(2_000_000, status, waited)
+    torch.cuda.synchronize()
+    assert status.item() == kvq8.DEV_TIMEOUT
+    assert 2_000_000 <= waited.item() < 1_000_000_000
+    # the context still works: a decode right after it matches the oracle
+    cfg = _unit_cfg(2, nkv=2, batch=1, ctx=700, cid=195)
+    case = Case(cfg)
+    out = case.decode()
+    assert case.status_bits() == 0
+    for h in range(cfg.nkv):
+        assert_close(out[0, 2 * h:2 * h + 2], case.oracle_unit(0, h))
+
+
 def test_append_bad_position_is_flagged(gpu_lib):
     nkv = 1
     cache = kvq8.alloc_cache(2, nkv)
