@@ -15,11 +15,13 @@
 // for K and for V: 160 bytes per (token, kv head).
 //
 // Decode: one CTA per (split, kv head, sequence), 4 warps walking the split in
-// 32-token chunks, each warp with its own online-softmax state.  Lane = token
-// for Q.K: s = sm_scale * sum_g scale_g * (sum_{d in g} q_d c_d - zero_g *
-// sum_{d in g} q_d), i.e. exactly q . dequant(k); lane = 4 dims for P.V.  The
-// warps' states are merged into one partial record per query head, in the
-// record format of the q8 decode, so the same combine kernel finishes it.
+// 32-token chunks (each staged by bulk copies), each warp with its own
+// online-softmax state.  Both contractions run on the tensor cores with the
+// codes as fp16 subnormals (the tensor-core decode section below); the score
+// is s = sm_scale * sum_g scale_g * (sum_{d in g} q_d c_d - zero_g *
+// sum_{d in g} q_d), i.e. exactly q . dequant(k).  The warps' states are merged
+// into one partial record per query head, in the record format of the q8
+// decode, so the same combine kernel finishes it.
 #include <cuda_fp16.h>
 #include <math.h>
 
