@@ -413,6 +413,48 @@ def test_int4_nibble_order_high_first():
     assert zero[0] == 0.0 and packed[0] == 0xF0 and not packed[1:].any()
 
 
+def test_int4_round_half_even_ties():
+    # [UltraQuant] §3.2 rounds with torch.round (half to even).  Group 0: min 0,
+    # max 15 -> scale exactly 1, zero 0, so each code is round(x) and x = k + 0.5
+    # is a tie; group 1: min -2.5, max 12.5 -> scale 1 and zero = round(2.5) = 2,
+    # then code = round(x + 2).  Half away from zero would give 1, 2, 3, 4, 14,
+    # 15 and zero 3.
+    x = np.full(128, 7.0, np.float32)
+    x[:8] = [0.0, 15.0, 0.5, 1.5, 2.5, 3.5, 13.5, 14.5]
+    x[64:70] = [-2.5, 12.5, 0.5, -1.5, 1.5, 10.5]
+    packed, scale, zero = oracle.int4_quantize_groups(x, 64)
+    assert scale.tolist() == [1.0, 1.0] and zero.tolist() == [0.0, 2.0]
+    codes = np.stack([packed >> 4, packed & 15], axis=1).reshape(-1)
+    assert codes[:8].tolist() == [0, 15, 0, 2, 2, 4, 14, 14]
+    assert codes[64:70].tolist() == [0, 14, 2, 0, 4, 12]    # rne(-0.5), rne(14.5), rne(2.5), rne(0.5), rne(3.5), rne(12.5)
+    assert np.all(codes[8:64] == 7) and np.all(codes[70:] == 9)
+
+
+def test_int4_codes_are_the_nearest_clamped_integers():
+    # brute force in exact rational arithmetic on the stored fp32 scale and zero:
+    # the code is the integer nearest to x/scale + zero (ties to even), clamped
+    # to [0, 15]; values within 1e-5 of a half-integer are left out (there the
+    # fp32 rounding of x/scale may decide either way)
+    from fractions import Fraction
+    x = _rows(23, 12, 3.0)
+    packed, scale, zero = oracle.int4_quantize_groups(x, 64)
+    codes = np.stack([packed >> 4, packed & 15], axis=-1).reshape(x.shape)
+    checked = 0
+    for r in range(x.shape[0]):
+        for gi in range(2):
+            s, z = Fraction(float(scale[r, gi])), Fraction(float(zero[r, gi]))
+            for d in range(64 * gi, 64 * gi + 64):
+                t = Fraction(float(x[r, d])) / s + z
+                fl = t.numerator // t.denominator
+                frac = t - fl
+                if abs(frac - Fraction(1, 2)) < Fraction(1, 100000):
+                    continue
+                want = min(15, max(0, fl + (1 if frac > Fraction(1, 2) else 0)))
+                assert codes[r, d] == want, (r, d, float(t))
+                checked += 1
+    assert checked > 0.99 * x.size
+
+
 # ---------------------------------------------------------------------------
 # mixed precision by token age (UltraQuant §3.3): old blocks 4-bit, recent int8
 # ---------------------------------------------------------------------------
