@@ -62,7 +62,7 @@ class Int4Case:
 
 def _rows_with_fixtures(n, seed):
     rng = np.random.default_rng(seed)
-    m = max(n, 4)
+    m = max(n, 5)
     x = (rng.standard_normal((m, HD)) * rng.uniform(0.01, 30, (m, 1))).astype(np.float32)
     g = json.load(open(os.path.join(GOLDEN, "int4_group64_hand_example.json")))
     row = np.full(HD, g["row_fill_group0"], np.float32)
@@ -72,7 +72,10 @@ def _rows_with_fixtures(n, seed):
     x[1] = 0.0                                   # all-zero row: both groups constant
     x[2, :64] = np.abs(x[2, :64]) + 1.0          # all-positive group: zero below 0
     x[3, 64:] = -np.abs(x[3, 64:]) - 1.0         # all-negative group: zero above 15
-    return x[:n] if n >= 4 else np.roll(x, -(4 - n), axis=0)[:n]
+    x[4] = 7.0                                   # scale exactly 1 in both groups: ties
+    x[4, :8] = [0.0, 15.0, 0.5, 1.5, 2.5, 3.5, 13.5, 14.5]      # codes on k + 1/2
+    x[4, 64:70] = [-2.5, 12.5, 0.5, -1.5, 1.5, 10.5]          # zero = round(2.5)
+    return x[:n] if n >= 5 else np.roll(x, -(5 - n), axis=0)[:n]
 
 
 @pytest.mark.parametrize("start,n_new", [(0, 1), (5, 37), (250, 300)])
