@@ -40,6 +40,7 @@ if ROOT not in sys.path:
 METRIC = "q8-KV decode attention: μs/step and achieved HBM GB/s (% of GB300 peak)"
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e nominal bandwidth (context beside the measured peak)
 THROTTLE_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
 
@@ -190,11 +191,15 @@ def recorded_traffic(kernel: str, workload: str):
 
 
 def cross_check_traffic(line):
-    """Traffic measured by ncu against the algorithmic bytes of the same launch:
+    """The roofline's fraction of the nominal HBM bandwidth beside the measured
+    one, and the traffic measured by ncu against the algorithmic bytes of the same launch:
     the ratio, and a flag when they differ by more than 5 %: above, bytes read
     more than once; below, bytes served from L2 or writes still in L2 (not yet
     written back) when the kernel ended."""
     r = line.get("roofline", {})
+    if r.get("unit") == "GB/s" and r.get("achieved"):
+        r["nominal_peak"] = NOMINAL_HBM_GBS
+        r["frac_of_nominal"] = round(r["achieved"] / NOMINAL_HBM_GBS, 4)
     if r.get("traffic") and r.get("algorithmic_bytes_per_launch"):
         ratio = r["traffic"] / r["algorithmic_bytes_per_launch"]
         r["traffic_over_algorithmic"] = round(ratio, 4)
