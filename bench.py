@@ -8,18 +8,33 @@ kvq8_decode_step call (two launches: the split kernel, which also appends the
 step's new token, and the merge, whose launch overlaps the split's tail
 through programmatic dependent launch; the three separate entry points --
 append, split, merge -- called one by one are timed beside it as `unfused`).
-The default workload is the 28-layer
-Qwen3-2B-shaped decode stack (16 query / 8 kv heads, hd 128, context 8192,
-batch 1), its layers folded into the batch dimension of one call.
+The default workload is the 28-layer Qwen3-2B-shaped decode stack (16 query /
+8 kv heads, hd 128, context 8192, batch 1), its layers folded into the batch
+dimension of one call.
 
 Prints one JSON line.  `value` is achieved algorithmic HBM throughput in GB/s
 (bytes a step must move / device time per step) summed over ranks;
 `us_per_step` and `ms_per_step` are the device time of one step.  Inputs are
-resident in HBM; the timed region rotates over several copies of the cache so
+resident in HBM; every timed loop rotates over several copies of the cache so
 that every step streams from HBM (the working set is far above L2).
+
+The dominant kernel's roofline comes from its own loop of at least 500
+back-to-back launches (whatever --steps says), with CUDA events on the
+launching stream around the loop; a second loop with events around every
+launch gives the duration of a launch on its own (what ncu reports per
+launch).  nvidia-smi samples the SM clock and throttle reasons over the
+loaded window (those loops and the timed steps, which follow them).
+
+With the default workload the line also carries `workloads`: the batched
+decode (batch 64, ragged 512-32K), the 128K decode with outlier channels, the
+single-head L=256 case, the bulk append, the INT4 group-64 decode and the
+mixed-precision decode, each timed the same way (K steps, the dominant
+kernel's loops, clocks).
+
 `--impl reference` times the CPU oracle on the host cores instead.
-Multi-GPU runs (torchrun) are independent replicas: the path needs no
-exchange between GPUs.
+`--gpus N` without a launcher around it starts N local ranks itself
+(torch.distributed.run); multi-GPU runs are independent replicas: the path
+needs no exchange between GPUs.
 """
 from __future__ import annotations
 
@@ -28,9 +43,11 @@ import hashlib
 import json
 import math
 import os
+import socket
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -38,24 +55,34 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "q8-KV decode attention: μs/step and achieved HBM GB/s (% of GB300 peak)"
+DEFAULT_WORKLOAD = "qwen3_2b_28layers_ctx8192"
+# the other workloads reported in the default run's `workloads` record
+SUB_WORKLOADS = ("batch64_ctx512to32768", "batch4_ctx131072_outliers", "single_head_l256",
+                 "append_batch8_4096tokens", "int4g64_batch8_ctx32768",
+                 "mixed_qwen3_2b_28layers_ctx8192")
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e nominal bandwidth (context beside the measured peak)
 THROTTLE_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+ROOF_MIN_LAUNCHES = 500     # launches of the dominant kernel's own loops
+ROOF_TARGET_S = 0.3         # device time of the back-to-back loop (at least)
+CLOCK_INTERVAL_MS = 50
 
 
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10000)
-    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("kvq8", "reference"), default="kvq8")
-    ap.add_argument("--workload", default="qwen3_2b_28layers_ctx8192")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--copies", type=int, default=0,
                     help="cache copies to rotate over (0 = enough to exceed 8x L2)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workloads' records in the default run")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = min(steps, 2000)")
     ap.add_argument("--no-f32", action="store_true",
                     help="skip the fp32-KV decode comparator leg")
@@ -101,35 +128,83 @@ def aggregate(per_rank_bytes: float, per_rank_seconds: float, device):
     return total, slowest
 
 
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def self_launch(n: int, argv) -> int:
+    """`--gpus N` run without a launcher: start N local ranks of this script
+    under torch.distributed.run (rendezvous on 127.0.0.1) and return their exit
+    status; rank 0 prints the line."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+           os.path.abspath(__file__), *argv]
+    return subprocess.run(cmd, cwd=ROOT).returncode
+
+
 # ---------------------------------------------------------------- clocks ---
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    """nvidia-smi samples of SM clock and throttle reasons, each stamped with the
+    host time of its arrival; stop() summarises the samples that fell inside
+    the window opened by open() and closed by close()."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, interval_ms: int = CLOCK_INTERVAL_MS):
         self.gpu = gpu_index
+        self.interval = interval_ms
         self.proc = None
+        self.thread = None
         self.error = None
+        self.samples = []
+        self.t0 = self.t1 = None
+        self._first = threading.Event()
 
-    def start(self):
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.monotonic(), line))
+            self._first.set()
+
+    def start(self, wait_s: float = 5.0):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError as e:
             self.error = f"nvidia-smi unavailable: {e}"
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        self._first.wait(wait_s)   # nvidia-smi is up before the loaded window opens
+        return self
+
+    def open(self):
+        self.t0 = time.monotonic()
+
+    def close(self):
+        self.t1 = time.monotonic()
 
     def stop(self):
         if self.proc is None:
             return {"error": self.error or "not started"}
-        time.sleep(0.15)
+        time.sleep(2 * self.interval / 1e3)
         self.proc.terminate()
-        out, _ = self.proc.communicate(timeout=10)
+        try:
+            self.proc.wait(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+        t0 = self.t0 if self.t0 is not None else -math.inf
+        t1 = (self.t1 if self.t1 is not None else math.inf) + 0.5 * self.interval / 1e3
         sm, smax, reasons = [], [], set()
-        for line in out.strip().splitlines():
+        for ts, line in self.samples:
+            if not t0 <= ts <= t1:
+                continue
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -141,10 +216,13 @@ class ClockSampler:
             for name, val in zip(THROTTLE_REASONS, f[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
+        window_ms = None if self.t0 is None or self.t1 is None else round((self.t1 - self.t0) * 1e3, 1)
         if not sm:
-            return {"error": "no samples"}
+            return {"error": "no samples in the loaded window", "window_ms": window_ms}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "window_ms": window_ms,
+                "interval_ms": self.interval,
+                "window": "the dominant kernel's loops and the timed steps right after them"}
 
 
 # ------------------------------------------------------------------ peaks ---
@@ -190,16 +268,26 @@ def recorded_traffic(kernel: str, workload: str):
     return rec.get("per_launch_bytes", {}).get(workload)
 
 
-def cross_check_traffic(line):
-    """The roofline's fraction of the nominal HBM bandwidth beside the measured
-    one, and the traffic measured by ncu against the algorithmic bytes of the same launch:
-    the ratio, and a flag when they differ by more than 5 %: above, bytes read
-    more than once; below, bytes served from L2 or writes still in L2 (not yet
-    written back) when the kernel ended."""
-    r = line.get("roofline", {})
-    if r.get("unit") == "GB/s" and r.get("achieved"):
+def finish_roofline(r: dict, us_per_step: float, clocks: dict, peak: float, peak_kind: str) -> dict:
+    """Fill the derived fields of a roofline record: achieved GB/s and its
+    fraction of the measured and the nominal peak, clock-normalised time, the
+    traffic check -- and refuse the figure when the kernel's mean launch is
+    longer than the whole step that contains it (an inconsistent measurement)."""
+    us = r["us_per_launch"]
+    r["peak"], r["peak_kind"], r["unit"] = peak, peak_kind, "GB/s"
+    if r.get("part_of_step", True) and us > us_per_step * 1.0005:
+        r["achieved"] = r["frac"] = None
+        r["rejected"] = (f"mean launch {us:.2f} us exceeds the step {us_per_step:.2f} us that contains it: "
+                         "not a valid roofline figure")
+    else:
+        achieved = r["algorithmic_bytes_per_launch"] / (us * 1e-6) / 1e9
+        r["achieved"] = round(achieved, 2)
+        r["frac"] = round(achieved / peak, 4)
         r["nominal_peak"] = NOMINAL_HBM_GBS
-        r["frac_of_nominal"] = round(r["achieved"] / NOMINAL_HBM_GBS, 4)
+        r["frac_of_nominal"] = round(achieved / NOMINAL_HBM_GBS, 4)
+    if isinstance(clocks, dict) and clocks.get("sm_mhz"):
+        r["sm_mhz_median"] = clocks["sm_mhz"]
+        r["us_x_sm_mhz"] = round(us * clocks["sm_mhz"], 1)   # SM cycles per launch at the median clock
     if r.get("traffic") and r.get("algorithmic_bytes_per_launch"):
         ratio = r["traffic"] / r["algorithmic_bytes_per_launch"]
         r["traffic_over_algorithmic"] = round(ratio, 4)
@@ -210,7 +298,7 @@ def cross_check_traffic(line):
                                   "still in L2 at the kernel's end")
         else:
             r["traffic_check"] = "within 5 % of the algorithmic bytes"
-    return line
+    return r
 
 
 # ------------------------------------------------------------- workloads ---
@@ -238,7 +326,20 @@ def f32_decode_bytes(cfg, lens):
     return tok * cfg.nkv * 2 * cfg.hd * 4 + 2 * cfg.batch * cfg.nqh * cfg.hd * 4
 
 
-def workload_config(cfg, lens, copies):
+def q8_cache_bytes(num_blocks: int, nkv: int, hd: int = 128) -> int:
+    """Bytes of one int8 cache (both pools and both scale arrays)."""
+    return num_blocks * nkv * 256 * (2 * hd + 8)
+
+
+def q8_copies(cache_bytes: int, requested: int = 0):
+    """(copies to rotate over, L2-resident?): enough copies that the working set
+    exceeds 8x L2; a cache of a few hundred KB stays in L2 by construction."""
+    l2_resident = cache_bytes * 8 < L2_BYTES // 16
+    return requested or (1 if l2_resident else max(2, math.ceil(8 * L2_BYTES / cache_bytes))), l2_resident
+
+
+def workload_config(cfg, lens, copies, world, sbytes):
+    """The `config` of a q8 decode line (the same dict in both arms)."""
     import numpy as np
     c = {"workload": cfg.name, "layers_folded_into_batch": cfg.layers,
          "batch": cfg.batch // max(cfg.layers, 1), "nqh": cfg.nqh, "nkv": cfg.nkv, "hd": cfg.hd,
@@ -246,9 +347,24 @@ def workload_config(cfg, lens, copies):
          [int(lens.min()), int(lens.max())], "tokens": int(np.asarray(lens).sum()),
          "step": "append 1 token per (layer, kv head) + split-KV decode + merge",
          "block_table": "seeded shuffled physical blocks"}
-    if copies:
+    if copies == 1:
+        c["l2"] = "one cache copy: L2-resident by construction, latency-bound"
+    else:
         c["l2"] = f"rotates {copies} cache copies; working set >> 129 MB L2, no flush"
+    c["parallelism"] = f"replicas{world}"
+    c["bytes_per_step"] = sbytes
+    c["arithmetic"] = "int8 x int8 -> int32 block dots, fp32 softmax and accumulation"
     return c
+
+
+def q8_decode_config(cfg, world):
+    """Everything the q8 decode `config` depends on, from the workload alone
+    (no device work): lens, the table's pool size, the rotation."""
+    from int8_quantized_kv_gb300 import workloads as wl
+    lens = wl.ctx_lens(cfg)
+    _, num_blocks = wl.block_table(cfg, lens)
+    copies, l2_resident = q8_copies(q8_cache_bytes(num_blocks, cfg.nkv, cfg.hd))
+    return lens, copies, l2_resident, workload_config(cfg, lens, copies, world, step_bytes(cfg, lens))
 
 
 # ------------------------------------------------------------ CPU oracle ---
@@ -343,26 +459,132 @@ def cpu_baseline(cfg, lens, target_seconds):
                             "sample": f"{len(units1)} units ({frac1:.1%} of the step's tokens), once"}}
 
 
-# ---------------------------------------------------------------- kvq8 arm ---
-def run_kvq8(args, rank, world, local):
+# ---------------------------------------------------------- GPU harness ---
+class Gpu:
+    """Per-rank device state shared by the workload runners."""
+
+    def __init__(self, args, rank, world, local):
+        import torch
+        self.args, self.rank, self.world, self.local = args, rank, world, local
+        self.dev = torch.device("cuda", local)
+        torch.cuda.set_device(self.dev)
+        dist_init(world, "nccl")
+        from int8_quantized_kv_gb300 import kvq8
+        kvq8.load()
+        self.stream = torch.cuda.current_stream(self.dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.dev)
+
+    def check_status(self, where: str):
+        v = int(self.status.item())
+        if v != 0:
+            raise RuntimeError(f"device status {v:#x} {where}")
+
+    def event(self):
+        import torch
+        return torch.cuda.Event(enable_timing=True)
+
+    def loop_s(self, fn, n: int, first: int = 0) -> float:
+        """Device seconds per call of fn(i), i = first .. first+n-1, back to back
+        (one pair of events around the whole loop)."""
+        import torch
+        e0, e1 = self.event(), self.event()
+        torch.cuda.synchronize()
+        e0.record(self.stream)
+        for i in range(first, first + n):
+            fn(i)
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / n
+
+    def isolated_s(self, fn, n: int) -> float:
+        """Mean device seconds of one call of fn(i) with events right around it,
+        over n calls: the duration of a launch on its own."""
+        import torch
+        evs = [(self.event(), self.event()) for _ in range(n)]
+        torch.cuda.synchronize()
+        for i, (a, b) in enumerate(evs):
+            a.record(self.stream)
+            fn(i)
+            b.record(self.stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs) / 1e3 / n
+
+    def measure(self, step, kernel_call, kernel_name, kernel_bytes, sbytes, launches_per_step,
+                part_of_step=True):
+        """The timing protocol of every workload.  After the warm-up steps: the
+        clock sampler starts; the dominant kernel's call runs in its own loops
+        (back to back for at least ROOF_TARGET_S and ROOF_MIN_LAUNCHES launches;
+        then ROOF_MIN_LAUNCHES launches each between its own events); then
+        exactly --steps steps run between one pair of events (barrier and
+        synchronize on both sides).  Returns (per-rank step seconds, whole-job
+        bytes, slowest rank's seconds, roofline record, clocks)."""
+        import torch
+        args = self.args
+        for i in range(max(3, args.warmup)):
+            step(i)
+        torch.cuda.synchronize()
+        self.check_status("during warm-up")
+        est = self.loop_s(kernel_call, 3)
+        n_b2b = max(ROOF_MIN_LAUNCHES, int(math.ceil(ROOF_TARGET_S / max(est, 1e-7))))
+        sampler = ClockSampler(self.local).start()
+        sampler.open()
+        b2b = self.loop_s(kernel_call, n_b2b)
+        iso = self.isolated_s(kernel_call, ROOF_MIN_LAUNCHES)
+        t_start, t_end = self.event(), self.event()
+        barrier()
+        torch.cuda.synchronize()
+        t_start.record(self.stream)
+        for i in range(args.steps):
+            step(i)
+        t_end.record(self.stream)
+        torch.cuda.synchronize()
+        sampler.close()
+        barrier()
+        clocks = sampler.stop()
+        self.check_status("in the timed region")
+        elapsed = t_start.elapsed_time(t_end) / 1e3
+        total, slowest = aggregate(sbytes * args.steps, elapsed, self.dev)
+        roof = {"bound": "hbm", "kernel": kernel_name, "algorithmic_bytes_per_launch": kernel_bytes,
+                "us_per_launch": round(b2b * 1e6, 3), "launches": n_b2b,
+                "us_per_launch_isolated": round(iso * 1e6, 3), "launches_isolated": ROOF_MIN_LAUNCHES,
+                "timing": ("us_per_launch: mean of a loop of back-to-back launches rotating the cache "
+                           "copies (CUDA events on the launching stream around the loop); "
+                           "us_per_launch_isolated: mean over launches each between its own events"),
+                "part_of_step": part_of_step}
+        return elapsed / args.steps, total, slowest, roof, clocks, launches_per_step * args.steps
+
+
+def finish_line(gpu, line, roof, clocks, us_per_step, traffic):
+    peak, kind = hbm_peak()
+    roof["traffic"] = traffic
+    line["roofline"] = finish_roofline(roof, us_per_step, clocks, peak, kind)
+    line["pct_of_hbm_peak"] = round(100 * (line["value"] / gpu.world) / peak, 2)
+    line["clocks"] = clocks
+    return line
+
+
+def base_line(gpu, value, steps, slowest, dtype, config):
+    per_step = slowest / steps
+    return {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": gpu.world,
+            "steps": steps, "warmup": gpu.args.warmup, "ms_per_step": round(per_step * 1e3, 5),
+            "us_per_step": round(per_step * 1e6, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": dtype, "data": "synthetic", "config": config}
+
+
+# ------------------------------------------------------------- q8 decode ---
+def bench_q8(gpu, cfg, full):
+    """The q8 decode step (kvq8_decode_step) on a decode workload."""
     import numpy as np
     import torch
     from int8_quantized_kv_gb300 import kvq8
     from int8_quantized_kv_gb300 import workloads as wl
-
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    dist_init(world, "nccl")
-    kvq8.load()
-    cfg = wl.WORKLOADS[args.workload]
-    lens = wl.ctx_lens(cfg)
+    args, dev, stream, status = gpu.args, gpu.dev, gpu.stream, gpu.status
+    lens, copies, l2_resident, config = q8_decode_config(cfg, gpu.world)
+    if args.copies:
+        copies = args.copies
+        config = workload_config(cfg, lens, copies, gpu.world, step_bytes(cfg, lens))
     table, num_blocks = wl.block_table(cfg, lens)
     max_blocks = table.shape[1]
-    cache_bytes = 2 * kvq8.kv_pool_bytes(num_blocks, cfg.nkv) + 2 * kvq8.scale_pool_bytes(num_blocks, cfg.nkv)
-    # a cache of a few hundred KB (the single-head case) stays in L2 by
-    # construction: latency-bound, timed as it is, no roofline claim
-    l2_resident = cache_bytes * 8 < L2_BYTES // 16
-    copies = args.copies or (1 if l2_resident else max(2, math.ceil(8 * L2_BYTES / cache_bytes)))
     sm = 1.0 / math.sqrt(cfg.hd)
 
     # fill cache copy 0 with the first L-1 tokens of every sequence; the step
@@ -374,7 +596,7 @@ def run_kvq8(args, rank, world, local):
     zero = torch.zeros(1, dtype=torch.int32, device=dev)
     # the fp32 comparator cache holds the same L tokens (the q8 cache has token
     # L-1 after the first step)
-    cf = None if args.no_f32 else kvq8.alloc_cachef32(num_blocks, cfg.nkv, dev)
+    cf = None if (args.no_f32 or not full) else kvq8.alloc_cachef32(num_blocks, cfg.nkv, dev)
     for b in range(cfg.batch):
         L = int(lens[b])
         k, v = wl.seq_kv(cfg, b, L)
@@ -386,36 +608,22 @@ def run_kvq8(args, rank, world, local):
         if cf is not None and L > 0:
             kvq8.appendf32(torch.from_numpy(k[None]).to(dev), torch.from_numpy(v[None]).to(dev), zero,
                            table_d[b:b + 1], cf)
-    caches = [c0]
-    for _ in range(copies - 1):
-        caches.append(kvq8.KVCache(*[t.clone() for t in c0]))
+    caches = [c0] + [kvq8.KVCache(*[t.clone() for t in c0]) for _ in range(copies - 1)]
     q_d = torch.from_numpy(wl.queries(cfg)).to(dev)
     nk_d, nv_d = torch.from_numpy(new_k).to(dev), torch.from_numpy(new_v).to(dev)
     start_d = torch.from_numpy((lens - 1).clip(min=0).astype(np.int32)).to(dev)
     lens_d = torch.from_numpy(lens).to(dev)
     ws = kvq8.alloc_workspace(cfg.batch, cfg.nqh, cfg.nkv, max_blocks, dev)
     out = torch.empty_like(q_d)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
     nk1, nv1 = nk_d[:, 0], nv_d[:, 0]   # the step's token, [batch][nkv][hd]
 
-    def step(i, ev=None):
-        c = caches[i % copies]
-        if ev is None:
-            kvq8.decode_step(q_d, nk1, nv1, c, table_d, lens_d, out, ws, sm_scale=sm,
-                             dev_status=status, stream=stream)
-        else:
-            # the step's work as three calls through their own entry points
-            # (append, split, combine), with events around the split kernel
-            # (the roofline's dominant kernel)
-            kvq8.quantize_append(nk_d, nv_d, start_d, table_d, c, dev_status=status, stream=stream)
-            ev[0].record(stream)
-            kvq8.decode_split(q_d, c, table_d, lens_d, ws, sm_scale=sm, dev_status=status,
-                              stream=stream)
-            ev[1].record(stream)
-            kvq8.decode_combine(cfg.batch, cfg.nqh, cfg.nkv, max_blocks, lens_d, ws, out,
-                                stream=stream)
+    def step(i):
+        kvq8.decode_step(q_d, nk1, nv1, caches[i % copies], table_d, lens_d, out, ws, sm_scale=sm,
+                         dev_status=status, stream=stream)
+
+    def split(i):
+        kvq8.decode_split(q_d, caches[i % copies], table_d, lens_d, ws, sm_scale=sm, dev_status=status,
+                          stream=stream)
 
     def unfused_step(i):
         c = caches[i % copies]
@@ -423,60 +631,34 @@ def run_kvq8(args, rank, world, local):
         kvq8.decode_split(q_d, c, table_d, lens_d, ws, sm_scale=sm, dev_status=status, stream=stream)
         kvq8.decode_combine(cfg.batch, cfg.nqh, cfg.nkv, max_blocks, lens_d, ws, out, stream=stream)
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    if status.item() != 0:
-        raise RuntimeError(f"device status {status.item():#x} during warm-up")
-
-    # device-timed region: K steps; every k_sample-th step runs as three calls
-    # with events around the split kernel for its roofline (a recorded event
-    # costs the stream about a microsecond, so not every step carries them)
-    k_sample = 10
-    split_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(0, args.steps, k_sample)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local)
-    barrier()
-    torch.cuda.synchronize()
-    sampler.start()
-    t_start.record(stream)
-    for i in range(args.steps):
-        step(i, split_ev[i // k_sample] if i % k_sample == 0 else None)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    clocks = sampler.stop()
-    barrier()
-    elapsed = t_start.elapsed_time(t_end) / 1e3
-    split_s = sum(a.elapsed_time(b) for a, b in split_ev) / 1e3 / len(split_ev)
-    launches = 2 * args.steps + len(split_ev)   # sampled steps run three calls
+    sbytes = step_bytes(cfg, lens)
+    split_bytes = split_kernel_bytes(cfg, lens)
+    per_step_s, total, slowest, roof, clocks, launches = gpu.measure(
+        step, split, "decode_split_kernel", split_bytes, sbytes, 2)
+    line = base_line(gpu, total / slowest / 1e9, args.steps, slowest, "int8", config)
+    line["gpu_launches"] = launches
+    finish_line(gpu, line, roof, clocks, line["us_per_step"],
+                recorded_traffic("decode_split_kernel", cfg.name))
+    if l2_resident:
+        line["roofline"]["note"] = "L2-resident, latency-bound case: no roofline claim"
+        line["roofline"]["achieved"] = line["roofline"]["frac"] = None
+    if not full:
+        return line
 
     # the same step as three launches (append, split, combine), for comparison
     n_unf = min(args.steps, 1000)
     for i in range(3):
         unfused_step(i)
-    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    u0.record(stream)
-    for i in range(n_unf):
-        unfused_step(i)
-    u1.record(stream)
-    torch.cuda.synchronize()
-    unfused_us = u0.elapsed_time(u1) * 1e3 / n_unf
-
-    sbytes = step_bytes(cfg, lens)
-    total_bytes, slowest = aggregate(sbytes * args.steps, elapsed, dev)
-    per_step = slowest / args.steps
-    value = total_bytes / slowest / 1e9
+    line["unfused"] = {"us_per_step": round(gpu.loop_s(unfused_step, n_unf) * 1e6, 2),
+                       "launches_per_step": 3, "calls_per_step": 3, "steps": n_unf,
+                       "path": "kvq8_quantize_append + kvq8_decode_split + kvq8_decode_combine"}
 
     # end to end: pinned host inputs in, result out, through the public calls
     e2e_steps = args.e2e_steps or min(args.steps, 2000)
     q_h = torch.from_numpy(wl.queries(cfg)).pin_memory()
     nk_h, nv_h = torch.from_numpy(new_k).pin_memory(), torch.from_numpy(new_v).pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-
     nk1_h, nv1_h = nk_h[:, 0], nv_h[:, 0]
-
     # a serving loop binds its buffers once (kvq8.DecodeStep) and makes one C
     # call per step; page-locked host buffers are read and written by the
     # kernels directly
@@ -509,63 +691,26 @@ def run_kvq8(args, rank, world, local):
     e2e_checked_s = host_loop(e2e_checked_step, e2e_steps)
     e_total, e_slowest = aggregate(sbytes * e2e_steps, e2e_s, dev)
     _, e_checked_slowest = aggregate(sbytes * e2e_steps, e2e_checked_s, dev)
-    h2d = (q_h.numel() + nk_h.numel() + nv_h.numel()) * 4
-    d2h = out_h.numel() * 4
-
-    if status.item() != 0:
-        raise RuntimeError(f"device status {status.item():#x} in the timed region")
-    comparator = None if cf is None else f32_comparator(args, cfg, lens, cf, q_d, table_d, lens_d, ws,
-                                                        out, status, stream, split_s)
-
-    peak, peak_kind = hbm_peak()
-    split_bytes = split_kernel_bytes(cfg, lens)
-    achieved = split_bytes / split_s / 1e9
-    traffic = recorded_traffic("decode_split_kernel", cfg.name)
-    line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 5),
-        "us_per_step": round(per_step * 1e6, 2), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int8", "data": "synthetic",
-        "config": dict(workload_config(cfg, lens, copies), parallelism=f"replicas{world}",
-                       bytes_per_step=sbytes,
-                       arithmetic="int8 x int8 -> int32 block dots, fp32 softmax and accumulation"),
-        "pct_of_hbm_peak": round(100 * (value / world) / peak, 2),
-        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel",
-                     "achieved": round(achieved, 2),
-                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "peak_kind": peak_kind, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": split_bytes,
-                     "us_per_launch": round(split_s * 1e6, 3)},
-        "e2e": {"value": round(e_total / e_slowest / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "us_per_step": round(e_slowest / e2e_steps * 1e6, 2), "steps": e2e_steps,
-                "path": ("kvq8.DecodeStep.run_host: one C call on buffers bound once; "
-                         + ("the kernels read Q and the new token from page-locked host memory and "
-                            "write the result there" if runners[0].host_direct else
-                            "copies through the device buffers")),
-                "checked_call_us_per_step": round(e_checked_slowest / e2e_steps * 1e6, 2)},
-        "gpu_launches": launches,
-        "unfused": {"us_per_step": round(unfused_us, 2), "launches_per_step": 3, "calls_per_step": 3,
-                    "path": "kvq8_quantize_append + kvq8_decode_split + kvq8_decode_combine"},
-        "clocks": clocks,
-    }
-    if comparator is not None:
-        line["fp32_kv_comparator"] = comparator
-    if l2_resident:
-        line["config"]["l2"] = (f"one cache copy of {cache_bytes / 1024:.0f} KiB: L2-resident by "
-                                "construction, latency-bound")
-        line["roofline"]["note"] = "L2-resident, latency-bound case: no roofline claim"
+    gpu.check_status("in the end-to-end steps")
+    line["e2e"] = {"value": round(e_total / e_slowest / 1e9, 2), "unit": "GB/s",
+                   "h2d_bytes_per_step": (q_h.numel() + nk_h.numel() + nv_h.numel()) * 4,
+                   "d2h_bytes_per_step": out_h.numel() * 4,
+                   "us_per_step": round(e_slowest / e2e_steps * 1e6, 2), "steps": e2e_steps,
+                   "path": ("kvq8.DecodeStep.run_host: one C call on buffers bound once; "
+                            + ("the kernels read Q and the new token from page-locked host memory and "
+                               "write the result there" if runners[0].host_direct else
+                               "copies through the device buffers")),
+                   "checked_call_us_per_step": round(e_checked_slowest / e2e_steps * 1e6, 2)}
+    if cf is not None:
+        line["fp32_kv_comparator"] = f32_comparator(gpu, cfg, lens, cf, q_d, table_d, lens_d, ws, out,
+                                                    roof["us_per_launch"] * 1e-6)
     if cfg.layers > 1 and cfg.batch == cfg.layers:
-        line["per_layer_graph"] = per_layer_graph(args, cfg, sbytes, caches[0], q_d, nk1, nv1, table_d,
-                                                  lens_d, out, status, sm, max_blocks)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg, lens, args.cpu_seconds)
-    if rank == 0:
-        print(json.dumps(cross_check_traffic(line)), flush=True)
+        line["per_layer_graph"] = per_layer_graph(gpu, cfg, sbytes, caches[0], q_d, nk1, nv1, table_d,
+                                                  lens_d, out, sm, max_blocks)
+    return line
 
 
-def per_layer_graph(args, cfg, sbytes, cache, q_d, nk1, nv1, table_d, lens_d, out_folded, status, sm,
-                    max_blocks):
+def per_layer_graph(gpu, cfg, sbytes, cache, q_d, nk1, nv1, table_d, lens_d, out_folded, sm, max_blocks):
     """The same step as cfg.layers separate kvq8_decode_step calls, one per
     layer (batch 1 each, its own workspace), captured once in a CUDA graph and
     replayed: the launch form of an engine that runs one layer at a time.  One
@@ -582,7 +727,7 @@ def per_layer_graph(args, cfg, sbytes, cache, q_d, nk1, nv1, table_d, lens_d, ou
     def calls():
         for b in range(n_layers):
             kvq8.decode_step(q_d[b:b + 1], nk1[b:b + 1], nv1[b:b + 1], cache, table_d[b:b + 1],
-                             lens_d[b:b + 1], outs[b:b + 1], wss[b], sm_scale=sm, dev_status=status,
+                             lens_d[b:b + 1], outs[b:b + 1], wss[b], sm_scale=sm, dev_status=gpu.status,
                              stream=s)
 
     s.wait_stream(torch.cuda.current_stream(dev))
@@ -595,15 +740,14 @@ def per_layer_graph(args, cfg, sbytes, cache, q_d, nk1, nv1, table_d, lens_d, ou
     for _ in range(3):
         g.replay()
     torch.cuda.synchronize()
-    n = max(10, min(args.steps, 200))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(20, min(gpu.args.steps, 500))
+    e0, e1 = gpu.event(), gpu.event()
     e0.record()
     for _ in range(n):
         g.replay()
     e1.record()
     torch.cuda.synchronize()
-    if status.item() != 0:
-        raise RuntimeError(f"device status {status.item():#x} in the per-layer calls")
+    gpu.check_status("in the per-layer calls")
     t = e0.elapsed_time(e1) / 1e3 / n
     d = (outs.double() - out_folded.double()).abs()
     return {"us_per_step": round(t * 1e6, 2), "value": round(sbytes / t / 1e9, 2), "unit": "GB/s",
@@ -612,7 +756,7 @@ def per_layer_graph(args, cfg, sbytes, cache, q_d, nk1, nv1, table_d, lens_d, ou
             "max_abs_diff_vs_folded": float(d.max())}
 
 
-def f32_comparator(args, cfg, lens, cf, q_d, table_d, lens_d, ws, out_q8, status, stream, split_s):
+def f32_comparator(gpu, cfg, lens, cf, q_d, table_d, lens_d, ws, out_q8, split_s):
     """The fp32-KV decode over the same context (the unquantised arm of the
     fp32-KV vs q8-KV comparison): its time and bandwidth beside the q8 split
     kernel's, and the per-dimension output delta between the two."""
@@ -620,24 +764,15 @@ def f32_comparator(args, cfg, lens, cf, q_d, table_d, lens_d, ws, out_q8, status
     from int8_quantized_kv_gb300 import kvq8
     sm = 1.0 / math.sqrt(cfg.hd)
     out = torch.empty_like(q_d)
-    n = min(args.steps, 500)
 
-    def run():
-        kvq8.decode_attnf32(q_d, cf, table_d, lens_d, out, ws, sm_scale=sm, dev_status=status,
-                            stream=stream)
+    def run(i):
+        kvq8.decode_attnf32(q_d, cf, table_d, lens_d, out, ws, sm_scale=sm, dev_status=gpu.status,
+                            stream=gpu.stream)
 
-    for _ in range(3):
-        run()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(n):
-        run()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    if status.item() != 0:
-        raise RuntimeError(f"device status {status.item():#x} in the fp32 decode")
-    t = e0.elapsed_time(e1) / 1e3 / n
+    for i in range(3):
+        run(i)
+    t = gpu.loop_s(run, max(20, min(gpu.args.steps, 500)))
+    gpu.check_status("in the fp32 decode")
     nbytes = f32_decode_bytes(cfg, lens)
     d = (out_q8.double() - out.double()).abs()
     return {"path": "kvf32_decode_attn (split + combine)", "us_per_decode": round(t * 1e6, 2),
@@ -660,23 +795,18 @@ def int4_step_bytes(cfg, lens):
             rows * 2 * (cfg.hd * 4 + cfg.hd // 2 + 16))
 
 
-def run_kvq4(args, rank, world, local):
+def bench_q4(gpu, cfg, full):
     """The 4-bit (asymmetric INT4 group-64) cache: a step appends one token per
     (sequence, kv head) and decodes with the fp32 query over the dequantised cache."""
     import numpy as np
     import torch
     from int8_quantized_kv_gb300 import kvq8
     from int8_quantized_kv_gb300 import workloads as wl
-
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    dist_init(world, "nccl")
-    kvq8.load()
-    cfg = wl.WORKLOADS[args.workload]
+    args, dev, stream, status = gpu.args, gpu.dev, gpu.stream, gpu.status
     lens = wl.ctx_lens(cfg)
     table, num_blocks = wl.block_table(cfg, lens)
     max_blocks = table.shape[1]
-    cache_bytes = num_blocks * 256 * kvq8.cache4_bytes_per_token(cfg.nkv)
+    cache_bytes = num_blocks * 256 * cfg.nkv * 2 * (cfg.hd // 2 + 16)
     copies = args.copies or max(2, math.ceil(8 * L2_BYTES / cache_bytes))
     sm = 1.0 / math.sqrt(cfg.hd)
     c0 = kvq8.alloc_cache4(num_blocks, cfg.nkv, dev)
@@ -699,54 +829,39 @@ def run_kvq4(args, rank, world, local):
     lens_d = torch.from_numpy(lens).to(dev)
     ws = kvq8.alloc_workspace(cfg.batch, cfg.nqh, cfg.nkv, max_blocks, dev)
     out = torch.empty_like(q_d)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream(dev)
 
-    def step(i, ev=None, bufs=None):
+    def step(i, bufs=None):
         qq, kk, vv, oo = bufs or (q_d, nk_d, nv_d, out)
         c = caches[i % copies]
         kvq8.quantize_append4(kk, vv, start_d, table_d, c, dev_status=status, stream=stream)
-        if ev is not None:
-            ev[0].record(stream)
-        kvq8.decode_attn4(qq, c, table_d, lens_d, oo, ws, sm_scale=sm, dev_status=status,
-                          stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
+        kvq8.decode_attn4(qq, c, table_d, lens_d, oo, ws, sm_scale=sm, dev_status=status, stream=stream)
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    if status.item() != 0:
-        raise RuntimeError(f"device status {status.item():#x} during warm-up")
-    k_sample = 10
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(0, args.steps, k_sample)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local)
-    barrier()
-    torch.cuda.synchronize()
-    sampler.start()
-    t_start.record(stream)
-    for i in range(args.steps):
-        step(i, evs[i // k_sample] if i % k_sample == 0 else None)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    clocks = sampler.stop()
-    barrier()
-    if status.item() != 0:
-        raise RuntimeError(f"device status {status.item():#x} in the timed region")
-    elapsed = t_start.elapsed_time(t_end) / 1e3
-    dec_s = sum(a.elapsed_time(b) for a, b in evs) / 1e3 / len(evs)
+    def decode(i):
+        kvq8.decode_attn4(q_d, caches[i % copies], table_d, lens_d, out, ws, sm_scale=sm,
+                          dev_status=status, stream=stream)
+
     sbytes = int4_step_bytes(cfg, lens)
-    total_bytes, slowest = aggregate(sbytes * args.steps, elapsed, dev)
-    per_step = slowest / args.steps
-    value = total_bytes / slowest / 1e9
+    dec_bytes = sbytes - cfg.batch * cfg.nkv * 2 * (cfg.hd * 4 + cfg.hd // 2 + 16)
+    per_step_s, total, slowest, roof, clocks, launches = gpu.measure(
+        step, decode, "kvq4_decode_attn (int4 split + combine)", dec_bytes, sbytes, 3)
+    config = {"workload": cfg.name, "batch": cfg.batch, "nqh": cfg.nqh, "nkv": cfg.nkv, "hd": cfg.hd,
+              "block_size": 256, "ctx": int(lens.max()), "tokens": int(lens.sum()),
+              "step": "append 1 token per (sequence, kv head) + INT4 split-KV decode + merge",
+              "block_table": "seeded shuffled physical blocks",
+              "l2": f"rotates {copies} cache copies; working set >> 129 MB L2, no flush",
+              "parallelism": f"replicas{gpu.world}", "bytes_per_step": sbytes,
+              "format": "asymmetric INT4 group-64 cache",
+              "arithmetic": "fp32 query x dequantised codes, fp32 softmax and accumulation"}
+    line = base_line(gpu, total / slowest / 1e9, args.steps, slowest, "int4", config)
+    line["gpu_launches"] = launches
+    finish_line(gpu, line, roof, clocks, line["us_per_step"], recorded_traffic("kvq4_decode_attn", cfg.name))
+    if not full:
+        return line
 
     e2e_steps = args.e2e_steps or min(args.steps, 2000)
     q_h = torch.from_numpy(wl.queries(cfg)).pin_memory()
     nk_h, nv_h = torch.from_numpy(new_k).pin_memory(), torch.from_numpy(new_v).pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-
     # the same public calls on the page-locked host buffers: the kernels read the
     # query and the new token there and write the result there (no copies)
     host_bufs = tuple(kvq8.HostMapped(t) for t in (q_h, nk_h, nv_h, out_h))
@@ -763,33 +878,14 @@ def run_kvq4(args, rank, world, local):
         e2e_step(i)
     e2e_s = time.perf_counter() - t0
     e_total, e_slowest = aggregate(sbytes * e2e_steps, e2e_s, dev)
-    peak, peak_kind = hbm_peak()
-    dec_bytes = sbytes - cfg.batch * cfg.nkv * 2 * (cfg.hd * 4 + cfg.hd // 2 + 16)
-    achieved = dec_bytes / dec_s / 1e9
-    line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 5),
-        "us_per_step": round(per_step * 1e6, 2), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int4", "data": "synthetic",
-        "config": dict(workload_config(cfg, lens, copies), parallelism=f"replicas{world}",
-                       bytes_per_step=sbytes, format="asymmetric INT4 group-64 cache",
-                       arithmetic="fp32 query x dequantised codes, fp32 softmax and accumulation"),
-        "pct_of_hbm_peak": round(100 * (value / world) / peak, 2),
-        "roofline": {"bound": "hbm", "kernel": "kvq4_decode_attn (int4 split + combine)",
-                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                     "traffic": recorded_traffic("kvq4_decode_attn", cfg.name),
-                     "algorithmic_bytes_per_launch": dec_bytes, "us_per_launch": round(dec_s * 1e6, 3)},
-        "e2e": {"value": round(e_total / e_slowest / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": (q_h.numel() + nk_h.numel() + nv_h.numel()) * 4,
-                "d2h_bytes_per_step": out_h.numel() * 4,
-                "us_per_step": round(e_slowest / e2e_steps * 1e6, 2), "steps": e2e_steps,
-                "path": "kvq4_quantize_append + kvq4_decode_attn on kvq8.HostMapped page-locked buffers: the kernels read the query and the new token and write the result there, no copies"},
-        "gpu_launches": 3 * args.steps,
-        "clocks": clocks,
-    }
-    if rank == 0:
-        print(json.dumps(cross_check_traffic(line)), flush=True)
+    line["e2e"] = {"value": round(e_total / e_slowest / 1e9, 2), "unit": "GB/s",
+                   "h2d_bytes_per_step": (q_h.numel() + nk_h.numel() + nv_h.numel()) * 4,
+                   "d2h_bytes_per_step": out_h.numel() * 4,
+                   "us_per_step": round(e_slowest / e2e_steps * 1e6, 2), "steps": e2e_steps,
+                   "path": ("kvq4_quantize_append + kvq4_decode_attn on kvq8.HostMapped page-locked "
+                            "buffers: the kernels read the query and the new token and write the "
+                            "result there, no copies")}
+    return line
 
 
 # ------------------------------------------------ mixed precision by age ---
@@ -804,29 +900,23 @@ def mixed_step_bytes(cfg, lens, n4):
             2 * cfg.batch * cfg.nqh * cfg.hd * 4)
 
 
-def run_mixed(args, rank, world, local):
+def bench_mixed(gpu, cfg, full):
     """Mixed precision by token age: every sequence's recent blocks in int8, the
     older ones requantised to 4-bit; a step is one decode over both
-    (kvmix_decode_attn: 4-bit split, int8 split, one combine).  The
-    requantisation of a block runs once per 256 generated tokens and is not in
-    the step."""
+    (kvmix_decode_attn).  The requantisation of a block runs once per 256
+    generated tokens and is not in the step."""
     import numpy as np
     import torch
     from int8_quantized_kv_gb300 import kvq8
     from int8_quantized_kv_gb300 import workloads as wl
-
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    dist_init(world, "nccl")
-    kvq8.load()
-    cfg = wl.WORKLOADS[args.workload]
+    args, dev, stream, status = gpu.args, gpu.dev, gpu.stream, gpu.status
     lens = wl.ctx_lens(cfg)
     n4 = wl.mixed_old_blocks(lens)
     table, num_blocks = wl.block_table(cfg, lens)
     max_blocks = table.shape[1]
     table4 = np.random.default_rng(1000 * cfg.config_id + 77).permutation(num_blocks)[:table.size]
     table4 = table4.astype(np.int32).reshape(table.shape)
-    cache_bytes = num_blocks * 256 * (kvq8.cache_bytes_per_token(cfg.nkv) + kvq8.cache4_bytes_per_token(cfg.nkv))
+    cache_bytes = num_blocks * 256 * cfg.nkv * ((2 * cfg.hd + 8) + 2 * (cfg.hd // 2 + 16))
     copies = args.copies or max(2, math.ceil(8 * L2_BYTES / cache_bytes))
     sm = 1.0 / math.sqrt(cfg.hd)
     c8 = kvq8.alloc_cache(num_blocks, cfg.nkv, dev)
@@ -839,7 +929,6 @@ def run_mixed(args, rank, world, local):
         kvq8.quantize_append(torch.from_numpy(k[None]).to(dev), torch.from_numpy(v[None]).to(dev), zero,
                              table_d[b:b + 1], c8)
     n4_d = torch.from_numpy(n4).to(dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
     kvq8.requantize_blocks(c8, table_d, c4, table4_d, torch.zeros_like(n4_d), n4_d, max(1, int(n4.max())),
                            dev_status=status)
     pairs = [(c8, c4)] + [(kvq8.KVCache(*[t.clone() for t in c8]), kvq8.KV4Cache(*[t.clone() for t in c4]))
@@ -848,7 +937,6 @@ def run_mixed(args, rank, world, local):
     lens_d = torch.from_numpy(lens).to(dev)
     ws = kvq8.alloc_mixed_workspace(cfg.batch, cfg.nqh, cfg.nkv, max_blocks, dev)
     out = torch.empty_like(q_d)
-    stream = torch.cuda.current_stream(dev)
 
     def step(i, bufs=None):
         qq, oo = bufs or (q_d, out)
@@ -856,35 +944,24 @@ def run_mixed(args, rank, world, local):
         kvq8.decode_attn_mixed(qq, a, table_d, b4, table4_d, lens_d, n4_d, oo, ws, sm_scale=sm,
                                dev_status=status, stream=stream)
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    if status.item() != 0:
-        raise RuntimeError(f"device status {status.item():#x} during warm-up")
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local)
-    barrier()
-    torch.cuda.synchronize()
-    sampler.start()
-    t_start.record(stream)
-    for i in range(args.steps):
-        step(i)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    clocks = sampler.stop()
-    barrier()
-    if status.item() != 0:
-        raise RuntimeError(f"device status {status.item():#x} in the timed region")
-    elapsed = t_start.elapsed_time(t_end) / 1e3
     sbytes = mixed_step_bytes(cfg, lens, n4)
-    total_bytes, slowest = aggregate(sbytes * args.steps, elapsed, dev)
-    per_step = slowest / args.steps
-    value = total_bytes / slowest / 1e9
+    per_step_s, total, slowest, roof, clocks, launches = gpu.measure(
+        step, step, "kvmix_decode_attn (both splits + combine)", sbytes, sbytes, 3, part_of_step=False)
+    config = dict(workload_config(cfg, lens, copies, gpu.world, sbytes), old_blocks_4bit=int(n4.max()),
+                  recent_blocks_int8=wl.MIXED_RECENT_BLOCKS,
+                  format="old 256-token blocks INT4 group-64 (requantised from int8), recent blocks int8",
+                  step="mixed decode (4-bit split + int8 split + combine); no append")
+    config["arithmetic"] = ("int8 rows: int8 x int8 -> int32 block dots; 4-bit rows: fp32 query x "
+                            "dequantised codes; fp32 softmax and accumulation")
+    line = base_line(gpu, total / slowest / 1e9, args.steps, slowest, "int8+int4", config)
+    line["gpu_launches"] = launches
+    finish_line(gpu, line, roof, clocks, line["us_per_step"], recorded_traffic("kvmix_decode_attn", cfg.name))
+    if not full:
+        return line
 
     e2e_steps = args.e2e_steps or min(args.steps, 2000)
     q_h = torch.from_numpy(wl.queries(cfg)).pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-
     # the same public call on the page-locked host buffers (no copies)
     host_bufs = (kvq8.HostMapped(q_h), kvq8.HostMapped(out_h))
 
@@ -900,48 +977,23 @@ def run_mixed(args, rank, world, local):
         e2e_step(i)
     e2e_s = time.perf_counter() - t0
     e_total, e_slowest = aggregate(sbytes * e2e_steps, e2e_s, dev)
-    peak, peak_kind = hbm_peak()
-    line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 5),
-        "us_per_step": round(per_step * 1e6, 2), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int8+int4", "data": "synthetic",
-        "config": dict(workload_config(cfg, lens, copies), parallelism=f"replicas{world}",
-                       bytes_per_step=sbytes, old_blocks_4bit=int(n4.max()),
-                       recent_blocks_int8=wl.MIXED_RECENT_BLOCKS,
-                       format="old 256-token blocks INT4 group-64 (requantised from int8), recent blocks int8",
-                       step="mixed decode (4-bit split + int8 split + combine); no append"),
-        "pct_of_hbm_peak": round(100 * (value / world) / peak, 2),
-        "roofline": {"bound": "hbm", "kernel": "kvmix_decode_attn (both splits + combine)",
-                     "achieved": round(value / world, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round((value / world) / peak, 4), "peak_kind": peak_kind,
-                     "traffic": recorded_traffic("kvmix_decode_attn", cfg.name),
-                     "algorithmic_bytes_per_launch": sbytes, "us_per_launch": round(per_step * 1e6, 3)},
-        "e2e": {"value": round(e_total / e_slowest / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": q_h.numel() * 4, "d2h_bytes_per_step": out_h.numel() * 4,
-                "us_per_step": round(e_slowest / e2e_steps * 1e6, 2), "steps": e2e_steps,
-                "path": "kvmix_decode_attn on kvq8.HostMapped page-locked buffers: the kernels read the query and write the result there, no copies"},
-        "gpu_launches": 3 * args.steps,
-        "clocks": clocks,
-    }
-    if rank == 0:
-        print(json.dumps(cross_check_traffic(line)), flush=True)
+    line["e2e"] = {"value": round(e_total / e_slowest / 1e9, 2), "unit": "GB/s",
+                   "h2d_bytes_per_step": q_h.numel() * 4, "d2h_bytes_per_step": out_h.numel() * 4,
+                   "us_per_step": round(e_slowest / e2e_steps * 1e6, 2), "steps": e2e_steps,
+                   "path": ("kvmix_decode_attn on kvq8.HostMapped page-locked buffers: the kernels read "
+                            "the query and write the result there, no copies")}
+    return line
 
 
 # ------------------------------------------------------------- bulk append ---
-def run_append(args, rank, world, local):
+def bench_append(gpu, cfg, full):
     """Quantise-append of n_new tokens per sequence (all kv heads) into the q8
     cache: 1288 algorithmic bytes per (token, kv head)."""
     import numpy as np
     import torch
     from int8_quantized_kv_gb300 import kvq8
     from int8_quantized_kv_gb300 import workloads as wl
-
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    dist_init(world, "nccl")
-    kvq8.load()
-    cfg = wl.WORKLOADS[args.workload]
+    args, dev, stream, status = gpu.args, gpu.dev, gpu.stream, gpu.status
     n_new = int(wl.ctx_lens(cfg).max())
     lens = np.full(cfg.batch, n_new, np.int32)
     table, num_blocks = wl.block_table(cfg, lens)
@@ -951,36 +1003,24 @@ def run_append(args, rank, world, local):
     k_d, v_d = torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev)
     start_d = torch.zeros(cfg.batch, dtype=torch.int32, device=dev)
     table_d = torch.from_numpy(table).to(dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream(dev)
 
-    def step():
+    def step(i):
         kvq8.quantize_append(k_d, v_d, start_d, table_d, cache, dev_status=status, stream=stream)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local)
-    barrier()
-    torch.cuda.synchronize()
-    sampler.start()
-    t_start.record(stream)
-    for _ in range(args.steps):
-        step()
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    clocks = sampler.stop()
-    barrier()
-    if status.item() != 0:
-        raise RuntimeError(f"device status {status.item():#x}")
-    elapsed = t_start.elapsed_time(t_end) / 1e3
     rows = cfg.batch * n_new * cfg.nkv
     sbytes = wl.algorithmic_append_bytes(rows, cfg.hd)
-    total_bytes, slowest = aggregate(sbytes * args.steps, elapsed, dev)
-    per_step = slowest / args.steps
-    value = total_bytes / slowest / 1e9
-    peak, peak_kind = hbm_peak()
+    per_step_s, total, slowest, roof, clocks, launches = gpu.measure(
+        step, step, "quantize_append_kernel", sbytes, sbytes, 1, part_of_step=False)
+    config = {"workload": cfg.name, "batch": cfg.batch, "n_new": n_new, "nkv": cfg.nkv,
+              "hd": cfg.hd, "parallelism": f"replicas{gpu.world}", "bytes_per_step": sbytes,
+              "l2": f"inputs {2 * k.nbytes / 2**20:.0f} MiB fp32 >> 129 MB L2, no flush",
+              "step": "quantise-append of every new (token, kv head) row into the int8 cache"}
+    line = base_line(gpu, total / slowest / 1e9, args.steps, slowest, "f32->int8", config)
+    line["gpu_launches"] = launches
+    finish_line(gpu, line, roof, clocks, line["us_per_step"],
+                recorded_traffic("quantize_append_kernel", cfg.name))
+    if not full:
+        return line
     k_h, v_h = torch.from_numpy(k).pin_memory(), torch.from_numpy(v).pin_memory()
     e2e_steps = args.e2e_steps or min(args.steps, 50)
     t0 = time.perf_counter()
@@ -991,28 +1031,55 @@ def run_append(args, rank, world, local):
         stream.synchronize()
     e2e_s = time.perf_counter() - t0
     e_total, e_slowest = aggregate(sbytes * e2e_steps, e2e_s, dev)
-    line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 5),
-        "us_per_step": round(per_step * 1e6, 2), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32->int8", "data": "synthetic",
-        "config": {"workload": cfg.name, "batch": cfg.batch, "n_new": n_new, "nkv": cfg.nkv,
-                   "hd": cfg.hd, "parallelism": f"replicas{world}", "bytes_per_step": sbytes,
-                   "l2": f"inputs {2 * k.nbytes / 2**20:.0f} MiB fp32 >> 129 MB L2, no flush"},
-        "pct_of_hbm_peak": round(100 * (value / world) / peak, 2),
-        "roofline": {"bound": "hbm", "kernel": "quantize_append_kernel", "achieved": round(value / world, 2),
-                     "peak": peak, "unit": "GB/s", "frac": round(value / world / peak, 4),
-                     "peak_kind": peak_kind, "traffic": recorded_traffic("quantize_append_kernel", cfg.name),
-                     "algorithmic_bytes_per_launch": sbytes,
-                     "us_per_launch": round(per_step * 1e6, 3)},
-        "e2e": {"value": round(e_total / e_slowest / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": 2 * k.nbytes, "d2h_bytes_per_step": 0,
-                "us_per_step": round(e_slowest / e2e_steps * 1e6, 2), "steps": e2e_steps},
-        "gpu_launches": args.steps,
-        "clocks": clocks,
-    }
+    line["e2e"] = {"value": round(e_total / e_slowest / 1e9, 2), "unit": "GB/s",
+                   "h2d_bytes_per_step": 2 * k.nbytes, "d2h_bytes_per_step": 0,
+                   "us_per_step": round(e_slowest / e2e_steps * 1e6, 2), "steps": e2e_steps}
+    return line
+
+
+# ------------------------------------------------------------- dispatch ---
+def runner_for(workload: str):
+    if workload.startswith("int4"):
+        return bench_q4
+    if workload.startswith("append"):
+        return bench_append
+    if workload.startswith("mixed"):
+        return bench_mixed
+    return bench_q8
+
+
+def sub_record(line: dict) -> dict:
+    """The compact record of a workload in the default run's `workloads`."""
+    r = line["roofline"]
+    keep = ("kernel", "us_per_launch", "us_per_launch_isolated", "launches", "achieved", "frac",
+            "frac_of_nominal", "us_x_sm_mhz", "traffic", "traffic_over_algorithmic", "algorithmic_bytes_per_launch",
+            "note", "rejected")
+    return {"us_per_step": line["us_per_step"], "GB_per_s": line["value"],
+            "frac": round(line["pct_of_hbm_peak"] / 100, 4), "steps": line["steps"],
+            "dtype": line["dtype"], "gpu_launches": line["gpu_launches"],
+            "roofline": {k: r[k] for k in keep if k in r}, "clocks": line["clocks"],
+            "config": line["config"]}
+
+
+def run_gpu(args, rank, world, local):
+    import torch
+    from int8_quantized_kv_gb300 import workloads as wl
+    gpu = Gpu(args, rank, world, local)
+    cfg = wl.WORKLOADS[args.workload]
+    line = runner_for(args.workload)(gpu, cfg, True)
+    torch.cuda.empty_cache()
+    if args.workload == DEFAULT_WORKLOAD and not args.no_workloads:
+        line["workloads"] = {}
+        for name in SUB_WORKLOADS:
+            rec = runner_for(name)(gpu, wl.WORKLOADS[name], False)
+            line["workloads"][name] = sub_record(rec)
+            torch.cuda.empty_cache()
+    if (rank == 0 and world == 1 and not args.no_cpu_baseline
+            and runner_for(args.workload) is bench_q8):
+        lens = wl.ctx_lens(cfg)
+        line["cpu_baseline"] = cpu_baseline(cfg, lens, args.cpu_seconds)
     if rank == 0:
-        print(json.dumps(cross_check_traffic(line)), flush=True)
+        print(json.dumps(line), flush=True)
 
 
 # ----------------------------------------------------------- reference arm ---
@@ -1023,10 +1090,10 @@ def run_reference(args, rank, world):
         return
     import numpy as np
     from int8_quantized_kv_gb300 import workloads as wl
-    if args.workload.startswith(("int4", "append", "mixed")):
+    if runner_for(args.workload) is not bench_q8:
         raise SystemExit("the reference arm times the q8 decode step; pick a decode workload")
     cfg = wl.WORKLOADS[args.workload]
-    lens = wl.ctx_lens(cfg)
+    lens, copies, _, config = q8_decode_config(cfg, world)
     threads = len(os.sched_getaffinity(0))
     sm = np.float32(1.0 / math.sqrt(cfg.hd))
     budget = 120.0 / max(1, args.steps + args.warmup)
@@ -1047,8 +1114,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int8", "data": "synthetic",
-        "config": dict(workload_config(cfg, lens, 0), parallelism="host cores"),
+        "vs_baseline": None, "dtype": "int8", "data": "synthetic", "config": config,
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -1058,21 +1124,23 @@ def run_reference(args, rank, world):
 
 
 def main(argv=None):
+    argv = list(sys.argv[1:] if argv is None else argv)
     args = parse_args(argv)
-    rank, world, local = dist_env()
     if args.steps < 1 or args.warmup < 0:
-        raise SystemExit("--steps must be >= 1")
+        raise SystemExit("--steps must be >= 1 and --warmup >= 0")
+    if args.gpus < 1:
+        raise SystemExit("--gpus must be >= 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        return self_launch(args.gpus, argv)
+    rank, world, local = dist_env()
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but the launcher started {world} rank(s)")
     if args.impl == "reference":
         run_reference(args, rank, world)
-    elif args.workload.startswith("int4"):
-        run_kvq4(args, rank, world, local)
-    elif args.workload.startswith("append"):
-        run_append(args, rank, world, local)
-    elif args.workload.startswith("mixed"):
-        run_mixed(args, rank, world, local)
     else:
-        run_kvq8(args, rank, world, local)
+        run_gpu(args, rank, world, local)
+    return 0
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main())

@@ -481,16 +481,21 @@ kvq8_status kvf32_decode_attn(const float *q, int batch, int nqh, int nkv, int h
  * split partial results go to a static device array of
  * KVQ8_NOALLOC_SCRATCH_BYTES that every GPU which loads the library holds
  * until the process exits.  The call allocates nothing.
- *   - Sizes whose kvq8_decode_workspace_bytes(...) exceeds
- *     KVQ8_NOALLOC_SCRATCH_BYTES are rejected with KVQ8_ERR_WORKSPACE before
- *     anything is enqueued.
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and remembers it; make
- *     that first call before any stream capture on the device.
+ *   - Arguments are checked exactly as kvq8_decode_attn checks them, in the
+ *     same order; then sizes whose kvq8_decode_workspace_bytes(...) exceeds
+ *     KVQ8_NOALLOC_SCRATCH_BYTES are rejected with KVQ8_ERR_WORKSPACE.  Every
+ *     error returns before anything is enqueued.
+ *   - The first call on a device that passes these checks looks up the
+ *     array's device address (cudaGetSymbolAddress, with that device
+ *     current) and remembers it for that device; make that first call before
+ *     any stream capture on the device.  The address belongs to the device's
+ *     context of that moment: after a cudaDeviceReset of the device, do not
+ *     call this entry point again in the same process.
  *   - All calls share the one array and leave their partial results in it; no
  *     part of it needs to start at zero, since a call writes every record it
- *     reads.  Calls that overlap on the GPU (other streams, other threads)
- *     race on it: serialise them.
+ *     reads, so the results equal kvq8_decode_attn's bit for bit.  Calls that
+ *     overlap on the GPU (other streams, other threads) race on it: serialise
+ *     them.
  */
 kvq8_status kvq8_decode_attn_noalloc(const float *q, int batch, int nqh, int nkv, int hd,
                                      const int8_t *k_pool, const int8_t *v_pool,

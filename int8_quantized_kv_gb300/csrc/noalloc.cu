@@ -25,7 +25,9 @@ void *g_scratch_addr[kMaxDevices];  // device address of g_decode_scratch, per d
 
 // In host code g_decode_scratch names a host-side shadow, not device memory;
 // the kernels must be given the address the runtime reports for the current
-// device.  Looked up once per device, with that device current.
+// device.  Looked up once per device, with that device current, on the first
+// call that reaches the kernels; the address belongs to the device's context
+// of that moment (a cudaDeviceReset discards it, see kvq8.h).
 kvq8_status scratch_for_current_device(void **addr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return KVQ8_ERR_CUDA;
@@ -48,17 +50,18 @@ extern "C" kvq8_status kvq8_decode_attn_noalloc(
     const int8_t *v_pool, const float *k_scale, const float *v_scale, int num_blocks,
     const int32_t *block_table, int max_blocks, int block_size, const int32_t *ctx_lens,
     float sm_scale, float *out, uint32_t *dev_status, void *stream) {
+    // Every argument check of kvq8_decode_attn, in its order: called without a
+    // workspace it returns before enqueuing anything -- an argument error, OK
+    // for an empty batch, or KVQ8_ERR_WORKSPACE once everything else is valid.
+    kvq8_status st = kvq8_decode_attn(q, batch, nqh, nkv, hd, k_pool, v_pool, k_scale, v_scale,
+                                      num_blocks, block_table, max_blocks, block_size, ctx_lens,
+                                      sm_scale, out, nullptr, 0, dev_status, stream);
+    if (st != KVQ8_ERR_WORKSPACE) return st;
     const size_t need =
         kvq8_decode_workspace_bytes(batch, nqh, nkv, hd, max_blocks, block_size);
-    if (need == 0)  // invalid or unsupported sizes: report them exactly as the regular entry point
-        return kvq8_decode_attn(q, batch, nqh, nkv, hd, k_pool, v_pool, k_scale, v_scale,
-                                num_blocks, block_table, max_blocks, block_size, ctx_lens,
-                                sm_scale, out, nullptr, 0, dev_status, stream);
-    if (need > (size_t)KVQ8_NOALLOC_SCRATCH_BYTES) return KVQ8_ERR_WORKSPACE;
-    if (batch == 0) return KVQ8_OK;
+    if (need == 0 || need > (size_t)KVQ8_NOALLOC_SCRATCH_BYTES) return KVQ8_ERR_WORKSPACE;
     void *scratch = nullptr;
-    const kvq8_status st = scratch_for_current_device(&scratch);
-    if (st != KVQ8_OK) return st;
+    if ((st = scratch_for_current_device(&scratch)) != KVQ8_OK) return st;
     return kvq8_decode_attn(q, batch, nqh, nkv, hd, k_pool, v_pool, k_scale, v_scale, num_blocks,
                             block_table, max_blocks, block_size, ctx_lens, sm_scale, out, scratch,
                             (size_t)KVQ8_NOALLOC_SCRATCH_BYTES, dev_status, stream);

@@ -22,3 +22,14 @@ def gpu_lib():
     from int8_quantized_kv_gb300 import kvq8
     kvq8.load()
     return kvq8
+
+
+def pytest_terminal_summary(terminalreporter):
+    """The largest output errors against the oracle, per GPU test."""
+    h = sys.modules.get("kvq8_harness")
+    if h is None or not getattr(h, "ERRORS", None):
+        return
+    tr = terminalreporter
+    tr.write_sep("-", "largest |gpu - oracle| per test (max-abs, relative to max |oracle|)")
+    for test, (err, rel) in sorted(h.ERRORS.items()):
+        tr.write_line(f"{err:10.3e} {rel:10.3e}  {test}")

@@ -140,6 +140,25 @@ def test_decode_validation(lib):
         == kvq8.ERR_INVALID_ARG
 
 
+def test_noalloc_checks_arguments_like_the_regular_entry_point(lib):
+    """kvq8_decode_attn_noalloc reports argument errors exactly as
+    kvq8_decode_attn does, before its scratch-size check and before any device
+    call: an empty batch is a no-op, a null query an argument error and a batch
+    beyond the grid limit unsupported, even for sizes beyond the scratch."""
+    def na(q=FAKE, batch=1, nqh=8, nkv=8, max_blocks=8, out=FAKE):
+        return lib.kvq8_decode_attn_noalloc(q, batch, nqh, nkv, 128, FAKE, FAKE, FAKE, FAKE, 4, FAKE,
+                                            max_blocks, 256, FAKE, 0.088, out, None, None)
+    big = dict(batch=512, nqh=64, max_blocks=512)
+    assert kvq8.decode_workspace_bytes(512, 64, 8, 512) > kvq8.NOALLOC_SCRATCH_BYTES
+    assert na(batch=0) == kvq8.OK
+    assert na(batch=0, max_blocks=0) == kvq8.ERR_INVALID_ARG
+    assert na(q=None, **big) == kvq8.ERR_INVALID_ARG
+    assert na(out=None, **big) == kvq8.ERR_INVALID_ARG
+    assert na(nqh=24) == kvq8.ERR_UNSUPPORTED
+    assert na(batch=65536) == kvq8.ERR_UNSUPPORTED
+    assert na(**big) == kvq8.ERR_WORKSPACE
+
+
 def test_host_buffer_entry_validation(lib):
     """The host-buffer entries check every argument before queueing a copy."""
     def app(**kw):

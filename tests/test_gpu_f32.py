@@ -1,8 +1,8 @@
 """The fp32 K/V cache (the comparator of the int8 cache) against the oracle.
 
 Append is a copy: the cache must hold the input rows bit for bit.  Decode
-outputs must be within 1e-4 + 1e-3*|ref| of fp64 attention over the same fp32
-K/V.  The comparison of [Day 9-3] §1 (one attention over fp32 K/V, the same
+outputs must be within 1e-4 max-abs and 1e-3 relative (max norm) of fp64
+attention over the same fp32 K/V.  The comparison of [Day 9-3] §1 (one attention over fp32 K/V, the same
 attention over the int8 cache, compare per dimension) run on the GPU must
 give the oracle's per-dimension deltas.
 """

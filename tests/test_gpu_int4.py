@@ -1,8 +1,8 @@
 """The 4-bit (asymmetric INT4 group-64) cache path against the oracle.
 
 Codes, scales and zeros must match the oracle's quantiser bit for bit; decode
-outputs (fp32 query over dequantised K/V) must be within 1e-4 + 1e-3*|ref|
-of fp64 attention over the oracle's dequantised K/V.
+outputs (fp32 query over dequantised K/V) must be within 1e-4 max-abs and
+1e-3 relative (max norm) of fp64 attention over the oracle's dequantised K/V.
 """
 import json
 import math

@@ -4,7 +4,7 @@ one decode over both.
 
 Requantised codes, scales and zeros must match the oracle's (INT4 rule applied
 to the int8 rows' fp32 values) bit for bit; decode outputs must be within
-1e-4 + 1e-3*|ref| of the oracle's mixed decode; with no old blocks the result
+1e-4 max-abs and 1e-3 relative (max norm) of the oracle's mixed decode; with no old blocks the result
 is the int8 decode's, with only old blocks the 4-bit decode's, bit for bit.
 """
 import numpy as np

@@ -1,7 +1,8 @@
 """CUDA path vs CPU oracle, through the C ABI, on seeded workloads.
 
 Quantised payloads and scales must match bit for bit; attention outputs must
-be within 1e-4 + 1e-3*|oracle| of the oracle's fp64 result on the same
+be within 1e-4 max-abs and 1e-3 relative (max norm) of the oracle's fp64
+result on the same
 quantised inputs.  Sizes span several tiles and ragged tails; the full-size
 workloads are checked on sampled (sequence, kv head) units.
 """

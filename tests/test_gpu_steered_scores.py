@@ -10,7 +10,7 @@ so the maximum is raised stage after stage in every split; "spike" puts one
 token far above all others two thirds of the way in, so everything
 accumulated before it is rescaled to almost nothing.  Each path (int8, INT4,
 fp32 K/V) is compared with the oracle on the same inputs, within
-1e-4 + 1e-3 * |oracle|, for every GQA group size.
+1e-4 max-abs and 1e-3 relative (max norm), for every GQA group size.
 """
 import numpy as np
 import pytest
