@@ -33,6 +33,15 @@
  * - Rounding: every float->int step rounds half to even in IEEE fp32, and
  *   every fp32 division is IEEE-correct, so quantised codes and scales are
  *   reproducible bit for bit on any IEEE machine.
+ * - Non-finite inputs (the pages state the rules for finite values only): a
+ *   unit of quantisation -- a K/V row of the int8 cache, a 64-value group of
+ *   the 4-bit cache, a 32-value block of the query in the int8 decode --
+ *   that holds a NaN or an infinity is quantised as if all its values were
+ *   zero, and KVQ8_DEV_NONFINITE is set.  So an int8 row gets scale 0 and
+ *   codes 0, a 4-bit group scale 1, zero -0 and codes 0, a query block scale
+ *   1/127 and codes 0; the cache and the outputs stay finite.  The fp32-query
+ *   decodes (4-bit and fp32 caches) and the fp32 cache take their inputs as
+ *   they are: IEEE arithmetic, unflagged.
  * - Supported shapes: hd == 128, block_size == 256, nqh % nkv == 0 with
  *   G = nqh/nkv in {1, 2, 4, 8}.  Anything else returns KVQ8_ERR_UNSUPPORTED.
  *
@@ -81,6 +90,8 @@ typedef enum kvq8_status {
 #define KVQ8_DEV_BAD_POSITION 0x4u   /* append position start_pos[b]+i outside the block table */
 #define KVQ8_DEV_TIMEOUT 0x8u        /* an internal pipeline wait gave up (never expected); the
                                         affected results are unspecified */
+#define KVQ8_DEV_NONFINITE 0x10u     /* a K/V row, a 4-bit group or a query 32-block held a NaN
+                                        or an infinity and was quantised as zeros (see below) */
 
 #define KVQ8_HEAD_DIM 128
 #define KVQ8_BLOCK_SIZE 256
@@ -158,7 +169,8 @@ kvq8_status kvq8_quantize_append_host(const float *k_new_host, const float *v_ne
  * the step the decode performs in its prologue can be checked bit for bit.
  * [Day 9-2] §2 segment 1: per 32-element block qm = max|x| (qm = 1 when
  * qm < 1e-6), block scale = qm * (1/127), code = round_half_even(x * (127/qm))
- * clamped to [-128, 127].
+ * clamped to [-128, 127].  A block holding a NaN or an infinity is quantised
+ * as zeros, as in the decode; this call has no status word to flag it in.
  *
  *   q         fp32 [n_rows][hd]
  *   q_codes   int8 [n_rows][hd]

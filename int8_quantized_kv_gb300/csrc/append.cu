@@ -3,7 +3,8 @@
 //
 // Quantisation rule: [Day 9-3] §2 and [Day 9-1] §2 (kv_quantize_per_head):
 // one fp32 scale = max|v|/127 per (token, kv head) row of 128 values, codes
-// round_half_even(v/scale) in [-127, 127].
+// round_half_even(v/scale) in [-127, 127]; a row holding a NaN or an infinity
+// (outside the rule) is stored as a row of zeros and flagged.
 //
 // Bulk append: one warp per run of 16 consecutive new tokens of one (sequence,
 // kv head), with no shared memory and no block barrier, so that warps stream
@@ -130,7 +131,7 @@ quantize_append_kernel(AppendParams p, int quarters, long long tasks) {
             for (int u = 0; u < 4; ++u) {
                 const int r = 4 * g + u;
                 cp_async_wait<kRing - 2>();   // row r has landed (rows r + 1 .. r + kRing - 2 may not)
-                const float4 xk = slots[rd][0][lane], xv = slots[rd][1][lane];
+                const float4 xks = slots[rd][0][lane], xvs = slots[rd][1][lane];
                 rd = rd + 1 == kRing ? 0 : rd + 1;
                 if (r + kRing - 1 < kRunTok) {   // into the slot of row r - 1, read before
                     cp_async16_cg(&slots[wr][0][lane], kp);
@@ -140,8 +141,9 @@ quantize_append_kernel(AppendParams p, int quarters, long long tasks) {
                     wr = wr + 1 == kRing ? 0 : wr + 1;
                 }
                 cp_async_commit();               // possibly empty: one group per row
-                const float sk = kv_row_scale(row_max_abs(xk));
-                const float sv = kv_row_scale(row_max_abs(xv));
+                float4 xk = xks, xv = xvs;
+                const float sk = kv_row_scale_checked(xk, p.dev_status);
+                const float sv = kv_row_scale_checked(xv, p.dev_status);
                 const uint32_t wk = low_bytes4(kv_code_bytes4(xk, sk));
                 const uint4 cv = kv_code_bytes4(xv, sv);
                 reinterpret_cast<uint32_t *>(krow + r * kHD + ((kchunk ^ (r & 7)) << 4))[kword] = wk;
@@ -175,10 +177,10 @@ quantize_append_kernel(AppendParams p, int quarters, long long tasks) {
         // part of a run (the ends of the appended range): row by row
         for (int r = (int)(lo - r0); r < (int)(hi - r0); ++r) {
             const size_t src = new_row_offset(p, b, h, r0 + r, start);
-            const float4 xk = reinterpret_cast<const float4 *>(p.k_new + src)[lane];
-            const float4 xv = reinterpret_cast<const float4 *>(p.v_new + src)[lane];
-            const float sk = kv_row_scale(row_max_abs(xk));
-            const float sv = kv_row_scale(row_max_abs(xv));
+            float4 xk = reinterpret_cast<const float4 *>(p.k_new + src)[lane];
+            float4 xv = reinterpret_cast<const float4 *>(p.v_new + src)[lane];
+            const float sk = kv_row_scale_checked(xk, p.dev_status);
+            const float sv = kv_row_scale_checked(xv, p.dev_status);
             reinterpret_cast<uint32_t *>(krow + r * kHD + ((kchunk ^ (r & 7)) << 4))[kword] =
                 low_bytes4(kv_code_bytes4(xk, sk));
             const uint4 cv = kv_code_bytes4(xv, sv);
@@ -222,17 +224,17 @@ quantize_append_token_kernel(AppendParams p) {
     const int slot = pos % kBS;
     const size_t src = ((size_t)b * p.nkv + h) * kHD;   // n_new == 1
     const size_t tile = (size_t)phys * p.nkv + h;
-    const float4 xk = reinterpret_cast<const float4 *>(p.k_new + src)[lane];
-    const float4 xv = reinterpret_cast<const float4 *>(p.v_new + src)[lane];
+    float4 xk = reinterpret_cast<const float4 *>(p.k_new + src)[lane];
+    float4 xv = reinterpret_cast<const float4 *>(p.v_new + src)[lane];
     {
-        const float s = kv_row_scale(row_max_abs(xk));
+        const float s = kv_row_scale_checked(xk, p.dev_status);
         unsigned char *row = reinterpret_cast<unsigned char *>(p.k_pool) + (tile * kBS + slot) * kHD;
         reinterpret_cast<uint32_t *>(row + (((lane >> 2) ^ (slot & 7)) << 4))[lane & 3] =
             low_bytes4(kv_code_bytes4(xk, s));
         if (lane == 0) p.k_scale[tile * kBS + slot] = s;
     }
     {
-        const float s = kv_row_scale(row_max_abs(xv));
+        const float s = kv_row_scale_checked(xv, p.dev_status);
         int8_t *vg = p.v_pool + tile * kHD * kBS + (size_t)(slot / kStageTok) * kTileVQuarter + slot % kStageTok;
         const uint4 c = kv_code_bytes4(xv, s);
         vg[(size_t)(4 * lane + 0) * kStageTok] = (int8_t)c.x;
@@ -248,7 +250,8 @@ quantize_q_kernel(const float *__restrict__ q, int64_t n_rows, int8_t *__restric
                   float *__restrict__ scales) {
     const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
     if (row >= n_rows) return;
-    quantize_q_row_warp(q + row * kHD, threadIdx.x & 31, codes + row * kHD, scales + row * kNQB);
+    // (kvq8_quantize_q has no status word: a non-finite block is zeroed unflagged)
+    quantize_q_row_warp(q + row * kHD, threadIdx.x & 31, codes + row * kHD, scales + row * kNQB, nullptr);
 }
 
 }  // namespace

@@ -154,10 +154,10 @@ __device__ __forceinline__ bool slot_turn_bounded(volatile int *done, int round,
 __device__ __noinline__ void append_new_token(const DecodeParams &p, int b, int h, int pos, int t,
                                                  int lane, unsigned char *st) {
     const size_t src = ((size_t)b * p.nkv + h) * kHD;
-    const float4 xk = reinterpret_cast<const float4 *>(p.k_new + src)[lane];
-    const float4 xv = reinterpret_cast<const float4 *>(p.v_new + src)[lane];
+    float4 xk = reinterpret_cast<const float4 *>(p.k_new + src)[lane];
+    float4 xv = reinterpret_cast<const float4 *>(p.v_new + src)[lane];
     const int phys = p.block_table[(size_t)b * p.max_blocks + pos / kBS];   // valid: the stage was copied
-    const float sk = kv_row_scale(row_max_abs(xk)), sv = kv_row_scale(row_max_abs(xv));
+    const float sk = kv_row_scale_checked(xk, p.dev_status), sv = kv_row_scale_checked(xv, p.dev_status);
     const uint32_t wk = low_bytes4(kv_code_bytes4(xk, sk));
     const uint4 cv = kv_code_bytes4(xv, sv);
     const int slot = pos % kBS;   // slot & 7 == t & 7: stages start at multiples of 64
@@ -412,7 +412,7 @@ decode_split_kernel(DecodeParams p) {
 #pragma unroll
             for (int i = 0; i < kQRows; ++i) {
                 const int g = warp + i * kConsumerWarps;
-                if (g < G) quantize_q_vals_warp(qx[i], lane, q_codes + g * kHD, q_scale + g * kNQB);
+                if (g < G) quantize_q_vals_warp(qx[i], lane, q_codes + g * kHD, q_scale + g * kNQB, p.dev_status);
             }
             named_barrier_sync(1, kConsumerWarps * 32);
             if (remaining > seg_n) {   // the next segment's unit follows this one

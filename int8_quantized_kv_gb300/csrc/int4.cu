@@ -55,8 +55,17 @@ __device__ __forceinline__ int int4_code(float x, float s, float z) {
 }
 
 // Quantises one row (lane l holds dims 4l..4l+3) and stores codes + params.
-__device__ __forceinline__ void int4_store_row(const float4 x, uint8_t *codes_row, float *param_row,
-                                               int lane) {
+// A 64-value group holding a NaN or an infinity (outside the rule) is
+// quantised as a group of zeros (scale 1, zero -0, codes 0) and
+// KVQ8_DEV_NONFINITE is set in *status (when non-null).
+__device__ __forceinline__ void int4_store_row(float4 x, uint8_t *codes_row, float *param_row,
+                                               int lane, uint32_t *status) {
+    const uint32_t bad = __ballot_sync(0xffffffffu, nonfinite(x.x) | nonfinite(x.y) | nonfinite(x.z) |
+                                                        nonfinite(x.w));
+    if (bad & (lane < 16 ? 0x0000ffffu : 0xffff0000u)) {   // uniform within the half warp
+        x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if ((lane & 15) == 0) flag_status(status, KVQ8_DEV_NONFINITE);
+    }
     float mx = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
     float mn = fminf(fminf(x.x, x.y), fminf(x.z, x.w));
     mx = half_max(mx);
@@ -93,9 +102,9 @@ int4_append_kernel(Int4AppendParams p) {
     const size_t row = ((size_t)phys * p.nkv + h) * kBS + pos % kBS;
     const size_t src = (((size_t)b * p.n_new + i) * p.nkv + h) * kHD;
     int4_store_row(reinterpret_cast<const float4 *>(p.k_new + src)[lane], p.k_codes + row * kRowBytes,
-                   p.k_param + row * 4, lane);
+                   p.k_param + row * 4, lane, p.dev_status);
     int4_store_row(reinterpret_cast<const float4 *>(p.v_new + src)[lane], p.v_codes + row * kRowBytes,
-                   p.v_param + row * 4, lane);
+                   p.v_param + row * 4, lane, p.dev_status);
 }
 
 // ---- requantisation int8 -> INT4 of whole blocks (mixed precision by token age) ----
@@ -132,7 +141,8 @@ int4_requantize_kernel(Int4RequantParams p) {
         const float sc = p.k_scale[tile8 * kBS + t];
         const float4 x = make_float4(__fmul_rn((float)(int8_t)(w & 0xff), sc), __fmul_rn((float)(int8_t)((w >> 8) & 0xff), sc),
                                      __fmul_rn((float)(int8_t)((w >> 16) & 0xff), sc), __fmul_rn((float)(int8_t)(w >> 24), sc));
-        int4_store_row(x, p.k_codes + (tile4 * kBS + t) * kRowBytes, p.k_param + (tile4 * kBS + t) * 4, lane);
+        int4_store_row(x, p.k_codes + (tile4 * kBS + t) * kRowBytes, p.k_param + (tile4 * kBS + t) * 4, lane,
+                       p.dev_status);
     }
     // V: one 64-token quarter at a time
     for (int qd = 0; qd < kBS / kStageTok; ++qd) {
@@ -153,7 +163,7 @@ int4_requantize_kernel(Int4RequantParams p) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) xs[i] = __fmul_rn((float)(int8_t)vt[(4 * lane + i) * kVtPitch + tq], sc);
             int4_store_row(make_float4(xs[0], xs[1], xs[2], xs[3]), p.v_codes + (tile4 * kBS + t) * kRowBytes,
-                           p.v_param + (tile4 * kBS + t) * 4, lane);
+                           p.v_param + (tile4 * kBS + t) * 4, lane, p.dev_status);
         }
     }
 }

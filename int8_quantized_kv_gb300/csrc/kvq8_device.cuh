@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "kvq8.h"
+
 namespace kvq8 {
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -83,23 +85,45 @@ __device__ __forceinline__ uint32_t low_bytes4(uint4 c) {
     return __byte_perm(__byte_perm(c.x, c.y, 0x0040), __byte_perm(c.z, c.w, 0x0040), 0x5410);
 }
 
-// Max |v| of a row held as a float4 per lane, not-a-number values left out
-// (0 for a row of them).  Non-negative floats order like their bit patterns,
-// so one unsigned warp reduction takes the maximum.
-__device__ __forceinline__ float row_max_abs(float4 x) {
-    const float a = fmaxf(fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))), 0.0f);
-    return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(a)));
+// True when v is a NaN or an infinity (all exponent bits set).
+__device__ __forceinline__ bool nonfinite(float v) {
+    return (__float_as_uint(v) & 0x7f800000u) == 0x7f800000u;
+}
+
+// Scale of a K/V row held as a float4 per lane (lane l: dims 4l..4l+3) by the
+// rule above, with the reading taken for values the pages do not cover: a row
+// holding a NaN or an infinity is quantised as a row of zeros (x is cleared,
+// scale 0, so every code is 0) and KVQ8_DEV_NONFINITE is set.  |v| as a bit
+// pattern: non-negative floats order like their bit patterns, infinity above
+// every finite value and NaN above infinity, so one unsigned warp reduction
+// gives both the row maximum and the test.
+__device__ __forceinline__ float kv_row_scale_checked(float4 &x, uint32_t *status) {
+    const uint32_t a = max(max(__float_as_uint(x.x) & 0x7fffffffu, __float_as_uint(x.y) & 0x7fffffffu),
+                           max(__float_as_uint(x.z) & 0x7fffffffu, __float_as_uint(x.w) & 0x7fffffffu));
+    const uint32_t m = __reduce_max_sync(0xffffffffu, a);
+    if (m >= 0x7f800000u) {   // warp-uniform
+        x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if ((threadIdx.x & 31) == 0) flag_status(status, KVQ8_DEV_NONFINITE);
+        return 0.0f;
+    }
+    return kv_row_scale(__uint_as_float(m));
 }
 
 // 32-block query rule ([Day 9-2] §2 segment 1) for one row of 128 values,
 // executed by one full warp: lane l holds element 32*k + l of block k in x[k].
 // qm = max |x| over the block (1 when below 1e-6); block scale = qm * (1/127);
-// code = round_half_even(x * (127/qm)) clamped to [-128, 127].
+// code = round_half_even(x * (127/qm)) clamped to [-128, 127].  A block that
+// holds a NaN or an infinity is quantised as a block of zeros (scale 1/127,
+// codes 0) and KVQ8_DEV_NONFINITE is set in *status (when non-null).
 __device__ __forceinline__ void quantize_q_vals_warp(const float (&xs)[4], int lane, int8_t *codes,
-                                                     float *scales) {
+                                                     float *scales, uint32_t *status) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const float x = xs[k];
+        float x = xs[k];
+        if (__any_sync(0xffffffffu, nonfinite(x))) {
+            x = 0.0f;
+            if (lane == 0) flag_status(status, KVQ8_DEV_NONFINITE);
+        }
         float qm = warp_max(fabsf(x));
         if (qm < 1e-6f) qm = 1.0f;
         const float iq = __fdiv_rn(127.0f, qm);
@@ -112,11 +136,11 @@ __device__ __forceinline__ void quantize_q_vals_warp(const float (&xs)[4], int l
 
 // The same for a row in global memory.
 __device__ __forceinline__ void quantize_q_row_warp(const float *__restrict__ row, int lane,
-                                                    int8_t *codes, float *scales) {
+                                                    int8_t *codes, float *scales, uint32_t *status) {
     float xs[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) xs[k] = row[32 * k + lane];
-    quantize_q_vals_warp(xs, lane, codes, scales);
+    quantize_q_vals_warp(xs, lane, codes, scales, status);
 }
 
 }  // namespace kvq8

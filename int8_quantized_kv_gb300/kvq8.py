@@ -20,7 +20,7 @@ Q_BLOCK = 32
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024   # KVQ8_NOALLOC_SCRATCH_BYTES in kvq8.h
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = range(5)
-DEV_BAD_BLOCK_ID, DEV_BAD_CTX_LEN, DEV_BAD_POSITION, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+DEV_BAD_BLOCK_ID, DEV_BAD_CTX_LEN, DEV_BAD_POSITION, DEV_TIMEOUT, DEV_NONFINITE = 0x1, 0x2, 0x4, 0x8, 0x10
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int

@@ -31,19 +31,44 @@
 #include "kvq8_oracle.h"
 
 /* ------------------------------------------------------------------------ */
+/* Non-finite inputs.  The pages state every rule for finite values only.   */
+/* Reading taken: a unit of quantisation (a K/V row, a query 32-block, an   */
+/* INT4 group) that holds a NaN or an infinity is quantised exactly as if   */
+/* all of its values were zero; each quantiser returns how many units it    */
+/* replaced so.  With finite input every float->int conversion below sees a */
+/* finite value inside the int range.                                       */
+/* ------------------------------------------------------------------------ */
+static int all_finite(const float *x, int n)
+{
+    for (int i = 0; i < n; ++i)
+        if (!isfinite(x[i]))
+            return 0;
+    return 1;
+}
+
+/* ------------------------------------------------------------------------ */
 /* K/V write path: per-(token, head) max-abs INT8 quantisation.             */
 /* [Day 9-3] §2 (quantisation rule taken from the engine's write path):     */
 /* over the hd values of one (token, head) row take max_abs, scale =       */
 /* max_abs/127, q = round(v/scale) clamped to [-127, 127], one fp32 scale   */
 /* per row; [Day 9-1] §2 (kv_quantize_per_head call, one scale per token    */
-/* per head).  An all-zero row (pages silent) gets scale 0 and codes 0.     */
+/* per head).  An all-zero row (pages silent) gets scale 0 and codes 0; so  */
+/* does a row holding a NaN or an infinity (counted in the return value).   */
 /* ------------------------------------------------------------------------ */
-void orc_kv_quantize_rows(const float *x, int64_t n_rows, int hd,
-                          int8_t *q, float *scale)
+int64_t orc_kv_quantize_rows(const float *x, int64_t n_rows, int hd,
+                             int8_t *q, float *scale)
 {
+    int64_t replaced = 0;
     for (int64_t r = 0; r < n_rows; ++r) {
         const float *v = x + r * (int64_t)hd;
         int8_t *qr = q + r * (int64_t)hd;
+        if (!all_finite(v, hd)) {
+            /* the row of zeros: max_abs 0, scale 0, every code 0 */
+            ++replaced;
+            scale[r] = 0.0f;
+            memset(qr, 0, (size_t)hd);
+            continue;
+        }
         float max_abs = 0.0f;
         for (int i = 0; i < hd; ++i) {
             float a = fabsf(v[i]);
@@ -65,6 +90,7 @@ void orc_kv_quantize_rows(const float *x, int64_t n_rows, int hd,
             qr[i] = (int8_t)(int)c;
         }
     }
+    return replaced;
 }
 
 /* Dequantisation v = q * scale ([Day 9-3] §2, the inverse of the rule above),
@@ -82,13 +108,21 @@ void orc_kv_dequantize_rows(const int8_t *q, const float *scale,
 /* [Day 9-2] §2 segment 1: per block qm = max|x|; if qm < 1e-6 then qm = 1; */
 /* block scale = qm * (1/127); iq = 127/qm; code = clamp(x*iq, -128, 127).  */
 /* The page's conversion to int8 is garbled; round-half-even is the reading */
-/* taken (same rule as K/V).  n must be a multiple of 32.                   */
+/* taken (same rule as K/V).  n must be a multiple of 32.  A block holding  */
+/* a NaN or an infinity is quantised as a block of zeros (qm 0 -> 1, scale  */
+/* 1/127, codes 0); the return value counts such blocks.                    */
 /* ------------------------------------------------------------------------ */
-void orc_q_quantize_blocks(const float *x, int64_t n, int8_t *qi, float *qsc)
+int64_t orc_q_quantize_blocks(const float *x, int64_t n, int8_t *qi, float *qsc)
 {
     const float kvq_inv = 1.0f / 127.0f;
+    static const float zeros[32];
+    int64_t replaced = 0;
     for (int64_t b = 0; b < n / 32; ++b) {
         const float *xb = x + b * 32;
+        if (!all_finite(xb, 32)) {
+            ++replaced;
+            xb = zeros;
+        }
         float qm = 0.0f;
         for (int i = 0; i < 32; ++i)
             qm = fmaxf(qm, fabsf(xb[i]));
@@ -106,6 +140,7 @@ void orc_q_quantize_blocks(const float *x, int64_t n, int8_t *qi, float *qsc)
             qi[b * 32 + i] = (int8_t)(int)c;
         }
     }
+    return replaced;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -287,14 +322,24 @@ int orc_attention_f64(const float *q, const float *k, const float *v,
 /* element in the high nibble.  Dequantise (q - zero) * scale.              */
 /* torch.round is round-half-even, so nearbyintf is the same rule.  scale   */
 /* and zero stay fp32 (the page keeps them in float tensors).               */
-/* n must be a multiple of group, group even.                               */
+/* n must be a multiple of group, group even (at most 1024).  A group that  */
+/* holds a NaN or an infinity is quantised as a group of zeros (scale 1,    */
+/* zero = round(-0/1) = -0, codes 0); the return value counts such groups.  */
 /* ------------------------------------------------------------------------ */
-void orc_int4_quantize_groups(const float *x, int64_t n, int group,
-                              uint8_t *packed, float *scale, float *zero)
+int64_t orc_int4_quantize_groups(const float *x, int64_t n, int group,
+                                 uint8_t *packed, float *scale, float *zero)
 {
+    static const float zeros[1024];
     int64_t ng = n / group;
+    int64_t replaced = 0;
+    if (group > 1024)
+        return -1;
     for (int64_t g = 0; g < ng; ++g) {
         const float *xg = x + g * group;
+        if (!all_finite(xg, group)) {
+            ++replaced;
+            xg = zeros;
+        }
         float mx = xg[0], mn = xg[0];
         for (int i = 1; i < group; ++i) {
             if (xg[i] > mx)
@@ -320,6 +365,7 @@ void orc_int4_quantize_groups(const float *x, int64_t n, int group,
             packed[(g * group + i) / 2] = (uint8_t)((c[0] << 4) | c[1]);
         }
     }
+    return replaced;
 }
 
 void orc_int4_dequantize_groups(const uint8_t *packed, const float *scale,

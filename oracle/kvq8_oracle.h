@@ -12,11 +12,11 @@
 extern "C" {
 #endif
 
-void orc_kv_quantize_rows(const float *x, int64_t n_rows, int hd,
-                          int8_t *q, float *scale);
+int64_t orc_kv_quantize_rows(const float *x, int64_t n_rows, int hd,
+                             int8_t *q, float *scale);
 void orc_kv_dequantize_rows(const int8_t *q, const float *scale,
                             int64_t n_rows, int hd, float *out);
-void orc_q_quantize_blocks(const float *x, int64_t n, int8_t *qi, float *qsc);
+int64_t orc_q_quantize_blocks(const float *x, int64_t n, int8_t *qi, float *qsc);
 void orc_scores_q8(const int8_t *qi, const float *qsc, int hd,
                    const int8_t *kq, const float *ks, int64_t L,
                    float sm_scale, double *s);
@@ -30,8 +30,8 @@ int orc_decode_q8_online(const int8_t *qi, const float *qsc, int hd,
                          float sm_scale, double *out);
 int orc_attention_f64(const float *q, const float *k, const float *v,
                       int64_t L, int hd, float sm_scale, double *out);
-void orc_int4_quantize_groups(const float *x, int64_t n, int group,
-                              uint8_t *packed, float *scale, float *zero);
+int64_t orc_int4_quantize_groups(const float *x, int64_t n, int group,
+                                 uint8_t *packed, float *scale, float *zero);
 void orc_int4_dequantize_groups(const uint8_t *packed, const float *scale,
                                 const float *zero, int64_t n, int group,
                                 float *out);

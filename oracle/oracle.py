@@ -57,14 +57,14 @@ def _load():
         i32 = ctypes.c_int
         f32 = ctypes.c_float
         sig = {
-            "orc_kv_quantize_rows": (None, [P, i64, i32, P, P]),
+            "orc_kv_quantize_rows": (i64, [P, i64, i32, P, P]),
             "orc_kv_dequantize_rows": (None, [P, P, i64, i32, P]),
-            "orc_q_quantize_blocks": (None, [P, i64, P, P]),
+            "orc_q_quantize_blocks": (i64, [P, i64, P, P]),
             "orc_scores_q8": (None, [P, P, i32, P, P, i64, f32, P]),
             "orc_decode_q8_three_pass": (i32, [P, P, i32, P, P, P, P, i64, f32, P, P]),
             "orc_decode_q8_online": (i32, [P, P, i32, P, P, P, P, i64, f32, P]),
             "orc_attention_f64": (i32, [P, P, P, i64, i32, f32, P]),
-            "orc_int4_quantize_groups": (None, [P, i64, i32, P, P, P]),
+            "orc_int4_quantize_groups": (i64, [P, i64, i32, P, P, P]),
             "orc_int4_dequantize_groups": (None, [P, P, P, i64, i32, P]),
             "orc_decode_mixed": (i32, [P, P, P, i32, P, P, i64, P, P, P, P, i64, f32, P]),
             "orc_version": (i32, []),
@@ -88,16 +88,19 @@ def _c(a, dtype):
 # --------------------------------------------------------------------------
 # element-level wrappers
 # --------------------------------------------------------------------------
-def kv_quantize_rows(x):
-    """Per-row max-abs INT8 quantisation. x: float32 [..., hd] -> (int8 [..., hd], float32 [...])."""
+def kv_quantize_rows(x, count_nonfinite=False):
+    """Per-row max-abs INT8 quantisation. x: float32 [..., hd] -> (int8 [..., hd], float32 [...]),
+    plus the number of rows quantised as zeros for holding a NaN or an infinity
+    when count_nonfinite."""
     x = _c(x, np.float32)
     hd = x.shape[-1]
     n = x.size // hd if hd else 0
     q = np.empty(x.shape, np.int8)
     s = np.empty(x.shape[:-1], np.float32)
+    replaced = 0
     if n:
-        _load().orc_kv_quantize_rows(_p(x), n, hd, _p(q), _p(s))
-    return q, s
+        replaced = int(_load().orc_kv_quantize_rows(_p(x), n, hd, _p(q), _p(s)))
+    return (q, s, replaced) if count_nonfinite else (q, s)
 
 
 def kv_dequantize_rows(q, scale):
@@ -111,16 +114,19 @@ def kv_dequantize_rows(q, scale):
     return out
 
 
-def q_quantize_blocks(x):
-    """32-block Q quantisation. x: float32 [..., hd] -> (int8 [..., hd], float32 [..., hd/32])."""
+def q_quantize_blocks(x, count_nonfinite=False):
+    """32-block Q quantisation. x: float32 [..., hd] -> (int8 [..., hd], float32 [..., hd/32]),
+    plus the number of blocks quantised as zeros for holding a NaN or an
+    infinity when count_nonfinite."""
     x = _c(x, np.float32)
     hd = x.shape[-1]
     assert hd % 32 == 0
     qi = np.empty(x.shape, np.int8)
     qsc = np.empty(x.shape[:-1] + (hd // 32,), np.float32)
+    replaced = 0
     if x.size:
-        _load().orc_q_quantize_blocks(_p(x), x.size, _p(qi), _p(qsc))
-    return qi, qsc
+        replaced = int(_load().orc_q_quantize_blocks(_p(x), x.size, _p(qi), _p(qsc)))
+    return (qi, qsc, replaced) if count_nonfinite else (qi, qsc)
 
 
 def scores_q8(qi, qsc, kq, ks, sm_scale):
@@ -177,8 +183,10 @@ def attention_f64(q, k, v, sm_scale):
     return out
 
 
-def int4_quantize_groups(x, group=64):
-    """Asymmetric INT4 per-group quantisation; returns (packed uint8, scale, zero)."""
+def int4_quantize_groups(x, group=64, count_nonfinite=False):
+    """Asymmetric INT4 per-group quantisation; returns (packed uint8, scale, zero),
+    plus the number of groups quantised as zeros for holding a NaN or an
+    infinity when count_nonfinite."""
     x = _c(x, np.float32)
     n = x.size
     assert n % group == 0 and group % 2 == 0
@@ -186,11 +194,12 @@ def int4_quantize_groups(x, group=64):
     ng = n // group
     scale = np.empty(x.shape[:-1] + (x.shape[-1] // group,), np.float32)
     zero = np.empty_like(scale)
+    replaced = 0
     if n:
-        _load().orc_int4_quantize_groups(_p(x), n, group, _p(packed),
-                                         _p(scale), _p(zero))
-    assert scale.size == ng
-    return packed, scale, zero
+        replaced = int(_load().orc_int4_quantize_groups(_p(x), n, group, _p(packed),
+                                                        _p(scale), _p(zero)))
+    assert scale.size == ng and replaced >= 0
+    return (packed, scale, zero, replaced) if count_nonfinite else (packed, scale, zero)
 
 
 def int4_dequantize_groups(packed, scale, zero, group=64):

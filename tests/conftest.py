@@ -30,6 +30,7 @@ def pytest_terminal_summary(terminalreporter):
     if h is None or not getattr(h, "ERRORS", None):
         return
     tr = terminalreporter
-    tr.write_sep("-", "largest |gpu - oracle| per test (max-abs, relative to max |oracle|)")
-    for test, (err, rel) in sorted(h.ERRORS.items()):
-        tr.write_line(f"{err:10.3e} {rel:10.3e}  {test}")
+    tr.write_sep("-", "largest d = gpu - oracle per test: max |d|, max |d|/max(1,|oracle|), "
+                      "max |d|/max |oracle|")
+    for test, vals in sorted(h.ERRORS.items()):
+        tr.write_line(" ".join(f"{v:10.3e}" for v in vals) + f"  {test}")

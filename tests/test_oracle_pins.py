@@ -506,3 +506,88 @@ def test_requantised_rows_stay_within_both_half_steps():
     y = oracle.int4_dequantize_groups(packed, sc, zr)
     bound = 0.5 * ks[:, None] * 1.0001 + 0.5 * np.repeat(sc, 64, axis=1) * 1.0001
     assert np.all(np.abs(y.astype(np.float64) - x) <= bound)
+
+
+# --------------------------------------------------------------------------
+# Non-finite inputs.  The pages give every rule for finite values only; the
+# reading taken is that a unit of quantisation (K/V row, query 32-block, INT4
+# group) holding a NaN or an infinity is quantised exactly as if all its
+# values were zero.  Pinned to the closed forms of the zero unit.
+# --------------------------------------------------------------------------
+_NONFINITE = (np.nan, np.inf, -np.inf)
+
+
+def test_nonfinite_kv_rows_quantise_as_the_zero_row():
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((7, 128)).astype(np.float32)
+    bad = {1: (5, np.nan), 3: (0, np.inf), 4: (127, -np.inf), 6: (64, np.nan)}
+    for r, (i, val) in bad.items():
+        x[r, i] = val
+    x[6, 65] = np.inf                       # two non-finite values in one row
+    q, s, n = oracle.kv_quantize_rows(x, count_nonfinite=True)
+    assert n == len(bad)
+    for r in bad:
+        # the zero row: max |v| = 0, scale +0, every code 0
+        assert s[r].view(np.uint32) == 0 and not q[r].any()
+    for r in (0, 2, 5):
+        # finite rows keep the page's rule: the max-abs element maps to +-127,
+        # scale = max|v| / 127 in fp32
+        m = np.abs(x[r]).max()
+        assert s[r] == np.float32(m) / np.float32(127.0)
+        assert abs(int(q[r][np.argmax(np.abs(x[r]))])) == 127
+    _, _, n_clean = oracle.kv_quantize_rows(x[[0, 2, 5]], count_nonfinite=True)
+    assert n_clean == 0
+
+
+def test_nonfinite_query_blocks_quantise_as_the_zero_block():
+    rng = np.random.default_rng(42)
+    x = rng.standard_normal((3, 128)).astype(np.float32)
+    x[0, 40] = np.nan        # block 1 of row 0
+    x[2, 127] = np.inf       # block 3 of row 2
+    x[2, 0] = -np.inf        # block 0 of row 2
+    qi, qsc, n = oracle.q_quantize_blocks(x, count_nonfinite=True)
+    assert n == 3
+    inv = np.float32(1.0) * np.float32(1.0 / 127.0)   # qm = 0 < 1e-6 -> 1
+    for r, blk in ((0, 1), (2, 3), (2, 0)):
+        assert qsc[r, blk] == inv and not qi[r, 32 * blk:32 * blk + 32].any()
+    # the other blocks are untouched: block max -> +-127 and scale max/127
+    for r, blk in ((0, 0), (0, 2), (1, 1), (2, 1)):
+        b = x[r, 32 * blk:32 * blk + 32]
+        assert qsc[r, blk] == np.float32(np.abs(b).max()) * np.float32(1.0 / 127.0)
+        assert abs(int(qi[r, 32 * blk + np.argmax(np.abs(b))])) == 127
+
+
+def test_nonfinite_int4_groups_quantise_as_the_zero_group():
+    rng = np.random.default_rng(43)
+    x = rng.standard_normal((4, 128)).astype(np.float32)
+    x[0, 3] = np.nan          # group 0 of row 0
+    x[1, 100] = np.inf        # group 1 of row 1
+    x[3, 0] = -np.inf
+    x[3, 127] = np.nan        # both groups of row 3
+    packed, sc, zr, n = oracle.int4_quantize_groups(x, 64, count_nonfinite=True)
+    assert n == 4
+    neg_zero = np.float32(-0.0).view(np.uint32)
+    for r, g in ((0, 0), (1, 1), (3, 0), (3, 1)):
+        # the zero group: max == min -> scale 1; zero = round(-0 / 1) = -0; codes 0
+        assert sc[r, g] == 1.0 and zr[r, g].view(np.uint32) == neg_zero
+        assert not packed[r, 32 * g:32 * g + 32].any()
+    for r, g in ((0, 1), (1, 0), (2, 0), (2, 1)):
+        grp = x[r, 64 * g:64 * g + 64]
+        assert sc[r, g] == (np.float32(grp.max()) - np.float32(grp.min())) / np.float32(15.0)
+
+
+@pytest.mark.parametrize("val", _NONFINITE)
+def test_nonfinite_rows_give_a_finite_decode(val):
+    # a context with a non-finite K row and a non-finite V row decodes like the
+    # same context with those rows zero (the zero K row scores 0, the zero V
+    # row adds nothing), and the output is finite
+    q, k, v = _random_unit(44, 300, G=2)
+    k_bad, v_bad = k.copy(), v.copy()
+    k_bad[17, 9] = val
+    v_bad[200, 100] = val
+    out, _ = oracle.decode_unit_q8(q, k_bad, v_bad, SM)
+    k0, v0 = k.copy(), v.copy()
+    k0[17] = 0.0
+    v0[200] = 0.0
+    ref, _ = oracle.decode_unit_q8(q, k0, v0, SM)
+    assert np.all(np.isfinite(out)) and np.array_equal(out, ref)
