@@ -339,9 +339,14 @@ kvq8_status kvq8_selftest_bounded_wait(uint32_t *dev_status, uint64_t timeout_ns
  * nibble; value = (code - zero) * scale.  The page's variance-dependent scale
  * tweak is marked there as an example, not the formula, and is not applied.
  *
- * Layout per (block, kv head) tile of 256 tokens:
- *   k_codes, v_codes uint8 [num_blocks][nkv][256][hd/2]   token-major
- *   k_param, v_param fp32  [num_blocks][nkv][256][4]      (scale0, zero0, scale1, zero1)
+ * Layout per (block, kv head) tile of 256 tokens (every code byte is the
+ * page's pair: byte i of a row = code[2i] << 4 | code[2i+1]):
+ *   k_codes uint8 [num_blocks][nkv][256][hd/2]       token-major rows
+ *   v_codes uint8 [num_blocks][nkv][8][hd/2][32]     per 32-token chunk, byte
+ *           column c (dims 2c, 2c+1) of its 32 tokens: token t of the chunk
+ *           (r = t % 16) at position 4*(2*((r%8)/2) + t/16) + 2*(r%2) + r/8,
+ *           the order in which the decode's tensor-core fragments take them
+ *   k_param, v_param fp32  [num_blocks][nkv][256][4]  (scale0, zero0, scale1, zero1)
  * 160 bytes per (token, kv head): 1280 bytes per token per layer for nkv = 8.
  */
 size_t kvq4_code_pool_bytes(int num_blocks, int nkv, int hd, int block_size);

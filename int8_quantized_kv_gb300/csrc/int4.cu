@@ -9,10 +9,15 @@
 // query against the dequantised K/V (the page dequantises and runs standard
 // attention).
 //
-// Cache layout (per (block, kv head) tile of 256 tokens):
-//   codes  uint8 [256][64]   token-major, byte i = code[2i] << 4 | code[2i+1]
-//   params fp32  [256][4]    (scale of dims 0-63, its zero, scale of 64-127, its zero)
-// for K and for V: 160 bytes per (token, kv head).
+// Cache layout (per (block, kv head) tile of 256 tokens); a code byte is
+// always the page's pair, byte i = code[2i] << 4 | code[2i+1]:
+//   K codes uint8 [256][64]            token-major rows
+//   V codes uint8 [8][64][32]          per 32-token chunk, byte column c (dims 2c,
+//                                      2c+1) of the chunk's tokens, token t at
+//                                      position v4_pos(t) (below)
+//   params  fp32  [256][4]             (scale of dims 0-63, its zero, scale of
+//                                      64-127, its zero), for K and for V
+// 160 bytes per (token, kv head).
 //
 // Decode: one CTA per (split, kv head, sequence), 4 warps walking the split in
 // 32-token chunks (each staged by bulk copies), each warp with its own
@@ -54,12 +59,12 @@ __device__ __forceinline__ int int4_code(float x, float s, float z) {
     return max(0, min(15, c));
 }
 
-// Quantises one row (lane l holds dims 4l..4l+3) and stores codes + params.
-// A 64-value group holding a NaN or an infinity (outside the rule) is
-// quantised as a group of zeros (scale 1, zero -0, codes 0) and
-// KVQ8_DEV_NONFINITE is set in *status (when non-null).
-__device__ __forceinline__ void int4_store_row(float4 x, uint8_t *codes_row, float *param_row,
-                                               int lane, uint32_t *status) {
+// Quantises one row (lane l holds dims 4l..4l+3): returns the lane's two code
+// bytes (dims 4l, 4l+1 in the low byte, 4l+2, 4l+3 in the high byte) and
+// stores the row's parameters.  A 64-value group holding a NaN or an infinity
+// (outside the rule) is quantised as a group of zeros (scale 1, zero -0,
+// codes 0) and KVQ8_DEV_NONFINITE is set in *status (when non-null).
+__device__ __forceinline__ uint32_t int4_quant_row(float4 x, float *param_row, int lane, uint32_t *status) {
     const uint32_t bad = __ballot_sync(0xffffffffu, nonfinite(x.x) | nonfinite(x.y) | nonfinite(x.z) |
                                                         nonfinite(x.w));
     if (bad & (lane < 16 ? 0x0000ffffu : 0xffff0000u)) {   // uniform within the half warp
@@ -74,12 +79,32 @@ __device__ __forceinline__ void int4_store_row(float4 x, uint8_t *codes_row, flo
     const float z = rintf(__fdiv_rn(-mn, s));
     const int c0 = int4_code(x.x, s, z), c1 = int4_code(x.y, s, z);
     const int c2 = int4_code(x.z, s, z), c3 = int4_code(x.w, s, z);
-    const uint16_t two = (uint16_t)(((c0 << 4) | c1) | (((c2 << 4) | c3) << 8));
-    reinterpret_cast<uint16_t *>(codes_row)[lane] = two;
     if ((lane & 15) == 0) {
         param_row[(lane >> 4) * 2 + 0] = s;
         param_row[(lane >> 4) * 2 + 1] = z;
     }
+    return (uint32_t)(((c0 << 4) | c1) | (((c2 << 4) | c3) << 8));
+}
+
+// Position of token t (0..31) of a chunk in its V byte column: the word
+// 2*t4 + k of the column holds, in bytes 0..3, the tokens 16k + 2*t4 + {0, 8,
+// 1, 9} -- so that in the P.V MMA (k index = token within the 16-token step)
+// lane t4's one 64-bit load gives, for both k-steps, the A-fragment pairs
+// {k = 2*t4, 2*t4 + 1} (bytes 0, 2) and {2*t4 + 8, 2*t4 + 9} (bytes 1, 3).
+__host__ __device__ __forceinline__ int v4_pos(int t) {
+    const int k = t >> 4, r = t & 15;
+    return 4 * (2 * ((r & 7) >> 1) + k) + 2 * (r & 1) + (r >> 3);
+}
+
+// Stores one quantised row (the lane's two code bytes) as a K row (token-major)
+// or into the V chunk layout at tile slot `slot`.
+__device__ __forceinline__ void int4_store_k_row(uint32_t two, uint8_t *codes_row, int lane) {
+    reinterpret_cast<uint16_t *>(codes_row)[lane] = (uint16_t)two;
+}
+__device__ __forceinline__ void int4_store_v_row(uint32_t two, uint8_t *v_tile, int slot, int lane) {
+    uint8_t *col = v_tile + (size_t)(slot >> 5) * (kChunk4 * kRowBytes) + v4_pos(slot & 31);
+    col[(size_t)(2 * lane) * kChunk4] = (uint8_t)(two & 0xff);
+    col[(size_t)(2 * lane + 1) * kChunk4] = (uint8_t)(two >> 8);
 }
 
 // One warp per new (token, kv head): K row then V row.
@@ -99,12 +124,15 @@ int4_append_kernel(Int4AppendParams p) {
         if (lane == 0) flag_status(p.dev_status, KVQ8_DEV_BAD_BLOCK_ID);
         return;
     }
-    const size_t row = ((size_t)phys * p.nkv + h) * kBS + pos % kBS;
+    const size_t tile = (size_t)phys * p.nkv + h;
+    const size_t row = tile * kBS + pos % kBS;
     const size_t src = (((size_t)b * p.n_new + i) * p.nkv + h) * kHD;
-    int4_store_row(reinterpret_cast<const float4 *>(p.k_new + src)[lane], p.k_codes + row * kRowBytes,
-                   p.k_param + row * 4, lane, p.dev_status);
-    int4_store_row(reinterpret_cast<const float4 *>(p.v_new + src)[lane], p.v_codes + row * kRowBytes,
-                   p.v_param + row * 4, lane, p.dev_status);
+    int4_store_k_row(int4_quant_row(reinterpret_cast<const float4 *>(p.k_new + src)[lane], p.k_param + row * 4,
+                                    lane, p.dev_status),
+                     p.k_codes + row * kRowBytes, lane);
+    int4_store_v_row(int4_quant_row(reinterpret_cast<const float4 *>(p.v_new + src)[lane], p.v_param + row * 4,
+                                    lane, p.dev_status),
+                     p.v_codes + tile * kBS * kRowBytes, pos % kBS, lane);
 }
 
 // ---- requantisation int8 -> INT4 of whole blocks (mixed precision by token age) ----
@@ -141,8 +169,8 @@ int4_requantize_kernel(Int4RequantParams p) {
         const float sc = p.k_scale[tile8 * kBS + t];
         const float4 x = make_float4(__fmul_rn((float)(int8_t)(w & 0xff), sc), __fmul_rn((float)(int8_t)((w >> 8) & 0xff), sc),
                                      __fmul_rn((float)(int8_t)((w >> 16) & 0xff), sc), __fmul_rn((float)(int8_t)(w >> 24), sc));
-        int4_store_row(x, p.k_codes + (tile4 * kBS + t) * kRowBytes, p.k_param + (tile4 * kBS + t) * 4, lane,
-                       p.dev_status);
+        int4_store_k_row(int4_quant_row(x, p.k_param + (tile4 * kBS + t) * 4, lane, p.dev_status),
+                         p.k_codes + (tile4 * kBS + t) * kRowBytes, lane);
     }
     // V: one 64-token quarter at a time
     for (int qd = 0; qd < kBS / kStageTok; ++qd) {
@@ -162,8 +190,9 @@ int4_requantize_kernel(Int4RequantParams p) {
             float xs[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) xs[i] = __fmul_rn((float)(int8_t)vt[(4 * lane + i) * kVtPitch + tq], sc);
-            int4_store_row(make_float4(xs[0], xs[1], xs[2], xs[3]), p.v_codes + (tile4 * kBS + t) * kRowBytes,
-                           p.v_param + (tile4 * kBS + t) * 4, lane, p.dev_status);
+            int4_store_v_row(int4_quant_row(make_float4(xs[0], xs[1], xs[2], xs[3]),
+                                            p.v_param + (tile4 * kBS + t) * 4, lane, p.dev_status),
+                             p.v_codes + tile4 * kBS * kRowBytes, t, lane);
         }
     }
 }
@@ -193,8 +222,9 @@ int4_requantize_kernel(Int4RequantParams p) {
 // point enters as a correction per (head, group),
 //   out[d][h] = 2^24 sum_t P'_g a_{t,d} - Z[h][g],  Z[h][g] = sum_t P'_g zero_g(t),
 // rescaled with the accumulator.  Row r of m-tile mt is dim 2*B + (r >= 8)
-// with byte B = 32*(mt/4) + 4*(r%8) + mt%4, so a lane reads one 32-bit word
-// per token and dim group.
+// with byte column B = 8*mt + r%8 of the chunk's dim-major V layout, so one
+// 64-bit load per lane and m-tile feeds both k-steps (v4_pos), with no byte
+// permutes, and the loads of a half warp fall in distinct banks.
 //
 // k-order of Q.K (k-step ks: group ks/4, sub = ks%4; lane t4 supplies the
 // nibbles of the word at byte 32*(ks/4) + 8*t4 + 4*(sub/2)): k = 2*t4 + e ->
@@ -222,7 +252,7 @@ __device__ __forceinline__ int qk_dim(int ks, int kk) {
 // and K and V parameter rows (512 B each) are contiguous in the cache (a chunk
 // starts at a multiple of 32 slots), so one lane brings each in with a 1-D
 // bulk copy, completing on the buffer's mbarrier; two buffers per warp.  The
-// staged rows keep the cache's 64-byte pitch; the fragment loads then meet
+// staged K rows keep the cache's 64-byte pitch; their fragment loads meet
 // 2-way bank conflicts, which cost nothing measurable (a cache layout that
 // removed them, with the rows' 32-byte pieces permuted, ran at the same speed).
 constexpr int kStageKOff = 0;
@@ -708,25 +738,20 @@ int4_decode_split_kernel(Int4DecodeParams p) {
             }
 
         // ---- P.V: out^T += V^T P'_g ----
+        // m-tile mt: rows g, g + 8 = dims 2c, 2c + 1 of byte column c = 8*mt + g;
+        // one 64-bit load gives the column's words 2*t4 (k-step 0) and 2*t4 + 1
+        // (k-step 1), each holding the A fragment of one MMA: high nibbles of
+        // bytes 0, 2 (rows g, k = 2*t4, 2*t4 + 1), low nibbles (rows g + 8), and
+        // the same of bytes 1, 3 (k = 2*t4 + 8, 2*t4 + 9)
 #pragma unroll
-        for (int ks2 = 0; ks2 < 2; ++ks2) {
-            // V: tokens 16*ks2 + 2*t4 + {0, 1, 8, 9}, bytes 32*gr + 4*g .. +3
-            uint32_t vw[4][2];
+        for (int mt = 0; mt < 8; ++mt) {
+            const int gr = mt >> 2;
+            const uint2 vw = *reinterpret_cast<const uint2 *>(st + kStageVOff + (8 * mt + g) * kChunk4 + 8 * t4);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-#pragma unroll
-                for (int gr = 0; gr < 2; ++gr) {
-                    const int t = 16 * ks2 + 2 * t4 + (j & 1) + 8 * (j >> 1);
-                    vw[j][gr] = *reinterpret_cast<const uint32_t *>(st + kStageVOff + t * kRowBytes + 32 * gr + 4 * g);
-                }
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                const int gr = mt >> 2, k = mt & 3;
-                const uint32_t sel = (uint32_t)(k | (k << 4) | ((4 + k) << 8) | ((4 + k) << 12));
-                const uint32_t r01 = __byte_perm(vw[0][gr], vw[1][gr], sel);
-                const uint32_t r89 = __byte_perm(vw[2][gr], vw[3][gr], sel);
-                const uint32_t a0 = nib_pair(r01, kHiNib), a1 = nib_pair(r01, kLoNib);
-                const uint32_t a2 = nib_pair(r89, kHiNib), a3 = nib_pair(r89, kLoNib);
+            for (int ks2 = 0; ks2 < 2; ++ks2) {
+                const uint32_t w = ks2 ? vw.y : vw.x, w8 = w >> 8;
+                const uint32_t a0 = nib_pair(w, kHiNib), a1 = nib_pair(w, kLoNib);
+                const uint32_t a2 = nib_pair(w8, kHiNib), a3 = nib_pair(w8, kLoNib);
 #pragma unroll
                 for (int hl = 0; hl < kParts; ++hl)
                     mma_f16_16816(acc[mt], a0, a1, a2, a3, bf[gr][hl][ks2][0], bf[gr][hl][ks2][1]);
@@ -771,7 +796,7 @@ int4_decode_split_kernel(Int4DecodeParams p) {
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
         const int gr = mt >> 2;
-        const int dim = 2 * (32 * gr + 4 * g + (mt & 3));
+        const int dim = 2 * (8 * mt + g);   // row g: even dim (its high nibble), row g + 8: the next
         const int h0 = hbase, h1 = hbase + 1;
         // rows g carry 16 c (high nibbles: even dims), in code steps of 2^-24
         if (writer && h0 < G) {

@@ -453,8 +453,8 @@ def selftest_bounded_wait(timeout_ns: int, dev_status, waited_ns=None, stream=No
 # ------------------------------------------------------------ 4-bit cache ---
 class KV4Cache(NamedTuple):
     """The asymmetric INT4 group-64 cache (layout in include/kvq8.h)."""
-    k_codes: object  # uint8 [num_blocks][nkv][256][64]
-    v_codes: object  # uint8 [num_blocks][nkv][256][64]
+    k_codes: object  # uint8 [num_blocks][nkv][256][64]  token-major rows
+    v_codes: object  # uint8 [num_blocks][nkv][256][64]  stored as [8 chunks][64 byte columns][32]
     k_param: object  # fp32 [num_blocks][nkv][256][4]  (scale0, zero0, scale1, zero1)
     v_param: object  # fp32 [num_blocks][nkv][256][4]
 

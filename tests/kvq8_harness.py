@@ -50,6 +50,24 @@ def _record(*vals):
         cur[i] = max(cur[i], v)
 
 
+def v4_pos(t):
+    """Position of token t (0..31) of a 32-token chunk in a byte column of the
+    4-bit cache's V codes: word 2*t4 + k of the column holds the tokens
+    16k + 2*t4 + {0, 8, 1, 9} in its bytes 0..3."""
+    t = np.asarray(t)
+    k, r = t >> 4, t & 15
+    return 4 * (2 * ((r & 7) >> 1) + k) + 2 * (r & 1) + (r >> 3)
+
+
+def v4_token_major(vc):
+    """V codes of the 4-bit cache, uint8 [num_blocks][nkv][256][64] as stored
+    (per 32-token chunk [64 byte columns][32 positions]), in token-major order
+    [num_blocks][nkv][256 tokens][64 bytes]."""
+    nb, nkv = vc.shape[:2]
+    x = vc.reshape(nb, nkv, 8, 64, 32)[..., v4_pos(np.arange(32))]
+    return np.ascontiguousarray(x.transpose(0, 1, 2, 4, 3).reshape(nb, nkv, 256, 64))
+
+
 def assert_close(gpu, ref, what=""):
     """Output parity bar: "within 1e-4 max-abs and 1e-3 relative" of the
     oracle, read as two bars on d = gpu - oracle:

@@ -273,3 +273,17 @@ def test_mixed_precision_validation(lib):
 def test_library_is_built_for_sm103a():
     assert "arch=compute_103a,code=sm_103a" in " ".join(kbuild.ARCH)
     assert os.path.exists(kbuild.LIB_PATH)
+
+
+def test_int4_v_chunk_positions_are_a_permutation():
+    # the 4-bit cache's V chunk layout places the 32 tokens of a chunk at 32
+    # distinct positions of a byte column (the test readers' copy of the rule)
+    from kvq8_harness import v4_pos
+    import numpy as np
+    pos = v4_pos(np.arange(32))
+    assert sorted(pos.tolist()) == list(range(32))
+    # word 2*t4 + k holds tokens 16k + 2*t4 + {0, 8, 1, 9} in bytes 0..3
+    for t4 in range(4):
+        for k in range(2):
+            toks = [16 * k + 2 * t4 + d for d in (0, 8, 1, 9)]
+            assert [int(v4_pos(t)) for t in toks] == [4 * (2 * t4 + k) + b for b in range(4)]

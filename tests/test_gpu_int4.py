@@ -15,7 +15,7 @@ import torch
 import oracle
 from int8_quantized_kv_gb300 import kvq8
 from int8_quantized_kv_gb300 import workloads as wl
-from kvq8_harness import SM_SCALE, assert_close
+from kvq8_harness import SM_SCALE, assert_close, v4_token_major
 
 pytestmark = pytest.mark.gpu
 HD = 128
@@ -92,7 +92,7 @@ def test_int4_append_bit_exact(gpu_lib, start, n_new):
                           torch.from_numpy(table).cuda(), cache, dev_status=status)
     torch.cuda.synchronize()
     assert status.item() == 0
-    kc, vc = cache.k_codes.cpu().numpy(), cache.v_codes.cpu().numpy()
+    kc, vc = cache.k_codes.cpu().numpy(), v4_token_major(cache.v_codes.cpu().numpy())
     kp, vp = cache.k_param.cpu().numpy(), cache.v_param.cpu().numpy()
     pos = start + np.arange(n_new)
     phys, slot = table[0, pos // 256], pos % 256

@@ -14,7 +14,7 @@ import torch
 import oracle
 from int8_quantized_kv_gb300 import kvq8
 from int8_quantized_kv_gb300 import workloads as wl
-from kvq8_harness import SM_SCALE, Case, assert_close, k_rows_logical, v_rows_logical
+from kvq8_harness import SM_SCALE, Case, assert_close, k_rows_logical, v4_token_major, v_rows_logical
 
 pytestmark = pytest.mark.gpu
 BS = 256
@@ -59,7 +59,7 @@ def test_requantised_tiles_bit_exact(gpu_lib):
     case = MixedCase(cfg, n4=[2, 3])
     assert case.status_bits() == 0
     pools = case.host_pools()
-    kc, vc = case.cache4.k_codes.cpu().numpy(), case.cache4.v_codes.cpu().numpy()
+    kc, vc = case.cache4.k_codes.cpu().numpy(), v4_token_major(case.cache4.v_codes.cpu().numpy())
     kp, vp = case.cache4.k_param.cpu().numpy(), case.cache4.v_param.cpu().numpy()
     for b in range(cfg.batch):
         for h in range(cfg.nkv):

@@ -15,7 +15,7 @@ import torch
 import oracle
 from int8_quantized_kv_gb300 import kvq8
 from int8_quantized_kv_gb300 import workloads as wl
-from kvq8_harness import SM_SCALE, Case, StepCase, assert_close, k_rows_logical, v_rows_logical
+from kvq8_harness import SM_SCALE, Case, StepCase, assert_close, k_rows_logical, v4_token_major, v_rows_logical
 
 pytestmark = pytest.mark.gpu
 HD = 128
@@ -162,7 +162,7 @@ def test_int4_append_nonfinite_groups_bit_exact(gpu_lib):
                           torch.from_numpy(table).cuda(), cache, dev_status=status)
     torch.cuda.synchronize()
     assert status.item() == kvq8.DEV_NONFINITE
-    kc, vc = cache.k_codes.cpu().numpy(), cache.v_codes.cpu().numpy()
+    kc, vc = cache.k_codes.cpu().numpy(), v4_token_major(cache.v_codes.cpu().numpy())
     kp, vp = cache.k_param.cpu().numpy(), cache.v_param.cpu().numpy()
     pos = start + np.arange(n_new)
     phys, slot = table[0, pos // 256], pos % 256
