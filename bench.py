@@ -86,6 +86,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = min(steps, 2000)")
     ap.add_argument("--no-f32", action="store_true",
                     help="skip the fp32-KV decode comparator leg")
+    ap.add_argument("--plain-step", action="store_true",
+                    help="time the decode step without KVQ8_STEP_CACHE_READY")
     return ap.parse_args(argv)
 
 
@@ -617,9 +619,14 @@ def bench_q8(gpu, cfg, full):
     out = torch.empty_like(q_d)
     nk1, nv1 = nk_d[:, 0], nv_d[:, 0]   # the step's token, [batch][nkv][hd]
 
+    # The steps of the timed loop differ only in their query and new token:
+    # the kernel before each step's split (the previous step's merge) writes
+    # only `out`, so every step may pass KVQ8_STEP_CACHE_READY
+    ready = not args.plain_step
+
     def step(i):
         kvq8.decode_step(q_d, nk1, nv1, caches[i % copies], table_d, lens_d, out, ws, sm_scale=sm,
-                         dev_status=status, stream=stream)
+                         dev_status=status, stream=stream, cache_ready=ready)
 
     def split(i):
         kvq8.decode_split(q_d, caches[i % copies], table_d, lens_d, ws, sm_scale=sm, dev_status=status,
@@ -637,6 +644,8 @@ def bench_q8(gpu, cfg, full):
         step, split, "decode_split_kernel", split_bytes, sbytes, 2)
     line = base_line(gpu, total / slowest / 1e9, args.steps, slowest, "int8", config)
     line["gpu_launches"] = launches
+    line["step_call"] = ("kvq8_decode_step_ex with KVQ8_STEP_CACHE_READY" if ready else
+                         "kvq8_decode_step_ex without flags")
     finish_line(gpu, line, roof, clocks, line["us_per_step"],
                 recorded_traffic("decode_split_kernel", cfg.name))
     if l2_resident:
@@ -664,7 +673,7 @@ def bench_q8(gpu, cfg, full):
     # kernels directly
     runners = [kvq8.DecodeStep(q_d, nk1, nv1, caches[j], table_d, lens_d, out, ws, sm_scale=sm,
                                dev_status=status, stream=stream, q_host=q_h, k_host=nk1_h, v_host=nv1_h,
-                               out_host=out_h) for j in range(copies)]
+                               out_host=out_h, cache_ready=ready) for j in range(copies)]
 
     def e2e_step(i):
         # host Q and the step's token in, the step, the result out; then the
@@ -715,7 +724,9 @@ def per_layer_graph(gpu, cfg, sbytes, cache, q_d, nk1, nv1, table_d, lens_d, out
     layer (batch 1 each, its own workspace), captured once in a CUDA graph and
     replayed: the launch form of an engine that runs one layer at a time.  One
     replay streams every layer's cache (the sum is far above L2), so replays
-    read from HBM like the folded step."""
+    read from HBM like the folded step.  Timed with KVQ8_STEP_CACHE_READY (each
+    layer's call follows the previous layer's merge, which writes only its
+    output) and without it."""
     import torch
     from int8_quantized_kv_gb300 import kvq8
     dev = q_d.device
@@ -723,36 +734,43 @@ def per_layer_graph(gpu, cfg, sbytes, cache, q_d, nk1, nv1, table_d, lens_d, out
     outs = torch.empty_like(q_d)
     wss = [kvq8.alloc_workspace(1, cfg.nqh, cfg.nkv, max_blocks, dev) for _ in range(n_layers)]
     s = torch.cuda.Stream(dev)
-
-    def calls():
-        for b in range(n_layers):
-            kvq8.decode_step(q_d[b:b + 1], nk1[b:b + 1], nv1[b:b + 1], cache, table_d[b:b + 1],
-                             lens_d[b:b + 1], outs[b:b + 1], wss[b], sm_scale=sm, dev_status=gpu.status,
-                             stream=s)
-
-    s.wait_stream(torch.cuda.current_stream(dev))
-    with torch.cuda.stream(s):
-        calls()                       # once outside the graph
-    s.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=s):
-        calls()
-    for _ in range(3):
-        g.replay()
-    torch.cuda.synchronize()
     n = max(20, min(gpu.args.steps, 500))
-    e0, e1 = gpu.event(), gpu.event()
-    e0.record()
-    for _ in range(n):
-        g.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    gpu.check_status("in the per-layer calls")
-    t = e0.elapsed_time(e1) / 1e3 / n
+
+    def timed(ready):
+        def calls():
+            for b in range(n_layers):
+                kvq8.decode_step(q_d[b:b + 1], nk1[b:b + 1], nv1[b:b + 1], cache, table_d[b:b + 1],
+                                 lens_d[b:b + 1], outs[b:b + 1], wss[b], sm_scale=sm, dev_status=gpu.status,
+                                 stream=s, cache_ready=ready)
+
+        s.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(s):
+            calls()                       # once outside the graph
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            calls()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = gpu.event(), gpu.event()
+        e0.record()
+        for _ in range(n):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        gpu.check_status("in the per-layer calls")
+        return e0.elapsed_time(e1) / 1e3 / n
+
+    t_plain = timed(False)
+    t = timed(True)
     d = (outs.double() - out_folded.double()).abs()
     return {"us_per_step": round(t * 1e6, 2), "value": round(sbytes / t / 1e9, 2), "unit": "GB/s",
             "calls_per_step": n_layers, "launches_per_step": 2 * n_layers, "replays": n,
-            "path": f"{n_layers} kvq8_decode_step calls (one layer each) in one CUDA graph",
+            "path": (f"{n_layers} kvq8_decode_step_ex calls (one layer each, KVQ8_STEP_CACHE_READY) in one "
+                     "CUDA graph"),
+            "plain_us_per_step": round(t_plain * 1e6, 2),
+            "plain_path": "the same calls without flags",
             "max_abs_diff_vs_folded": float(d.max())}
 
 

@@ -271,6 +271,32 @@ kvq8_status kvq8_decode_step(const float *q, const float *k_new, const float *v_
                              uint32_t *dev_status, void *stream);
 
 /*
+ * kvq8_decode_step_ex -- kvq8_decode_step with flags (0 = kvq8_decode_step).
+ *
+ * KVQ8_STEP_CACHE_READY: the caller vouches that the cache blocks this call
+ * reads (apart from its new tokens' slots, which it writes itself),
+ * block_table and ctx_lens held their final values before the kernel that
+ * precedes this call in the stream began (they are not written by that
+ * kernel, nor by anything it does not wait for).  The split kernel then runs
+ * its prologue and starts copying the cache into shared memory without
+ * waiting for that kernel; only the reads of q, k_new and v_new and the
+ * writes of the workspace, the pools' new-token slots and out wait for it.
+ * A decode that runs one layer per call after the layer's own projections
+ * (which write q, k_new and v_new only) meets this; so does a chain of steps
+ * that differ only in those inputs.  Results are identical with and without
+ * the flag.  Flags outside KVQ8_STEP_CACHE_READY return KVQ8_ERR_INVALID_ARG.
+ */
+#define KVQ8_STEP_CACHE_READY 0x1u
+kvq8_status kvq8_decode_step_ex(const float *q, const float *k_new, const float *v_new,
+                                int batch, int nqh, int nkv, int hd,
+                                int8_t *k_pool, int8_t *v_pool, float *k_scale, float *v_scale,
+                                int num_blocks, const int32_t *block_table,
+                                int max_blocks, int block_size,
+                                const int32_t *ctx_lens, float sm_scale, float *out,
+                                void *workspace, size_t workspace_bytes,
+                                uint32_t *dev_status, uint32_t flags, void *stream);
+
+/*
  * kvq8_decode_step_host -- kvq8_decode_step from host memory and back, the
  * call a serving loop makes each step: the inputs q_host (fp32
  * [batch][nqh][hd]), k_new_host and v_new_host (fp32 [batch][nkv][hd]) and the

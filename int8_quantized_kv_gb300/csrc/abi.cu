@@ -77,6 +77,7 @@ kvq8_status fill_decode_params(const float *q, int batch, int nqh, int nkv,
     p->dev_status = dev_status;
     p->out = nullptr;
     p->first_q8_block = nullptr;
+    p->cache_ready = 0;
     p->ws_meta2 = nullptr;
     p->ws_ml2 = nullptr;
     p->ws_acc2 = nullptr;
@@ -346,6 +347,25 @@ kvq8_status kvq8_decode_step(const float *q, const float *k_new, const float *v_
                                                ctx_lens, sm_scale, out, workspace, workspace_bytes,
                                                dev_status, &p, &plan);
     if (st != KVQ8_OK || batch == 0) return st;
+    return launch_decode_step(p, plan, (cudaStream_t)stream);
+}
+
+kvq8_status kvq8_decode_step_ex(const float *q, const float *k_new, const float *v_new, int batch,
+                                int nqh, int nkv, int hd, int8_t *k_pool, int8_t *v_pool,
+                                float *k_scale, float *v_scale, int num_blocks,
+                                const int32_t *block_table, int max_blocks, int block_size,
+                                const int32_t *ctx_lens, float sm_scale, float *out, void *workspace,
+                                size_t workspace_bytes, uint32_t *dev_status, uint32_t flags,
+                                void *stream) {
+    if (flags & ~(uint32_t)KVQ8_STEP_CACHE_READY) return KVQ8_ERR_INVALID_ARG;
+    DecodeParams p;
+    DecodePlan plan;
+    const kvq8_status st = prepare_decode_step(q, k_new, v_new, batch, nqh, nkv, hd, k_pool, v_pool, k_scale,
+                                               v_scale, num_blocks, block_table, max_blocks, block_size,
+                                               ctx_lens, sm_scale, out, workspace, workspace_bytes,
+                                               dev_status, &p, &plan);
+    if (st != KVQ8_OK || batch == 0) return st;
+    p.cache_ready = (flags & KVQ8_STEP_CACHE_READY) ? 1 : 0;
     return launch_decode_step(p, plan, (cudaStream_t)stream);
 }
 

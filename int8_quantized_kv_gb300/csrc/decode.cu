@@ -198,8 +198,12 @@ decode_split_kernel(DecodeParams p) {
     const int cap = p.max_blocks * kBS;
     // Launched as a programmatic dependent of the previous kernel in the stream
     // (its launch overlaps that kernel's end), whose outputs may be this
-    // kernel's inputs: every thread waits for it here first.
-    pdl_wait();
+    // kernel's inputs: every thread waits for it here first -- unless the
+    // caller vouches that the cache, the block table and the context lengths
+    // were final before that kernel began (cache_ready): then the prologue and
+    // the producer's copies go ahead, and only the consumers wait (they read
+    // the query and the new token and write the workspace).
+    if (!p.cache_ready) pdl_wait();
     Misc *misc = reinterpret_cast<Misc *>(smem + Lay::oMisc);
     int8_t *q_codes = reinterpret_cast<int8_t *>(smem + Lay::oQCodes);
     float *q_scale = reinterpret_cast<float *>(smem + Lay::oQScale);
@@ -355,6 +359,7 @@ decode_split_kernel(DecodeParams p) {
         }
     } else {
         // =========================== consumer warps ==========================
+        if (p.cache_ready) pdl_wait();
         unsigned char *scratch = smem + Lay::oScratch + warp * Lay::kScratch;
         __half *p_hi = reinterpret_cast<__half *>(scratch);
         __half *p_lo = p_hi + G * kPRowHalves;
@@ -745,24 +750,43 @@ decode_combine_kernel(DecodeParams p, int G) {
         *o = s_sum > 0.0f ? a / s_sum : 0.0f;
         return;
     }
-    float m = -INFINITY;
-    for (int j = 0; j < meta0.y; ++j) m = fmaxf(m, p.ws_ml[((r00 + j) * G + g) * 2]);
-    for (int j = 0; j < meta1.y; ++j) m = fmaxf(m, p.ws_ml2[((r10 + j) * G + g) * 2]);
-    float s_sum = 0.0f, a = 0.0f;
-    if (m != -INFINITY) {
-        for (int j = 0; j < meta0.y; ++j) {
-            const size_t r = (r00 + j) * G + g;
-            const float f = exp2f(p.ws_ml[r * 2] - m);
-            s_sum = fmaf(p.ws_ml[r * 2 + 1], f, s_sum);
-            a = fmaf(p.ws_acc[r * kHD + d], f, a);
+    // more records (a call of few long units, or two sources): groups of
+    // kCombineRegs records, each group loaded at once and merged into the
+    // running state with the same rescaling rule
+    float m = -INFINITY, s_sum = 0.0f, a = 0.0f;
+    auto merge_group = [&](const float *ml, const float *accp, size_t r0, int n) {
+        float mr[kCombineRegs], sr[kCombineRegs], ar[kCombineRegs];
+        float mg = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kCombineRegs; ++j) {
+            if (j < n) {
+                const size_t r = (r0 + j) * G + g;
+                const float2 v = *reinterpret_cast<const float2 *>(ml + r * 2);
+                mr[j] = v.x;
+                sr[j] = v.y;
+                ar[j] = accp[r * kHD + d];
+                mg = fmaxf(mg, v.x);
+            }
         }
-        for (int j = 0; j < meta1.y; ++j) {
-            const size_t r = (r10 + j) * G + g;
-            const float f = exp2f(p.ws_ml2[r * 2] - m);
-            s_sum = fmaf(p.ws_ml2[r * 2 + 1], f, s_sum);
-            a = fmaf(p.ws_acc2[r * kHD + d], f, a);
+        if (mg == -INFINITY) return;
+        const float m_new = fmaxf(m, mg);
+        const float f_old = exp2f(m - m_new);   // 0 while m is -inf
+        s_sum *= f_old;
+        a *= f_old;
+#pragma unroll
+        for (int j = 0; j < kCombineRegs; ++j) {
+            if (j < n) {
+                const float f = exp2f(mr[j] - m_new);
+                s_sum = fmaf(sr[j], f, s_sum);
+                a = fmaf(ar[j], f, a);
+            }
         }
-    }
+        m = m_new;
+    };
+    for (int j0 = 0; j0 < meta0.y; j0 += kCombineRegs)
+        merge_group(p.ws_ml, p.ws_acc, r00 + j0, min(kCombineRegs, meta0.y - j0));
+    for (int j0 = 0; j0 < meta1.y; j0 += kCombineRegs)
+        merge_group(p.ws_ml2, p.ws_acc2, r10 + j0, min(kCombineRegs, meta1.y - j0));
     *o = s_sum > 0.0f ? a / s_sum : 0.0f;
 }
 

@@ -683,9 +683,10 @@ int4_decode_split_kernel(Int4DecodeParams p) {
                 }
 #pragma unroll
                 for (int gr = 0; gr < 2; ++gr) {
-                    const __half h0 = __float2half_rn(pg[gr][0]), h1 = __float2half_rn(pg[gr][1]);
-                    const uint32_t hi = pack_half2(__half2float(h0), __half2float(h1));
-                    const uint32_t lo = pack_half2(pg[gr][0] - __half2float(h0), pg[gr][1] - __half2float(h1));
+                    const __half2 hh = __floats2half2_rn(pg[gr][0], pg[gr][1]);
+                    const float2 hf = __half22float2(hh);
+                    const uint32_t hi = *reinterpret_cast<const uint32_t *>(&hh);
+                    const uint32_t lo = pack_half2(pg[gr][0] - hf.x, pg[gr][1] - hf.y);
                     if constexpr (kPack2) {
                         // lanes t4 = 1, 3 store in the other order: two banks per g
                         const int w0 = t4 & 1;

@@ -109,6 +109,11 @@ struct DecodeParams {
     const int32_t *first_q8_block;
     const int2 *ws_meta2;
     const float *ws_ml2, *ws_acc2;
+    // Nonzero: the cache, block_table and ctx_lens were final before the
+    // kernel preceding this call in the stream began, so the split kernel's
+    // prologue and copies run before it waits for that kernel (only q, k_new,
+    // v_new and the workspace wait).  Zero: every thread waits first.
+    int cache_ready;
 };
 cudaError_t launch_decode_split(const DecodeParams &p, int group, cudaStream_t s);
 cudaError_t launch_decode_combine(const DecodeParams &p, int group, cudaStream_t s);

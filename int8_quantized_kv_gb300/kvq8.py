@@ -20,6 +20,7 @@ Q_BLOCK = 32
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024   # KVQ8_NOALLOC_SCRATCH_BYTES in kvq8.h
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = range(5)
+STEP_CACHE_READY = 0x1   # KVQ8_STEP_CACHE_READY
 DEV_BAD_BLOCK_ID, DEV_BAD_CTX_LEN, DEV_BAD_POSITION, DEV_TIMEOUT, DEV_NONFINITE = 0x1, 0x2, 0x4, 0x8, 0x10
 
 _P = ctypes.c_void_p
@@ -48,6 +49,8 @@ SIGNATURES = {
     "kvq8_decode_combine": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
     "kvq8_decode_step": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _I,
                               _P, _F, _P, _P, _SZ, _P, _P]),
+    "kvq8_decode_step_ex": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _I,
+                                 _P, _F, _P, _P, _SZ, _P, ctypes.c_uint32, _P]),
     "kvq8_decode_step_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I,
                                    _P, _I, _I, _P, _F, _P, _P, _SZ, _P, _P]),
     "kvq8_host_device_pointer": (_P, [_P]),
@@ -270,21 +273,21 @@ def decode_attn(q, cache: KVCache, block_table, ctx_lens, out, workspace,
 
 
 def decode_step(q, k_new, v_new, cache: KVCache, block_table, ctx_lens, out, workspace,
-                sm_scale: Optional[float] = None, dev_status=None, stream=None):
+                sm_scale: Optional[float] = None, dev_status=None, stream=None, cache_ready: bool = False):
     """One decode step: append k_new/v_new (fp32 [batch][nkv][128]) at position
     ctx_lens-1 and attend over ctx_lens tokens (two launches: the split kernel,
     which also appends the token, and the combine, a programmatic dependent of
-    the split)."""
+    the split).  cache_ready: KVQ8_STEP_CACHE_READY (kvq8_decode_step_ex)."""
     _need_cuda(q, k_new, v_new, block_table, ctx_lens, out, workspace, *cache, dev_status)
     batch, nqh, nkv, hd, max_blocks = _decode_common(q, cache, block_table, ctx_lens)
     sm = 1.0 / math.sqrt(hd) if sm_scale is None else sm_scale
-    st = load().kvq8_decode_step(
+    st = load().kvq8_decode_step_ex(
         _ptr(q), _ptr(k_new), _ptr(v_new), batch, nqh, nkv, hd, _ptr(cache.k_pool),
         _ptr(cache.v_pool), _ptr(cache.k_scale), _ptr(cache.v_scale), cache.num_blocks,
         _ptr(block_table), max_blocks, BLOCK_SIZE, _ptr(ctx_lens), sm, _ptr(out),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status),
-        _stream(stream))
-    _check("kvq8_decode_step", st)
+        STEP_CACHE_READY if cache_ready else 0, _stream(stream))
+    _check("kvq8_decode_step_ex", st)
 
 
 def decode_step_host(q_host, k_host, v_host, out_host, q, k_new, v_new, cache: KVCache, block_table,
@@ -359,7 +362,7 @@ class DecodeStep:
 
     def __init__(self, q, k_new, v_new, cache: KVCache, block_table, ctx_lens, out, workspace,
                  sm_scale: Optional[float] = None, dev_status=None, stream=None,
-                 q_host=None, k_host=None, v_host=None, out_host=None):
+                 q_host=None, k_host=None, v_host=None, out_host=None, cache_ready: bool = False):
         _need_cuda(q, k_new, v_new, block_table, ctx_lens, out, workspace, *cache, dev_status)
         batch, nqh, nkv, hd, max_blocks = _decode_common(q, cache, block_table, ctx_lens)
         sm = 1.0 / math.sqrt(hd) if sm_scale is None else sm_scale
@@ -370,7 +373,10 @@ class DecodeStep:
                   _P(_ptr(cache.k_scale)), _P(_ptr(cache.v_scale)), _I(cache.num_blocks),
                   _P(_ptr(block_table)), _I(max_blocks), _I(BLOCK_SIZE), _P(_ptr(ctx_lens)), _F(sm)]
         tail = [_P(_ptr(workspace)), _SZ(workspace.numel() * workspace.element_size()), _P(_ptr(dev_status)), st]
-        self._dev_args = tuple([_P(_ptr(q)), _P(_ptr(k_new)), _P(_ptr(v_new))] + common + [_P(_ptr(out))] + tail)
+        flags = [ctypes.c_uint32(STEP_CACHE_READY if cache_ready else 0)]
+        ex_tail = tail[:-1] + flags + tail[-1:]
+        self._dev_args = tuple([_P(_ptr(q)), _P(_ptr(k_new)), _P(_ptr(v_new))] + common + [_P(_ptr(out))] +
+                               ex_tail)
         self._keep = (q, k_new, v_new, cache, block_table, ctx_lens, out, workspace, dev_status, stream)
         self._host_fn = None
         hosts = (q_host, k_host, v_host, out_host)
@@ -383,18 +389,20 @@ class DecodeStep:
                 raise ValueError("host and device buffers differ in shape")
             mapped = [lib.kvq8_host_device_pointer(_ptr(h)) for h in hosts]
             if all(mapped):
-                self._host_fn = lib.kvq8_decode_step
+                self._host_fn = lib.kvq8_decode_step_ex
                 self._host_args = tuple([_P(mapped[0]), _P(mapped[1]), _P(mapped[2])] + common +
-                                        [_P(mapped[3])] + tail)
+                                        [_P(mapped[3])] + ex_tail)
             else:
+                if cache_ready:
+                    raise ValueError("cache_ready needs page-locked host buffers (the copying path has no flags)")
                 self._host_fn = lib.kvq8_decode_step_host
                 self._host_args = tuple([_P(_ptr(h)) for h in hosts] + list(self._dev_args[:3]) + common +
                                         [self._dev_args[3 + len(common)]] + tail)
             self._keep = self._keep + hosts
-        self.host_direct = self._host_fn is not None and self._host_fn is lib.kvq8_decode_step
+        self.host_direct = self._host_fn is not None and self._host_fn is lib.kvq8_decode_step_ex
 
     def run(self):
-        _check("kvq8_decode_step", self._lib.kvq8_decode_step(*self._dev_args))
+        _check("kvq8_decode_step_ex", self._lib.kvq8_decode_step_ex(*self._dev_args))
 
     def run_host(self):
         if self._host_fn is None:

@@ -159,6 +159,20 @@ def test_noalloc_checks_arguments_like_the_regular_entry_point(lib):
     assert na(**big) == kvq8.ERR_WORKSPACE
 
 
+def test_decode_step_ex_flags(lib):
+    """kvq8_decode_step_ex refuses undefined flag bits before anything else;
+    with 0 or KVQ8_STEP_CACHE_READY it checks its arguments as kvq8_decode_step."""
+    def step_ex(flags, q=FAKE, batch=1):
+        return lib.kvq8_decode_step_ex(q, FAKE, FAKE, batch, 8, 8, 128, FAKE, FAKE, FAKE, FAKE, 4, FAKE, 4,
+                                       256, FAKE, 0.088, FAKE, None, 0, None, flags, None)
+    assert step_ex(0x2) == kvq8.ERR_INVALID_ARG
+    assert step_ex(0x80000000) == kvq8.ERR_INVALID_ARG
+    for flags in (0, kvq8.STEP_CACHE_READY):
+        assert step_ex(flags, batch=0) == kvq8.OK
+        assert step_ex(flags, q=None) == kvq8.ERR_INVALID_ARG
+        assert step_ex(flags) == kvq8.ERR_WORKSPACE
+
+
 def test_host_buffer_entry_validation(lib):
     """The host-buffer entries check every argument before queueing a copy."""
     def app(**kw):

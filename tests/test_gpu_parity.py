@@ -488,14 +488,78 @@ def test_output_fed_back_as_query_without_sync(gpu_lib):
         kvq8.decode_step(x, case.k_new_d, case.v_new_d, case.cache, case.table_d, case.lens_d, o, ws,
                          dev_status=case.status)
 
+    def step_ready(x, o):
+        # the cache, table and lengths are final before each call's preceding
+        # kernel begins (only the query comes from it): the flagged step still
+        # waits for its query
+        kvq8.decode_step(x, case.k_new_d, case.v_new_d, case.cache, case.table_d, case.lens_d, o, ws,
+                         dev_status=case.status, cache_ready=True)
+
     step(case.q_d, torch.empty_like(case.q_d))   # the appended token is in place from here on
-    for call in (attn, step):
+    for call in (attn, step, step_ready):
         fast = _chain(call, case.q_d, 6, sync_between=False)
         slow = _chain(call, case.q_d, 6, sync_between=True)
         for a, b in zip(fast, slow):
             assert np.isfinite(a).all()
             assert np.array_equal(a, b)
     assert case.status_bits() == 0
+
+
+def test_decode_step_cache_ready_flag_gives_identical_results(gpu_lib):
+    # KVQ8_STEP_CACHE_READY only lets the split kernel start copying earlier
+    cfg = wl.scaled(wl.BATCH64_RAGGED, batch=7, ctx_range=(1, 6000))
+    a, b = StepCase(cfg), StepCase(cfg)
+    ws = kvq8.alloc_workspace(cfg.batch, cfg.nqh, cfg.nkv, a.max_blocks)
+    plain = a.step(ws)
+    out = torch.full_like(b.q_d, float("nan"))
+    kvq8.decode_step(b.q_d, b.k_new_d, b.v_new_d, b.cache, b.table_d, b.lens_d, out, ws,
+                     dev_status=b.status, cache_ready=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), plain)
+    pa, pb = a.host_pools(), b.host_pools()
+    for bb in range(cfg.batch):
+        for h in range(cfg.nkv):
+            for x, y in zip(a.gather_unit(pa, bb, h), b.gather_unit(pb, bb, h)):
+                assert np.array_equal(x, y)
+    _check_step(b, out.cpu().numpy())
+    assert b.status_bits() == 0
+
+
+@pytest.mark.parametrize("cache_ready", [False, True])
+def test_per_layer_step_calls_in_a_graph(gpu_lib, cache_ready):
+    """A decode that runs one layer per call: 28 kvq8_decode_step calls at batch
+    1 (one per layer of the Qwen3-2B stack, each with its own workspace, all in
+    one pool), captured in a CUDA graph and replayed twice; every layer's output
+    against the oracle, and the flagged chain against the plain one bit for bit."""
+    cfg = wl.scaled(wl.QWEN3_2B_28L_8K, ctx=1500)
+    case = StepCase(cfg)
+    layers = cfg.batch
+    wss = [kvq8.alloc_workspace(1, cfg.nqh, cfg.nkv, case.max_blocks) for _ in range(layers)]
+    outs = torch.full_like(case.q_d, float("nan"))
+    s = torch.cuda.Stream()
+
+    def calls():
+        for l in range(layers):
+            kvq8.decode_step(case.q_d[l:l + 1], case.k_new_d[l:l + 1], case.v_new_d[l:l + 1], case.cache,
+                             case.table_d[l:l + 1], case.lens_d[l:l + 1], outs[l:l + 1], wss[l],
+                             dev_status=case.status, stream=s, cache_ready=cache_ready)
+
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        calls()
+    s.synchronize()
+    first = outs.cpu().numpy()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        calls()
+    outs.fill_(float("nan"))
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    got = outs.cpu().numpy()
+    assert np.array_equal(got, first)
+    assert case.status_bits() == 0
+    _check_step(case, got)
 
 
 def test_decode_step_equals_append_then_decode(gpu_lib):
