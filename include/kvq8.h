@@ -23,6 +23,13 @@
  *   memory themselves over the host link, which pays for the small per-step
  *   buffers (q, the new token's k_new and v_new, out), not for the pools or
  *   the workspace.
+ * - The last kernel of every decode call (the split merge) lets the next
+ *   kernel of the stream launch before it completes (programmatic dependent
+ *   launch): a kernel launched after it with the programmatic stream
+ *   serialisation attribute must wait for it (griddepcontrol.wait /
+ *   cudaGridDependencySynchronize) before reading `out`; every kernel of this
+ *   library does.  Kernels launched without that attribute start after it
+ *   completes, as usual.
  * - Work is enqueued asynchronously on `stream`.  Argument errors are
  *   detected on the host and returned before anything is enqueued.  A
  *   failed launch returns KVQ8_ERR_CUDA (the CUDA error is left for
@@ -284,7 +291,8 @@ kvq8_status kvq8_decode_step(const float *q, const float *k_new, const float *v_
  * A decode that runs one layer per call after the layer's own projections
  * (which write q, k_new and v_new only) meets this; so does a chain of steps
  * that differ only in those inputs.  Results are identical with and without
- * the flag.  Flags outside KVQ8_STEP_CACHE_READY return KVQ8_ERR_INVALID_ARG.
+ * the flag.
+ * Flags outside KVQ8_STEP_CACHE_READY return KVQ8_ERR_INVALID_ARG.
  */
 #define KVQ8_STEP_CACHE_READY 0x1u
 kvq8_status kvq8_decode_step_ex(const float *q, const float *k_new, const float *v_new,

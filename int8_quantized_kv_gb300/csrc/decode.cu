@@ -146,16 +146,14 @@ __device__ __forceinline__ bool slot_turn_bounded(volatile int *done, int round,
 }
 
 // A decode step's new token of unit (b, h), position pos = ctx_lens[b] - 1,
-// which is row t of the stage staged at st: quantised by the warp ([Day 9-3]
-// §2 rule, the same functions as the append kernels; lane l holds dims
-// 4l..4l+3), written over the row the copy brought in (K row with its chunk
+// which is row t of the stage staged at st (xk, xv: the token's K and V rows,
+// lane l holding dims 4l..4l+3, loaded by the caller ahead of time):
+// quantised by the warp ([Day 9-3] §2 rule, the same functions as the append
+// kernels), written over the row the copy brought in (K row with its chunk
 // order, V column of the dim-major quarter, both scales) and into the pools
 // and scale arrays.  Only this CTA reads that position in this launch.
 __device__ __noinline__ void append_new_token(const DecodeParams &p, int b, int h, int pos, int t,
-                                                 int lane, unsigned char *st) {
-    const size_t src = ((size_t)b * p.nkv + h) * kHD;
-    float4 xk = reinterpret_cast<const float4 *>(p.k_new + src)[lane];
-    float4 xv = reinterpret_cast<const float4 *>(p.v_new + src)[lane];
+                                                 int lane, unsigned char *st, float4 xk, float4 xv) {
     const int phys = p.block_table[(size_t)b * p.max_blocks + pos / kBS];   // valid: the stage was copied
     const float sk = kv_row_scale_checked(xk, p.dev_status), sv = kv_row_scale_checked(xv, p.dev_status);
     const uint32_t wk = low_bytes4(kv_code_bytes4(xk, sk));
@@ -406,9 +404,23 @@ decode_split_kernel(DecodeParams p) {
             // a decode step appends its new token at position ctx_lens[b] - 1
             // (none for an empty context or one beyond the table)
             int app_pos = -1;
-            if (p.k_new) {
+            if (!kMixed && p.k_new) {   // (a mixed-precision decode appends nothing)
                 const int Lraw = p.ctx_lens[b];
                 if (Lraw >= 1 && Lraw <= cap) app_pos = Lraw - 1;
+            }
+
+            // the warp that decodes the stage holding the new token loads the
+            // token's K and V rows now, beside the query rows, so that their
+            // latencies overlap (G = 8: at the stage, its registers are spent)
+            constexpr bool kPreloadNew = G <= 4;
+            float4 nxk = make_float4(0.f, 0.f, 0.f, 0.f), nxv = nxk;
+            if (kPreloadNew && app_pos >= sp.x) {
+                const int sj = (app_pos - sp.x) / kStageTok - off;
+                if (sj >= 0 && sj < seg_n && sj % kConsumerWarps == warp) {
+                    const size_t src = ((size_t)b * p.nkv + h) * kHD;
+                    nxk = reinterpret_cast<const float4 *>(p.k_new + src)[lane];
+                    nxv = reinterpret_cast<const float4 *>(p.v_new + src)[lane];
+                }
             }
 
             // segment 1: quantise this unit's G query heads once
@@ -449,8 +461,14 @@ decode_split_kernel(DecodeParams p) {
                     const float *vs_st = ks_st + kStageTok;
                     const int nvalid = min(kStageTok, L - (sp.x + (off + j) * kStageTok));
                     const int tnew = app_pos - (sp.x + (off + j) * kStageTok);
-                    if (tnew >= 0 && tnew < kStageTok)
-                        append_new_token(p, b, h, app_pos, tnew, lane, const_cast<unsigned char *>(st));
+                    if (tnew >= 0 && tnew < kStageTok) {
+                        if (!kPreloadNew) {
+                            const size_t src = ((size_t)b * p.nkv + h) * kHD;
+                            nxk = reinterpret_cast<const float4 *>(p.k_new + src)[lane];
+                            nxv = reinterpret_cast<const float4 *>(p.v_new + src)[lane];
+                        }
+                        append_new_token(p, b, h, app_pos, tnew, lane, const_cast<unsigned char *>(st), nxk, nxv);
+                    }
                     const int ta = lane, tb = lane + 32;
                     const bool va = ta < nvalid, vb = tb < nvalid;
 
@@ -698,49 +716,64 @@ decode_split_kernel(DecodeParams p) {
 // The records come from one split kernel, or from two (mixed precision by
 // token age: the 4-bit split over [0, x) and the int8 split over [x, L)).
 constexpr int kCombineRegs = 8;   // records merged from registers (more: the loop below)
+constexpr int kCombineWide = 32;  // records of one source merged after one load round
 
 __global__ void __launch_bounds__(kHD)
 decode_combine_kernel(DecodeParams p, int G) {
-    pdl_wait();  // the split kernel's records are visible after this
-    // the next kernel may be scheduled now: a kernel of this library that
-    // follows (the next step's append, a split) waits for this grid to
-    // complete before it reads anything
+    // The next kernel of the stream may be scheduled at once: every kernel of
+    // this library waits for the grid before it to complete before it reads
+    // what that grid writes (a decode step's split kernel, with the cache
+    // declared ready, reads only the cache before that), and its CTAs take the
+    // SMs that the split kernel before this one leaves.
     pdl_launch_dependents();
+    pdl_wait();  // the split kernel's records are visible after this
     const int qh = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
     const int h = qh / G, g = qh % G;
     const int cap = p.max_blocks * kBS;
+    const size_t u = (size_t)b * p.nkv + h;
+    // the unit's record directories are loaded beside its length (one load
+    // round); an entry is used only when the length says the unit has records
+    // in that source (an empty unit's entry is not written by the split)
+    const int2 meta0_raw = p.ws_meta[u];
+    const int2 meta1_raw = p.ws_meta2 ? p.ws_meta2[u] : make_int2(0, 0);
     const int2 sp = seq_span(p, b, cap);
     float *o = p.out + ((size_t)b * p.nqh + qh) * kHD + d;
     if (sp.y == 0) { *o = 0.0f; return; }
-    const size_t u = (size_t)b * p.nkv + h;
     // source 0: this decode's records over [x, L); source 1: the 4-bit split's over [0, x)
     const bool has0 = sp.y > sp.x, has1 = p.ws_meta2 != nullptr && sp.x > 0;
-    const int2 meta0 = has0 ? p.ws_meta[u] : make_int2(0, 0);
-    const int2 meta1 = has1 ? p.ws_meta2[u] : make_int2(0, 0);
+    const int2 meta0 = has0 ? meta0_raw : make_int2(0, 0);
+    const int2 meta1 = has1 ? meta1_raw : make_int2(0, 0);
     const size_t r00 = (size_t)meta0.x + u, r10 = (size_t)meta1.x + u;
-    if (meta1.y == 0 && meta0.y <= kCombineRegs) {
+    // the records of one source (both single-source paths below read these, so
+    // that a call whose records all come from one split kernel gives the same
+    // bits whichever source slot holds them)
+    const bool one = meta0.y == 0 || meta1.y == 0;
+    const float *ml1 = meta0.y ? p.ws_ml : p.ws_ml2, *acc1 = meta0.y ? p.ws_acc : p.ws_acc2;
+    const size_t r01 = meta0.y ? r00 : r10;
+    const int n1 = meta0.y ? meta0.y : meta1.y;
+    if (one && n1 <= kCombineRegs) {
         // the usual case: every record's (M, S) and accumulator loaded at once,
         // then merged in the same order as below
         float mr[kCombineRegs], sr[kCombineRegs], ar[kCombineRegs];
 #pragma unroll
         for (int j = 0; j < kCombineRegs; ++j) {
-            if (j < meta0.y) {
-                const size_t r = (r00 + j) * G + g;
-                const float2 ml = *reinterpret_cast<const float2 *>(p.ws_ml + r * 2);
+            if (j < n1) {
+                const size_t r = (r01 + j) * G + g;
+                const float2 ml = *reinterpret_cast<const float2 *>(ml1 + r * 2);
                 mr[j] = ml.x;
                 sr[j] = ml.y;
-                ar[j] = p.ws_acc[r * kHD + d];
+                ar[j] = acc1[r * kHD + d];
             }
         }
         float m = -INFINITY;
 #pragma unroll
         for (int j = 0; j < kCombineRegs; ++j)
-            if (j < meta0.y) m = fmaxf(m, mr[j]);
+            if (j < n1) m = fmaxf(m, mr[j]);
         float s_sum = 0.0f, a = 0.0f;
         if (m != -INFINITY) {
 #pragma unroll
             for (int j = 0; j < kCombineRegs; ++j) {
-                if (j < meta0.y) {
+                if (j < n1) {
                     const float f = exp2f(mr[j] - m);
                     s_sum = fmaf(sr[j], f, s_sum);
                     a = fmaf(ar[j], f, a);
@@ -750,9 +783,40 @@ decode_combine_kernel(DecodeParams p, int G) {
         *o = s_sum > 0.0f ? a / s_sum : 0.0f;
         return;
     }
-    // more records (a call of few long units, or two sources): groups of
-    // kCombineRegs records, each group loaded at once and merged into the
-    // running state with the same rescaling rule
+    if (one && n1 <= kCombineWide) {
+        // up to 32 records of one source (a call of few long units): one load
+        // round, then the same merge
+        float2 mlr[kCombineWide];
+        float ar[kCombineWide];
+#pragma unroll
+        for (int j = 0; j < kCombineWide; ++j) {
+            if (j < n1) {
+                const size_t r = (r01 + j) * G + g;
+                mlr[j] = *reinterpret_cast<const float2 *>(ml1 + r * 2);
+                ar[j] = acc1[r * kHD + d];
+            }
+        }
+        float m = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kCombineWide; ++j)
+            if (j < n1) m = fmaxf(m, mlr[j].x);
+        float s_sum = 0.0f, a = 0.0f;
+        if (m != -INFINITY) {
+#pragma unroll
+            for (int j = 0; j < kCombineWide; ++j) {
+                if (j < n1) {
+                    const float f = exp2f(mlr[j].x - m);
+                    s_sum = fmaf(mlr[j].y, f, s_sum);
+                    a = fmaf(ar[j], f, a);
+                }
+            }
+        }
+        *o = s_sum > 0.0f ? a / s_sum : 0.0f;
+        return;
+    }
+    // more records, or two sources: groups of kCombineRegs records, each group
+    // loaded at once and merged into the running state with the same
+    // rescaling rule
     float m = -INFINITY, s_sum = 0.0f, a = 0.0f;
     auto merge_group = [&](const float *ml, const float *accp, size_t r0, int n) {
         float mr[kCombineRegs], sr[kCombineRegs], ar[kCombineRegs];

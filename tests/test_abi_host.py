@@ -161,7 +161,7 @@ def test_noalloc_checks_arguments_like_the_regular_entry_point(lib):
 
 def test_decode_step_ex_flags(lib):
     """kvq8_decode_step_ex refuses undefined flag bits before anything else;
-    with 0 or KVQ8_STEP_CACHE_READY it checks its arguments as kvq8_decode_step."""
+    with its defined flags it checks its arguments as kvq8_decode_step."""
     def step_ex(flags, q=FAKE, batch=1):
         return lib.kvq8_decode_step_ex(q, FAKE, FAKE, batch, 8, 8, 128, FAKE, FAKE, FAKE, FAKE, 4, FAKE, 4,
                                        256, FAKE, 0.088, FAKE, None, 0, None, flags, None)
