@@ -201,7 +201,11 @@ decode_split_kernel(DecodeParams p) {
     // were final before that kernel began (cache_ready): then the prologue and
     // the producer's copies go ahead, and only the consumers wait (they read
     // the query and the new token and write the workspace).
-    if (!p.cache_ready) pdl_wait();
+    // In a mixed-precision decode (kMixed) the kernel before is the 4-bit split
+    // of the same call, which writes nothing this kernel reads (it released
+    // this one right after its own wait): no wait here; this kernel waits for
+    // it at its end instead, before completing.
+    if (!kMixed && !p.cache_ready) pdl_wait();
     Misc *misc = reinterpret_cast<Misc *>(smem + Lay::oMisc);
     int8_t *q_codes = reinterpret_cast<int8_t *>(smem + Lay::oQCodes);
     float *q_scale = reinterpret_cast<float *>(smem + Lay::oQScale);
@@ -357,7 +361,7 @@ decode_split_kernel(DecodeParams p) {
         }
     } else {
         // =========================== consumer warps ==========================
-        if (p.cache_ready) pdl_wait();
+        if (!kMixed && p.cache_ready) pdl_wait();
         unsigned char *scratch = smem + Lay::oScratch + warp * Lay::kScratch;
         __half *p_hi = reinterpret_cast<__half *>(scratch);
         __half *p_lo = p_hi + G * kPRowHalves;
@@ -706,6 +710,7 @@ decode_split_kernel(DecodeParams p) {
             if (++h == p.nkv) { h = 0; ++b; }
         }
     }
+    if (kMixed) pdl_wait();   // the 4-bit split's records are complete before this grid is
     pdl_launch_dependents();
     __syncthreads();
 }

@@ -326,6 +326,11 @@ int4_decode_split_kernel(Int4DecodeParams p) {
     constexpr bool kPack = G <= 4;
     constexpr bool kPack2 = G <= 2;
     pdl_wait();
+    // In a mixed-precision decode the next kernel is the int8 split over the
+    // recent tokens, which reads nothing this kernel writes: it may start now
+    // and take the SMs this grid leaves (it waits for this grid before it
+    // completes, so the merge after it sees both splits' records).
+    if (p.n4_blocks) pdl_launch_dependents();
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t4 = lane & 3;
