@@ -88,6 +88,10 @@ def parse_args(argv=None):
                     help="skip the fp32-KV decode comparator leg")
     ap.add_argument("--plain-step", action="store_true",
                     help="time the decode step without KVQ8_STEP_CACHE_READY")
+    ap.add_argument("--roof-launches", type=int, default=ROOF_MIN_LAUNCHES,
+                    help="launches of each of the dominant kernel's loops (at least)")
+    ap.add_argument("--roof-seconds", type=float, default=ROOF_TARGET_S,
+                    help="device time of the back-to-back loop (at least)")
     return ap.parse_args(argv)
 
 
@@ -527,11 +531,12 @@ class Gpu:
         torch.cuda.synchronize()
         self.check_status("during warm-up")
         est = self.loop_s(kernel_call, 3)
-        n_b2b = max(ROOF_MIN_LAUNCHES, int(math.ceil(ROOF_TARGET_S / max(est, 1e-7))))
+        n_roof = max(1, args.roof_launches)
+        n_b2b = max(n_roof, int(math.ceil(args.roof_seconds / max(est, 1e-7))))
         sampler = ClockSampler(self.local).start()
         sampler.open()
         b2b = self.loop_s(kernel_call, n_b2b)
-        iso = self.isolated_s(kernel_call, ROOF_MIN_LAUNCHES)
+        iso = self.isolated_s(kernel_call, n_roof)
         t_start, t_end = self.event(), self.event()
         barrier()
         torch.cuda.synchronize()
@@ -548,7 +553,7 @@ class Gpu:
         total, slowest = aggregate(sbytes * args.steps, elapsed, self.dev)
         roof = {"bound": "hbm", "kernel": kernel_name, "algorithmic_bytes_per_launch": kernel_bytes,
                 "us_per_launch": round(b2b * 1e6, 3), "launches": n_b2b,
-                "us_per_launch_isolated": round(iso * 1e6, 3), "launches_isolated": ROOF_MIN_LAUNCHES,
+                "us_per_launch_isolated": round(iso * 1e6, 3), "launches_isolated": n_roof,
                 "timing": ("us_per_launch: mean of a loop of back-to-back launches rotating the cache "
                            "copies (CUDA events on the launching stream around the loop); "
                            "us_per_launch_isolated: mean over launches each between its own events"),
