@@ -265,6 +265,7 @@ constexpr uint64_t kWait4Ns = 2000000000ull;                      // bound of ev
 
 template <int G>
 struct Int4Smem {
+    float qrows[G * kHD];            // the unit's query rows
     uint4 qa[8][32];                 // per k-step and lane: a0 high, a2 high, a0 low, a2 low
     float qq[8][2];                  // Q_g per head
     float qmax[kWarps4];
@@ -335,6 +336,16 @@ int4_decode_split_kernel(Int4DecodeParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t4 = lane & 3;
     const int cap = p.max_blocks * kBS;
+    // the unit's query rows, loaded beside the context length (no load of
+    // the prologue waits for another but the block id after the length)
+    constexpr int kQV = (G * 32 + kWarps4 * 32 - 1) / (kWarps4 * 32);   // float4 per thread
+    const float4 *qsrc = reinterpret_cast<const float4 *>(p.q + ((size_t)b * p.nqh + (size_t)h * G) * kHD);
+    float4 qv[kQV];
+#pragma unroll
+    for (int r = 0; r < kQV; ++r) {
+        const int i = threadIdx.x + r * kWarps4 * 32;
+        qv[r] = i < G * 32 ? qsrc[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     int L = p.ctx_lens[b];
     if (L < 0 || L > cap) {
         if (threadIdx.x == 0 && split == 0 && h == 0) flag_status(p.dev_status, KVQ8_DEV_BAD_CTX_LEN);
@@ -376,11 +387,16 @@ int4_decode_split_kernel(Int4DecodeParams p) {
                                              bar0 + 8 * i, pol, lane) >= 0) << i;
     bool aborted = false;
 
-    const float *qrow = p.q + ((size_t)b * p.nqh + (size_t)h * G) * kHD;
+    const float *qrow = sm.qrows;
     // power of two 2^k with max |q| * 2^k in [2^13, 2^14)
     {
         float m = 0.0f;
-        for (int i = threadIdx.x; i < G * kHD; i += kWarps4 * 32) m = fmaxf(m, fabsf(qrow[i]));
+#pragma unroll
+        for (int r = 0; r < kQV; ++r) {
+            const int i = threadIdx.x + r * kWarps4 * 32;
+            if (i < G * 32) reinterpret_cast<float4 *>(sm.qrows)[i] = qv[r];
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(qv[r].x), fabsf(qv[r].y)), fmaxf(fabsf(qv[r].z), fabsf(qv[r].w))));
+        }
         m = warp_max(m);
         if (lane == 0) sm.qmax[warp] = m;
     }
@@ -921,11 +937,20 @@ cudaError_t launch_int4_split_g(const Int4DecodeParams &p, cudaStream_t s) {
                                         (int)smem);
         },
         [&] {
+            // a programmatic dependent of the previous kernel in the stream: every
+            // thread waits for that kernel first (its outputs may be this
+            // kernel's inputs, and a merge kernel before it may still read the
+            // workspace), but the launch itself overlaps its end
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(p.nsplit, p.nkv, p.batch);
             cfg.blockDim = dim3(kWarps4 * 32);
             cfg.dynamicSmemBytes = smem;
             cfg.stream = s;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
             return cudaLaunchKernelEx(&cfg, int4_decode_split_kernel<G>, p);
         });
 }
