@@ -55,11 +55,18 @@ namespace {
 constexpr int kConsumerWarps = 7;
 constexpr int kSplitThreads = (kConsumerWarps + 1) * 32;
 constexpr int kSmemLimit = 232448;          // 227 KiB opt-in per CTA on sm_103a
+// In a mixed-precision decode the int8 split runs after the 4-bit split of the
+// same call and takes each SM as that grid leaves it.  With a ring this small
+// (and its registers) it fits beside one CTA of the 4-bit split (about 48 KiB
+// of an SM's 228 KiB), so it starts on an SM as soon as two of its three
+// 4-bit CTAs are done, instead of waiting for the last, which would run
+// alone with a third of the SM's warps.
+constexpr int kSmemLimitMixed = 184320;
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 constexpr int kPRowHalves = 72;             // P row: 64 tokens + 8 halves of padding
 constexpr float kLazyLog2 = 8.0f;           // running-max slack (log2 units), see segment 2b
 
-template <int G>
+template <int G, int kLimit = kSmemLimit>
 struct SplitLayout {
     // per consumer warp: P (hi, lo) [G][72] halves during a stage, or the
     // warp's final state (acc [G][128], M [G], S [G]) when a segment ends
@@ -68,7 +75,7 @@ struct SplitLayout {
     static constexpr int kQScale = G * kNQB * 4;
     static constexpr int kMisc = 128;
     static constexpr int kFixed = kConsumerWarps * kScratch + kQCodes + kQScale + kMisc;
-    static constexpr int kStages = (kSmemLimit - kFixed - 512) / (kStageBytes + 16 + 16 + 4);
+    static constexpr int kStages = (kLimit - kFixed - 512) / (kStageBytes + 16 + 16 + 4);
     static constexpr int oRing = 0;
     static constexpr int oScratch = kStages * kStageBytes;
     static constexpr int oQCodes = oScratch + kConsumerWarps * kScratch;
@@ -80,7 +87,7 @@ struct SplitLayout {
     static constexpr int oDone = oSkip + kStages * 4;
     static constexpr int kBytes = oDone + kStages * 4;
     static_assert(oMisc % 16 == 0 && oFull % 16 == 0 && oScratch % 16 == 0, "alignment");
-    static_assert(kBytes <= kSmemLimit, "shared memory budget");
+    static_assert(kBytes <= kLimit, "shared memory budget");
     static_assert(kStages >= 8, "ring too shallow");
     static_assert(G * 2 * kPRowHalves * 2 <= kScratch, "P fits the warp scratch");
 };
@@ -189,7 +196,7 @@ __device__ __noinline__ void append_new_token(const DecodeParams &p, int b, int 
 template <int G, bool kMixed>
 __global__ void __launch_bounds__(kSplitThreads, 1)
 decode_split_kernel(DecodeParams p) {
-    using Lay = SplitLayout<G>;
+    using Lay = SplitLayout<G, kMixed ? kSmemLimitMixed : kSmemLimit>;
     extern __shared__ __align__(1024) unsigned char smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
@@ -873,7 +880,7 @@ int device_sm_count() {
 
 template <int G, bool kMixed>
 cudaError_t launch_split_gm(const DecodeParams &p, cudaStream_t s) {
-    using Lay = SplitLayout<G>;
+    using Lay = SplitLayout<G, kMixed ? kSmemLimitMixed : kSmemLimit>;
     static std::atomic<uint64_t> configured{0};
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;

@@ -933,8 +933,13 @@ cudaError_t launch_int4_split_g(const Int4DecodeParams &p, cudaStream_t s) {
     return launch_after_setting(
         configured,
         [] {
-            return cudaFuncSetAttribute(int4_decode_split_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)smem);
+            // the largest shared-memory carveout: in a mixed-precision decode the
+            // int8 split joins an SM while one of these CTAs still runs there
+            cudaError_t e = cudaFuncSetAttribute(int4_decode_split_kernel<G>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            return cudaFuncSetAttribute(int4_decode_split_kernel<G>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                        (int)cudaSharedmemCarveoutMaxShared);
         },
         [&] {
             // a programmatic dependent of the previous kernel in the stream: every
