@@ -188,3 +188,31 @@ def test_int4_decode_on_host_mapped_buffers(gpu_lib):
     assert np.array_equal(out_h.numpy(), dev_out)
     with pytest.raises(ValueError):
         kvq8.HostMapped(torch.zeros(4))          # pageable: not addressable by the device
+
+
+def test_int4_back_to_back_calls_share_the_workspace(gpu_lib):
+    # three calls on one stream and one workspace with no synchronisation in
+    # between, the second with another query: each split may start before the
+    # merge of the call before it has read the workspace, and must wait for it
+    # (programmatic dependent launch); every output equals its own decode
+    cfg = wl.Workload("int4_b2b", 530, batch=3, nqh=8, nkv=2, ctx_range=(700, 3000))
+    case = Int4Case(cfg)
+    q1 = case.q
+    q2 = np.random.default_rng(531).standard_normal(q1.shape).astype(np.float32) * 2.0
+    q1_d, q2_d = case.q_d, torch.from_numpy(q2).cuda()
+    ws = kvq8.alloc_workspace(cfg.batch, cfg.nqh, cfg.nkv, case.max_blocks)
+    outs = [torch.full_like(q1_d, float("nan")) for _ in range(3)]
+    for q_d, out in zip((q1_d, q2_d, q1_d), outs):
+        kvq8.decode_attn4(q_d, case.cache, case.table_d, case.lens_d, out, ws, sm_scale=SM_SCALE,
+                          dev_status=case.status)
+    torch.cuda.synchronize()
+    assert case.status.item() == 0
+    o1, o2, o3 = (o.cpu().numpy() for o in outs)
+    assert np.array_equal(o1, o3)
+    G = cfg.group
+    for q, o in ((q1, o1), (q2, o2)):
+        case.q = q
+        for b in range(cfg.batch):
+            for h in range(cfg.nkv):
+                assert_close(o[b, h * G:(h + 1) * G], case.oracle_unit(b, h), f"int4 back to back b={b} h={h}")
+    case.q = q1

@@ -146,3 +146,31 @@ def test_mixed_qwen_shape_sampled(gpu_lib):
     rng = np.random.default_rng(7)
     for b, h in {(int(rng.integers(cfg.batch)), int(rng.integers(cfg.nkv))) for _ in range(5)}:
         assert_close(out[b, h * G:(h + 1) * G], case.oracle_mixed(b, h), f"qwen mixed b={b} h={h}")
+
+
+def test_mixed_back_to_back_calls_share_the_workspace(gpu_lib):
+    # three calls on one stream and one workspace with no synchronisation in
+    # between, the second with another query: the 4-bit split of a call may
+    # start before the merge of the call before it has read the workspace, and
+    # must wait for it; every output equals its own decode
+    cfg = wl.Workload("mix_b2b", 760, batch=3, nqh=8, nkv=2, ctx_range=(900, 2600))
+    case = MixedCase(cfg, n4=[2, 3, 1], seed=7)
+    q1 = case.q
+    q2 = np.random.default_rng(761).standard_normal(q1.shape).astype(np.float32) * 2.0
+    q1_d, q2_d = case.q_d, torch.from_numpy(q2).cuda()
+    ws = kvq8.alloc_mixed_workspace(cfg.batch, cfg.nqh, cfg.nkv, case.max_blocks)
+    outs = [torch.full_like(q1_d, float("nan")) for _ in range(3)]
+    for q_d, out in zip((q1_d, q2_d, q1_d), outs):
+        kvq8.decode_attn_mixed(q_d, case.cache, case.table_d, case.cache4, case.table4_d, case.lens_d,
+                               case.n4_d, out, ws, sm_scale=SM_SCALE, dev_status=case.status)
+    torch.cuda.synchronize()
+    assert case.status_bits() == 0
+    o1, o2, o3 = (o.cpu().numpy() for o in outs)
+    assert np.array_equal(o1, o3)
+    G = cfg.group
+    for q, o in ((q1, o1), (q2, o2)):
+        case.q = q
+        for b in range(cfg.batch):
+            for h in range(cfg.nkv):
+                assert_close(o[b, h * G:(h + 1) * G], case.oracle_mixed(b, h), f"mixed back to back b={b} h={h}")
+    case.q = q1
