@@ -826,9 +826,41 @@ decode_combine_kernel(DecodeParams p, int G) {
         *o = s_sum > 0.0f ? a / s_sum : 0.0f;
         return;
     }
-    // more records, or two sources: groups of kCombineRegs records, each group
-    // loaded at once and merged into the running state with the same
-    // rescaling rule
+    if (!one && meta0.y + meta1.y <= kCombineRegs) {
+        // two sources, few records (a mixed-precision call of long units): both
+        // sources' records loaded in one round (source 0's first), then merged
+        float mr[kCombineRegs], sr[kCombineRegs], ar[kCombineRegs];
+#pragma unroll
+        for (int j = 0; j < kCombineRegs; ++j) {
+            if (j < meta0.y + meta1.y) {
+                const bool s0 = j < meta0.y;
+                const size_t r = ((s0 ? r00 + j : r10 + (j - meta0.y))) * G + g;
+                const float2 ml = *reinterpret_cast<const float2 *>((s0 ? p.ws_ml : p.ws_ml2) + r * 2);
+                mr[j] = ml.x;
+                sr[j] = ml.y;
+                ar[j] = (s0 ? p.ws_acc : p.ws_acc2)[r * kHD + d];
+            }
+        }
+        float m = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kCombineRegs; ++j)
+            if (j < meta0.y + meta1.y) m = fmaxf(m, mr[j]);
+        float s_sum = 0.0f, a = 0.0f;
+        if (m != -INFINITY) {
+#pragma unroll
+            for (int j = 0; j < kCombineRegs; ++j) {
+                if (j < meta0.y + meta1.y) {
+                    const float f = exp2f(mr[j] - m);
+                    s_sum = fmaf(sr[j], f, s_sum);
+                    a = fmaf(ar[j], f, a);
+                }
+            }
+        }
+        *o = s_sum > 0.0f ? a / s_sum : 0.0f;
+        return;
+    }
+    // more records: groups of kCombineRegs records, each group loaded at once
+    // and merged into the running state with the same rescaling rule
     float m = -INFINITY, s_sum = 0.0f, a = 0.0f;
     auto merge_group = [&](const float *ml, const float *accp, size_t r0, int n) {
         float mr[kCombineRegs], sr[kCombineRegs], ar[kCombineRegs];
