@@ -517,7 +517,11 @@ kvq8_status kvq4_decode_attn(const float *q, int batch, int nqh, int nkv, int hd
     p.dev_status = dev_status;
     cudaStream_t s = (cudaStream_t)stream;
     if (launch_int4_decode_split(p, plan.group, s) != cudaSuccess) return KVQ8_ERR_CUDA;
-    if (launch_decode_combine(c, plan.group, s) != cudaSuccess) return KVQ8_ERR_CUDA;
+    // the split's records sit at u * nsplit + j: a merge without the directory
+    // when they fit its registers
+    const cudaError_t e = p.nsplit <= 8 ? launch_decode_combine_fixed(c, plan.group, p.nsplit, s)
+                                        : launch_decode_combine(c, plan.group, s);
+    if (e != cudaSuccess) return KVQ8_ERR_CUDA;
     return KVQ8_OK;
 }
 

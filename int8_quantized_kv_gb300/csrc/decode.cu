@@ -898,6 +898,50 @@ decode_combine_kernel(DecodeParams p, int G) {
     *o = s_sum > 0.0f ? a / s_sum : 0.0f;
 }
 
+// The merge of the 4-bit decode, whose split writes unit u's records at
+// u * nsplit + j: the records are loaded beside the unit's length (one load
+// round, no record directory), and the length says how many of them this call
+// wrote (int4_split_count); merged in the order of decode_combine_kernel.
+__global__ void __launch_bounds__(kHD)
+decode_combine_fixed_kernel(DecodeParams p, int G, int ns) {
+    pdl_launch_dependents();   // as in decode_combine_kernel
+    pdl_wait();
+    const int qh = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+    const int h = qh / G, g = qh % G;
+    const size_t u = (size_t)b * p.nkv + h;
+    const int L = clamp_len(p.ctx_lens[b], p.max_blocks * kBS);
+    float mr[kCombineRegs], sr[kCombineRegs], ar[kCombineRegs];
+#pragma unroll
+    for (int j = 0; j < kCombineRegs; ++j) {
+        if (j < ns) {
+            const size_t r = (u * ns + j) * G + g;
+            const float2 ml = *reinterpret_cast<const float2 *>(p.ws_ml + r * 2);
+            mr[j] = ml.x;
+            sr[j] = ml.y;
+            ar[j] = p.ws_acc[r * kHD + d];
+        }
+    }
+    float *o = p.out + ((size_t)b * p.nqh + qh) * kHD + d;
+    if (L == 0) { *o = 0.0f; return; }
+    const int n1 = int4_split_count(L, ns);
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kCombineRegs; ++j)
+        if (j < n1) m = fmaxf(m, mr[j]);
+    float s_sum = 0.0f, a = 0.0f;
+    if (m != -INFINITY) {
+#pragma unroll
+        for (int j = 0; j < kCombineRegs; ++j) {
+            if (j < n1) {
+                const float f = exp2f(mr[j] - m);
+                s_sum = fmaf(sr[j], f, s_sum);
+                a = fmaf(ar[j], f, a);
+            }
+        }
+    }
+    *o = s_sum > 0.0f ? a / s_sum : 0.0f;
+}
+
 int device_sm_count() {
     static int cached[64] = {0};
     int dev = 0;
@@ -964,6 +1008,21 @@ cudaError_t launch_decode_split(const DecodeParams &p, int group, cudaStream_t s
         case 8: return launch_split_g<8>(p, s);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_decode_combine_fixed(const DecodeParams &p, int group, int nsplit, cudaStream_t s) {
+    if (nsplit < 1 || nsplit > kCombineRegs) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.nqh, p.batch);
+    cfg.blockDim = dim3(kHD);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_combine_fixed_kernel, p, group, nsplit);
 }
 
 cudaError_t launch_decode_combine(const DecodeParams &p, int group, cudaStream_t s) {

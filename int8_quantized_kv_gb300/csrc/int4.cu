@@ -356,11 +356,11 @@ int4_decode_split_kernel(Int4DecodeParams p) {
     // this unit's nsplit splits share its L tokens evenly (whole chunks), so
     // that a unit shorter than the table (a short context, or the 4-bit part
     // of a mixed-precision sequence) still keeps every CTA of the grid busy
-    const int st = max(kChunk4, ((L + p.nsplit - 1) / p.nsplit + kChunk4 - 1) / kChunk4 * kChunk4);
+    const int st = int4_split_tokens(L, p.nsplit);
+    static_assert(kChunk4 == 32, "int4_split_tokens cuts units into 32-token chunks");
     if (split == 0 && threadIdx.x == 0) {
         // records of unit u are u*nsplit + j; the combine reads first + u + j
-        const int nvalid = (L + st - 1) / st;
-        p.ws_meta[u] = make_int2((int)(u * (p.nsplit - 1)), nvalid);
+        p.ws_meta[u] = make_int2((int)(u * (p.nsplit - 1)), int4_split_count(L, p.nsplit));
     }
     const int tok_begin = split * st;
     if (tok_begin >= L) return;

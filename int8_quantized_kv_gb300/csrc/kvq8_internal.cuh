@@ -117,8 +117,23 @@ struct DecodeParams {
 };
 cudaError_t launch_decode_split(const DecodeParams &p, int group, cudaStream_t s);
 cudaError_t launch_decode_combine(const DecodeParams &p, int group, cudaStream_t s);
+// The merge of the 4-bit decode: unit u's records are u * nsplit + j for its
+// int4_split_count(L, nsplit) splits j (nsplit <= 8), read without the record
+// directory.
+cudaError_t launch_decode_combine_fixed(const DecodeParams &p, int group, int nsplit, cudaStream_t s);
 
 // ------------------------------------------------------------ INT4 cache --
+// A unit of L tokens cut into nsplit splits of whole 32-token chunks (the
+// 4-bit decode): tokens per split, and how many splits hold tokens.
+__host__ __device__ inline int int4_split_tokens(int L, int nsplit) {
+    const int st = ((L + nsplit - 1) / nsplit + 31) / 32 * 32;
+    return st > 32 ? st : 32;
+}
+__host__ __device__ inline int int4_split_count(int L, int nsplit) {
+    const int st = int4_split_tokens(L, nsplit);
+    return (L + st - 1) / st;
+}
+
 struct Int4AppendParams {
     const float *k_new, *v_new;   // [batch][n_new][nkv][hd]
     int batch, n_new, nkv;
