@@ -282,17 +282,19 @@ struct Int4Smem {
 // Fills `buf` (its mbarrier `bar`) with chunk `cidx` of this warp's split:
 // lane 0 issues the four bulk copies, or, when the chunk does not exist or its
 // block id is invalid, completes the barrier's phase with a plain arrival.
+// The block id of logical block hint_lb is hint_phys (loaded earlier; -1: no
+// hint).
 // Every call completes exactly one phase of `bar`.  Returns the block id (-1
 // for no data).  The buffer's earlier contents were read and written through
 // the generic proxy; the proxy fence orders those accesses (of every lane: the
 // caller synchronises the warp first) before the copies' writes.
 __device__ __forceinline__ int int4_fetch_chunk(const Int4DecodeParams &p, int b, int h, int tok_begin,
                                                 int nchunks, int cidx, unsigned char *buf, uint32_t bar,
-                                                uint64_t pol, int lane) {
+                                                uint64_t pol, int lane, int hint_lb = -1, int hint_phys = -1) {
     int phys = -1;
     if (cidx < nchunks) {
         const int t0 = tok_begin + cidx * kChunk4;
-        phys = p.block_table[(size_t)b * p.max_blocks + t0 / kBS];
+        phys = t0 / kBS == hint_lb ? hint_phys : p.block_table[(size_t)b * p.max_blocks + t0 / kBS];
         if (phys < 0 || phys >= p.num_blocks) {
             if (lane == 0) flag_status(p.dev_status, KVQ8_DEV_BAD_BLOCK_ID);
             phys = -1;
@@ -346,6 +348,17 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         const int i = threadIdx.x + r * kWarps4 * 32;
         qv[r] = i < G * 32 ? qsrc[i] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    // the block ids of this warp's first chunks, loaded beside the length too,
+    // for a unit that fills the table (the usual case outside a mixed-precision
+    // decode); used only when the length confirms where the split starts
+    const int st_full = int4_split_tokens(cap, p.nsplit);
+    int hint_lb[kBufs4], hint_phys[kBufs4];
+#pragma unroll
+    for (int i = 0; i < kBufs4; ++i) {
+        const int lb = (split * st_full + kChunk4 * (warp + kWarps4 * i)) / kBS;
+        hint_lb[i] = (!p.n4_blocks && lb < p.max_blocks) ? lb : -1;
+        hint_phys[i] = hint_lb[i] >= 0 ? p.block_table[(size_t)b * p.max_blocks + lb] : -1;
+    }
     int L = p.ctx_lens[b];
     if (L < 0 || L > cap) {
         if (threadIdx.x == 0 && split == 0 && h == 0) flag_status(p.dev_status, KVQ8_DEV_BAD_CTX_LEN);
@@ -381,10 +394,12 @@ int4_decode_split_kernel(Int4DecodeParams p) {
     }
     __syncwarp();
     unsigned valid = 0, fill_par = 0, pending = (1u << kBufs4) - 1;
+    const bool hinted = st == st_full;   // the split starts where the hints assumed
 #pragma unroll
     for (int i = 0; i < kBufs4; ++i)
         valid |= (unsigned)(int4_fetch_chunk(p, b, h, tok_begin, nchunks, warp + kWarps4 * i, sm.u.stage[warp][i],
-                                             bar0 + 8 * i, pol, lane) >= 0) << i;
+                                             bar0 + 8 * i, pol, lane, hinted ? hint_lb[i] : -1,
+                                             hint_phys[i]) >= 0) << i;
     bool aborted = false;
 
     const float *qrow = sm.qrows;
