@@ -25,7 +25,11 @@ namespace kvq8 {
 namespace {
 
 constexpr int kAppendWarps = 8;                  // one-token kernel: warps per CTA
-constexpr int kBulkWarps = 4;                    // bulk kernel: warps per CTA (one quarter)
+// Bulk kernel: one warp per CTA.  A CTA decodes about 4 us of work, so the
+// grid's tail (the last CTAs, each unable to draw an SM's share of the
+// bandwidth alone) is short: 57.6 -> 55.7 us at 8 x 4096 tokens against CTAs
+// of four warps (one quarter), whose tail was four times longer.
+constexpr int kBulkWarps = 1;
 constexpr int kQTok = kStageTok;                 // the V layout's 64-token quarter
 constexpr int kRunTok = 16;                      // tokens per bulk warp
 constexpr int kRunsPerQuarter = kQTok / kRunTok;
@@ -65,10 +69,10 @@ __device__ __forceinline__ size_t new_row_offset(const AppendParams &p, int b, i
 
 // Bulk append, one warp per task w = ((b * quarters + x) * nkv + h) * 4 + j:
 // tokens 16j..16j+15 of quarter x (counted from the quarter of the first new
-// token) of sequence b, kv head h.  The four runs of a quarter sit in one CTA,
-// so that the 16-byte pieces of each V row are all written at about the same
-// time.
-__global__ void __launch_bounds__(kBulkWarps * 32, 8)
+// token) of sequence b, kv head h.  The four runs of a quarter are consecutive
+// CTAs, dispatched together, so that the 16-byte pieces of each V row are all
+// written at about the same time.
+__global__ void __launch_bounds__(kBulkWarps * 32, 32 / kBulkWarps)
 quantize_append_kernel(AppendParams p, int quarters, long long tasks) {
     __shared__ __align__(16) float4 ring[kBulkWarps][kRing][2][32];   // [warp][slot][K, V][lane]
 
