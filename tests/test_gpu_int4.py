@@ -216,3 +216,20 @@ def test_int4_back_to_back_calls_share_the_workspace(gpu_lib):
             for h in range(cfg.nkv):
                 assert_close(o[b, h * G:(h + 1) * G], case.oracle_unit(b, h), f"int4 back to back b={b} h={h}")
     case.q = q1
+
+
+def test_int4_merge_without_directory_ragged(gpu_lib):
+    # 64 units: at most 8 splits per unit, so the merge reads each unit's
+    # records at u * nsplit + j without the record directory and takes their
+    # count from the unit's length; lengths from empty to several blocks,
+    # several too short to give every split a chunk
+    lens = np.array([0, 1, 31, 33, 200, 1000, 3000, 5000], np.int32)
+    cfg = wl.Workload("int4_fixed_merge", 540, batch=8, nqh=32, nkv=8, ctx=int(lens.max()))
+    case = Int4Case(cfg, lens=lens)
+    out = case.decode()
+    assert case.status.item() == 0
+    assert not out[0].any()
+    G = cfg.group
+    for b in range(1, cfg.batch):
+        for h in range(cfg.nkv):
+            assert_close(out[b, h * G:(h + 1) * G], case.oracle_unit(b, h), f"int4 fixed merge b={b} h={h}")
