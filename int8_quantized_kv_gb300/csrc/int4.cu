@@ -110,6 +110,11 @@ __device__ __forceinline__ void int4_store_v_row(uint32_t two, uint8_t *v_tile, 
 // One warp per new (token, kv head): K row then V row.
 __global__ void __launch_bounds__(kAppendWarps4 * 32)
 int4_append_kernel(Int4AppendParams p) {
+    // A programmatic dependent of the kernel before it, whose outputs it may
+    // read: it waits for it first.  The next kernel (a decode's split, which
+    // waits for this one before it reads anything) may launch at once.
+    pdl_wait();
+    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int i = blockIdx.x * kAppendWarps4 + warp, h = blockIdx.y, b = blockIdx.z;
     if (i >= p.n_new) return;
@@ -936,9 +941,17 @@ cudaError_t launch_int4_requantize(const Int4RequantParams &p, cudaStream_t s) {
 }
 
 cudaError_t launch_int4_append(const Int4AppendParams &p, cudaStream_t s) {
-    dim3 grid((p.n_new + kAppendWarps4 - 1) / kAppendWarps4, p.nkv, p.batch);
-    int4_append_kernel<<<grid, kAppendWarps4 * 32, 0, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((p.n_new + kAppendWarps4 - 1) / kAppendWarps4, p.nkv, p.batch);
+    cfg.blockDim = dim3(kAppendWarps4 * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, int4_append_kernel, p);
 }
 
 template <int G>
