@@ -76,7 +76,11 @@ __global__ void __launch_bounds__(kBulkWarps * 32, 32 / kBulkWarps)
 quantize_append_kernel(AppendParams p, int quarters, long long tasks) {
     __shared__ __align__(16) float4 ring[kBulkWarps][kRing][2][32];   // [warp][slot][K, V][lane]
 
-    pdl_launch_dependents();  // let the next kernel of the stream be scheduled now
+    // a programmatic dependent of the kernel before it, whose outputs it may
+    // read: it waits for it first; the next kernel of the stream may be
+    // scheduled now (it waits for this grid before it reads what it writes)
+    pdl_launch_dependents();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const long long task = (long long)blockIdx.x * kBulkWarps + (threadIdx.x >> 5);
     if (task >= tasks) return;
@@ -280,9 +284,18 @@ cudaError_t launch_quantize_append(const AppendParams &p, cudaStream_t s) {
         const long long tasks = (long long)kRunsPerQuarter * quarters * p.nkv * p.batch;
         const long long blocks = (tasks + kBulkWarps - 1) / kBulkWarps;
         if (blocks > INT_MAX) return cudaErrorInvalidConfiguration;
-        quantize_append_kernel<<<(unsigned)blocks, kBulkWarps * 32, 0, s>>>(p, quarters, tasks);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)blocks);
+        cfg.blockDim = dim3(kBulkWarps * 32);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, quantize_append_kernel, p, quarters, tasks);
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_q(const float *q, int64_t n_rows, int8_t *codes, float *scales,
