@@ -847,17 +847,18 @@ def bench_q4(gpu, cfg, full):
                                   table_d[b:b + 1], c0)
     caches = [c0] + [kvq8.KV4Cache(*[t.clone() for t in c0]) for _ in range(copies - 1)]
     q_d = torch.from_numpy(wl.queries(cfg)).to(dev)
+    # the step's token, [batch][nkv][hd] (kvq4_decode_step's layout)
+    new_k, new_v = np.ascontiguousarray(new_k[:, 0]), np.ascontiguousarray(new_v[:, 0])
     nk_d, nv_d = torch.from_numpy(new_k).to(dev), torch.from_numpy(new_v).to(dev)
-    start_d = torch.from_numpy((lens - 1).clip(min=0).astype(np.int32)).to(dev)
     lens_d = torch.from_numpy(lens).to(dev)
     ws = kvq8.alloc_workspace(cfg.batch, cfg.nqh, cfg.nkv, max_blocks, dev)
     out = torch.empty_like(q_d)
 
     def step(i, bufs=None):
         qq, kk, vv, oo = bufs or (q_d, nk_d, nv_d, out)
-        c = caches[i % copies]
-        kvq8.quantize_append4(kk, vv, start_d, table_d, c, dev_status=status, stream=stream)
-        kvq8.decode_attn4(qq, c, table_d, lens_d, oo, ws, sm_scale=sm, dev_status=status, stream=stream)
+        # one call: the split kernel appends the token (n_new = 1) and decodes
+        kvq8.decode_step4(qq, kk, vv, caches[i % copies], table_d, lens_d, oo, ws, sm_scale=sm,
+                          dev_status=status, stream=stream)
 
     def decode(i):
         kvq8.decode_attn4(q_d, caches[i % copies], table_d, lens_d, out, ws, sm_scale=sm,
@@ -866,10 +867,11 @@ def bench_q4(gpu, cfg, full):
     sbytes = int4_step_bytes(cfg, lens)
     dec_bytes = sbytes - cfg.batch * cfg.nkv * 2 * (cfg.hd * 4 + cfg.hd // 2 + 16)
     per_step_s, total, slowest, roof, clocks, launches = gpu.measure(
-        step, decode, "kvq4_decode_attn (int4 split + combine)", dec_bytes, sbytes, 3)
+        step, decode, "kvq4_decode_attn (int4 split + combine)", dec_bytes, sbytes, 2)
     config = {"workload": cfg.name, "batch": cfg.batch, "nqh": cfg.nqh, "nkv": cfg.nkv, "hd": cfg.hd,
               "block_size": 256, "ctx": int(lens.max()), "tokens": int(lens.sum()),
-              "step": "append 1 token per (sequence, kv head) + INT4 split-KV decode + merge",
+              "step": "kvq4_decode_step: the INT4 split-KV decode, which also appends the step's token "
+                      "of every (sequence, kv head), + merge",
               "block_table": "seeded shuffled physical blocks",
               "l2": f"rotates {copies} cache copies; working set >> 129 MB L2, no flush",
               "parallelism": f"replicas{gpu.world}", "bytes_per_step": sbytes,

@@ -414,6 +414,34 @@ kvq8_status kvq4_decode_attn(const float *q, int batch, int nqh, int nkv, int hd
                              float *out, void *workspace, size_t workspace_bytes,
                              uint32_t *dev_status, void *stream);
 
+/*
+ * kvq4_decode_step -- one decode step over the 4-bit cache in one call: append
+ * the step's new token of every sequence at position ctx_lens[b] - 1 (the
+ * group-64 rule of kvq4_quantize_append) and attend over the context including
+ * it.  Same results as kvq4_quantize_append (n_new = 1, start_pos[b] =
+ * ctx_lens[b] - 1) followed by kvq4_decode_attn, in two launches: the split
+ * kernel also appends the new token (the warp that decodes the 32-token chunk
+ * holding it quantises the token into that chunk and into the cache), then
+ * the merge.  Both are programmatic dependents of the kernel before them in
+ * the stream; each waits for that kernel's results before it reads anything.
+ * The block holding a sequence's new position must belong to that sequence
+ * alone.
+ *
+ *   k_new, v_new  fp32 [batch][nkv][hd], 16-byte aligned (sequences with
+ *                 ctx_lens[b] == 0 append nothing and yield 0; a ctx_lens[b]
+ *                 beyond the table is flagged, clamped, and appends nothing)
+ *   k_codes .. v_param  written at the new token's slot only
+ * Other arguments, workspace included, as kvq4_decode_attn.
+ */
+kvq8_status kvq4_decode_step(const float *q, const float *k_new, const float *v_new,
+                             int batch, int nqh, int nkv, int hd,
+                             uint8_t *k_codes, uint8_t *v_codes, float *k_param, float *v_param,
+                             int num_blocks, const int32_t *block_table,
+                             int max_blocks, int block_size,
+                             const int32_t *ctx_lens, float sm_scale, float *out,
+                             void *workspace, size_t workspace_bytes,
+                             uint32_t *dev_status, void *stream);
+
 /* ------------------------- mixed precision by token age (NEXT row) --- */
 
 /*
@@ -433,7 +461,9 @@ kvq8_status kvq4_decode_attn(const float *q, int batch, int nqh, int nkv, int hd
  * sizes the grid.  A range outside [0, max_blocks) or longer than max_count
  * sets KVQ8_DEV_BAD_POSITION (the part inside is still done); a tile id
  * outside its pool sets KVQ8_DEV_BAD_BLOCK_ID and is skipped.  The int8 tiles
- * are left as they were.
+ * are left as they were.  Whole tiles are converted: slots past a sequence's
+ * last token are converted from whatever they hold (never read as tokens), and
+ * a non-finite leftover there sets KVQ8_DEV_NONFINITE like any other.
  */
 kvq8_status kvmix_requantize(int batch, int nkv, int hd,
                              const int8_t *k_pool, const int8_t *v_pool,

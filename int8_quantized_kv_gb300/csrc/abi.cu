@@ -475,12 +475,14 @@ kvq8_status kvq4_quantize_append(const float *k_new, const float *v_new, int bat
     return KVQ8_OK;
 }
 
-kvq8_status kvq4_decode_attn(const float *q, int batch, int nqh, int nkv, int hd,
-                             const uint8_t *k_codes, const uint8_t *v_codes, const float *k_param,
-                             const float *v_param, int num_blocks, const int32_t *block_table,
-                             int max_blocks, int block_size, const int32_t *ctx_lens,
-                             float sm_scale, float *out, void *workspace, size_t workspace_bytes,
-                             uint32_t *dev_status, void *stream) {
+// The 4-bit decode, and with k_new / v_new a decode step (the split kernel
+// also appends the new token at ctx_lens[b] - 1).
+static kvq8_status run_kvq4_decode(const float *q, const float *k_new, const float *v_new, int batch, int nqh,
+                                   int nkv, int hd, const uint8_t *k_codes, const uint8_t *v_codes,
+                                   const float *k_param, const float *v_param, int num_blocks,
+                                   const int32_t *block_table, int max_blocks, int block_size,
+                                   const int32_t *ctx_lens, float sm_scale, float *out, void *workspace,
+                                   size_t workspace_bytes, uint32_t *dev_status, void *stream) {
     kvq8_status st = check_decode_args(q, batch, nqh, nkv, hd, (const int8_t *)k_codes,
                                        (const int8_t *)v_codes, k_param, v_param, num_blocks,
                                        block_table, max_blocks, block_size, ctx_lens);
@@ -495,6 +497,8 @@ kvq8_status kvq4_decode_attn(const float *q, int batch, int nqh, int nkv, int hd
     c.out = out;
     Int4DecodeParams p;
     p.q = q;
+    p.k_new = k_new;
+    p.v_new = v_new;
     p.n4_blocks = nullptr;
     p.batch = batch;
     p.nqh = nqh;
@@ -523,6 +527,29 @@ kvq8_status kvq4_decode_attn(const float *q, int batch, int nqh, int nkv, int hd
                                         : launch_decode_combine(c, plan.group, s);
     if (e != cudaSuccess) return KVQ8_ERR_CUDA;
     return KVQ8_OK;
+}
+
+kvq8_status kvq4_decode_attn(const float *q, int batch, int nqh, int nkv, int hd,
+                             const uint8_t *k_codes, const uint8_t *v_codes, const float *k_param,
+                             const float *v_param, int num_blocks, const int32_t *block_table,
+                             int max_blocks, int block_size, const int32_t *ctx_lens,
+                             float sm_scale, float *out, void *workspace, size_t workspace_bytes,
+                             uint32_t *dev_status, void *stream) {
+    return run_kvq4_decode(q, nullptr, nullptr, batch, nqh, nkv, hd, k_codes, v_codes, k_param, v_param,
+                           num_blocks, block_table, max_blocks, block_size, ctx_lens, sm_scale, out, workspace,
+                           workspace_bytes, dev_status, stream);
+}
+
+kvq8_status kvq4_decode_step(const float *q, const float *k_new, const float *v_new, int batch, int nqh,
+                             int nkv, int hd, uint8_t *k_codes, uint8_t *v_codes, float *k_param,
+                             float *v_param, int num_blocks, const int32_t *block_table, int max_blocks,
+                             int block_size, const int32_t *ctx_lens, float sm_scale, float *out,
+                             void *workspace, size_t workspace_bytes, uint32_t *dev_status, void *stream) {
+    if (batch > 0 && (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)))
+        return KVQ8_ERR_INVALID_ARG;
+    return run_kvq4_decode(q, k_new, v_new, batch, nqh, nkv, hd, k_codes, v_codes, k_param, v_param,
+                           num_blocks, block_table, max_blocks, block_size, ctx_lens, sm_scale, out, workspace,
+                           workspace_bytes, dev_status, stream);
 }
 
 size_t kvf32_pool_bytes(int num_blocks, int nkv, int hd, int block_size) {
@@ -701,6 +728,8 @@ kvq8_status kvmix_decode_attn(const float *q, int batch, int nqh, int nkv, int h
     c.ws_acc2 = c4.ws_acc;
     Int4DecodeParams p;
     p.q = q;
+    p.k_new = nullptr;
+    p.v_new = nullptr;
     p.n4_blocks = n4_blocks;
     p.batch = batch;
     p.nqh = nqh;

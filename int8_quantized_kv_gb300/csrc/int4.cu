@@ -317,7 +317,39 @@ __device__ __forceinline__ int int4_fetch_chunk(const Int4DecodeParams &p, int b
     return phys;
 }
 
-template <int G>
+// A decode step's new token of unit (b, h), position pos = ctx_lens[b] - 1,
+// which is row t of the chunk staged at st: quantised by the warp (the group-64
+// rule of int4_append_kernel), written over the row the copy brought in (K
+// row, the V chunk's columns at v4_pos(t), both parameter rows) and into the
+// cache.  Only this warp reads that position in this launch.
+__device__ __noinline__ void int4_append_new_token(const Int4DecodeParams &p, int b, int h, int pos, int t,
+                                                   int lane, unsigned char *st) {
+    const int phys = p.block_table[(size_t)b * p.max_blocks + pos / kBS];   // valid: the chunk was staged
+    const size_t tile = (size_t)phys * p.nkv + h;
+    const size_t row = tile * kBS + pos % kBS;
+    const size_t src = ((size_t)b * p.nkv + h) * kHD;
+    float *kpar = reinterpret_cast<float *>(st + kStageKpOff) + 4 * t;
+    float *vpar = reinterpret_cast<float *>(st + kStageVpOff) + 4 * t;
+    const uint32_t kt = int4_quant_row(reinterpret_cast<const float4 *>(p.k_new + src)[lane], kpar, lane,
+                                       p.dev_status);
+    const uint32_t vt = int4_quant_row(reinterpret_cast<const float4 *>(p.v_new + src)[lane], vpar, lane,
+                                       p.dev_status);
+    // the staged chunk
+    int4_store_k_row(kt, st + kStageKOff + t * kRowBytes, lane);
+    st[kStageVOff + (2 * lane) * kChunk4 + v4_pos(t)] = (uint8_t)(vt & 0xff);
+    st[kStageVOff + (2 * lane + 1) * kChunk4 + v4_pos(t)] = (uint8_t)(vt >> 8);
+    // the cache (the pools of a decode step are the caller's writable buffers)
+    int4_store_k_row(kt, const_cast<uint8_t *>(p.k_codes) + row * kRowBytes, lane);
+    int4_store_v_row(vt, const_cast<uint8_t *>(p.v_codes) + tile * kBS * kRowBytes, pos % kBS, lane);
+    __syncwarp();   // the parameter rows written by lanes 0 and 16
+    if (lane < 4) {
+        const_cast<float *>(p.k_param)[row * 4 + lane] = kpar[lane];
+        const_cast<float *>(p.v_param)[row * 4 + lane] = vpar[lane];
+    }
+    __syncwarp();   // the patched chunk is read by every lane below
+}
+
+template <int G, bool kStep>
 __global__ void __launch_bounds__(kWarps4 * 32, 3)
 int4_decode_split_kernel(Int4DecodeParams p) {
     // kPack (G <= 4): the 8 MMA columns carry the high fp16 parts of the
@@ -365,6 +397,9 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         hint_phys[i] = hint_lb[i] >= 0 ? p.block_table[(size_t)b * p.max_blocks + lb] : -1;
     }
     int L = p.ctx_lens[b];
+    // a decode step appends its new token at position ctx_lens[b] - 1 (none
+    // for an empty context or one beyond the table)
+    const int app_pos = (kStep && L >= 1 && L <= cap) ? L - 1 : -1;
     if (L < 0 || L > cap) {
         if (threadIdx.x == 0 && split == 0 && h == 0) flag_status(p.dev_status, KVQ8_DEV_BAD_CTX_LEN);
         L = max(0, min(L, cap));
@@ -533,6 +568,10 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         if ((valid >> bi) & 1u) {
         const int t0 = tok_begin + cidx * kChunk4;
         const int ntok = min(kChunk4, tok_end - t0);
+        if constexpr (kStep) {
+            if (app_pos >= t0 && app_pos < t0 + ntok)
+                int4_append_new_token(p, b, h, app_pos, app_pos - t0, lane, const_cast<unsigned char *>(st));
+        }
         const float4 *kps = reinterpret_cast<const float4 *>(st + kStageKpOff);
         const float4 *vps = reinterpret_cast<const float4 *>(st + kStageVpOff);
         // K rows, V words and parameters are read from the staging buffer just
@@ -905,10 +944,10 @@ bool make_int4_plan(int batch, int nkv, int max_blocks, int resident_ctas, int *
 
 template <int G>
 cudaError_t int4_occupancy(int *per) {
-    cudaError_t e = cudaFuncSetAttribute(int4_decode_split_kernel<G>,
+    cudaError_t e = cudaFuncSetAttribute(int4_decode_split_kernel<G, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Int4Smem<G>));
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per, int4_decode_split_kernel<G>, kWarps4 * 32,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per, int4_decode_split_kernel<G, false>, kWarps4 * 32,
                                                          sizeof(Int4Smem<G>));
 }
 
@@ -954,8 +993,8 @@ cudaError_t launch_int4_append(const Int4AppendParams &p, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, int4_append_kernel, p);
 }
 
-template <int G>
-cudaError_t launch_int4_split_g(const Int4DecodeParams &p, cudaStream_t s) {
+template <int G, bool kStep>
+cudaError_t launch_int4_split_gs(const Int4DecodeParams &p, cudaStream_t s) {
     constexpr size_t smem = sizeof(Int4Smem<G>);
     static std::atomic<uint64_t> configured{0};
     return launch_after_setting(
@@ -963,10 +1002,11 @@ cudaError_t launch_int4_split_g(const Int4DecodeParams &p, cudaStream_t s) {
         [] {
             // the largest shared-memory carveout: in a mixed-precision decode the
             // int8 split joins an SM while one of these CTAs still runs there
-            cudaError_t e = cudaFuncSetAttribute(int4_decode_split_kernel<G>,
+            cudaError_t e = cudaFuncSetAttribute(int4_decode_split_kernel<G, kStep>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
-            return cudaFuncSetAttribute(int4_decode_split_kernel<G>, cudaFuncAttributePreferredSharedMemoryCarveout,
+            return cudaFuncSetAttribute(int4_decode_split_kernel<G, kStep>,
+                                        cudaFuncAttributePreferredSharedMemoryCarveout,
                                         (int)cudaSharedmemCarveoutMaxShared);
         },
         [&] {
@@ -984,8 +1024,13 @@ cudaError_t launch_int4_split_g(const Int4DecodeParams &p, cudaStream_t s) {
             attr[0].val.programmaticStreamSerializationAllowed = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            return cudaLaunchKernelEx(&cfg, int4_decode_split_kernel<G>, p);
+            return cudaLaunchKernelEx(&cfg, int4_decode_split_kernel<G, kStep>, p);
         });
+}
+
+template <int G>
+cudaError_t launch_int4_split_g(const Int4DecodeParams &p, cudaStream_t s) {
+    return p.k_new ? launch_int4_split_gs<G, true>(p, s) : launch_int4_split_gs<G, false>(p, s);
 }
 
 cudaError_t launch_int4_decode_split(const Int4DecodeParams &p, int group, cudaStream_t s) {

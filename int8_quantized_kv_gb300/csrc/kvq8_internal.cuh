@@ -147,6 +147,10 @@ struct Int4AppendParams {
 
 struct Int4DecodeParams {
     const float *q;               // [batch][nqh][hd]
+    // A decode step's new token ([batch][nkv][hd] each; null otherwise): the
+    // split kernel quantises it into position ctx_lens[b] - 1, in the chunk it
+    // stages and in the cache, which is then the caller's writable buffer
+    const float *k_new, *v_new;
     const int32_t *n4_blocks;     // null, or: only tokens [0, 256 * n4_blocks[b]) (mixed precision)
     int batch, nqh, nkv;
     const uint8_t *k_codes, *v_codes;

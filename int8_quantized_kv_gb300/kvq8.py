@@ -62,6 +62,8 @@ SIGNATURES = {
                                   _P, _P, _P, _P, _P, _P]),
     "kvq4_decode_attn": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _I,
                               _P, _F, _P, _P, _SZ, _P, _P]),
+    "kvq4_decode_step": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _I, _I,
+                              _P, _F, _P, _P, _SZ, _P, _P]),
     "kvmix_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "kvmix_requantize": (_I, [_I, _I, _I, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _P,
                               _I, _I, _P, _P, _I, _P, _P]),
@@ -515,6 +517,23 @@ def decode_attn4(q, cache: KV4Cache, block_table, ctx_lens, out, workspace,
         block_table.shape[1], BLOCK_SIZE, _ptr(ctx_lens), sm, _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream))
     _check("kvq4_decode_attn", st)
+
+
+def decode_step4(q, k_new, v_new, cache: KV4Cache, block_table, ctx_lens, out, workspace,
+                 sm_scale: Optional[float] = None, dev_status=None, stream=None):
+    """One decode step over the 4-bit cache: append k_new/v_new (fp32
+    [batch][nkv][128]) at position ctx_lens-1 and attend over ctx_lens tokens
+    (two launches: the split kernel, which also appends the token, and the
+    merge)."""
+    _need_cuda(q, k_new, v_new, block_table, ctx_lens, out, workspace, *cache, dev_status)
+    batch, nqh, hd = q.shape
+    sm = 1.0 / math.sqrt(hd) if sm_scale is None else sm_scale
+    st = load().kvq4_decode_step(
+        _ptr(q), _ptr(k_new), _ptr(v_new), batch, nqh, cache.nkv, hd, _ptr(cache.k_codes),
+        _ptr(cache.v_codes), _ptr(cache.k_param), _ptr(cache.v_param), cache.num_blocks,
+        _ptr(block_table), block_table.shape[1], BLOCK_SIZE, _ptr(ctx_lens), sm, _ptr(out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream))
+    _check("kvq4_decode_step", st)
 
 
 # ------------------------------------------------------------- fp32 cache ---

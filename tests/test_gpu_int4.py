@@ -233,3 +233,68 @@ def test_int4_merge_without_directory_ragged(gpu_lib):
     for b in range(1, cfg.batch):
         for h in range(cfg.nkv):
             assert_close(out[b, h * G:(h + 1) * G], case.oracle_unit(b, h), f"int4 fixed merge b={b} h={h}")
+
+
+@pytest.mark.parametrize("G", [1, 4, 8])
+def test_int4_decode_step_appends_the_token(gpu_lib, G):
+    # kvq4_decode_step on a cache holding L - 1 tokens: the new token lands at
+    # position L - 1 bit for bit as the oracle quantises it, the output equals
+    # the oracle's decode over the L tokens, and both equal a separate append
+    # followed by a decode, bit for bit; an empty sequence appends nothing
+    cfg = wl.Workload(f"int4_step_g{G}", 550 + G, batch=5, nqh=2 * G, nkv=2, ctx_range=(2, 1500))
+    lens = wl.ctx_lens(cfg)
+    lens[0], lens[1], lens[2] = 0, 1, 257          # empty, only the new token, a block's first slot
+    table, num_blocks = wl.block_table(cfg, lens, spare_blocks=2)
+    table_d = torch.from_numpy(table).cuda()
+    lens_d = torch.from_numpy(lens).cuda()
+    zero = torch.zeros(1, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    caches = [kvq8.alloc_cache4(num_blocks, cfg.nkv) for _ in range(2)]
+    k_new = np.zeros((cfg.batch, cfg.nkv, HD), np.float32)
+    v_new = np.zeros_like(k_new)
+    for b in range(cfg.batch):
+        L = int(lens[b])
+        if L == 0:
+            continue
+        k, v = wl.seq_kv(cfg, b, L)
+        k_new[b], v_new[b] = k[L - 1], v[L - 1]
+        if L > 1:
+            for c in caches:
+                kvq8.quantize_append4(torch.from_numpy(k[None, :L - 1]).cuda(),
+                                      torch.from_numpy(v[None, :L - 1]).cuda(), zero, table_d[b:b + 1], c,
+                                      dev_status=status)
+    q = wl.queries(cfg)
+    q_d, kn_d, vn_d = torch.from_numpy(q).cuda(), torch.from_numpy(k_new).cuda(), torch.from_numpy(v_new).cuda()
+    ws = kvq8.alloc_workspace(cfg.batch, cfg.nqh, cfg.nkv, table.shape[1])
+    out_step = torch.full_like(q_d, float("nan"))
+    kvq8.decode_step4(q_d, kn_d, vn_d, caches[0], table_d, lens_d, out_step, ws, sm_scale=SM_SCALE,
+                      dev_status=status)
+    # the same as a separate append of the token and a decode
+    start = torch.from_numpy((lens - 1).clip(min=0).astype(np.int32)).cuda()
+    has = torch.from_numpy((lens > 0).astype(np.int32)).cuda()
+    for b in range(cfg.batch):
+        if lens[b] > 0:
+            kvq8.quantize_append4(kn_d[b:b + 1, None], vn_d[b:b + 1, None], start[b:b + 1], table_d[b:b + 1],
+                                  caches[1], dev_status=status)
+    out_two = torch.full_like(q_d, float("nan"))
+    kvq8.decode_attn4(q_d, caches[1], table_d, lens_d, out_two, ws, sm_scale=SM_SCALE, dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0 and has.numel() == cfg.batch
+    o_step, o_two = out_step.cpu().numpy(), out_two.cpu().numpy()
+    assert np.array_equal(o_step, o_two)
+    assert not o_step[0].any()
+    kc, vc = caches[0].k_codes.cpu().numpy(), v4_token_major(caches[0].v_codes.cpu().numpy())
+    kp, vp = caches[0].k_param.cpu().numpy(), caches[0].v_param.cpu().numpy()
+    case = Int4Case.__new__(Int4Case)
+    case.cfg, case.lens, case.q = cfg, lens, q
+    for b in range(1, cfg.batch):
+        L = int(lens[b])
+        phys, slot = table[b, (L - 1) // 256], (L - 1) % 256
+        for h in range(cfg.nkv):
+            for x, codes, par in ((k_new[b, h], kc, kp), (v_new[b, h], vc, vp)):
+                packed, sc, zr = oracle.int4_quantize_groups(x[None], 64)
+                assert np.array_equal(codes[phys, h, slot], packed[0])
+                got = par[phys, h, slot]
+                assert np.array_equal(got[[0, 2]].view(np.uint32), sc[0].view(np.uint32))
+                assert np.array_equal(got[[1, 3]].view(np.uint32), zr[0].view(np.uint32))
+            assert_close(o_step[b, h * G:(h + 1) * G], case.oracle_unit(b, h), f"int4 step G={G} b={b} h={h}")

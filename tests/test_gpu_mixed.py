@@ -26,6 +26,10 @@ class MixedCase(Case):
 
     def __init__(self, cfg, n4, lens=None, seed=0):
         super().__init__(cfg, lens=lens)
+        # requantisation converts whole 256-token tiles: the slots past a
+        # sequence's end hold whatever the pool held (never read as tokens);
+        # zeros there keep the status word free of flags raised by leftovers
+        self._zero_unused_slots()
         B, mb = self.table.shape
         rng = np.random.default_rng(900 + seed)
         self.num_blocks4 = B * mb + 3
@@ -37,6 +41,18 @@ class MixedCase(Case):
         zero = torch.zeros(B, dtype=torch.int32, device="cuda")
         kvq8.requantize_blocks(self.cache, self.table_d, self.cache4, self.table4_d, zero, self.n4_d,
                                max(1, int(self.n4.max())), dev_status=self.status)
+        torch.cuda.synchronize()
+
+    def _zero_unused_slots(self):
+        torch.cuda.synchronize()
+        B, mb = self.table.shape
+        for b in range(B):
+            L = int(self.lens[b])
+            j = L // 256                      # the sequence's last, partly filled block
+            if L % 256 and j < mb and self.table[b, j] >= 0:
+                phys = int(self.table[b, j])
+                self.cache.k_scale[phys, :, L % 256:] = 0.0
+                self.cache.v_scale[phys, :, L % 256:] = 0.0
         torch.cuda.synchronize()
 
     def decode_mixed(self):
