@@ -352,12 +352,11 @@ __device__ __noinline__ void int4_append_new_token(const Int4DecodeParams &p, in
 template <int G, bool kStep>
 __global__ void __launch_bounds__(kWarps4 * 32, 3)
 int4_decode_split_kernel(Int4DecodeParams p) {
-    // kPack (G <= 4): the 8 MMA columns carry the high fp16 parts of the
-    // operand facing the heads in columns 0-3 and the low parts in 4-7, so one
-    // MMA does both halves; lane (g, t4) then owns token 16*mt + g + 8*(t4/2)
-    // and heads 2*(t4%2) + j of the scores, and its accumulator columns hold
-    // the high (t4 < 2) or low (t4 >= 2) parts for those heads, added at the
-    // end.  kPack2 (G <= 2): columns 0-1 high parts, 2-3 low parts, 4-7 zero;
+    // kPack (G <= 4): the 8 MMA columns carry both fp16 parts (high, low) of
+    // the operand facing the heads, so one MMA does both halves.  kPackH
+    // (G = 4): column 2j + e is part e of head j, so lane (g, t4) holds both
+    // parts of head t4 (scores of tokens 16*mt + g + 8*r, accumulator columns),
+    // added in the lane.  kPack2 (G <= 2): columns 0-1 high parts, 2-3 low parts, 4-7 zero;
     // one shuffle joins the halves (lanes t4 = 0, 1 keep rows g, g + 8) and a
     // second moves the second m-tile's scores to lanes t4 = 2, 3, so that lane
     // (g, t4) owns token 16*(t4/2) + g + 8*(t4%2) and both heads: no lane
@@ -365,6 +364,8 @@ int4_decode_split_kernel(Int4DecodeParams p) {
     // and each product takes two MMAs.
     constexpr bool kPack = G <= 4;
     constexpr bool kPack2 = G <= 2;
+    constexpr bool kPackH = kPack && !kPack2;
+    constexpr int kHL = kPackH ? 1 : 2;   // heads per lane
     pdl_wait();
     // In a mixed-precision decode the next kernel is the int8 split over the
     // recent tokens, which reads nothing this kernel writes: it may start now
@@ -468,9 +469,9 @@ int4_decode_split_kernel(Int4DecodeParams p) {
     uint32_t qb[8][2];
     if constexpr (kPack) {
         // kPack2: column gg = head gg % 2 (gg < 4; high part for gg < 2), zero
-        // for gg >= 4; kPack: head gg % 4, high part for gg < 4
-        const int hq = kPack2 ? (g < 4 ? (g & 1) : G) : (g & 3);
-        const bool low = kPack2 ? (g & 2) != 0 : g >= 4;
+        // for gg >= 4; kPackH: head gg / 2, high part for even gg
+        const int hq = kPack2 ? (g < 4 ? (g & 1) : G) : (g >> 1);
+        const bool low = kPack2 ? (g & 2) != 0 : (g & 1) != 0;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             float x[4] = {0.f, 0.f, 0.f, 0.f};
@@ -533,7 +534,7 @@ int4_decode_split_kernel(Int4DecodeParams p) {
     __syncthreads();
     // this lane's heads (score and accumulator columns): 2*(t4 % 2) + j when
     // packed, 2*t4 + j otherwise
-    const int hbase = kPack2 ? 0 : (kPack ? 2 * (t4 & 1) : 2 * t4);
+    const int hbase = kPack2 ? 0 : (kPackH ? t4 : 2 * t4);
     float qq[2][2];
 #pragma unroll
     for (int j = 0; j < 2; ++j)
@@ -541,11 +542,10 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         for (int gr = 0; gr < 2; ++gr) qq[j][gr] = sm.qq[hbase + j][gr];
     const float score_scale = p.sm_scale_log2 / qscale;
 
-    // scores per lane: kPack 1 token x 2 heads per m-tile, else 2 tokens (rows
-    // g, g + 8) x 2 heads
-    constexpr int kR = kPack ? 1 : 2;
+    // scores per lane: kPack2 1 token x 2 heads, kPackH 4 tokens (rows g, g + 8
+    // of both m-tiles) x 1 head, else 4 tokens x 2 heads
+    constexpr int kR = kPack2 ? 1 : 2;
     constexpr int kM = kPack2 ? 1 : 2;   // score m-slots per lane
-    const int tsel = kPack ? 8 * (t4 >> 1) : 0;   // this lane's token offset when packed
     const int tok2 = 16 * (t4 >> 1) + g + 8 * (t4 & 1);   // kPack2: this lane's token
     float M[2] = {-INFINITY, -INFINITY}, Sl[2] = {0.0f, 0.0f}, Zl[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
     float acc[8][4];
@@ -626,23 +626,17 @@ int4_decode_split_kernel(Int4DecodeParams p) {
                         const float keep = lo_lane ? d[gr][2 + j] : d[gr][j];
                         dtm[mt][gr][j] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
                     }
-            } else if constexpr (kPack) {
-                // lane t4 < 2 holds the high parts of rows g and g + 8, lane t4 ^ 2
-                // the low parts: each keeps one row and receives the other part
-                const bool lo_lane = t4 >= 2;
-                const float4 k4 = kps[16 * mt + g + tsel];
+            } else if constexpr (kPackH) {
+                // columns 2*t4, 2*t4 + 1: the high and low parts of head t4, rows
+                // g and g + 8
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    float dt[2];
-#pragma unroll
-                    for (int gr = 0; gr < 2; ++gr) {
-                        const float send = lo_lane ? d[gr][j] : d[gr][2 + j];
-                        const float keep = lo_lane ? d[gr][2 + j] : d[gr][j];
-                        dt[gr] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-                    }
-                    const float x = k4.x * fmaf(dt[0], kNibUnit, -k4.y * qq[j][0]) +
-                                    k4.z * fmaf(dt[1], kNibUnit, -k4.w * qq[j][1]);
-                    sc[mt][0][j] = x * score_scale;
+                for (int r = 0; r < 2; ++r) {
+                    const float4 k4 = kps[16 * mt + g + 8 * r];
+                    const float dt0 = d[0][2 * r] + d[0][2 * r + 1];
+                    const float dt1 = d[1][2 * r] + d[1][2 * r + 1];
+                    const float x = k4.x * fmaf(dt0, kNibUnit, -k4.y * qq[0][0]) +
+                                    k4.z * fmaf(dt1, kNibUnit, -k4.w * qq[0][1]);
+                    sc[mt][r][0] = x * score_scale;
                 }
             } else {
 #pragma unroll
@@ -674,15 +668,16 @@ int4_decode_split_kernel(Int4DecodeParams p) {
             }
         }
         // token of score (mt, r) of this lane
-        auto tok_of = [&](int mt, int r) {
-            return kPack2 ? tok2 : 16 * mt + g + (kPack ? tsel : 8 * r);
-        };
+        auto tok_of = [&](int mt, int r) { return kPack2 ? tok2 : 16 * mt + g + 8 * r; };
         if (partial) {
 #pragma unroll
             for (int mt = 0; mt < kM; ++mt)
 #pragma unroll
                 for (int r = 0; r < kR; ++r)
-                    if (tok_of(mt, r) >= ntok) sc[mt][r][0] = sc[mt][r][1] = -INFINITY;
+                    if (tok_of(mt, r) >= ntok) {
+#pragma unroll
+                        for (int j = 0; j < kHL; ++j) sc[mt][r][j] = -INFINITY;
+                    }
         }
         // this lane's score tokens' V parameters (zero past the end: stale slots)
         float4 vp[kM][kR];
@@ -696,7 +691,7 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         // this lane's own maxima; the warp reduces them only when some lane's
         // score passes its head's running maximum by more than 2^8 (below)
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
+        for (int j = 0; j < kHL; ++j)
 #pragma unroll
             for (int mt = 0; mt < kM; ++mt)
 #pragma unroll
@@ -717,16 +712,16 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         // some lane's score of a head is above M + 8 exactly when the head's
         // maximum over the chunk is, so the lanes' own maxima decide whether
         // to raise, and the maxima are reduced over the lanes sharing the head
-        // (all g, and t4 ^ 2 when packed, all lanes when kPack2) only then
-        const bool grow = mloc[0] > M[0] + 8.0f || mloc[1] > M[1] + 8.0f;
+        // (all g, and all lanes when kPack2) only then
+        const bool grow = mloc[0] > M[0] + 8.0f || (kHL > 1 && mloc[1] > M[1] + 8.0f);
         float alpha[2] = {1.0f, 1.0f};
         bool rescale = e_new != e_cur;
         if (__any_sync(0xffffffffu, grow)) {
             rescale = true;
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
+            for (int j = 0; j < kHL; ++j) {
                 if constexpr (kPack2) mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 1));
-                if constexpr (kPack) mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 2));
+                if constexpr (kPack2) mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 2));
                 mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 4));
                 mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 8));
                 mloc[j] = fmaxf(mloc[j], __shfl_xor_sync(0xffffffffu, mloc[j], 16));
@@ -737,9 +732,9 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         }
         const float two = __int_as_float((127 + max(-126, min(127, e_cur - e_new))) << 23);
         // P'_g = w * vscale_g * 2^-e, high and low fp16 parts, into the freed K
-        // area for the transposing loads: kPack [group][32 tokens][high parts of
-        // heads 0-3 | low parts] (kPack2: words 0, 1 = high and low parts of heads
-        // 0-1; words 2, 3 unwritten, their B columns zeroed after the load), else
+        // area for the transposing loads: kPackH [group][32 tokens][(high, low)
+        // of heads 0-3] (kPack2: words 0, 1 = high and low parts of heads 0-1;
+        // words 2, 3 unwritten, their B columns zeroed after the load), else
         // [group][part][32 tokens][8 heads]
         uint32_t *ptile = reinterpret_cast<uint32_t *>(const_cast<unsigned char *>(st) + kStageKOff);
         __syncwarp();   // every lane is done reading the K rows
@@ -753,7 +748,7 @@ int4_decode_split_kernel(Int4DecodeParams p) {
                 // the token's V scales in units of 2^e (exact: inv is a power of two)
                 const float vx = vp[mt][r].x * inv, vz = vp[mt][r].z * inv;
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
+                for (int j = 0; j < kHL; ++j) {
                     const float w = ex2_approx(sc[mt][r][j] - M[j]);   // 0 for invalid tokens (-inf)
                     wsum[j] += w;
                     pg[0][j] = w * vx;
@@ -763,6 +758,13 @@ int4_decode_split_kernel(Int4DecodeParams p) {
                 }
 #pragma unroll
                 for (int gr = 0; gr < 2; ++gr) {
+                    if constexpr (kPackH) {
+                        // word 4t + t4: the high part (low half) and the low part of
+                        // this lane's head; 32 distinct banks per store
+                        const float hf = __half2float(__float2half_rn(pg[gr][0]));
+                        ptile[(gr * kChunk4 + t) * 4 + t4] = pack_half2(hf, pg[gr][0] - hf);
+                        continue;
+                    }
                     const __half2 hh = __floats2half2_rn(pg[gr][0], pg[gr][1]);
                     const float2 hf = __half22float2(hh);
                     const uint32_t hi = *reinterpret_cast<const uint32_t *>(&hh);
@@ -772,11 +774,6 @@ int4_decode_split_kernel(Int4DecodeParams p) {
                         const int w0 = t4 & 1;
                         ptile[(gr * kChunk4 + t) * 4 + w0] = w0 ? lo : hi;
                         ptile[(gr * kChunk4 + t) * 4 + (w0 ^ 1)] = w0 ? hi : lo;
-                    } else if constexpr (kPack) {
-                        // words 4t + t4 and 4t + (t4 ^ 2): 32 distinct banks per store
-                        const bool lo_lane = t4 >= 2;
-                        ptile[(gr * kChunk4 + t) * 4 + t4] = lo_lane ? lo : hi;
-                        ptile[(gr * kChunk4 + t) * 4 + (t4 ^ 2)] = lo_lane ? hi : lo;
                     } else {
                         ptile[((gr * 2 + 0) * kChunk4 + t) * 4 + t4] = hi;
                         ptile[((gr * 2 + 1) * kChunk4 + t) * 4 + t4] = lo;
@@ -784,13 +781,13 @@ int4_decode_split_kernel(Int4DecodeParams p) {
                 }
             }
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < kHL; ++j) {
             Sl[j] = fmaf(Sl[j], alpha[j], wsum[j]);
             Zl[j][0] = fmaf(Zl[j][0], alpha[j] * two, zs[j][0]);
             Zl[j][1] = fmaf(Zl[j][1], alpha[j] * two, zs[j][1]);
         }
         if (rescale) {  // warp-uniform; accumulator columns are this lane's heads
-            const float f0 = alpha[0] * two, f1 = alpha[1] * two;
+            const float f0 = alpha[0] * two, f1 = (kPackH ? alpha[0] : alpha[1]) * two;
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
                 acc[mt][0] *= f0; acc[mt][1] *= f1;
@@ -855,25 +852,31 @@ int4_decode_split_kernel(Int4DecodeParams p) {
 
     // ---- this warp's state: the lanes of this lane's heads ----
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < kHL; ++j) {
 #pragma unroll
-        for (int o = kPack2 ? 1 : (kPack ? 2 : 4); o < 32; o <<= 1) {
+        for (int o = kPack2 ? 1 : 4; o < 32; o <<= 1) {
             Sl[j] += __shfl_xor_sync(0xffffffffu, Sl[j], o);
             Zl[j][0] += __shfl_xor_sync(0xffffffffu, Zl[j][0], o);
             Zl[j][1] += __shfl_xor_sync(0xffffffffu, Zl[j][1], o);
         }
     }
-    if constexpr (kPack) {
-        // add the low parts' columns (lane t4 ^ 1 when kPack2, else t4 ^ 2) into
-        // the high parts'
+    if constexpr (kPack2) {
+        // add the low parts' columns (lane t4 ^ 1) into the high parts'
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[mt][i] += __shfl_xor_sync(0xffffffffu, acc[mt][i], kPack2 ? 1 : 2);
+            for (int i = 0; i < 4; ++i) acc[mt][i] += __shfl_xor_sync(0xffffffffu, acc[mt][i], 1);
+    } else if constexpr (kPackH) {
+        // the low part's column (2*t4 + 1) into the high part's (2*t4), in the lane
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            acc[mt][0] += acc[mt][1];
+            acc[mt][2] += acc[mt][3];
+        }
     }
     const float unit_scale = __int_as_float((127 + max(-126, min(127, e_cur))) << 23);
     __syncthreads();   // every warp is done with its staging buffers
-    const bool writer = kPack2 ? t4 == 0 : (!kPack || t4 < 2);
+    const bool writer = kPack2 ? t4 == 0 : true;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
         const int gr = mt >> 2;
@@ -884,14 +887,14 @@ int4_decode_split_kernel(Int4DecodeParams p) {
             sm.u.red.acc[warp][h0][dim] = fmaf(acc[mt][0], kNibUnit * 0.0625f, -Zl[0][gr]) * unit_scale;
             sm.u.red.acc[warp][h0][dim + 1] = fmaf(acc[mt][2], kNibUnit, -Zl[0][gr]) * unit_scale;
         }
-        if (writer && h1 < G) {
+        if (writer && kHL > 1 && h1 < G) {
             sm.u.red.acc[warp][h1][dim] = fmaf(acc[mt][1], kNibUnit * 0.0625f, -Zl[1][gr]) * unit_scale;
             sm.u.red.acc[warp][h1][dim + 1] = fmaf(acc[mt][3], kNibUnit, -Zl[1][gr]) * unit_scale;
         }
     }
     if (g == 0 && writer) {
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
+        for (int j = 0; j < kHL; ++j)
             if (hbase + j < G) {
                 sm.u.red.ml[warp][hbase + j][0] = M[j];
                 sm.u.red.ml[warp][hbase + j][1] = Sl[j];
