@@ -176,3 +176,60 @@ def test_int4_append_nonfinite_groups_bit_exact(gpu_lib):
             assert np.array_equal(got[:, [0, 2]].view(np.uint32), sc.view(np.uint32))
             assert np.array_equal(got[:, [1, 3]].view(np.uint32), zr.view(np.uint32))
     assert replaced >= 19
+
+
+@pytest.mark.parametrize("val", [np.nan, np.inf, -np.inf])
+def test_int4_decode_step_appends_a_nonfinite_token_as_zeros(gpu_lib, val):
+    # kvq4_decode_step's own append follows the same reading: a 64-value group
+    # of the new K (or V) row holding a NaN or an infinity is stored as the zero
+    # group (scale 1, zero -0, codes 0), the status carries the non-finite bit,
+    # and the output is finite and equals the oracle's over the stored cache
+    cfg = wl.Workload("nonfinite_step4", 913, batch=3, nqh=8, nkv=2, ctx_range=(2, 900))
+    lens = wl.ctx_lens(cfg)
+    table, num_blocks = wl.block_table(cfg, lens, spare_blocks=1)
+    table_d, lens_d = torch.from_numpy(table).cuda(), torch.from_numpy(lens).cuda()
+    cache = kvq8.alloc_cache4(num_blocks, cfg.nkv)
+    zero = torch.zeros(1, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k_new = np.zeros((cfg.batch, cfg.nkv, HD), np.float32)
+    v_new = np.zeros_like(k_new)
+    full = []
+    for b in range(cfg.batch):
+        L = int(lens[b])
+        k, v = wl.seq_kv(cfg, b, L)
+        full.append((k.copy(), v.copy()))
+        k_new[b], v_new[b] = k[L - 1], v[L - 1]
+        kvq8.quantize_append4(torch.from_numpy(k[None, :L - 1]).cuda(), torch.from_numpy(v[None, :L - 1]).cuda(),
+                              zero, table_d[b:b + 1], cache, dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    k_new[0, 1, 17] = val                   # first group of a K row
+    v_new[2, 0, 90] = val                   # second group of a V row
+    q = wl.queries(cfg)
+    out = torch.full((cfg.batch, cfg.nqh, HD), float("nan"), device="cuda")
+    ws = kvq8.alloc_workspace(cfg.batch, cfg.nqh, cfg.nkv, table.shape[1])
+    kvq8.decode_step4(torch.from_numpy(q).cuda(), torch.from_numpy(k_new).cuda(), torch.from_numpy(v_new).cuda(),
+                      cache, table_d, lens_d, out, ws, sm_scale=SM_SCALE, dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == kvq8.DEV_NONFINITE
+    o = out.cpu().numpy()
+    assert np.all(np.isfinite(o))
+    kc, vc = cache.k_codes.cpu().numpy(), v4_token_major(cache.v_codes.cpu().numpy())
+    kp, vp = cache.k_param.cpu().numpy(), cache.v_param.cpu().numpy()
+    G = cfg.group
+    for b in range(cfg.batch):
+        L = int(lens[b])
+        phys, slot = table[b, (L - 1) // 256], (L - 1) % 256
+        for h in range(cfg.nkv):
+            k_h, v_h = full[b][0][:, h].copy(), full[b][1][:, h].copy()
+            k_h[L - 1], v_h[L - 1] = k_new[b, h], v_new[b, h]
+            for x, codes, par in ((k_h[L - 1], kc, kp), (v_h[L - 1], vc, vp)):
+                packed, sc, zr = oracle.int4_quantize_groups(x[None], 64)
+                assert np.array_equal(codes[phys, h, slot], packed[0])
+                got = par[phys, h, slot]
+                assert np.array_equal(got[[0, 2]].view(np.uint32), sc[0].view(np.uint32))
+                assert np.array_equal(got[[1, 3]].view(np.uint32), zr[0].view(np.uint32))
+            kd = oracle.int4_dequantize_groups(*oracle.int4_quantize_groups(k_h, 64), 64)
+            vd = oracle.int4_dequantize_groups(*oracle.int4_quantize_groups(v_h, 64), 64)
+            ref = np.stack([oracle.attention_f64(q[b, h * G + g], kd, vd, SM_SCALE) for g in range(G)])
+            assert_close(o[b, h * G:(h + 1) * G], ref, f"int4 nonfinite step b={b} h={h}")
