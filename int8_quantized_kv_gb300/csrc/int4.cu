@@ -356,8 +356,8 @@ int4_decode_split_kernel(Int4DecodeParams p) {
     // the operand facing the heads, so one MMA does both halves.  kPackH
     // (G = 4): column 2j + e is part e of head j, so lane (g, t4) holds both
     // parts of head t4 (scores of tokens 16*mt + g + 8*r, accumulator columns),
-    // added in the lane.  kPack2 (G <= 2): columns 0-1 high parts, 2-3 low parts, 4-7 zero;
-    // one shuffle joins the halves (lanes t4 = 0, 1 keep rows g, g + 8) and a
+    // added in the lane.  kPack2 (G <= 2): columns 0-1 high parts, 2-3 low
+    // parts, 4-7 zero; one shuffle joins the halves (lanes t4 = 0, 1 keep rows g, g + 8) and a
     // second moves the second m-tile's scores to lanes t4 = 2, 3, so that lane
     // (g, t4) owns token 16*(t4/2) + g + 8*(t4%2) and both heads: no lane
     // works on padding heads.  Otherwise (G = 8) the columns are the 8 heads
