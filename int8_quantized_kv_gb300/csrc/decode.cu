@@ -154,14 +154,16 @@ __device__ __forceinline__ bool slot_turn_bounded(volatile int *done, int round,
 
 // A decode step's new token of unit (b, h), position pos = ctx_lens[b] - 1,
 // which is row t of the stage staged at st (xk, xv: the token's K and V rows,
-// lane l holding dims 4l..4l+3, loaded by the caller ahead of time):
+// lane l holding dims 4l..4l+3, and phys: the id of the cache block holding
+// pos, all loaded by the caller ahead of time; phys = -1: loaded here):
 // quantised by the warp ([Day 9-3] §2 rule, the same functions as the append
 // kernels), written over the row the copy brought in (K row with its chunk
 // order, V column of the dim-major quarter, both scales) and into the pools
-// and scale arrays.  Only this CTA reads that position in this launch.
+// and scale arrays.  Only this CTA reads that position in this launch.  The
+// block id is valid: the stage was copied.
 __device__ __noinline__ void append_new_token(const DecodeParams &p, int b, int h, int pos, int t,
-                                                 int lane, unsigned char *st, float4 xk, float4 xv) {
-    const int phys = p.block_table[(size_t)b * p.max_blocks + pos / kBS];   // valid: the stage was copied
+                                                 int lane, unsigned char *st, float4 xk, float4 xv, int phys) {
+    if (phys < 0) phys = p.block_table[(size_t)b * p.max_blocks + pos / kBS];
     const float sk = kv_row_scale_checked(xk, p.dev_status), sv = kv_row_scale_checked(xv, p.dev_status);
     const uint32_t wk = low_bytes4(kv_code_bytes4(xk, sk));
     const uint4 cv = kv_code_bytes4(xv, sv);
@@ -421,16 +423,19 @@ decode_split_kernel(DecodeParams p) {
             }
 
             // the warp that decodes the stage holding the new token loads the
-            // token's K and V rows now, beside the query rows, so that their
-            // latencies overlap (G = 8: at the stage, its registers are spent)
+            // token's K and V rows and its block id now, beside the query rows,
+            // so that their latencies overlap and none is left for the stage
+            // (G = 8: at the stage, its registers are spent)
             constexpr bool kPreloadNew = G <= 4;
             float4 nxk = make_float4(0.f, 0.f, 0.f, 0.f), nxv = nxk;
+            int nphys = -1;
             if (kPreloadNew && app_pos >= sp.x) {
                 const int sj = (app_pos - sp.x) / kStageTok - off;
                 if (sj >= 0 && sj < seg_n && sj % kConsumerWarps == warp) {
                     const size_t src = ((size_t)b * p.nkv + h) * kHD;
                     nxk = reinterpret_cast<const float4 *>(p.k_new + src)[lane];
                     nxv = reinterpret_cast<const float4 *>(p.v_new + src)[lane];
+                    nphys = p.block_table[(size_t)b * p.max_blocks + app_pos / kBS];
                 }
             }
 
@@ -478,7 +483,7 @@ decode_split_kernel(DecodeParams p) {
                             nxk = reinterpret_cast<const float4 *>(p.k_new + src)[lane];
                             nxv = reinterpret_cast<const float4 *>(p.v_new + src)[lane];
                         }
-                        append_new_token(p, b, h, app_pos, tnew, lane, const_cast<unsigned char *>(st), nxk, nxv);
+                        append_new_token(p, b, h, app_pos, tnew, lane, const_cast<unsigned char *>(st), nxk, nxv, nphys);
                     }
                     const int ta = lane, tb = lane + 32;
                     const bool va = ta < nvalid, vb = tb < nvalid;

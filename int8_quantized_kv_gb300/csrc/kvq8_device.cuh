@@ -114,18 +114,27 @@ __device__ __forceinline__ float kv_row_scale_checked(float4 &x, uint32_t *statu
 // qm = max |x| over the block (1 when below 1e-6); block scale = qm * (1/127);
 // code = round_half_even(x * (127/qm)) clamped to [-128, 127].  A block that
 // holds a NaN or an infinity is quantised as a block of zeros (scale 1/127,
-// codes 0) and KVQ8_DEV_NONFINITE is set in *status (when non-null).
+// codes 0) and KVQ8_DEV_NONFINITE is set in *status (when non-null).  The
+// four block maxima are four independent unsigned warp reductions of |x| as
+// bit patterns (the order of kv_row_scale_checked), which also detect the
+// non-finite blocks.
 __device__ __forceinline__ void quantize_q_vals_warp(const float (&xs)[4], int lane, int8_t *codes,
                                                      float *scales, uint32_t *status) {
+    uint32_t mb[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) mb[k] = __reduce_max_sync(0xffffffffu, __float_as_uint(xs[k]) & 0x7fffffffu);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         float x = xs[k];
-        if (__any_sync(0xffffffffu, nonfinite(x))) {
+        float qm;
+        if (mb[k] >= 0x7f800000u) {   // warp-uniform
             x = 0.0f;
+            qm = 1.0f;
             if (lane == 0) flag_status(status, KVQ8_DEV_NONFINITE);
+        } else {
+            qm = __uint_as_float(mb[k]);
+            if (qm < 1e-6f) qm = 1.0f;
         }
-        float qm = warp_max(fabsf(x));
-        if (qm < 1e-6f) qm = 1.0f;
         const float iq = __fdiv_rn(127.0f, qm);
         int c = __float2int_rn(__fmul_rn(x, iq));
         c = max(-128, min(127, c));
