@@ -698,7 +698,7 @@ decode_split_kernel(DecodeParams p) {
 #pragma unroll
                     for (int w = 0; w < kConsumerWarps; ++w) {
                         const float *r = reinterpret_cast<const float *>(smem + Lay::oScratch + w * Lay::kScratch);
-                        const float f = exp2f(r[G * kHD + g] - m);
+                        const float f = ex2_approx(r[G * kHD + g] - m);
                         s_sum = fmaf(r[G * kHD + G + g], f, s_sum);
                         a = fmaf(r[g * kHD + d], f, a);
                     }
@@ -729,9 +729,12 @@ decode_split_kernel(DecodeParams p) {
 
 // Merge of the partial records of one (sequence, query head); thread = dim.
 // [Day 9-2] §2 segment 3 generalised to several partial states:
-// M = max_i M_i, S = sum_i S_i 2^(M_i - M), out = sum_i acc_i 2^(M_i - M) / S.
-// The records come from one split kernel, or from two (mixed precision by
-// token age: the 4-bit split over [0, x) and the int8 split over [x, L)).
+// M = max_i M_i, S = sum_i S_i 2^(M_i - M), out = sum_i acc_i 2^(M_i - M) / S,
+// the factors 2^(M_i - M) <= 1 by the approximate base-2 exponential, as the
+// split kernel's weights (the library's accurate exp2f cost this short kernel
+// about 0.5 us of its critical path).  The records come from one split kernel,
+// or from two (mixed precision by token age: the 4-bit split over [0, x) and
+// the int8 split over [x, L)).
 constexpr int kCombineRegs = 8;   // records merged from registers (more: the loop below)
 constexpr int kCombineWide = 32;  // records of one source merged after one load round
 
@@ -791,7 +794,7 @@ decode_combine_kernel(DecodeParams p, int G) {
 #pragma unroll
             for (int j = 0; j < kCombineRegs; ++j) {
                 if (j < n1) {
-                    const float f = exp2f(mr[j] - m);
+                    const float f = ex2_approx(mr[j] - m);
                     s_sum = fmaf(sr[j], f, s_sum);
                     a = fmaf(ar[j], f, a);
                 }
@@ -822,7 +825,7 @@ decode_combine_kernel(DecodeParams p, int G) {
 #pragma unroll
             for (int j = 0; j < kCombineWide; ++j) {
                 if (j < n1) {
-                    const float f = exp2f(mlr[j].x - m);
+                    const float f = ex2_approx(mlr[j].x - m);
                     s_sum = fmaf(mlr[j].y, f, s_sum);
                     a = fmaf(ar[j], f, a);
                 }
@@ -855,7 +858,7 @@ decode_combine_kernel(DecodeParams p, int G) {
 #pragma unroll
             for (int j = 0; j < kCombineRegs; ++j) {
                 if (j < meta0.y + meta1.y) {
-                    const float f = exp2f(mr[j] - m);
+                    const float f = ex2_approx(mr[j] - m);
                     s_sum = fmaf(sr[j], f, s_sum);
                     a = fmaf(ar[j], f, a);
                 }
@@ -883,13 +886,13 @@ decode_combine_kernel(DecodeParams p, int G) {
         }
         if (mg == -INFINITY) return;
         const float m_new = fmaxf(m, mg);
-        const float f_old = exp2f(m - m_new);   // 0 while m is -inf
+        const float f_old = ex2_approx(m - m_new);   // 0 while m is -inf
         s_sum *= f_old;
         a *= f_old;
 #pragma unroll
         for (int j = 0; j < kCombineRegs; ++j) {
             if (j < n) {
-                const float f = exp2f(mr[j] - m_new);
+                const float f = ex2_approx(mr[j] - m_new);
                 s_sum = fmaf(sr[j], f, s_sum);
                 a = fmaf(ar[j], f, a);
             }
@@ -938,7 +941,7 @@ decode_combine_fixed_kernel(DecodeParams p, int G, int ns) {
 #pragma unroll
         for (int j = 0; j < kCombineRegs; ++j) {
             if (j < n1) {
-                const float f = exp2f(mr[j] - m);
+                const float f = ex2_approx(mr[j] - m);
                 s_sum = fmaf(sr[j], f, s_sum);
                 a = fmaf(ar[j], f, a);
             }

@@ -912,7 +912,7 @@ int4_decode_split_kernel(Int4DecodeParams p) {
         if (m != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < kWarps4; ++w) {
-                const float f = exp2f(sm.u.red.ml[w][gq][0] - m);
+                const float f = ex2_approx(sm.u.red.ml[w][gq][0] - m);
                 s_sum = fmaf(sm.u.red.ml[w][gq][1], f, s_sum);
                 a = fmaf(sm.u.red.acc[w][gq][d], f, a);
             }
