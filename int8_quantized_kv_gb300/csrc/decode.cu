@@ -551,7 +551,7 @@ decode_split_kernel(DecodeParams p) {
 #pragma unroll
                         for (int g = 0; g < G; ++g) {
                             const float m_new = fmaxf(M[g], redux_max_f32(fmaxf(sa[g], sb[g])));
-                            alpha[g] = exp2f(M[g] - m_new);   // 0 while M is -inf
+                            alpha[g] = ex2_approx(M[g] - m_new);   // 0 while M is -inf
                             M[g] = m_new;
                         }
                     } else {
