@@ -454,6 +454,14 @@ decode_split_kernel(DecodeParams p) {
                 if (nbq < p.batch) load_q_rows(nbq, nh);
             }
 
+            // this CTA holds the unit's first stage (off == 0): it publishes where
+            // the unit's records are, CTAs c .. c_last (computed here, off the
+            // path of the segment's end)
+            int meta_n = 0;
+            if (tid == 0 && off == 0) {
+                const long long end_u = lo + kbase + nb;
+                meta_n = (int)((end_u * C + T - 1) / T) - c;
+            }
             float M[G], Sl[G], acc[8][4];
 #pragma unroll
             for (int g = 0; g < G; ++g) { M[g] = -INFINITY; Sl[g] = 0.0f; }
@@ -687,35 +695,35 @@ decode_split_kernel(DecodeParams p) {
             }
             named_barrier_sync(1, kConsumerWarps * 32);
             const size_t rec = (size_t)c + u;
-            for (int idx = tid; idx < G * kHD; idx += kConsumerWarps * 32) {
-                const int g = idx / kHD, d = idx % kHD;
+            // four dims per thread: one pass for G <= 4
+            for (int idx = tid; idx < G * kHD / 4; idx += kConsumerWarps * 32) {
+                const int g = idx / (kHD / 4), d = (idx % (kHD / 4)) * 4;
                 float m = -INFINITY;
 #pragma unroll
                 for (int w = 0; w < kConsumerWarps; ++w)
                     m = fmaxf(m, reinterpret_cast<const float *>(smem + Lay::oScratch + w * Lay::kScratch)[G * kHD + g]);
-                float s_sum = 0.0f, a = 0.0f;
+                float s_sum = 0.0f;
+                float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                 if (m != -INFINITY) {
 #pragma unroll
                     for (int w = 0; w < kConsumerWarps; ++w) {
                         const float *r = reinterpret_cast<const float *>(smem + Lay::oScratch + w * Lay::kScratch);
                         const float f = ex2_approx(r[G * kHD + g] - m);
                         s_sum = fmaf(r[G * kHD + G + g], f, s_sum);
-                        a = fmaf(r[g * kHD + d], f, a);
+                        const float4 v = *reinterpret_cast<const float4 *>(r + g * kHD + d);
+                        a.x = fmaf(v.x, f, a.x);
+                        a.y = fmaf(v.y, f, a.y);
+                        a.z = fmaf(v.z, f, a.z);
+                        a.w = fmaf(v.w, f, a.w);
                     }
                 }
-                p.ws_acc[(rec * G + g) * kHD + d] = a;
+                *reinterpret_cast<float4 *>(p.ws_acc + (rec * G + g) * kHD + d) = a;
                 if (d == 0) {
                     p.ws_ml[(rec * G + g) * 2 + 0] = m;
                     p.ws_ml[(rec * G + g) * 2 + 1] = s_sum;
                 }
             }
-            if (tid == 0 && off == 0) {
-                // this CTA holds the unit's first stage: publish where its records are
-                const long long start_u = lo + kbase;
-                const long long end_u = start_u + nb;
-                const int c_last = (int)((end_u * C + T - 1) / T) - 1;
-                p.ws_meta[u] = make_int2(c, c_last - c + 1);
-            }
+            if (tid == 0 && off == 0) p.ws_meta[u] = make_int2(c, meta_n);
             remaining -= seg_n;
             kbase += seg_n;
             off = 0;
