@@ -11,7 +11,9 @@
 // sum at the end (segment 3).  The softmax runs in base 2 (scores are
 // pre-multiplied by log2(e)), which leaves the normalised weights unchanged.
 //
-// GB300 structure of the split kernel (one CTA per SM, 8 warps):
+// GB300 structure of the split kernel (one CTA per SM, 8 warps; for G = 2 and
+// a call of at least 16 units two CTAs per SM, each with half the ring and at
+// most 128 registers a thread, see kSmemLimit2):
 //  * Work: the cache is a sequence of 64-token stages, unit by unit (unit =
 //    (sequence, kv head)); CTA c takes stages [c*T/C, (c+1)*T/C), i.e. an
 //    equal share regardless of how ragged the contexts are.  Where a unit
@@ -62,6 +64,16 @@ constexpr int kSmemLimit = 232448;          // 227 KiB opt-in per CTA on sm_103a
 // 4-bit CTAs are done, instead of waiting for the last, which would run
 // alone with a third of the SM's warps.
 constexpr int kSmemLimitMixed = 184320;
+// Two CTAs per SM (G = 2, calls of at least 16 units): each gets half of the
+// SM's 228 KiB less the per-CTA reserve (a 6-stage ring) and at most 128
+// registers a thread (the G = 2 consumer fits with 4 bytes spilled).  The 14
+// consumer warps of an SM then hide more of each stage's latency: the 28-layer
+// 8K step streams at 96 % of the copy peak instead of 95 %.  A call of fewer
+// units keeps one CTA per SM: with twice the CTAs a unit's record count would
+// pass what the merge reads in one round, and a few-unit call is latency-bound.
+constexpr int kSmemLimit2 = 115712;
+constexpr int kTwoPerSmMinUnits = 16;
+constexpr int kTwoPerSmMinStages = 16;   // per CTA, counted on the table's width
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 constexpr int kPRowHalves = 72;             // P row: 64 tokens + 8 halves of padding
 constexpr float kLazyLog2 = 8.0f;           // running-max slack (log2 units), see segment 2b
@@ -88,7 +100,7 @@ struct SplitLayout {
     static constexpr int kBytes = oDone + kStages * 4;
     static_assert(oMisc % 16 == 0 && oFull % 16 == 0 && oScratch % 16 == 0, "alignment");
     static_assert(kBytes <= kLimit, "shared memory budget");
-    static_assert(kStages >= 8, "ring too shallow");
+    static_assert(kStages >= 6, "ring too shallow");
     static_assert(G * 2 * kPRowHalves * 2 <= kScratch, "P fits the warp scratch");
 };
 
@@ -195,10 +207,15 @@ __device__ __noinline__ void append_new_token(const DecodeParams &p, int b, int 
     __syncwarp();   // the patched rows are read by every lane below
 }
 
-template <int G, bool kMixed>
-__global__ void __launch_bounds__(kSplitThreads, 1)
+// The ring and register budget of a split-kernel instantiation: a mixed
+// decode's int8 split, a two-per-SM grid, or the default.
+template <int G, bool kMixed, int kCtas>
+using SplitLay = SplitLayout<G, kMixed ? kSmemLimitMixed : (kCtas == 2 ? kSmemLimit2 : kSmemLimit)>;
+
+template <int G, bool kMixed, int kCtas>
+__global__ void __launch_bounds__(kSplitThreads, kCtas)
 decode_split_kernel(DecodeParams p) {
-    using Lay = SplitLayout<G, kMixed ? kSmemLimitMixed : kSmemLimit>;
+    using Lay = SplitLay<G, kMixed, kCtas>;
     extern __shared__ __align__(1024) unsigned char smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
@@ -970,14 +987,14 @@ int device_sm_count() {
     return cached[dev];
 }
 
-template <int G, bool kMixed>
+template <int G, bool kMixed, int kCtas>
 cudaError_t launch_split_gm(const DecodeParams &p, cudaStream_t s) {
-    using Lay = SplitLayout<G, kMixed ? kSmemLimitMixed : kSmemLimit>;
+    using Lay = SplitLay<G, kMixed, kCtas>;
     static std::atomic<uint64_t> configured{0};
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(min(sms, kMaxCtas));
+    cfg.gridDim = dim3(min(sms * kCtas, kMaxCtas));
     cfg.blockDim = dim3(kSplitThreads);
     cfg.dynamicSmemBytes = Lay::kBytes;
     cfg.stream = s;
@@ -989,15 +1006,23 @@ cudaError_t launch_split_gm(const DecodeParams &p, cudaStream_t s) {
     return launch_after_setting(
         configured,
         [] {
-            return cudaFuncSetAttribute(decode_split_kernel<G, kMixed>,
+            return cudaFuncSetAttribute(decode_split_kernel<G, kMixed, kCtas>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
         },
-        [&] { return cudaLaunchKernelEx(&cfg, decode_split_kernel<G, kMixed>, p); });
+        [&] { return cudaLaunchKernelEx(&cfg, decode_split_kernel<G, kMixed, kCtas>, p); });
 }
 
 template <int G>
 cudaError_t launch_split_g(const DecodeParams &p, cudaStream_t s) {
-    return p.first_q8_block ? launch_split_gm<G, true>(p, s) : launch_split_gm<G, false>(p, s);
+    if (p.first_q8_block) return launch_split_gm<G, true, 1>(p, s);
+    if constexpr (G == 2) {
+        const int64_t units = (int64_t)p.batch * p.nkv;
+        const int64_t stages_max = units * p.max_blocks * (kBS / kStageTok);
+        const int sms = device_sm_count();
+        if (units >= kTwoPerSmMinUnits && stages_max >= (int64_t)kTwoPerSmMinStages * 2 * sms)
+            return launch_split_gm<G, false, 2>(p, s);
+    }
+    return launch_split_gm<G, false, 1>(p, s);
 }
 
 }  // namespace
