@@ -64,13 +64,15 @@ constexpr int kSmemLimit = 232448;          // 227 KiB opt-in per CTA on sm_103a
 // 4-bit CTAs are done, instead of waiting for the last, which would run
 // alone with a third of the SM's warps.
 constexpr int kSmemLimitMixed = 184320;
-// Two CTAs per SM (G = 2, calls of at least 16 units): each gets half of the
-// SM's 228 KiB less the per-CTA reserve (a 6-stage ring) and at most 128
-// registers a thread (the G = 2 consumer fits with 4 bytes spilled).  The 14
-// consumer warps of an SM then hide more of each stage's latency: the 28-layer
-// 8K step streams at 96 % of the copy peak instead of 95 %.  A call of fewer
-// units keeps one CTA per SM: with twice the CTAs a unit's record count would
-// pass what the merge reads in one round, and a few-unit call is latency-bound.
+// Two CTAs per SM (G = 2, calls of at least 16 units, and the int8 part of a
+// G = 2 mixed-precision decode): each gets half of the SM's 228 KiB less the
+// per-CTA reserve (a 6-stage ring) and at most 128 registers a thread (the
+// G = 2 consumer fits with 4 bytes spilled).  The 14 consumer warps of an SM
+// then hide more of each stage's latency: the 28-layer 8K step streams at 96 %
+// of the copy peak instead of 95 %.  Such a CTA also fits beside one CTA of
+// the 4-bit split.  A call of fewer units keeps one CTA per SM: with twice the
+// CTAs a unit's record count would pass what the merge reads in one round, and
+// a few-unit call is latency-bound.
 constexpr int kSmemLimit2 = 115712;
 constexpr int kTwoPerSmMinUnits = 16;
 constexpr int kTwoPerSmMinStages = 16;   // per CTA, counted on the table's width
@@ -207,10 +209,10 @@ __device__ __noinline__ void append_new_token(const DecodeParams &p, int b, int 
     __syncwarp();   // the patched rows are read by every lane below
 }
 
-// The ring and register budget of a split-kernel instantiation: a mixed
-// decode's int8 split, a two-per-SM grid, or the default.
+// The ring and register budget of a split-kernel instantiation: a two-per-SM
+// grid, a mixed decode's int8 split, or the default.
 template <int G, bool kMixed, int kCtas>
-using SplitLay = SplitLayout<G, kMixed ? kSmemLimitMixed : (kCtas == 2 ? kSmemLimit2 : kSmemLimit)>;
+using SplitLay = SplitLayout<G, kCtas == 2 ? kSmemLimit2 : (kMixed ? kSmemLimitMixed : kSmemLimit)>;
 
 template <int G, bool kMixed, int kCtas>
 __global__ void __launch_bounds__(kSplitThreads, kCtas)
@@ -1014,7 +1016,10 @@ cudaError_t launch_split_gm(const DecodeParams &p, cudaStream_t s) {
 
 template <int G>
 cudaError_t launch_split_g(const DecodeParams &p, cudaStream_t s) {
-    if (p.first_q8_block) return launch_split_gm<G, true, 1>(p, s);
+    if (p.first_q8_block) {
+        if constexpr (G == 2) return launch_split_gm<G, true, 2>(p, s);
+        return launch_split_gm<G, true, 1>(p, s);
+    }
     if constexpr (G == 2) {
         const int64_t units = (int64_t)p.batch * p.nkv;
         const int64_t stages_max = units * p.max_blocks * (kBS / kStageTok);
