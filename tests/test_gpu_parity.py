@@ -222,6 +222,20 @@ def test_decode_zero_length_sequences(gpu_lib):
             assert_close(out[b, h * 2:(h + 1) * 2], case.oracle_unit(b, h))
 
 
+def test_decode_two_ctas_per_sm_ragged(gpu_lib):
+    # G = 2 over 32 units and a 47-block table: the split runs two CTAs per SM
+    # (6-stage rings); ragged lengths, an empty and a one-token sequence
+    cfg = _unit_cfg(2, nkv=8, batch=4, ctx_range=(1, 12000), cid=135)
+    lens = np.array([0, 11900, 1, 7777], np.int32)
+    case = Case(cfg, lens=lens)
+    out = case.decode()
+    assert not out[0].any()
+    for b in (1, 2, 3):
+        for h in range(cfg.nkv):
+            assert_close(out[b, h * 2:(h + 1) * 2], case.oracle_unit(b, h), f"b={b} h={h}")
+    assert case.status_bits() == 0
+
+
 def test_single_head_l256_and_fp32_kv_delta(gpu_lib):
     cfg = wl.SINGLE_HEAD_L256
     case = Case(cfg)
@@ -439,6 +453,15 @@ def test_decode_step_empty_sequences_and_ragged_batch(gpu_lib):
     lens = np.array([0, 700, 0, 1, 333], np.int32)
     case = StepCase(cfg, lens=lens)
     _check_step(case, case.step())
+
+
+def test_decode_step_two_ctas_per_sm(gpu_lib):
+    # the decode step on the two-CTAs-per-SM grid (G = 2, 32 units, 47 blocks)
+    cfg = _unit_cfg(2, nkv=8, batch=4, ctx_range=(1, 12000), cid=425)
+    lens = np.array([11900, 1, 0, 5000], np.int32)
+    case = StepCase(cfg, lens=lens)
+    _check_step(case, case.step())
+    assert case.status_bits() == 0
 
 
 def test_decode_step_unit_over_many_ctas(gpu_lib):
