@@ -758,8 +758,10 @@ decode_split_kernel(DecodeParams p) {
 // [Day 9-2] §2 segment 3 generalised to several partial states:
 // M = max_i M_i, S = sum_i S_i 2^(M_i - M), out = sum_i acc_i 2^(M_i - M) / S,
 // the factors 2^(M_i - M) <= 1 by the approximate base-2 exponential, as the
-// split kernel's weights (the library's accurate exp2f cost this short kernel
-// about 0.5 us of its critical path).  The records come from one split kernel,
+// split kernel's weights, and the final division by the fast approximate one
+// (S >= 1 and far below 2^126, where it is within 2 ulp; the library's exact
+// exp2f and division cost this short kernel about 0.6 us of its critical
+// path).  The records come from one split kernel,
 // or from two (mixed precision by token age: the 4-bit split over [0, x) and
 // the int8 split over [x, L)).
 constexpr int kCombineRegs = 8;   // records merged from registers (more: the loop below)
@@ -827,7 +829,7 @@ decode_combine_kernel(DecodeParams p, int G) {
                 }
             }
         }
-        *o = s_sum > 0.0f ? a / s_sum : 0.0f;
+        *o = s_sum > 0.0f ? __fdividef(a, s_sum) : 0.0f;
         return;
     }
     if (one && n1 <= kCombineWide) {
@@ -858,7 +860,7 @@ decode_combine_kernel(DecodeParams p, int G) {
                 }
             }
         }
-        *o = s_sum > 0.0f ? a / s_sum : 0.0f;
+        *o = s_sum > 0.0f ? __fdividef(a, s_sum) : 0.0f;
         return;
     }
     if (!one && meta0.y + meta1.y <= kCombineRegs) {
@@ -891,7 +893,7 @@ decode_combine_kernel(DecodeParams p, int G) {
                 }
             }
         }
-        *o = s_sum > 0.0f ? a / s_sum : 0.0f;
+        *o = s_sum > 0.0f ? __fdividef(a, s_sum) : 0.0f;
         return;
     }
     // more records: groups of kCombineRegs records, each group loaded at once
@@ -930,7 +932,7 @@ decode_combine_kernel(DecodeParams p, int G) {
         merge_group(p.ws_ml, p.ws_acc, r00 + j0, min(kCombineRegs, meta0.y - j0));
     for (int j0 = 0; j0 < meta1.y; j0 += kCombineRegs)
         merge_group(p.ws_ml2, p.ws_acc2, r10 + j0, min(kCombineRegs, meta1.y - j0));
-    *o = s_sum > 0.0f ? a / s_sum : 0.0f;
+    *o = s_sum > 0.0f ? __fdividef(a, s_sum) : 0.0f;
 }
 
 // The merge of the 4-bit decode, whose split writes unit u's records at
@@ -974,7 +976,7 @@ decode_combine_fixed_kernel(DecodeParams p, int G, int ns) {
             }
         }
     }
-    *o = s_sum > 0.0f ? a / s_sum : 0.0f;
+    *o = s_sum > 0.0f ? __fdividef(a, s_sum) : 0.0f;
 }
 
 int device_sm_count() {

@@ -460,8 +460,11 @@ int4_decode_split_kernel(Int4DecodeParams p) {
     float qmax = 0.0f;
 #pragma unroll
     for (int w = 0; w < kWarps4; ++w) qmax = fmaxf(qmax, sm.qmax[w]);
-    const int qexp = (qmax > 0.0f && isfinite(qmax)) ? 13 - ilogbf(qmax) : 0;
-    const float qscale = ldexpf(1.0f, max(-120, min(120, qexp)));
+    // 2^qk with qk = 13 - ilogb(max |q|), clamped to [-120, 120], built from
+    // the exponent bits (a subnormal maximum reads as 2^-127: clamped alike)
+    const int qexp = (qmax > 0.0f && isfinite(qmax)) ? 13 - ((int)((__float_as_uint(qmax) >> 23) & 0xff) - 127) : 0;
+    const int qk = max(-120, min(120, qexp));
+    const float qscale = __int_as_float((127 + qk) << 23);
     // B fragments of Q in the Q.K k-order (column gg of lane (gg, tt); the
     // values facing high nibbles, k = 2*tt + e, carry q / 16).  kPack: kept in
     // registers, column gg = head gg % 4, high part for gg < 4, low part else;
@@ -540,7 +543,7 @@ int4_decode_split_kernel(Int4DecodeParams p) {
     for (int j = 0; j < 2; ++j)
 #pragma unroll
         for (int gr = 0; gr < 2; ++gr) qq[j][gr] = sm.qq[hbase + j][gr];
-    const float score_scale = p.sm_scale_log2 / qscale;
+    const float score_scale = p.sm_scale_log2 * __int_as_float((127 - qk) << 23);   // / qscale, exactly
 
     // scores per lane: kPack2 1 token x 2 heads, kPackH 4 tokens (rows g, g + 8
     // of both m-tiles) x 1 head, else 4 tokens x 2 heads
